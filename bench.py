@@ -1,0 +1,365 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged heterogeneous-rank LoRA delta on GB300.
+
+One step = one pass of the hot path over one batch: the token plan, the decode delta for
+the batch's decode tokens and the tensor-core segment delta for its prefill segments,
+for every projection of the workload.  Metric: LoRA-delta tokens/s per layer
+(tokens x layers / step time), plus the dominant kernel's roofline fraction.
+
+  python bench.py [--workload NAME] [--steps K] [--warmup W] [--gpus N]
+  python bench.py --impl reference ...      # the fp64 CPU oracle on the host cores
+
+For N > 1 (torchrun, one process per GPU) every rank serves its own batch (seed + rank):
+the delta has no cross-token exchange, so ranks are independent replicas (weak scaling)
+and the only collectives are the timing barrier and the max-over-ranks reduction.
+
+Timing: W untimed warm-up steps; K timed steps, each preceded by a 2 x L2 write that
+evicts the pool and inputs from L2 (the flush itself is outside the per-step CUDA-event
+intervals); barrier + synchronize on both sides of the timed region; max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from rank_delta_paged_gb300 import workloads as W  # noqa: E402
+
+DEFAULT_WORKLOAD = "decode_7b"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=0, help="timed steps (0 = about 2 s of work)")
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            mp = json.load(f)
+        return float(mp["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def algorithmic_bytes(w: W.Workload) -> float:
+    """Per step: every used adapter's A^T and B rows once, x and y0 read, y written,
+    for every projection (2 bytes per fp16 element)."""
+    used = w.used_adapters()
+    adapter = sum(4.0 * int(w.ranks[a]) * w.hidden for a in used)
+    xy = 6.0 * w.hidden * w.T
+    return w.n_proj * (adapter + xy)
+
+
+def algorithmic_flops(w: W.Workload) -> float:
+    idx = w.token_adapter_idx
+    r = np.where(idx >= 0, w.ranks[np.maximum(idx, 0)], 0).astype(np.float64)
+    return w.n_proj * 4.0 * w.hidden * float(r.sum())
+
+
+# ---------------------------------------------------------------- clocks sampling
+class ClockSampler:
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str):
+        self.uuid = uuid
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            if self.uuid and self.uuid not in f[0]:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+def oracle_rate(w: W.Workload, seconds: float):
+    """Tokens/s per layer of the fp64 oracle on a bounded token sample (projection 0)."""
+    import oracle
+    x, y0 = w.x(0), w.y0(0)
+    rng = np.random.default_rng(1)
+    per_call = min(w.T, 64)
+    done, t_used, calls = 0, 0.0, 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        sel = np.sort(rng.choice(w.T, per_call, replace=False)).astype(np.int32)
+        s = time.perf_counter()
+        oracle.workload_reference(w, p=0, sel=sel, x=x, y0=y0)
+        t_used += time.perf_counter() - s
+        done += per_call
+        calls += 1
+    # one layer = n_proj / n_layers projections of the same work
+    proj_per_layer = w.n_proj // w.n_layers
+    rate = done / (t_used * proj_per_layer)
+    sample = (f"{calls} oracle calls x {per_call} random tokens of projection 0 "
+              f"({done} token-projections, {t_used:.1f} s), scaled to {proj_per_layer} "
+              f"projection(s) per layer")
+    return rate, oracle.threads(), sample
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    w = W.by_name(args.workload, seed=args.seed)
+    steps = args.steps or 3
+    warm = args.warmup
+    seconds = max(2.0, min(20.0, 60.0 / max(1, steps + warm)))
+    for _ in range(warm):
+        oracle_rate(w, 0.5)
+    rates, cores, sample = [], 1, ""
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        r, cores, sample = oracle_rate(w, seconds)
+        rates.append(r)
+    wall = time.perf_counter() - t0
+    value = statistics.mean(rates)
+    line = {
+        "impl": "reference", "metric": "lora_delta_tokens_per_s_per_layer", "value": value,
+        "unit": "tokens/s/layer", "n_gpus": args.gpus, "steps": steps, "warmup": warm,
+        "ms_per_step": 1e3 * wall / steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": config_of(w, "oracle bounded sample; no L2 concerns on the CPU"),
+        "cpu_baseline": {"value": value, "unit": "tokens/s/layer", "cores": cores,
+                         "kind": "oracle", "sample": f"each step: {sample}"},
+        "e2e": {"value": value, "unit": "tokens/s/layer", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w: W.Workload, l2: str):
+    used = w.used_adapters()
+    return {"workload": w.name, "hidden": w.hidden, "projections": w.n_proj, "layers": w.n_layers,
+            "tokens": w.T, "prefill_segments": w.n_seg, "adapters": w.n_adapters,
+            "unique_adapters": int(used.size), "pool_pages": w.num_pages,
+            "kv_pages": w.kv_pages, "l2": l2}
+
+
+# ---------------------------------------------------------------- our arm
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    import torch
+    import torch.distributed as dist
+    import rank_delta_paged_gb300 as rdp
+    from rank_delta_paged_gb300.harness import PoolSession
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    rdp.build.build()
+    lib = rdp.lib()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    w = W.by_name(args.workload, seed=args.seed + rank)
+    used = w.used_adapters()
+    sess = PoolSession(w, device=local)
+    stream = torch.cuda.current_stream()
+    sess.load(used, stream)
+    dev = torch.device("cuda", local)
+    xs, ys, y0s = [], [], []
+    for p in range(w.n_proj):
+        x, y0, idx, seg = sess.device_inputs(p)
+        xs.append(x)
+        y0s.append(y0)
+        ys.append(y0.clone())
+    n_seg = w.n_seg
+    l2 = int(torch.cuda.get_device_properties(local).L2_cache_size)
+    flush = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=dev)
+
+    def step():
+        for p in range(w.n_proj):
+            rdp.slora_lora_apply(sess.pool, p, xs[p], ys[p], w.T, idx, seg, n_seg, None, stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    # size K so the timed region lasts about 2 s (clock sampling needs samples under load)
+    if args.steps > 0:
+        K = args.steps
+    else:
+        t0 = time.perf_counter()
+        for _ in range(5):
+            flush.zero_()
+            step()
+        torch.cuda.synchronize()
+        per = (time.perf_counter() - t0) / 5
+        K = int(min(20000, max(10, 2.0 / max(per, 1e-6))))
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    launches0 = rdp.slora_pool_launch_count(sess.pool)
+    uuid = ""
+    try:
+        uuid = str(torch.cuda.get_device_properties(local).uuid)
+    except Exception:
+        pass
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(uuid) as clk:
+        for k in range(K):
+            flush.zero_()
+            starts[k].record(stream)
+            step()
+            ends[k].record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    launches = rdp.slora_pool_launch_count(sess.pool) - launches0
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = float(sum(step_ms))
+    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    tok = torch.tensor([float(w.T)], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.all_reduce(tok, op=dist.ReduceOp.SUM)
+    total_ms = float(t.item())
+    ms_per_step = total_ms / K
+    value = float(tok.item()) * w.n_layers / (ms_per_step / 1e3)
+
+    # dominant kernel roofline: the delta kernels are the whole step
+    hbm, peak_kind = peaks()
+    alg_bytes = algorithmic_bytes(w)
+    achieved = alg_bytes / (ms_per_step / 1e3) / 1e9
+    kernel_stats = rdp.slora_pool_kernel_stats(sess.pool) if hasattr(rdp, "slora_pool_kernel_stats") else None
+
+    # ---- end to end through the C ABI from pinned host buffers --------------------
+    hx = [torch.from_numpy(w.x(p).view(np.int16)).view(torch.float16).pin_memory() for p in range(w.n_proj)]
+    hy0 = [torch.from_numpy(w.y0(p).view(np.int16)).view(torch.float16).pin_memory() for p in range(w.n_proj)]
+    hidx = torch.from_numpy(w.token_adapter_idx).pin_memory()
+    hseg = None if w.seg_indptr is None else torch.from_numpy(w.seg_indptr).pin_memory()
+    hy = [torch.empty_like(h) for h in hy0]
+    hy = [h.pin_memory() for h in hy]
+    adapter_bytes = sum(4 * int(w.ranks[a]) * w.hidden * w.n_proj for a in used)
+    h2d = sum(h.numel() * 2 for h in hx) + sum(h.numel() * 2 for h in hy0) + hidx.numel() * 4 + \
+        (0 if hseg is None else hseg.numel() * 4) + adapter_bytes
+    d2h = sum(h.numel() * 2 for h in hy)
+    e2e_ms = []
+    for k in range(args.e2e_steps + 2):
+        sess.evict(used, stream)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        idx.copy_(hidx, non_blocking=True)
+        if hseg is not None:
+            seg.copy_(hseg, non_blocking=True)
+        sess.load(used, stream)
+        for p in range(w.n_proj):
+            xs[p].copy_(hx[p], non_blocking=True)
+            ys[p].copy_(hy0[p], non_blocking=True)
+            rdp.slora_lora_apply(sess.pool, p, xs[p], ys[p], w.T, idx, seg, n_seg, None, stream)
+            hy[p].copy_(ys[p], non_blocking=True)
+        torch.cuda.synchronize()
+        if k >= 2:
+            e2e_ms.append(1e3 * (time.perf_counter() - t0))
+    e2e_t = torch.tensor([statistics.mean(e2e_ms)], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
+    e2e_value = float(tok.item()) * w.n_layers / (float(e2e_t.item()) / 1e3)
+    status = sess.device_status()
+    if status != 0:
+        print(f"device status {status} after the run", file=sys.stderr)
+        return 3
+
+    line = {
+        "metric": "lora_delta_tokens_per_s_per_layer", "value": value, "unit": "tokens/s/layer",
+        "n_gpus": world, "steps": K, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded; random-init adapters, no dataset)",
+        "config": config_of(w, "flushed: 2 x L2 written before every timed step, outside the "
+                               "per-step CUDA-event intervals"),
+        "gpu_launches": int(launches),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": None,
+                     "kernel": "whole delta step (plan + delta kernels)",
+                     "peak_kind": f"{peak_kind} HBM copy bandwidth",
+                     "algorithmic_bytes_per_step": alg_bytes},
+        "e2e": {"value": e2e_value, "unit": "tokens/s/layer", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h),
+                "includes": "H2D of x, y0, token map; cold load of the batch's adapters from the "
+                            "pinned store (copy + page scatter); delta; D2H of y; eviction"},
+        "flops_per_step": algorithmic_flops(w),
+        "clocks": clk.summary(),
+    }
+    if kernel_stats is not None:
+        line["kernels"] = kernel_stats
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, cores, sample = oracle_rate(w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s/layer", "cores": cores,
+                                "kind": "oracle", "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    sess.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,224 @@
+/*
+ * slora.h -- C ABI of libslora.so: a Unified Paging pool of LoRA adapter rows and
+ * the heterogeneous-rank batched LoRA delta over it, on one GB300 (sm_103a).
+ *
+ * What the library computes (for every token t whose adapter is a):
+ *
+ *     y[t] <- y[t] + s_a * (x[t] A_a) B_a
+ *
+ * with A_a (hidden x r_a) and B_a (r_a x hidden) fp16, accumulation in fp32 and one
+ * final rounding of y to fp16.  Sources: S-LoRA: Serving Thousands of Concurrent LoRA
+ * Adapters (explainer), "What this paper explains" (shapes of A and B; the delta is
+ * kept separate from the shared base) and "The mechanism" (one base, the delta x A B
+ * computed on the fly per request's adapter; a host-resident adapter store; Unified
+ * Paging of adapter tiles and KV blocks in one pool with a block table); S-LoRA:
+ * Multiplexing Thousands of Fine-Tuned Adapters on a Single GPU, section 2 (the
+ * per-token loop with a per-adapter scaling) and section 3 (one kernel invocation for a
+ * batch of heterogeneous-rank adapters, gathering hidden states and matching them to
+ * the adapters' pages through the paging table).
+ *
+ * Pool layout.  The pool is one device allocation of `num_pages` fixed-size pages;
+ * a page holds one fp16 row of length `hidden` (hidden * 2 bytes).  An adapter with
+ * rank r occupies 2 * r * n_proj pages: for each projection p, the r rows of A^T
+ * (row j = column j of A) followed by the r rows of B.  Its page table lists those
+ * pages in that order: pt[p][0..r) for A^T, pt[p][r..2r) for B.  Pages are handed out
+ * from one free list shared with the caller's KV blocks (slora_pages_alloc/free), so
+ * adapter pages and KV pages interleave in the pool (Unified Paging: explainer, "The
+ * mechanism" and "What to notice when reading"; S-LoRA: Multiplexing ..., section 2).
+ *
+ * Conventions for every call:
+ *   - Every call returns slora_status; SLORA_OK is 0.  No C++ exception crosses the
+ *     boundary.  slora_last_error() gives a message for the calling thread's most
+ *     recent failure.
+ *   - "host" pointers are ordinary CPU pointers; "device" pointers are CUDA device
+ *     pointers on the pool's device.  The caller owns every buffer it passes; the pool
+ *     owns its device pool, page tables, adapter directory, pinned host store, side
+ *     stream and events.
+ *   - slora_stream_t is a cudaStream_t (NULL = the legacy default stream).  Calls that
+ *     take a stream enqueue work on it and return without waiting, unless noted.
+ *   - One pool is used by one host thread at a time.
+ *   - Device-side checks never trap: a kernel that meets a bad adapter index, a
+ *     non-resident adapter, an out-of-range page or a segment whose tokens disagree on
+ *     their adapter records a code in the pool's device status word and skips that
+ *     work; slora_get_device_status() reads and clears it.
+ */
+#ifndef SLORA_H
+#define SLORA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct slora_pool *slora_pool_t;
+typedef struct slora_pagealloc *slora_pagealloc_t;
+typedef void *slora_stream_t; /* a cudaStream_t */
+
+typedef enum slora_status {
+    SLORA_OK = 0,
+    SLORA_ERR_INVALID_ARG = 1,      /* bad pointer, size, id, rank or projection */
+    SLORA_ERR_POOL_FULL = 2,        /* not enough free pages (nothing was allocated) */
+    SLORA_ERR_NOT_REGISTERED = 3,   /* adapter id not in the host store */
+    SLORA_ERR_NOT_RESIDENT = 4,     /* adapter id not loaded in the pool */
+    SLORA_ERR_ALREADY_RESIDENT = 5, /* single-adapter load of a resident adapter */
+    SLORA_ERR_CUDA = 6,             /* a CUDA runtime call failed (see slora_last_error) */
+    SLORA_ERR_DEVICE_CHECK = 7,     /* a kernel skipped work after a failed check */
+    SLORA_ERR_DEVICE_TIMEOUT = 8,   /* a bounded device wait gave up */
+    SLORA_ERR_HOST_ALLOC = 9,       /* pinned or ordinary host allocation failed */
+    SLORA_ERR_ALREADY_REGISTERED = 10,
+    SLORA_ERR_UNSUPPORTED = 11      /* device is not sm_103 or a size exceeds a kernel limit */
+} slora_status;
+
+/* Device status codes (slora_get_device_status), first error wins. */
+#define SLORA_DEV_OK 0
+#define SLORA_DEV_BAD_ADAPTER 1   /* token adapter index >= max_adapters or < -1 */
+#define SLORA_DEV_NOT_RESIDENT 2  /* token's adapter has no pages in the pool */
+#define SLORA_DEV_BAD_PAGE 3      /* page-table entry outside [0, num_pages) */
+#define SLORA_DEV_BAD_SEGMENT 4   /* segment tokens disagree on their adapter, or bad bounds */
+#define SLORA_DEV_TIMEOUT 5       /* a bounded wait inside a kernel gave up */
+
+const char *slora_status_str(slora_status s);
+/* Message of the calling thread's last failed call ("" if none).  Valid until the
+ * thread's next failing call. */
+const char *slora_last_error(void);
+/* Library version as major * 10000 + minor * 100 + patch. */
+int32_t slora_version(void);
+
+/* ---------------------------------------------------------------------------
+ * Host page allocator.  The free list behind the pool, usable without a GPU.
+ * Pages are int32 indices in [0, num_pages).  shuffle_seed != 0 permutes the free
+ * list once at creation (a seeded Fisher-Yates shuffle driven by splitmix64) so that
+ * consecutive allocations land on scattered pages; 0 keeps ascending order.
+ * alloc() pops n pages or fails with SLORA_ERR_POOL_FULL and allocates nothing.
+ * free() returns pages; a page that is out of range or not allocated fails the whole
+ * call with SLORA_ERR_INVALID_ARG before any page is returned.
+ * ------------------------------------------------------------------------- */
+slora_status slora_pagealloc_create(int64_t num_pages, uint64_t shuffle_seed,
+                                    slora_pagealloc_t *out);
+slora_status slora_pagealloc_destroy(slora_pagealloc_t a);
+slora_status slora_pagealloc_alloc(slora_pagealloc_t a, int64_t n, int32_t *out_pages /*host [n]*/);
+slora_status slora_pagealloc_free(slora_pagealloc_t a, int64_t n, const int32_t *pages /*host [n]*/);
+slora_status slora_pagealloc_num_free(slora_pagealloc_t a, int64_t *out);
+
+/* ---------------------------------------------------------------------------
+ * Pool.
+ *   device        CUDA device ordinal (must be compute capability 10.3)
+ *   hidden        row length; a multiple of 64, 64 <= hidden <= 16384
+ *   num_pages     pool slots, 1 <= num_pages < 2^31; pool bytes = num_pages * hidden * 2
+ *   n_proj        projections per adapter (e.g. layers x {q,k,v,o}); >= 1
+ *   max_adapters  adapter ids are 0 .. max_adapters-1
+ *   shuffle_seed  free-list permutation (see the page allocator)
+ * Allocates the device pool, page-table arena, directory and status word, and a
+ * non-blocking side stream for adapter uploads.  destroy() waits for the pool's own
+ * streams, then frees everything it owns, including the pinned host store.
+ * ------------------------------------------------------------------------- */
+slora_status slora_pool_create(int device, int32_t hidden, int64_t num_pages, int32_t n_proj,
+                               int32_t max_adapters, uint64_t shuffle_seed, slora_pool_t *out);
+slora_status slora_pool_destroy(slora_pool_t pool);
+/* Free slots in the pool (host bookkeeping; no device sync). */
+slora_status slora_pool_num_free(slora_pool_t pool, int64_t *out);
+/* Device address of page 0 (page i starts at base + i * hidden * 2 bytes). */
+slora_status slora_pool_base(slora_pool_t pool, void **out);
+
+/* KV side of the unified allocator.  pages_alloc pops n slots from the same free list
+ * adapters use and writes them to out_pages (host).  pages_free returns KV slots; it
+ * records an event on `stream` after which the slots may be rewritten by adapter
+ * loads, so work already enqueued on `stream` may still read them. */
+slora_status slora_pages_alloc(slora_pool_t pool, int64_t n, int32_t *out_pages);
+slora_status slora_pages_free(slora_pool_t pool, int64_t n, const int32_t *pages,
+                              slora_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Host adapter store (explainer, "The mechanism": all adapters live in host memory and
+ * only those the running batch needs are fetched to the GPU).
+ * register() copies the caller's factors into pinned host memory owned by the pool:
+ *   At_host  fp16 [n_proj][rank][hidden]  rows of A^T (row j = column j of A)
+ *   B_host   fp16 [n_proj][rank][hidden]  rows of B
+ *   rank     1 <= rank <= 1024; scaling is the default s for this adapter
+ * The caller's buffers may be freed when the call returns.
+ * unregister() evicts the adapter first if it is resident (see evict).
+ * ------------------------------------------------------------------------- */
+slora_status slora_adapter_register(slora_pool_t pool, int32_t adapter_id, int32_t rank,
+                                    float scaling, const uint16_t *At_host,
+                                    const uint16_t *B_host);
+slora_status slora_adapter_unregister(slora_pool_t pool, int32_t adapter_id,
+                                      slora_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Load / evict (explainer, "Algorithm / figure walkthrough" steps 2 and 4; "The
+ * mechanism": unused adapters leave GPU memory and stay on the host).
+ *
+ * load() takes 2 * rank * n_proj pages from the free list, writes the adapter's page
+ * table, and on the pool's side stream: copies the pinned store rows to a device
+ * staging buffer (cudaMemcpyAsync), runs the page-scatter kernel (staging row i ->
+ * its page, bit for bit), and publishes the directory entry.  `stream` then waits on
+ * an event recorded after that work, so kernels enqueued later on `stream` see the
+ * adapter; the host call does not wait for the copy.  The side stream first waits for
+ * the most recent page release (evict / pages_free), so slots freed by work still in
+ * flight are not overwritten early.
+ * adapters_load() does the same for a list: ids that are already resident are
+ * skipped; if the missing ones do not all fit, nothing is loaded and
+ * SLORA_ERR_POOL_FULL is returned.
+ * evict() enqueues on `stream` the clearing of the directory entry, returns the
+ * adapter's pages to the free list and records the release event on `stream`.
+ * ------------------------------------------------------------------------- */
+slora_status slora_adapter_load(slora_pool_t pool, int32_t adapter_id, slora_stream_t stream);
+slora_status slora_adapters_load(slora_pool_t pool, int32_t n, const int32_t *adapter_ids /*host*/,
+                                 slora_stream_t stream);
+slora_status slora_adapter_evict(slora_pool_t pool, int32_t adapter_id, slora_stream_t stream);
+slora_status slora_adapter_is_resident(slora_pool_t pool, int32_t adapter_id, int32_t *out);
+
+/* ---------------------------------------------------------------------------
+ * The hot path: y += s * (x A) B for a batch of tokens, each with its own adapter.
+ *
+ *   proj               projection index, 0 <= proj < n_proj
+ *   x                  device fp16 [T][hidden], row-major, 16-byte aligned
+ *   y                  device fp16 [T][hidden], in/out (y0 in, y0 + delta out); may not
+ *                      alias x
+ *   T                  tokens, 0 <= T <= 1 << 20 (T = 0 is a no-op)
+ *   token_adapter_idx  device int32 [T]; adapter id per token, -1 = no adapter (y kept)
+ *   seg_indptr         device int32 [n_seg + 1] or NULL.  Tokens in
+ *                      [seg_indptr[i], seg_indptr[i+1]) form prefill segment i; every
+ *                      token of a segment must carry the same adapter id.  Segments
+ *                      run as dense contractions on the tensor cores (the one place the
+ *                      work is a real GEMM); every other token takes the decode path.
+ *                      The host reads nothing from it.
+ *   n_seg              number of segments (0 if seg_indptr is NULL)
+ *   scaling            device float [max_adapters] overriding the registered scaling,
+ *                      or NULL to use the registered values
+ *   stream             work is enqueued on this stream; nothing waits
+ *
+ * Tokens with a non-resident or out-of-range adapter are skipped (y unchanged) and
+ * set a device status code.  Each token's result does not depend on the other tokens
+ * in the batch, their order, or which pages hold its adapter.
+ * Scratch: the pool keeps device scratch for the token plan, sized on first use and
+ * grown when a larger T arrives (a growth synchronises the pool's device).
+ * ------------------------------------------------------------------------- */
+slora_status slora_lora_apply(slora_pool_t pool, int32_t proj, const void *x, void *y, int32_t T,
+                              const int32_t *token_adapter_idx, const int32_t *seg_indptr,
+                              int32_t n_seg, const float *scaling, slora_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Observability / test hooks.
+ * adapter_pages(): the adapter's page table for projection proj, 2 * rank int32 entries
+ *   (A^T rows then B rows) written to out (host).
+ * adapter_rank(): registered rank.
+ * page_read(): synchronously copies one page (hidden fp16) to host_out.
+ * get_device_status(): synchronises the pool's device, returns the device status word
+ *   (SLORA_DEV_*) and resets it to 0.
+ * ------------------------------------------------------------------------- */
+slora_status slora_adapter_pages(slora_pool_t pool, int32_t adapter_id, int32_t proj,
+                                 int32_t *out);
+slora_status slora_adapter_rank(slora_pool_t pool, int32_t adapter_id, int32_t *out);
+slora_status slora_page_read(slora_pool_t pool, int32_t page, uint16_t *host_out);
+slora_status slora_get_device_status(slora_pool_t pool, int32_t *status);
+/* Number of kernels this pool has launched so far (scatter, directory, plan and delta
+ * kernels), counted on the host at each launch. */
+slora_status slora_pool_launch_count(slora_pool_t pool, int64_t *out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SLORA_H */

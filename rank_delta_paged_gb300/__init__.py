@@ -1,0 +1,254 @@
+"""Python binding of libslora.so: the paged heterogeneous-rank LoRA delta on GB300.
+
+Every function here has the name of the C entry point it calls (see ``include/slora.h``)
+and only marshals arguments: device pointers, host pointers and sizes go through
+``ctypes``; torch tensors and numpy arrays are accepted wherever the C call takes a
+pointer and are passed as their data pointer.  No step of the hot path runs in Python
+and there is no fallback: if ``libslora.so`` is missing, every call raises.
+
+Build the library with ``rank_delta_paged_gb300.build.build()`` (nvcc, sm_103a).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+from . import build as _build
+
+__all__ = [
+    "SloraError", "lib", "library_path",
+    "slora_status_str", "slora_last_error", "slora_version",
+    "slora_pagealloc_create", "slora_pagealloc_destroy", "slora_pagealloc_alloc",
+    "slora_pagealloc_free", "slora_pagealloc_num_free",
+    "slora_pool_create", "slora_pool_destroy", "slora_pool_num_free", "slora_pool_base",
+    "slora_pages_alloc", "slora_pages_free",
+    "slora_adapter_register", "slora_adapter_unregister",
+    "slora_adapter_load", "slora_adapters_load", "slora_adapter_evict", "slora_adapter_is_resident",
+    "slora_lora_apply",
+    "slora_adapter_pages", "slora_adapter_rank", "slora_page_read", "slora_get_device_status",
+    "slora_pool_launch_count",
+]
+
+_I32, _I64, _U64, _F32, _P = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float, ctypes.c_void_p
+_PP = ctypes.POINTER(ctypes.c_void_p)
+
+# name -> argtypes (every function returns slora_status unless listed in _RESTYPE)
+_SIGS = {
+    "slora_status_str": [ctypes.c_int],
+    "slora_last_error": [],
+    "slora_version": [],
+    "slora_pagealloc_create": [_I64, _U64, _PP],
+    "slora_pagealloc_destroy": [_P],
+    "slora_pagealloc_alloc": [_P, _I64, _P],
+    "slora_pagealloc_free": [_P, _I64, _P],
+    "slora_pagealloc_num_free": [_P, _P],
+    "slora_pool_create": [ctypes.c_int, _I32, _I64, _I32, _I32, _U64, _PP],
+    "slora_pool_destroy": [_P],
+    "slora_pool_num_free": [_P, _P],
+    "slora_pool_base": [_P, _PP],
+    "slora_pages_alloc": [_P, _I64, _P],
+    "slora_pages_free": [_P, _I64, _P, _P],
+    "slora_adapter_register": [_P, _I32, _I32, _F32, _P, _P],
+    "slora_adapter_unregister": [_P, _I32, _P],
+    "slora_adapter_load": [_P, _I32, _P],
+    "slora_adapters_load": [_P, _I32, _P, _P],
+    "slora_adapter_evict": [_P, _I32, _P],
+    "slora_adapter_is_resident": [_P, _I32, _P],
+    "slora_lora_apply": [_P, _I32, _P, _P, _I32, _P, _P, _I32, _P, _P],
+    "slora_adapter_pages": [_P, _I32, _I32, _P],
+    "slora_adapter_rank": [_P, _I32, _P],
+    "slora_page_read": [_P, _I32, _P],
+    "slora_get_device_status": [_P, _P],
+    "slora_pool_launch_count": [_P, _P],
+}
+_RESTYPE = {"slora_status_str": ctypes.c_char_p, "slora_last_error": ctypes.c_char_p,
+            "slora_version": _I32}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SloraError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn} -> {msg}")
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libslora.so (raises if it was not built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(f"libslora.so is not built ({path}); run "
+                                   "rank_delta_paged_gb300.build.build() first")
+            L = ctypes.CDLL(path)
+            for name, args in _SIGS.items():
+                fn = getattr(L, name)
+                fn.argtypes = args
+                fn.restype = _RESTYPE.get(name, ctypes.c_int)
+            _lib = L
+    return _lib
+
+
+def _ptr(a) -> Optional[int]:
+    """Data pointer of a torch tensor / numpy array / int / None."""
+    if a is None:
+        return None
+    if isinstance(a, int):
+        return a
+    if hasattr(a, "data_ptr"):
+        return int(a.data_ptr())
+    if hasattr(a, "ctypes"):
+        return int(a.ctypes.data)
+    raise TypeError(f"cannot take a pointer of {type(a)}")
+
+
+def _stream(s) -> Optional[int]:
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s
+    return int(s.cuda_stream)  # torch.cuda.Stream
+
+
+def _call(name: str, *args) -> None:
+    st = getattr(lib(), name)(*args)
+    if st != 0:
+        raise SloraError(name, st, slora_last_error())
+
+
+def slora_status_str(s: int) -> str:
+    return lib().slora_status_str(int(s)).decode()
+
+
+def slora_last_error() -> str:
+    return lib().slora_last_error().decode()
+
+
+def slora_version() -> int:
+    return int(lib().slora_version())
+
+
+# ---- host page allocator --------------------------------------------------------
+def slora_pagealloc_create(num_pages: int, shuffle_seed: int = 0) -> int:
+    h = ctypes.c_void_p()
+    _call("slora_pagealloc_create", num_pages, shuffle_seed, ctypes.byref(h))
+    return h.value
+
+
+def slora_pagealloc_destroy(a: int) -> None:
+    _call("slora_pagealloc_destroy", a)
+
+
+def slora_pagealloc_alloc(a: int, n: int, out_pages) -> None:
+    _call("slora_pagealloc_alloc", a, n, _ptr(out_pages))
+
+
+def slora_pagealloc_free(a: int, n: int, pages) -> None:
+    _call("slora_pagealloc_free", a, n, _ptr(pages))
+
+
+def slora_pagealloc_num_free(a: int) -> int:
+    v = ctypes.c_int64()
+    _call("slora_pagealloc_num_free", a, ctypes.byref(v))
+    return v.value
+
+
+# ---- pool -------------------------------------------------------------------------
+def slora_pool_create(device: int, hidden: int, num_pages: int, n_proj: int, max_adapters: int,
+                      shuffle_seed: int = 0) -> int:
+    h = ctypes.c_void_p()
+    _call("slora_pool_create", device, hidden, num_pages, n_proj, max_adapters, shuffle_seed,
+          ctypes.byref(h))
+    return h.value
+
+
+def slora_pool_destroy(pool: int) -> None:
+    _call("slora_pool_destroy", pool)
+
+
+def slora_pool_num_free(pool: int) -> int:
+    v = ctypes.c_int64()
+    _call("slora_pool_num_free", pool, ctypes.byref(v))
+    return v.value
+
+
+def slora_pool_base(pool: int) -> int:
+    v = ctypes.c_void_p()
+    _call("slora_pool_base", pool, ctypes.byref(v))
+    return v.value
+
+
+def slora_pages_alloc(pool: int, n: int, out_pages) -> None:
+    _call("slora_pages_alloc", pool, n, _ptr(out_pages))
+
+
+def slora_pages_free(pool: int, n: int, pages, stream=None) -> None:
+    _call("slora_pages_free", pool, n, _ptr(pages), _stream(stream))
+
+
+def slora_adapter_register(pool: int, adapter_id: int, rank: int, scaling: float, At_host,
+                           B_host) -> None:
+    _call("slora_adapter_register", pool, adapter_id, rank, scaling, _ptr(At_host), _ptr(B_host))
+
+
+def slora_adapter_unregister(pool: int, adapter_id: int, stream=None) -> None:
+    _call("slora_adapter_unregister", pool, adapter_id, _stream(stream))
+
+
+def slora_adapter_load(pool: int, adapter_id: int, stream=None) -> None:
+    _call("slora_adapter_load", pool, adapter_id, _stream(stream))
+
+
+def slora_adapters_load(pool: int, n: int, adapter_ids, stream=None) -> None:
+    _call("slora_adapters_load", pool, n, _ptr(adapter_ids), _stream(stream))
+
+
+def slora_adapter_evict(pool: int, adapter_id: int, stream=None) -> None:
+    _call("slora_adapter_evict", pool, adapter_id, _stream(stream))
+
+
+def slora_adapter_is_resident(pool: int, adapter_id: int) -> bool:
+    v = ctypes.c_int32()
+    _call("slora_adapter_is_resident", pool, adapter_id, ctypes.byref(v))
+    return bool(v.value)
+
+
+def slora_lora_apply(pool: int, proj: int, x, y, T: int, token_adapter_idx, seg_indptr=None,
+                     n_seg: int = 0, scaling=None, stream=None) -> None:
+    _call("slora_lora_apply", pool, proj, _ptr(x), _ptr(y), T, _ptr(token_adapter_idx),
+          _ptr(seg_indptr), n_seg, _ptr(scaling), _stream(stream))
+
+
+def slora_adapter_pages(pool: int, adapter_id: int, proj: int, out) -> None:
+    _call("slora_adapter_pages", pool, adapter_id, proj, _ptr(out))
+
+
+def slora_adapter_rank(pool: int, adapter_id: int) -> int:
+    v = ctypes.c_int32()
+    _call("slora_adapter_rank", pool, adapter_id, ctypes.byref(v))
+    return v.value
+
+
+def slora_page_read(pool: int, page: int, host_out) -> None:
+    _call("slora_page_read", pool, page, _ptr(host_out))
+
+
+def slora_get_device_status(pool: int) -> int:
+    v = ctypes.c_int32()
+    _call("slora_get_device_status", pool, ctypes.byref(v))
+    return v.value
+
+
+def slora_pool_launch_count(pool: int) -> int:
+    v = ctypes.c_int64()
+    _call("slora_pool_launch_count", pool, ctypes.byref(v))
+    return v.value

@@ -1,0 +1,83 @@
+// Internal declarations shared by the host code and the kernels of libslora.so.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "slora.h"
+
+namespace slora {
+
+// One adapter's directory entry on the device, indexed by adapter id.
+// pt_off < 0 means "not resident".  The page table of projection p starts at
+// pt_arena[pt_off + p * 2 * rank]: rank A^T pages, then rank B pages.
+struct alignas(16) DirEntry {
+    int32_t rank;
+    float scaling;
+    int64_t pt_off;
+};
+static_assert(sizeof(DirEntry) == 16, "DirEntry layout");
+
+// A run of consecutive staging rows that land on consecutive page-table entries.
+struct ScatterRun {
+    int64_t staging_row0;   // first row in the staging buffer
+    int64_t pt_index0;      // first page-table arena entry
+    int64_t nrows;
+};
+
+// Directory update carried as a kernel argument.
+struct DirUpdate {
+    int32_t adapter_id;
+    int32_t rank;
+    float scaling;
+    int32_t pad;
+    int64_t pt_off;
+};
+
+constexpr int kMaxRunsPerLaunch = 512;     // 512 * 24 B fits the 32 KiB parameter space
+constexpr int kMaxDirUpdatesPerLaunch = 512;
+
+struct ScatterArgs {
+    int32_t n_runs;
+    ScatterRun runs[kMaxRunsPerLaunch];
+};
+struct DirArgs {
+    int32_t n;
+    DirUpdate upd[kMaxDirUpdatesPerLaunch];
+};
+
+// Kernel launchers (scatter.cu).
+cudaError_t launch_scatter(const uint16_t *staging, const int32_t *pt_arena, uint16_t *pool,
+                           int64_t num_pages, int32_t hidden, const ScatterArgs &args,
+                           int32_t *status, cudaStream_t stream);
+cudaError_t launch_dir_update(DirEntry *dir, const DirArgs &args, cudaStream_t stream);
+
+// Everything the hot-path kernels read about the pool.
+struct PoolView {
+    const uint16_t *pool;      // [num_pages][hidden] fp16
+    const int32_t *pt_arena;
+    const DirEntry *dir;
+    int64_t num_pages;
+    int32_t hidden;
+    int32_t n_proj;
+    int32_t max_adapters;
+    int32_t *status;           // device status word
+};
+
+// Device scratch of the token plan (decode.cu), owned by the pool.
+struct PlanScratch {
+    void *base = nullptr;
+    size_t bytes = 0;
+    int32_t cap_tokens = 0;
+};
+size_t plan_scratch_bytes(int32_t T, int32_t max_adapters);
+
+// The hot path (decode.cu / prefill.cu).
+cudaError_t launch_lora_apply(const PoolView &pv, int32_t proj, const uint16_t *x, uint16_t *y,
+                              int32_t T, const int32_t *idx, const int32_t *seg_indptr,
+                              int32_t n_seg, const float *scaling, const PlanScratch &scratch,
+                              int num_sms, cudaStream_t stream, int *launches);
+
+}  // namespace slora

@@ -1,0 +1,591 @@
+// The Unified Paging pool, the pinned host adapter store, adapter load / evict and the
+// host side of the hot path (S-LoRA: Serving Thousands of Concurrent LoRA Adapters
+// (explainer), "The mechanism" and "Algorithm / figure walkthrough"; S-LoRA:
+// Multiplexing Thousands of Fine-Tuned Adapters on a Single GPU, section 2).
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <unordered_set>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "host_common.h"
+#include "internal.h"
+#include "slora.h"
+
+using namespace slora;
+
+namespace {
+
+struct AdapterRec {
+    bool registered = false;
+    bool resident = false;
+    int32_t rank = 0;
+    float scaling = 0.f;
+    uint16_t *store = nullptr;     // pinned [n_proj][2*rank][hidden]: A^T rows then B rows
+    int32_t *pt_host = nullptr;    // pinned [n_proj][2*rank] page table
+    cudaEvent_t pt_event = nullptr;  // recorded after the last copy out of pt_host
+    bool pt_event_pending = false;
+    int64_t pt_off = -1;           // arena offset while resident
+};
+
+}  // namespace
+
+struct slora_pool {
+    int device = 0;
+    int32_t hidden = 0;
+    int64_t num_pages = 0;
+    int32_t n_proj = 0;
+    int32_t max_adapters = 0;
+    int num_sms = 0;
+
+    PageAlloc pages;
+    RangeAlloc arena;
+    int64_t arena_cap = 0;
+
+    uint16_t *pool_dev = nullptr;
+    int32_t *pt_dev = nullptr;
+    DirEntry *dir_dev = nullptr;
+    int32_t *status_dev = nullptr;
+
+    cudaStream_t side = nullptr;
+    cudaEvent_t release_event = nullptr;
+    bool release_pending = false;
+    cudaEvent_t load_event = nullptr;
+
+    uint16_t *staging = nullptr;
+    int64_t staging_rows = 0;
+
+    PlanScratch plan;
+    std::vector<AdapterRec> adapters;
+    int64_t launches = 0;  // kernels launched by this pool
+};
+
+namespace {
+
+#define CUDA_TRY(expr)                                                                    \
+    do {                                                                                  \
+        cudaError_t _e = (expr);                                                          \
+        if (_e != cudaSuccess)                                                            \
+            return fail(SLORA_ERR_CUDA, "%s failed: %s (%s:%d)", #expr, cudaGetErrorString(_e), \
+                        __FILE__, __LINE__);                                              \
+    } while (0)
+
+slora_status set_device(slora_pool *p)
+{
+    CUDA_TRY(cudaSetDevice(p->device));
+    return SLORA_OK;
+}
+
+bool valid_id(const slora_pool *p, int32_t id) { return id >= 0 && id < p->max_adapters; }
+
+int64_t adapter_rows(const slora_pool *p, const AdapterRec &a)
+{
+    return 2ll * a.rank * p->n_proj;
+}
+
+void free_pool_memory(slora_pool *p)
+{
+    if (p->side)
+        cudaStreamSynchronize(p->side);
+    cudaDeviceSynchronize();
+    for (auto &a : p->adapters) {
+        if (a.store) cudaFreeHost(a.store);
+        if (a.pt_host) cudaFreeHost(a.pt_host);
+        if (a.pt_event) cudaEventDestroy(a.pt_event);
+        a = AdapterRec();
+    }
+    if (p->pool_dev) cudaFree(p->pool_dev);
+    if (p->pt_dev) cudaFree(p->pt_dev);
+    if (p->dir_dev) cudaFree(p->dir_dev);
+    if (p->status_dev) cudaFree(p->status_dev);
+    if (p->staging) cudaFree(p->staging);
+    if (p->plan.base) cudaFree(p->plan.base);
+    if (p->release_event) cudaEventDestroy(p->release_event);
+    if (p->load_event) cudaEventDestroy(p->load_event);
+    if (p->side) cudaStreamDestroy(p->side);
+}
+
+// Staging rows: enough for the largest registered adapter, at least 64 MiB, at most
+// 512 MiB (loads larger than that are split into several copy + scatter rounds).
+slora_status ensure_staging(slora_pool *p, int64_t want_rows)
+{
+    const int64_t row_bytes = 2ll * p->hidden;
+    int64_t lo = (64ll << 20) / row_bytes, hi = (512ll << 20) / row_bytes;
+    int64_t rows = std::max<int64_t>(lo, std::min<int64_t>(hi, want_rows));
+    if (p->staging && p->staging_rows >= rows)
+        return SLORA_OK;
+    if (p->staging) {
+        CUDA_TRY(cudaStreamSynchronize(p->side));
+        cudaFree(p->staging);
+        p->staging = nullptr;
+        p->staging_rows = 0;
+    }
+    CUDA_TRY(cudaMalloc(&p->staging, (size_t)(rows * row_bytes)));
+    p->staging_rows = rows;
+    return SLORA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+slora_status slora_pool_create(int device, int32_t hidden, int64_t num_pages, int32_t n_proj,
+                               int32_t max_adapters, uint64_t shuffle_seed, slora_pool_t *out)
+{
+    if (!out)
+        return fail(SLORA_ERR_INVALID_ARG, "pool_create: out is NULL");
+    *out = nullptr;
+    if (hidden < 64 || hidden > 16384 || hidden % 64 != 0)
+        return fail(SLORA_ERR_INVALID_ARG, "pool_create: hidden=%d (multiple of 64 in [64, 16384])", hidden);
+    if (num_pages < 1 || num_pages >= (int64_t)INT32_MAX)
+        return fail(SLORA_ERR_INVALID_ARG, "pool_create: num_pages=%lld", (long long)num_pages);
+    if (n_proj < 1 || max_adapters < 1 || max_adapters > (1 << 24))
+        return fail(SLORA_ERR_INVALID_ARG, "pool_create: n_proj=%d max_adapters=%d", n_proj, max_adapters);
+    int ndev = 0;
+    CUDA_TRY(cudaGetDeviceCount(&ndev));
+    if (device < 0 || device >= ndev)
+        return fail(SLORA_ERR_INVALID_ARG, "pool_create: device %d of %d", device, ndev);
+    cudaDeviceProp prop;
+    CUDA_TRY(cudaGetDeviceProperties(&prop, device));
+    if (!(prop.major == 10 && prop.minor == 3))
+        return fail(SLORA_ERR_UNSUPPORTED, "pool_create: device %d is sm_%d%d; this library is built for sm_103a",
+                    device, prop.major, prop.minor);
+
+    auto *p = new (std::nothrow) slora_pool;
+    if (!p)
+        return fail(SLORA_ERR_HOST_ALLOC, "pool_create");
+    p->device = device;
+    p->hidden = hidden;
+    p->num_pages = num_pages;
+    p->n_proj = n_proj;
+    p->max_adapters = max_adapters;
+    p->num_sms = prop.multiProcessorCount;
+    slora_status st = SLORA_OK;
+    try {
+        p->pages.init(num_pages, shuffle_seed);
+        p->adapters.resize((size_t)max_adapters);
+    } catch (...) {
+        delete p;
+        return fail(SLORA_ERR_HOST_ALLOC, "pool_create: host bookkeeping for %lld pages", (long long)num_pages);
+    }
+    // Each page belongs to at most one adapter, so num_pages arena entries always
+    // suffice in total; twice that leaves room for fragmentation.
+    p->arena_cap = 2 * num_pages;
+    p->arena.init(p->arena_cap);
+
+    auto cuda_fail = [&](cudaError_t e, const char *what) {
+        st = fail(SLORA_ERR_CUDA, "pool_create: %s: %s", what, cudaGetErrorString(e));
+    };
+    cudaError_t e;
+    if ((e = cudaSetDevice(device)) != cudaSuccess) cuda_fail(e, "cudaSetDevice");
+    else if ((e = cudaMalloc(&p->pool_dev, (size_t)num_pages * (size_t)hidden * 2)) != cudaSuccess) cuda_fail(e, "pool");
+    else if ((e = cudaMalloc(&p->pt_dev, (size_t)p->arena_cap * 4)) != cudaSuccess) cuda_fail(e, "page-table arena");
+    else if ((e = cudaMalloc(&p->dir_dev, (size_t)max_adapters * sizeof(DirEntry))) != cudaSuccess) cuda_fail(e, "directory");
+    else if ((e = cudaMalloc(&p->status_dev, 4)) != cudaSuccess) cuda_fail(e, "status");
+    else if ((e = cudaStreamCreateWithFlags(&p->side, cudaStreamNonBlocking)) != cudaSuccess) cuda_fail(e, "side stream");
+    else if ((e = cudaEventCreateWithFlags(&p->release_event, cudaEventDisableTiming)) != cudaSuccess) cuda_fail(e, "event");
+    else if ((e = cudaEventCreateWithFlags(&p->load_event, cudaEventDisableTiming)) != cudaSuccess) cuda_fail(e, "event");
+    else if ((e = cudaMemset(p->status_dev, 0, 4)) != cudaSuccess) cuda_fail(e, "memset");
+    else if ((e = cudaMemset(p->dir_dev, 0xff, (size_t)max_adapters * sizeof(DirEntry))) != cudaSuccess) cuda_fail(e, "memset");
+    else if ((e = cudaDeviceSynchronize()) != cudaSuccess) cuda_fail(e, "sync");
+    if (st != SLORA_OK) {
+        free_pool_memory(p);
+        delete p;
+        return st;
+    }
+    *out = p;
+    return SLORA_OK;
+}
+
+slora_status slora_pool_destroy(slora_pool_t p)
+{
+    if (!p)
+        return SLORA_OK;
+    cudaSetDevice(p->device);
+    free_pool_memory(p);
+    delete p;
+    return SLORA_OK;
+}
+
+slora_status slora_pool_num_free(slora_pool_t p, int64_t *out)
+{
+    if (!p || !out)
+        return fail(SLORA_ERR_INVALID_ARG, "pool_num_free");
+    *out = p->pages.num_free();
+    return SLORA_OK;
+}
+
+slora_status slora_pool_base(slora_pool_t p, void **out)
+{
+    if (!p || !out)
+        return fail(SLORA_ERR_INVALID_ARG, "pool_base");
+    *out = p->pool_dev;
+    return SLORA_OK;
+}
+
+slora_status slora_pages_alloc(slora_pool_t p, int64_t n, int32_t *out_pages)
+{
+    if (!p)
+        return fail(SLORA_ERR_INVALID_ARG, "pages_alloc: null pool");
+    return p->pages.alloc(n, out_pages);
+}
+
+slora_status slora_pages_free(slora_pool_t p, int64_t n, const int32_t *pages, slora_stream_t stream)
+{
+    if (!p)
+        return fail(SLORA_ERR_INVALID_ARG, "pages_free: null pool");
+    slora_status st = p->pages.release(n, pages);
+    if (st != SLORA_OK)
+        return st;
+    if ((st = set_device(p)) != SLORA_OK)
+        return st;
+    CUDA_TRY(cudaEventRecord(p->release_event, (cudaStream_t)stream));
+    p->release_pending = true;
+    return SLORA_OK;
+}
+
+slora_status slora_adapter_register(slora_pool_t p, int32_t id, int32_t rank, float scaling,
+                                    const uint16_t *At_host, const uint16_t *B_host)
+{
+    if (!p || !valid_id(p, id) || rank < 1 || rank > 1024 || !At_host || !B_host)
+        return fail(SLORA_ERR_INVALID_ARG, "adapter_register: id=%d rank=%d", id, rank);
+    AdapterRec &a = p->adapters[(size_t)id];
+    if (a.registered)
+        return fail(SLORA_ERR_ALREADY_REGISTERED, "adapter_register: id=%d", id);
+    slora_status st = set_device(p);
+    if (st != SLORA_OK)
+        return st;
+    const size_t row = (size_t)p->hidden;
+    const size_t rows = 2ull * (size_t)rank * (size_t)p->n_proj;
+    AdapterRec n;
+    n.rank = rank;
+    n.scaling = scaling;
+    if (cudaHostAlloc((void **)&n.store, rows * row * 2, cudaHostAllocDefault) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(SLORA_ERR_HOST_ALLOC, "adapter_register: %zu pinned bytes", rows * row * 2);
+    }
+    if (cudaHostAlloc((void **)&n.pt_host, rows * 4, cudaHostAllocDefault) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFreeHost(n.store);
+        return fail(SLORA_ERR_HOST_ALLOC, "adapter_register: page table");
+    }
+    if (cudaEventCreateWithFlags(&n.pt_event, cudaEventDisableTiming) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFreeHost(n.store);
+        cudaFreeHost(n.pt_host);
+        return fail(SLORA_ERR_CUDA, "adapter_register: event");
+    }
+    // store layout per projection: A^T rows 0..r-1 then B rows 0..r-1, the page-table order
+    for (int32_t pr = 0; pr < p->n_proj; ++pr) {
+        uint16_t *dst = n.store + (size_t)pr * 2 * rank * row;
+        memcpy(dst, At_host + (size_t)pr * rank * row, (size_t)rank * row * 2);
+        memcpy(dst + (size_t)rank * row, B_host + (size_t)pr * rank * row, (size_t)rank * row * 2);
+    }
+    n.registered = true;
+    a = n;
+    return SLORA_OK;
+}
+
+slora_status slora_adapter_evict(slora_pool_t p, int32_t id, slora_stream_t stream);
+
+slora_status slora_adapter_unregister(slora_pool_t p, int32_t id, slora_stream_t stream)
+{
+    if (!p || !valid_id(p, id))
+        return fail(SLORA_ERR_INVALID_ARG, "adapter_unregister: id=%d", id);
+    AdapterRec &a = p->adapters[(size_t)id];
+    if (!a.registered)
+        return fail(SLORA_ERR_NOT_REGISTERED, "adapter_unregister: id=%d", id);
+    if (a.resident) {
+        slora_status st = slora_adapter_evict(p, id, stream);
+        if (st != SLORA_OK)
+            return st;
+    }
+    slora_status st = set_device(p);
+    if (st != SLORA_OK)
+        return st;
+    // the side stream may still copy out of the store
+    CUDA_TRY(cudaStreamSynchronize(p->side));
+    cudaFreeHost(a.store);
+    cudaFreeHost(a.pt_host);
+    cudaEventDestroy(a.pt_event);
+    a = AdapterRec();
+    return SLORA_OK;
+}
+
+slora_status slora_adapters_load(slora_pool_t p, int32_t n, const int32_t *ids, slora_stream_t stream)
+{
+    if (!p || n < 0 || (n > 0 && !ids))
+        return fail(SLORA_ERR_INVALID_ARG, "adapters_load: n=%d", n);
+    std::vector<int32_t> todo;
+    std::unordered_set<int32_t> seen;
+    int64_t need_pages = 0, max_rows = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        int32_t id = ids[i];
+        if (!valid_id(p, id))
+            return fail(SLORA_ERR_INVALID_ARG, "adapters_load: id=%d", id);
+        const AdapterRec &a = p->adapters[(size_t)id];
+        if (!a.registered)
+            return fail(SLORA_ERR_NOT_REGISTERED, "adapters_load: id=%d", id);
+        if (a.resident || !seen.insert(id).second)
+            continue;
+        todo.push_back(id);
+        need_pages += adapter_rows(p, a);
+        max_rows = std::max(max_rows, adapter_rows(p, a));
+    }
+    if (todo.empty())
+        return SLORA_OK;
+    if (need_pages > p->pages.num_free())
+        return fail(SLORA_ERR_POOL_FULL, "adapters_load: %lld pages needed, %lld free",
+                    (long long)need_pages, (long long)p->pages.num_free());
+    slora_status st = set_device(p);
+    if (st != SLORA_OK)
+        return st;
+    if ((st = ensure_staging(p, max_rows)) != SLORA_OK)
+        return st;
+
+    // Host bookkeeping first (pages + arena), with rollback if the arena is too fragmented.
+    std::vector<int32_t> done;
+    for (int32_t id : todo) {
+        AdapterRec &a = p->adapters[(size_t)id];
+        int64_t rows = adapter_rows(p, a);
+        int64_t off = p->arena.alloc(rows);
+        if (off < 0) {
+            for (int32_t d : done) {
+                AdapterRec &b = p->adapters[(size_t)d];
+                p->pages.release(adapter_rows(p, b), b.pt_host);
+                p->arena.release(b.pt_off, adapter_rows(p, b));
+                b.pt_off = -1;
+            }
+            return fail(SLORA_ERR_POOL_FULL, "adapters_load: page-table arena fragmented");
+        }
+        if (a.pt_event_pending) {  // a previous load may still be copying out of pt_host
+            CUDA_TRY(cudaEventSynchronize(a.pt_event));
+            a.pt_event_pending = false;
+        }
+        p->pages.alloc(rows, a.pt_host);  // cannot fail: counted above
+        a.pt_off = off;
+        done.push_back(id);
+    }
+
+    cudaStream_t side = p->side;
+    if (p->release_pending)
+        CUDA_TRY(cudaStreamWaitEvent(side, p->release_event, 0));
+    const int64_t row_elems = p->hidden;
+    ScatterArgs sargs;
+    sargs.n_runs = 0;
+    int64_t cursor = 0;  // staging rows filled in this round
+    auto flush = [&]() -> slora_status {
+        if (sargs.n_runs == 0)
+            return SLORA_OK;
+        CUDA_TRY(launch_scatter(p->staging, p->pt_dev, p->pool_dev, p->num_pages, p->hidden, sargs,
+                                p->status_dev, side));
+        p->launches += 1;
+        sargs.n_runs = 0;
+        cursor = 0;
+        return SLORA_OK;
+    };
+    for (int32_t id : todo) {
+        AdapterRec &a = p->adapters[(size_t)id];
+        int64_t rows = adapter_rows(p, a);
+        CUDA_TRY(cudaMemcpyAsync(p->pt_dev + a.pt_off, a.pt_host, (size_t)rows * 4,
+                                 cudaMemcpyHostToDevice, side));
+        CUDA_TRY(cudaEventRecord(a.pt_event, side));
+        a.pt_event_pending = true;
+        int64_t r0 = 0;
+        while (r0 < rows) {
+            if (cursor == p->staging_rows || sargs.n_runs == kMaxRunsPerLaunch) {
+                if ((st = flush()) != SLORA_OK)
+                    return st;
+            }
+            int64_t take = std::min(rows - r0, p->staging_rows - cursor);
+            CUDA_TRY(cudaMemcpyAsync(p->staging + cursor * row_elems, a.store + r0 * row_elems,
+                                     (size_t)(take * row_elems * 2), cudaMemcpyHostToDevice, side));
+            ScatterRun &run = sargs.runs[sargs.n_runs++];
+            run.staging_row0 = cursor;
+            run.pt_index0 = a.pt_off + r0;
+            run.nrows = take;
+            cursor += take;
+            r0 += take;
+        }
+    }
+    if ((st = flush()) != SLORA_OK)
+        return st;
+    DirArgs dargs;
+    dargs.n = 0;
+    for (size_t i = 0; i < todo.size(); ++i) {
+        AdapterRec &a = p->adapters[(size_t)todo[i]];
+        DirUpdate &u = dargs.upd[dargs.n++];
+        u.adapter_id = todo[i];
+        u.rank = a.rank;
+        u.scaling = a.scaling;
+        u.pad = 0;
+        u.pt_off = a.pt_off;
+        if (dargs.n == kMaxDirUpdatesPerLaunch || i + 1 == todo.size()) {
+            CUDA_TRY(launch_dir_update(p->dir_dev, dargs, side));
+            p->launches += 1;
+            dargs.n = 0;
+        }
+    }
+    CUDA_TRY(cudaEventRecord(p->load_event, side));
+    CUDA_TRY(cudaStreamWaitEvent((cudaStream_t)stream, p->load_event, 0));
+    for (int32_t id : todo)
+        p->adapters[(size_t)id].resident = true;
+    return SLORA_OK;
+}
+
+slora_status slora_adapter_load(slora_pool_t p, int32_t id, slora_stream_t stream)
+{
+    if (!p || !valid_id(p, id))
+        return fail(SLORA_ERR_INVALID_ARG, "adapter_load: id=%d", id);
+    const AdapterRec &a = p->adapters[(size_t)id];
+    if (!a.registered)
+        return fail(SLORA_ERR_NOT_REGISTERED, "adapter_load: id=%d", id);
+    if (a.resident)
+        return fail(SLORA_ERR_ALREADY_RESIDENT, "adapter_load: id=%d", id);
+    return slora_adapters_load(p, 1, &id, stream);
+}
+
+slora_status slora_adapter_evict(slora_pool_t p, int32_t id, slora_stream_t stream)
+{
+    if (!p || !valid_id(p, id))
+        return fail(SLORA_ERR_INVALID_ARG, "adapter_evict: id=%d", id);
+    AdapterRec &a = p->adapters[(size_t)id];
+    if (!a.registered)
+        return fail(SLORA_ERR_NOT_REGISTERED, "adapter_evict: id=%d", id);
+    if (!a.resident)
+        return fail(SLORA_ERR_NOT_RESIDENT, "adapter_evict: id=%d", id);
+    slora_status st = set_device(p);
+    if (st != SLORA_OK)
+        return st;
+    DirArgs dargs;
+    dargs.n = 1;
+    dargs.upd[0] = DirUpdate{id, a.rank, a.scaling, 0, -1};
+    CUDA_TRY(launch_dir_update(p->dir_dev, dargs, (cudaStream_t)stream));
+    p->launches += 1;
+    int64_t rows = adapter_rows(p, a);
+    // pt_host still holds the pages handed out at load time
+    if ((st = p->pages.release(rows, a.pt_host)) != SLORA_OK)
+        return st;
+    p->arena.release(a.pt_off, rows);
+    a.pt_off = -1;
+    a.resident = false;
+    CUDA_TRY(cudaEventRecord(p->release_event, (cudaStream_t)stream));
+    p->release_pending = true;
+    return SLORA_OK;
+}
+
+slora_status slora_adapter_is_resident(slora_pool_t p, int32_t id, int32_t *out)
+{
+    if (!p || !valid_id(p, id) || !out)
+        return fail(SLORA_ERR_INVALID_ARG, "adapter_is_resident: id=%d", id);
+    *out = p->adapters[(size_t)id].resident ? 1 : 0;
+    return SLORA_OK;
+}
+
+slora_status slora_adapter_rank(slora_pool_t p, int32_t id, int32_t *out)
+{
+    if (!p || !valid_id(p, id) || !out)
+        return fail(SLORA_ERR_INVALID_ARG, "adapter_rank: id=%d", id);
+    const AdapterRec &a = p->adapters[(size_t)id];
+    if (!a.registered)
+        return fail(SLORA_ERR_NOT_REGISTERED, "adapter_rank: id=%d", id);
+    *out = a.rank;
+    return SLORA_OK;
+}
+
+slora_status slora_adapter_pages(slora_pool_t p, int32_t id, int32_t proj, int32_t *out)
+{
+    if (!p || !valid_id(p, id) || !out || proj < 0 || proj >= (p ? p->n_proj : 0))
+        return fail(SLORA_ERR_INVALID_ARG, "adapter_pages: id=%d proj=%d", id, proj);
+    const AdapterRec &a = p->adapters[(size_t)id];
+    if (!a.registered)
+        return fail(SLORA_ERR_NOT_REGISTERED, "adapter_pages: id=%d", id);
+    if (!a.resident)
+        return fail(SLORA_ERR_NOT_RESIDENT, "adapter_pages: id=%d", id);
+    memcpy(out, a.pt_host + (size_t)proj * 2 * a.rank, (size_t)2 * a.rank * 4);
+    return SLORA_OK;
+}
+
+slora_status slora_page_read(slora_pool_t p, int32_t page, uint16_t *host_out)
+{
+    if (!p || page < 0 || page >= p->num_pages || !host_out)
+        return fail(SLORA_ERR_INVALID_ARG, "page_read: page=%d", page);
+    slora_status st = set_device(p);
+    if (st != SLORA_OK)
+        return st;
+    CUDA_TRY(cudaDeviceSynchronize());
+    CUDA_TRY(cudaMemcpy(host_out, p->pool_dev + (size_t)page * p->hidden, (size_t)p->hidden * 2,
+                        cudaMemcpyDeviceToHost));
+    return SLORA_OK;
+}
+
+slora_status slora_get_device_status(slora_pool_t p, int32_t *status)
+{
+    if (!p || !status)
+        return fail(SLORA_ERR_INVALID_ARG, "get_device_status");
+    slora_status st = set_device(p);
+    if (st != SLORA_OK)
+        return st;
+    CUDA_TRY(cudaDeviceSynchronize());
+    CUDA_TRY(cudaMemcpy(status, p->status_dev, 4, cudaMemcpyDeviceToHost));
+    CUDA_TRY(cudaMemset(p->status_dev, 0, 4));
+    CUDA_TRY(cudaDeviceSynchronize());
+    return SLORA_OK;
+}
+
+slora_status slora_lora_apply(slora_pool_t p, int32_t proj, const void *x, void *y, int32_t T,
+                              const int32_t *idx, const int32_t *seg_indptr, int32_t n_seg,
+                              const float *scaling, slora_stream_t stream)
+{
+    if (!p)
+        return fail(SLORA_ERR_INVALID_ARG, "lora_apply: null pool");
+    if (proj < 0 || proj >= p->n_proj)
+        return fail(SLORA_ERR_INVALID_ARG, "lora_apply: proj=%d of %d", proj, p->n_proj);
+    if (T < 0 || T > (1 << 20))
+        return fail(SLORA_ERR_INVALID_ARG, "lora_apply: T=%d", T);
+    if (T == 0)
+        return SLORA_OK;
+    if (!x || !y || !idx || x == y)
+        return fail(SLORA_ERR_INVALID_ARG, "lora_apply: null or aliased x / y / index pointer");
+    if (((uintptr_t)x | (uintptr_t)y) & 15)
+        return fail(SLORA_ERR_INVALID_ARG, "lora_apply: x and y must be 16-byte aligned");
+    if (n_seg < 0 || (n_seg > 0 && !seg_indptr) || n_seg > T)
+        return fail(SLORA_ERR_INVALID_ARG, "lora_apply: n_seg=%d", n_seg);
+    slora_status st = set_device(p);
+    if (st != SLORA_OK)
+        return st;
+    if (T > p->plan.cap_tokens) {
+        int32_t cap = std::max(T, 1024);
+        size_t bytes = plan_scratch_bytes(cap, p->max_adapters);
+        CUDA_TRY(cudaDeviceSynchronize());
+        if (p->plan.base)
+            cudaFree(p->plan.base);
+        p->plan = PlanScratch();
+        CUDA_TRY(cudaMalloc(&p->plan.base, bytes));
+        CUDA_TRY(cudaMemset(p->plan.base, 0, bytes));
+        p->plan.bytes = bytes;
+        p->plan.cap_tokens = cap;
+    }
+    PoolView pv{p->pool_dev, p->pt_dev, p->dir_dev, p->num_pages, p->hidden, p->n_proj,
+                p->max_adapters, p->status_dev};
+    int launched = 0;
+    cudaError_t e = launch_lora_apply(pv, proj, (const uint16_t *)x, (uint16_t *)y, T, idx, seg_indptr,
+                                      n_seg, scaling, p->plan, p->num_sms, (cudaStream_t)stream, &launched);
+    p->launches += launched;
+    if (e != cudaSuccess)
+        return fail(SLORA_ERR_CUDA, "lora_apply: launch failed: %s", cudaGetErrorString(e));
+    return SLORA_OK;
+}
+
+slora_status slora_pool_launch_count(slora_pool_t p, int64_t *out)
+{
+    if (!p || !out)
+        return fail(SLORA_ERR_INVALID_ARG, "pool_launch_count");
+    *out = p->launches;
+    return SLORA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,311 @@
+"""GPU parity: libslora.so against the fp64 CPU oracle on the same seeded inputs.
+
+Floating point: |y_gpu - ref| <= 1e-3 + 1e-2 * |ref| per element (fp16 in, fp32
+accumulation, fp16 out), plus a delta-only variant (y0 = 0) where the same bound applies
+to the delta itself.  Exact-arithmetic inputs and page contents: bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import rank_delta_paged_gb300 as rdp
+from rank_delta_paged_gb300 import workloads as W
+from rank_delta_paged_gb300.harness import PoolSession
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL = 1e-3, 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    rdp.build.build()
+    rdp.lib()
+
+
+def to_np(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().view(torch.int16).numpy().view(np.float16)
+
+
+def dev_f16(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.float16)
+
+
+def run(sess: PoolSession, p=0, idx=None, x=None, y0=None, seg="auto", scaling=None):
+    w = sess.w
+    x = w.x(p) if x is None else x
+    y0 = w.y0(p) if y0 is None else y0
+    idx = w.token_adapter_idx if idx is None else idx
+    xd, yd = dev_f16(x), dev_f16(y0)
+    idd = torch.from_numpy(np.ascontiguousarray(idx, dtype=np.int32)).cuda()
+    if seg == "auto":
+        seg = w.seg_indptr
+    segd = None if seg is None else torch.from_numpy(np.ascontiguousarray(seg, np.int32)).cuda()
+    sess.apply(p, xd, yd, idd, segd, scaling=scaling)
+    torch.cuda.synchronize()
+    return to_np(yd)
+
+
+def assert_close(got, ref, what=""):
+    ok = oracle.within_tolerance(got, ref, ATOL, RTOL)
+    if not ok.all():
+        bad = np.argwhere(~ok)[:5]
+        raise AssertionError(f"{what}: {int((~ok).sum())} of {ok.size} outside tolerance; first "
+                             f"{[(tuple(b), float(got[tuple(b)]), float(ref[tuple(b)])) for b in bad]}")
+
+
+def session_all_loaded(w):
+    s = PoolSession(w)
+    s.load(range(w.n_adapters))
+    return s
+
+
+# ------------------------------------------------------------------ parity
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_tiny_decode_parity(seed):
+    w = W.tiny_decode(seed=seed)
+    with session_all_loaded(w) as s:
+        got = run(s)
+        assert s.device_status() == 0
+    assert_close(got, oracle.workload_reference(w), "tiny_decode")
+
+
+@pytest.mark.parametrize("values", ["exact"])
+@pytest.mark.parametrize("make", [W.tiny_decode, lambda **k: W.decode_7b(T=96, **k),
+                                  lambda **k: W.prefill_7b(n_seg=5, seg_len=136, **k)])
+def test_exact_inputs_bit_exact(make, values):
+    w = make(values=values)
+    with session_all_loaded(w) as s:
+        got = run(s)
+        assert s.device_status() == 0
+    ref = oracle.workload_reference(w)
+    assert np.array_equal(got.view(np.uint16), ref.astype(np.float16).view(np.uint16))
+
+
+def test_delta_only_variant():
+    w = W.decode_7b(T=64, values="delta")
+    with session_all_loaded(w) as s:
+        got = run(s)
+    ref = oracle.workload_reference(w)
+    assert_close(got, ref, "delta-only")
+    assert np.abs(ref).max() > 0.01
+
+
+def test_decode_7b_full_size():
+    w = W.decode_7b()
+    with session_all_loaded(w) as s:
+        got = run(s)
+        assert s.device_status() == 0
+    assert_close(got, oracle.workload_reference(w), "decode_7b")
+
+
+def test_prefill_7b_full_size_sampled():
+    w = W.prefill_7b()
+    with session_all_loaded(w) as s:
+        got = run(s)
+        assert s.device_status() == 0
+    rng = np.random.default_rng(0)
+    edges = np.concatenate([np.arange(a, a + 3) for a in w.seg_indptr[:-1]] +
+                           [np.arange(b - 3, b) for b in w.seg_indptr[1:]])
+    sel = np.unique(np.concatenate([edges, rng.choice(w.T, 200, replace=False)])).astype(np.int32)
+    ref = oracle.workload_reference(w, sel=sel)
+    assert_close(got[sel], ref, "prefill_7b")
+
+
+def test_prefill_ragged_segments():
+    """Segments that are not multiples of the 128-token tile, one of a single token, and
+    decode tokens before and after the segment range."""
+    rng = np.random.default_rng(5)
+    ranks = np.array([8, 16, 32, 64, 128, 8, 24], np.int32)
+    lens = [1, 127, 129, 300, 64, 5]
+    pre, post = 7, 9
+    ids = [rng.integers(0, 7, pre)]
+    for i, L in enumerate(lens):
+        ids.append(np.full(L, i % 7))
+    ids.append(rng.integers(-1, 7, post))
+    idx = np.concatenate(ids).astype(np.int32)
+    indptr = np.concatenate([[pre], pre + np.cumsum(lens)]).astype(np.int32)
+    w = W.Workload("ragged", 1024, 1, ranks, idx, indptr, num_pages=2 * 2 * int(ranks.sum()),
+                   kv_pages=2 * int(ranks.sum()), shuffle_seed=99, seed=11)
+    with session_all_loaded(w) as s:
+        got = run(s)
+        assert s.device_status() == 0
+    assert_close(got, oracle.workload_reference(w), "ragged segments")
+
+
+def test_decode_13b_cold_load_then_apply():
+    w = W.decode_13b_zoo()
+    used = w.used_adapters()
+    with PoolSession(w) as s:
+        s.register(range(w.n_adapters))          # the whole zoo sits in the pinned host store
+        stream = torch.cuda.current_stream()
+        s.load(used, stream=stream)              # cold: fetch the batch's adapters
+        got = run(s)
+        assert s.device_status() == 0
+        # everything else stayed on the host
+        assert not rdp.slora_adapter_is_resident(s.pool, int(np.setdiff1d(np.arange(w.n_adapters), used)[0]))
+    assert_close(got, oracle.workload_reference(w), "decode_13b")
+
+
+def test_mixed_iteration_one_layer():
+    w = W.mixed_iteration(n_layers=1, pool_bytes=2 << 30)
+    used = w.used_adapters()
+    with PoolSession(w) as s:
+        s.load(used)
+        for p in range(w.n_proj):
+            got = run(s, p=p)
+            sel = np.unique(np.concatenate([w.decode_tokens(), np.arange(0, w.T, 37)])).astype(np.int32)
+            assert_close(got[sel], oracle.workload_reference(w, p=p, sel=sel), f"mixed p={p}")
+        assert s.device_status() == 0
+
+
+# ------------------------------------------------------------------ pool semantics
+
+def test_page_gather_bit_exact_and_reload():
+    w = W.decode_7b(T=32, n_adapters=12)
+    with PoolSession(w) as s:
+        s.load(range(w.n_adapters))
+        first = {}
+        for a in range(w.n_adapters):
+            r = int(w.ranks[a])
+            pt = np.empty(2 * r, np.int32)
+            rdp.slora_adapter_pages(s.pool, a, 0, pt)
+            first[a] = pt.copy()
+            At, B = w.factors(a)
+            want = np.concatenate([At[0], B[0]]).view(np.uint16)
+            page = np.empty(w.hidden, np.uint16)
+            for j in range(2 * r):
+                rdp.slora_page_read(s.pool, int(pt[j]), page)
+                assert np.array_equal(page, want[j]), (a, j)
+        allp = np.concatenate(list(first.values()))
+        assert len(np.unique(allp)) == allp.size                 # no page shared
+        assert not set(allp.tolist()) & set(s.kv_pages.tolist())  # none taken from KV
+        y_before = run(s)
+        # evict everything, release half of the KV slots, take some free slots so the
+        # reload lands elsewhere (partly on former KV slots), reload in reverse order
+        s.evict(range(w.n_adapters))
+        kv_half = s.kv_pages[: s.kv_pages.size // 2].copy()
+        rdp.slora_pages_free(s.pool, kv_half.size, kv_half)
+        hold = np.empty(97, np.int32)
+        rdp.slora_pages_alloc(s.pool, 97, hold)
+        s.load(range(w.n_adapters)[::-1])
+        moved = 0
+        for a in range(w.n_adapters):
+            r = int(w.ranks[a])
+            pt = np.empty(2 * r, np.int32)
+            rdp.slora_adapter_pages(s.pool, a, 0, pt)
+            moved += int(not np.array_equal(pt, first[a]))
+            At, B = w.factors(a)
+            want = np.concatenate([At[0], B[0]]).view(np.uint16)
+            page = np.empty(w.hidden, np.uint16)
+            for j in range(0, 2 * r, 3):
+                rdp.slora_page_read(s.pool, int(pt[j]), page)
+                assert np.array_equal(page, want[j])
+        assert moved > 0
+        y_after = run(s)
+        assert np.array_equal(y_before.view(np.uint16), y_after.view(np.uint16))
+
+
+def test_batch_order_invariance_bit_exact():
+    w = W.decode_7b(T=200, n_adapters=20)
+    perm = np.random.default_rng(3).permutation(w.T)
+    with session_all_loaded(w) as s:
+        y = run(s)
+        yp = run(s, idx=w.token_adapter_idx[perm], x=w.x()[perm], y0=w.y0()[perm])
+    assert np.array_equal(yp.view(np.uint16), y[perm].view(np.uint16))
+
+
+def test_zero_B_leaves_y_unchanged():
+    w = W.tiny_decode(seed=4)
+    w.prefetch_factors(range(w.n_adapters))
+    for a in range(w.n_adapters):
+        At, B = w.factors(a)
+        B[...] = 0
+    with session_all_loaded(w) as s:
+        got = run(s)
+    assert np.array_equal(got.view(np.uint16), w.y0().view(np.uint16))
+
+
+def test_base_only_tokens_and_errors_are_skipped():
+    w = W.tiny_decode(seed=8, T=16)
+    with PoolSession(w) as s:
+        s.load([0, 1, 2])                       # adapter 3 stays on the host
+        idx = w.token_adapter_idx.copy()
+        idx[0] = -1
+        idx[1] = 3                               # not resident
+        got = run(s, idx=idx)
+        assert s.device_status() == rdp_dev("NOT_RESIDENT")
+        y0 = w.y0()
+        assert np.array_equal(got[0].view(np.uint16), y0[0].view(np.uint16))
+        assert np.array_equal(got[1].view(np.uint16), y0[1].view(np.uint16))
+        keep = idx != 3
+        ref = oracle.workload_reference(w, sel=np.nonzero(keep)[0].astype(np.int32))
+        # reference for the kept tokens with the modified map
+        ref = oracle.lora_delta(w.x(), y0, np.where(keep, idx, -1).astype(np.int32), w.ranks,
+                                w.scaling(), [(w.factors(a)[0][0], w.factors(a)[1][0]) for a in range(4)])
+        assert_close(got, ref, "base-only/skip")
+        idx[2] = 17                              # beyond max_adapters
+        run(s, idx=idx)
+        assert s.device_status() in (rdp_dev("BAD_ADAPTER"), rdp_dev("NOT_RESIDENT"))
+        assert s.device_status() == 0           # cleared by the read
+
+
+def rdp_dev(name):
+    return {"BAD_ADAPTER": 1, "NOT_RESIDENT": 2, "BAD_PAGE": 3, "BAD_SEGMENT": 4}[name]
+
+
+def test_odd_ranks_and_ragged_token_counts():
+    ranks = np.array([1, 3, 8, 17, 128, 40], np.int32)
+    for T in (1, 2, 33, 257):
+        idx = np.random.default_rng(T).integers(-1, len(ranks), T).astype(np.int32)
+        w = W.Workload(f"odd{T}", 512, 1, ranks, idx, None, num_pages=4 * int(ranks.sum()),
+                       kv_pages=int(ranks.sum()), shuffle_seed=5, seed=T)
+        with session_all_loaded(w) as s:
+            got = run(s)
+            assert s.device_status() == 0
+        assert_close(got, oracle.workload_reference(w), f"odd ranks T={T}")
+
+
+def test_scaling_override_and_projection_select():
+    ranks = np.array([16, 32, 8], np.int32)
+    idx = np.array([0, 1, 2, 1, 0, 2, 2], np.int32)
+    w = W.Workload("proj3", 768, 3, ranks, idx, None, num_pages=2 * 3 * 2 * int(ranks.sum()),
+                   kv_pages=0, shuffle_seed=1, seed=4)
+    override = np.array([0.5, -2.0, 3.0], np.float32)
+    with session_all_loaded(w) as s:
+        for p in range(3):
+            got = run(s, p=p)
+            assert_close(got, oracle.workload_reference(w, p=p), f"proj {p}")
+        sd = torch.from_numpy(override).cuda()
+        got = run(s, p=2, scaling=sd)
+    factors = [(w.factors(a)[0][2], w.factors(a)[1][2]) for a in range(3)]
+    ref = oracle.lora_delta(w.x(2), w.y0(2), idx, ranks, override, factors)
+    assert_close(got, ref, "scaling override")
+
+
+def test_empty_batch_is_noop():
+    w = W.tiny_decode()
+    with session_all_loaded(w) as s:
+        y = torch.zeros(1, w.hidden, dtype=torch.float16, device="cuda")
+        x = torch.zeros_like(y)
+        idx = torch.zeros(1, dtype=torch.int32, device="cuda")
+        rdp.slora_lora_apply(s.pool, 0, x, y, 0, idx)
+        torch.cuda.synchronize()
+        assert int(y.abs().sum()) == 0
+
+
+def test_pool_full_loads_nothing():
+    w = W.decode_7b(T=8, n_adapters=10)
+    with PoolSession(w) as s:
+        free = rdp.slora_pool_num_free(s.pool)
+        hold = np.empty(free - 10, np.int32)
+        rdp.slora_pages_alloc(s.pool, free - 10, hold)
+        with pytest.raises(rdp.SloraError) as e:
+            s.load(range(w.n_adapters))
+        assert e.value.status == 2
+        assert rdp.slora_pool_num_free(s.pool) == 10
+        assert not any(rdp.slora_adapter_is_resident(s.pool, a) for a in range(w.n_adapters))
