@@ -318,7 +318,8 @@ def main():
         torch.cuda.synchronize()
         if k >= 2:
             e2e_ms.append(1e3 * (time.perf_counter() - t0))
-    e2e_t = torch.tensor([statistics.mean(e2e_ms)], dtype=torch.float64, device=dev)
+    e2e_t = torch.tensor([statistics.mean(e2e_ms) if e2e_ms else float("nan")], dtype=torch.float64,
+                         device=dev)
     if world > 1:
         dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
     e2e_value = float(tok.item()) * w.n_layers / (float(e2e_t.item()) / 1e3)

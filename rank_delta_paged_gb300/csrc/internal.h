@@ -70,9 +70,10 @@ struct PoolView {
 struct PlanScratch {
     void *base = nullptr;
     size_t bytes = 0;
-    int32_t cap_tokens = 0;
+    int32_t cap_tokens = 0;   // tokens the layout was carved for
+    int32_t max_rank = 0;     // largest adapter rank the layout was carved for
 };
-size_t plan_scratch_bytes(int32_t T, int32_t max_adapters);
+size_t plan_scratch_bytes(int32_t T, int32_t max_rank, int32_t hidden);
 
 // The hot path (decode.cu / prefill.cu).
 cudaError_t launch_lora_apply(const PoolView &pv, int32_t proj, const uint16_t *x, uint16_t *y,

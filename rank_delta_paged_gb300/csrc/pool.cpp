@@ -61,6 +61,7 @@ struct slora_pool {
     PlanScratch plan;
     std::vector<AdapterRec> adapters;
     int64_t launches = 0;  // kernels launched by this pool
+    int32_t max_rank = 0;  // largest registered rank (sizes the plan scratch)
 };
 
 namespace {
@@ -286,6 +287,8 @@ slora_status slora_adapter_register(slora_pool_t p, int32_t id, int32_t rank, fl
     }
     n.registered = true;
     a = n;
+    if (rank > p->max_rank)
+        p->max_rank = rank;
     return SLORA_OK;
 }
 
@@ -557,9 +560,10 @@ slora_status slora_lora_apply(slora_pool_t p, int32_t proj, const void *x, void 
     slora_status st = set_device(p);
     if (st != SLORA_OK)
         return st;
-    if (T > p->plan.cap_tokens) {
-        int32_t cap = std::max(T, 1024);
-        size_t bytes = plan_scratch_bytes(cap, p->max_adapters);
+    const int32_t want_rank = std::max(p->max_rank, 1);
+    if (T > p->plan.cap_tokens || want_rank > p->plan.max_rank) {
+        int32_t cap = std::max(T, std::max(p->plan.cap_tokens, 256));
+        size_t bytes = plan_scratch_bytes(cap, want_rank, p->hidden);
         CUDA_TRY(cudaDeviceSynchronize());
         if (p->plan.base)
             cudaFree(p->plan.base);
@@ -568,6 +572,7 @@ slora_status slora_lora_apply(slora_pool_t p, int32_t proj, const void *x, void 
         CUDA_TRY(cudaMemset(p->plan.base, 0, bytes));
         p->plan.bytes = bytes;
         p->plan.cap_tokens = cap;
+        p->plan.max_rank = want_rank;
     }
     PoolView pv{p->pool_dev, p->pt_dev, p->dir_dev, p->num_pages, p->hidden, p->n_proj,
                 p->max_adapters, p->status_dev};
