@@ -200,8 +200,13 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const __grid_cons
     for (int i = tid; i < Tc; i += kPlanThreads) {
         const int t = a.t_begin + i;
         int slot = -1;
-        if (t < lo || t >= hi) {
-            const int ad = a.idx[t];
+        const bool in_seg = t >= lo && t < hi;
+        const int ad = a.idx[t];
+        // segment tokens run on the tensor cores unless their adapter's rank is too large
+        // for that path; segment errors are reported there
+        const bool mine = !in_seg || (ad >= 0 && ad < a.pv.max_adapters && a.pv.dir[ad].pt_off >= 0 &&
+                                      a.pv.dir[ad].rank > kMaxPrefillRank);
+        if (mine) {
             if (ad >= 0 && ad < a.pv.max_adapters) {
                 const DirEntry e = a.pv.dir[ad];
                 if (e.pt_off >= 0 && e.rank > 0 && e.rank <= kMaxRank) {
@@ -716,7 +721,7 @@ cudaError_t launch_lora_apply(const PoolView &pv, int32_t proj, const uint16_t *
         const int32_t te = tb + kMaxPlanTokens < T ? tb + kMaxPlanTokens : T;
         int hs = 1024;
         while (hs < 2 * (te - tb)) hs <<= 1;
-        PlanArgs pa{pv, proj, idx, T, seg_indptr, 0 * n_seg, tb, te, hs, L};
+        PlanArgs pa{pv, proj, idx, T, seg_indptr, n_seg, tb, te, hs, L};
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(1);
         cfg.blockDim = dim3(kPlanThreads);
@@ -737,6 +742,11 @@ cudaError_t launch_lora_apply(const PoolView &pv, int32_t proj, const uint16_t *
         cfg2.attrs = attr;
         cfg2.numAttrs = 1;
         e = cudaLaunchKernelEx(&cfg2, delta_kernel, da);
+        if (e != cudaSuccess) return e;
+        *launches += 1;
+    }
+    if (n_seg > 0) {
+        cudaError_t e = launch_prefill(pv, proj, x, y, T, idx, seg_indptr, n_seg, scaling, num_sms, stream);
         if (e != cudaSuccess) return e;
         *launches += 1;
     }

@@ -75,6 +75,15 @@ struct PlanScratch {
 };
 size_t plan_scratch_bytes(int32_t T, int32_t max_rank, int32_t hidden);
 
+// Segments whose adapter rank is at most this run on the tensor cores (prefill.cu);
+// larger ranks take the decode path.  At most kMaxSegments segments per call.
+constexpr int kMaxPrefillRank = 128;
+constexpr int kMaxSegments = 4096;
+
+cudaError_t launch_prefill(const PoolView &pv, int32_t proj, const uint16_t *x, uint16_t *y, int32_t T,
+                           const int32_t *idx, const int32_t *seg_indptr, int32_t n_seg,
+                           const float *scaling, int num_sms, cudaStream_t stream);
+
 // The hot path (decode.cu / prefill.cu).
 cudaError_t launch_lora_apply(const PoolView &pv, int32_t proj, const uint16_t *x, uint16_t *y,
                               int32_t T, const int32_t *idx, const int32_t *seg_indptr,

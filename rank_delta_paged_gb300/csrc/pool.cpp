@@ -555,8 +555,8 @@ slora_status slora_lora_apply(slora_pool_t p, int32_t proj, const void *x, void 
         return fail(SLORA_ERR_INVALID_ARG, "lora_apply: null or aliased x / y / index pointer");
     if (((uintptr_t)x | (uintptr_t)y) & 15)
         return fail(SLORA_ERR_INVALID_ARG, "lora_apply: x and y must be 16-byte aligned");
-    if (n_seg < 0 || (n_seg > 0 && !seg_indptr) || n_seg > T)
-        return fail(SLORA_ERR_INVALID_ARG, "lora_apply: n_seg=%d", n_seg);
+    if (n_seg < 0 || (n_seg > 0 && !seg_indptr) || n_seg > T || n_seg > kMaxSegments)
+        return fail(SLORA_ERR_INVALID_ARG, "lora_apply: n_seg=%d (at most min(T, %d))", n_seg, kMaxSegments);
     slora_status st = set_device(p);
     if (st != SLORA_OK)
         return st;

@@ -309,3 +309,52 @@ def test_pool_full_loads_nothing():
         assert e.value.status == 2
         assert rdp.slora_pool_num_free(s.pool) == 10
         assert not any(rdp.slora_adapter_is_resident(s.pool, a) for a in range(w.n_adapters))
+
+
+def test_segment_edge_cases():
+    """A segment whose adapter has rank > 128 (routed to the decode path), a base-only
+    segment (-1), an empty segment, and single-token segments."""
+    ranks = np.array([8, 200, 16, 256], np.int32)
+    lens = [130, 0, 70, 1, 1, 40]
+    seg_adapter = [1, 2, -1, 0, 3, 1]
+    idx = np.concatenate([np.full(L, a) for L, a in zip(lens, seg_adapter)] +
+                         [np.array([0, 1, 2, 3, -1], np.int32)]).astype(np.int32)
+    indptr = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    w = W.Workload("seg_edges", 512, 1, ranks, idx, indptr, num_pages=2 * 2 * int(ranks.sum()),
+                   kv_pages=int(ranks.sum()), shuffle_seed=3, seed=21)
+    with session_all_loaded(w) as s:
+        got = run(s)
+        assert s.device_status() == 0
+    assert_close(got, oracle.workload_reference(w), "segment edges")
+
+
+def test_segment_with_mixed_adapters_is_rejected():
+    ranks = np.array([16, 32], np.int32)
+    idx = np.array([0] * 100 + [1] + [0] * 27 + [1] * 50, np.int32)   # first 128-token tile mixed
+    indptr = np.array([0, 128, 178], np.int32)
+    w = W.Workload("seg_mixed", 256, 1, ranks, idx, indptr, num_pages=8 * int(ranks.sum()),
+                   kv_pages=0, shuffle_seed=0, seed=2)
+    with session_all_loaded(w) as s:
+        got = run(s)
+        assert s.device_status() == rdp_dev("BAD_SEGMENT")
+    y0 = w.y0()
+    # the mixed tile is skipped (y unchanged); the second segment is computed
+    assert np.array_equal(got[:128].view(np.uint16), y0[:128].view(np.uint16))
+    assert_close(got[128:], oracle.workload_reference(w, sel=np.arange(128, 178, dtype=np.int32)),
+                 "second segment")
+
+
+def test_prefill_exact_all_ranks_bit_exact():
+    """Exact-arithmetic inputs through the tensor-core path for every rank class and a
+    hidden size that is not a multiple of the 256-column tile."""
+    ranks = np.array([8, 16, 24, 32, 64, 100, 128], np.int32)
+    lens = [128, 129, 64, 200, 17, 128, 256]
+    idx = np.concatenate([np.full(L, i) for i, L in enumerate(lens)]).astype(np.int32)
+    indptr = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    w = W.Workload("prefill_exact", 704, 1, ranks, idx, indptr, num_pages=2 * 2 * int(ranks.sum()),
+                   kv_pages=int(ranks.sum()), shuffle_seed=8, seed=5, values="exact")
+    with session_all_loaded(w) as s:
+        got = run(s)
+        assert s.device_status() == 0
+    ref = oracle.workload_reference(w)
+    assert np.array_equal(got.view(np.uint16), ref.astype(np.float16).view(np.uint16))
