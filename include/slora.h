@@ -200,6 +200,34 @@ slora_status slora_lora_apply(slora_pool_t pool, int32_t proj, const void *x, vo
                               int32_t n_seg, const float *scaling, slora_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * slora_lora_apply_noalloc: the same computation as slora_lora_apply, with the same
+ * arguments, for callers that must not allocate device memory during the call.  The
+ * S-LoRA pages have no counterpart for it; it exists for callers whose device memory
+ * is owned and accounted by a host framework's allocator, or whose serving step cannot
+ * absorb a cudaMalloc / cudaFree and the device synchronisation around it (the pool's
+ * own plan scratch is allocated on first use and re-allocated when a larger batch or a
+ * larger registered rank arrives).
+ *
+ * Scratch: one fixed 8 MiB device array inside the library, which every GPU that loads
+ * the library holds until the process exits.  The call allocates and frees nothing.
+ * Limit: the token plan of the call must fit that array; it needs about
+ *   T' * (44 + 16 * (ceil(R / 8) + ceil(hidden / 2048)) + 4 * R) bytes,
+ * with T' = min(T, 4096) and R the largest rank registered in the pool (about 3.3 MiB
+ * for T' = 4096, R = 128, hidden = 4096).  A call beyond it returns
+ * SLORA_ERR_UNSUPPORTED with the sizes in slora_last_error() and launches nothing.
+ * The first call on a device looks up the array's device address (once per device,
+ * with that device current); make that first call before any stream capture.
+ * Every call on a device shares the one array and leaves its plan there; the kernels
+ * rewrite every field they read, so nothing needs clearing between calls.  Calls whose
+ * kernels overlap on the GPU (other streams, other pools, other threads) race on the
+ * array: order them on one stream or synchronise between them.
+ * ------------------------------------------------------------------------- */
+slora_status slora_lora_apply_noalloc(slora_pool_t pool, int32_t proj, const void *x, void *y,
+                                      int32_t T, const int32_t *token_adapter_idx,
+                                      const int32_t *seg_indptr, int32_t n_seg,
+                                      const float *scaling, slora_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Observability / test hooks.
  * adapter_pages(): the adapter's page table for projection proj, 2 * rank int32 entries
  *   (A^T rows then B rows) written to out (host).

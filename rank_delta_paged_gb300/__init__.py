@@ -26,7 +26,7 @@ __all__ = [
     "slora_pages_alloc", "slora_pages_free",
     "slora_adapter_register", "slora_adapter_unregister",
     "slora_adapter_load", "slora_adapters_load", "slora_adapter_evict", "slora_adapter_is_resident",
-    "slora_lora_apply",
+    "slora_lora_apply", "slora_lora_apply_noalloc",
     "slora_adapter_pages", "slora_adapter_rank", "slora_page_read", "slora_get_device_status",
     "slora_pool_launch_count",
 ]
@@ -57,6 +57,7 @@ _SIGS = {
     "slora_adapter_evict": [_P, _I32, _P],
     "slora_adapter_is_resident": [_P, _I32, _P],
     "slora_lora_apply": [_P, _I32, _P, _P, _I32, _P, _P, _I32, _P, _P],
+    "slora_lora_apply_noalloc": [_P, _I32, _P, _P, _I32, _P, _P, _I32, _P, _P],
     "slora_adapter_pages": [_P, _I32, _I32, _P],
     "slora_adapter_rank": [_P, _I32, _P],
     "slora_page_read": [_P, _I32, _P],
@@ -225,6 +226,14 @@ def slora_adapter_is_resident(pool: int, adapter_id: int) -> bool:
 def slora_lora_apply(pool: int, proj: int, x, y, T: int, token_adapter_idx, seg_indptr=None,
                      n_seg: int = 0, scaling=None, stream=None) -> None:
     _call("slora_lora_apply", pool, proj, _ptr(x), _ptr(y), T, _ptr(token_adapter_idx),
+          _ptr(seg_indptr), n_seg, _ptr(scaling), _stream(stream))
+
+
+def slora_lora_apply_noalloc(pool: int, proj: int, x, y, T: int, token_adapter_idx,
+                             seg_indptr=None, n_seg: int = 0, scaling=None, stream=None) -> None:
+    """slora_lora_apply without device allocation: plan scratch in the library's fixed
+    device array (see include/slora.h for the size limit and the sharing rules)."""
+    _call("slora_lora_apply_noalloc", pool, proj, _ptr(x), _ptr(y), T, _ptr(token_adapter_idx),
           _ptr(seg_indptr), n_seg, _ptr(scaling), _stream(stream))
 
 

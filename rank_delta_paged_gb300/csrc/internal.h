@@ -90,4 +90,15 @@ cudaError_t launch_lora_apply(const PoolView &pv, int32_t proj, const uint16_t *
                               int32_t n_seg, const float *scaling, const PlanScratch &scratch,
                               int num_sms, cudaStream_t stream, int *launches);
 
+// What the hot path needs to know about a pool, for entry points defined outside
+// pool.cpp (pool.cpp).  *launches points at the pool's kernel-launch counter.
+struct PoolHotPath {
+    PoolView pv;
+    int device;
+    int num_sms;
+    int32_t max_rank;
+    int64_t *launches;
+};
+slora_status pool_hot_path(slora_pool_t pool, PoolHotPath *out);
+
 }  // namespace slora

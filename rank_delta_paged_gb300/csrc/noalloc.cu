@@ -1,0 +1,106 @@
+// slora_lora_apply_noalloc: the batched LoRA delta without any device allocation.
+//
+// slora_lora_apply keeps its token-plan scratch in memory the pool allocates on first
+// use and re-allocates (after a device synchronisation) when a larger batch or a larger
+// adapter rank arrives.  Some callers cannot allow that: code that runs under a host
+// framework whose allocator must own and account for every device byte, or a serving
+// step with a fixed latency budget in which a cudaMalloc / cudaFree (and the device-wide
+// synchronisation around them) is not acceptable.  This entry point serves them: its
+// scratch is one file-scope device array of a fixed size, kNoAllocScratchBytes, which
+// every GPU that loads this library holds until the process exits.  The caller passes
+// the pool, inputs and outputs exactly as for slora_lora_apply.
+#include <cstdio>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "host_common.h"
+#include "internal.h"
+#include "slora.h"
+
+namespace slora {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 8u << 20;   // 8 MiB
+constexpr int kMaxDevices = 64;
+
+// Shared by every call of the entry point on a device; holds the last call's plan.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_mu;
+void *g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on `device` (which must be current).  The name of
+// the array in host code is only a host-side stand-in, so the address is fetched once per
+// device with cudaGetSymbolAddress and cached.
+slora_status scratch_for_device(int device, void **out)
+{
+    if (device < 0 || device >= kMaxDevices)
+        return fail(SLORA_ERR_UNSUPPORTED, "lora_apply_noalloc: device %d beyond %d", device, kMaxDevices);
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_scratch_ptr[device]) {
+        void *ptr = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess || ptr == nullptr)
+            return fail(SLORA_ERR_CUDA, "lora_apply_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+        g_scratch_ptr[device] = ptr;
+    }
+    *out = g_scratch_ptr[device];
+    return SLORA_OK;
+}
+
+}  // namespace
+}  // namespace slora
+
+using namespace slora;
+
+extern "C" slora_status slora_lora_apply_noalloc(slora_pool_t pool, int32_t proj, const void *x, void *y,
+                                                 int32_t T, const int32_t *token_adapter_idx,
+                                                 const int32_t *seg_indptr, int32_t n_seg,
+                                                 const float *scaling, slora_stream_t stream)
+{
+    PoolHotPath hp;
+    slora_status st = pool_hot_path(pool, &hp);
+    if (st != SLORA_OK)
+        return st;
+    if (proj < 0 || proj >= hp.pv.n_proj)
+        return fail(SLORA_ERR_INVALID_ARG, "lora_apply_noalloc: proj=%d of %d", proj, hp.pv.n_proj);
+    if (T < 0 || T > (1 << 20))
+        return fail(SLORA_ERR_INVALID_ARG, "lora_apply_noalloc: T=%d", T);
+    if (T == 0)
+        return SLORA_OK;
+    if (!x || !y || !token_adapter_idx || x == y)
+        return fail(SLORA_ERR_INVALID_ARG, "lora_apply_noalloc: null or aliased x / y / index pointer");
+    if (((uintptr_t)x | (uintptr_t)y) & 15)
+        return fail(SLORA_ERR_INVALID_ARG, "lora_apply_noalloc: x and y must be 16-byte aligned");
+    if (n_seg < 0 || (n_seg > 0 && !seg_indptr) || n_seg > T || n_seg > kMaxSegments)
+        return fail(SLORA_ERR_INVALID_ARG, "lora_apply_noalloc: n_seg=%d (at most min(T, %d))", n_seg,
+                    kMaxSegments);
+    const int32_t max_rank = hp.max_rank > 0 ? hp.max_rank : 1;
+    const size_t need = plan_scratch_bytes(T, max_rank, hp.pv.hidden);
+    if (need > kNoAllocScratchBytes)
+        return fail(SLORA_ERR_UNSUPPORTED,
+                    "lora_apply_noalloc: this batch needs %zu bytes of plan scratch (T=%d, largest registered "
+                    "rank %d, hidden %d) but the static scratch holds %zu; use slora_lora_apply or a smaller batch",
+                    need, T, max_rank, hp.pv.hidden, kNoAllocScratchBytes);
+    cudaError_t e = cudaSetDevice(hp.device);
+    if (e != cudaSuccess)
+        return fail(SLORA_ERR_CUDA, "lora_apply_noalloc: cudaSetDevice: %s", cudaGetErrorString(e));
+    void *scratch = nullptr;
+    if ((st = scratch_for_device(hp.device, &scratch)) != SLORA_OK)
+        return st;
+    // The plan kernel writes every scratch field the delta kernel reads (header, claim
+    // counter, per-group counters) before it is read, so nothing needs clearing here.
+    PlanScratch ps;
+    ps.base = scratch;
+    ps.bytes = kNoAllocScratchBytes;
+    ps.cap_tokens = T;
+    ps.max_rank = max_rank;
+    int launched = 0;
+    e = launch_lora_apply(hp.pv, proj, (const uint16_t *)x, (uint16_t *)y, T, token_adapter_idx, seg_indptr,
+                          n_seg, scaling, ps, hp.num_sms, (cudaStream_t)stream, &launched);
+    *hp.launches += launched;
+    if (e != cudaSuccess)
+        return fail(SLORA_ERR_CUDA, "lora_apply_noalloc: launch failed: %s", cudaGetErrorString(e));
+    return SLORA_OK;
+}

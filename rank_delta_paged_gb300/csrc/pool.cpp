@@ -594,3 +594,16 @@ slora_status slora_pool_launch_count(slora_pool_t p, int64_t *out)
 }
 
 }  // extern "C"
+
+slora_status slora::pool_hot_path(slora_pool_t p, PoolHotPath *out)
+{
+    if (!p || !out)
+        return fail(SLORA_ERR_INVALID_ARG, "null pool");
+    out->pv = PoolView{p->pool_dev, p->pt_dev, p->dir_dev, p->num_pages, p->hidden, p->n_proj,
+                       p->max_adapters, p->status_dev};
+    out->device = p->device;
+    out->num_sms = p->num_sms;
+    out->max_rank = p->max_rank;
+    out->launches = &p->launches;
+    return SLORA_OK;
+}
