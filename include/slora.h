@@ -211,9 +211,10 @@ slora_status slora_lora_apply(slora_pool_t pool, int32_t proj, const void *x, vo
  * Scratch: one fixed 8 MiB device array inside the library, which every GPU that loads
  * the library holds until the process exits.  The call allocates and frees nothing.
  * Limit: the token plan of the call must fit that array; it needs about
- *   T' * (44 + 16 * (ceil(R / 8) + ceil(hidden / 2048)) + 4 * R) bytes,
- * with T' = min(T, 4096) and R the largest rank registered in the pool (about 3.3 MiB
- * for T' = 4096, R = 128, hidden = 4096).  A call beyond it returns
+ *   T' * (8 + 48 * (ceil(R / 8) + ceil(hidden / 2048)) + 4 * (R + 4)) bytes,
+ * with R the largest rank registered in the pool and T' = min(T, 16384) when
+ * max_adapters <= 2048, else min(T, 2048) (about 0.7 MiB for T' = 512, R = 128,
+ * hidden = 4096; about 5.4 MiB for T' = 4096).  A call beyond it returns
  * SLORA_ERR_UNSUPPORTED with the sizes in slora_last_error() and launches nothing.
  * The first call on a device looks up the array's device address (once per device,
  * with that device current); make that first call before any stream capture.

@@ -12,17 +12,22 @@
 //
 //   plan_kernel (one CTA): groups the decode tokens by adapter in a shared-memory hash
 //     table and writes the work list: shrink items (adapter, 8 rank rows, <= 4 tokens)
-//     first, then expand items (adapter, 2048 output columns, <= 4 tokens).
+//     first, then expand items (adapter, 1024 output columns, <= 4 tokens), each list in
+//     descending rank.  Each item carries its group's fields.
 //
-//   delta_kernel (one persistent CTA per SM): claims items in list order from a global
-//     counter.  Warp 0 streams each item's page rows into a 4-stage shared-memory ring
-//     with 1-D bulk copies (TMA engine), several tiles ahead of the compute:
-//       shrink  u[t][j] = sum_k x[t][k] * At[j][k]     (A^T rows + x rows per K tile;
-//               fp32 partials per thread, one butterfly reduce-scatter per warp, written
-//               to a small fp32 scratch, then a release increment of the group's counter)
+//   delta_kernel (persistent, 128 threads, two CTAs per SM when ranks are at most 128):
+//     each CTA takes a fixed subset of the items (rounds over the list in alternating
+//     direction), loads their descriptors, page indices and token ids into shared memory,
+//     then streams their page rows with cp.async: every thread copies its own 16-byte piece
+//     of each row segment into a 4-deep per-thread ring, 3 tiles ahead of its arithmetic,
+//     so no barrier guards the ring.  The threads compute
+//       shrink  u[t][j] = sum_k x[t][k] * At[j][k]     (A^T rows + x rows per 1024-element
+//               K tile; fp32 partials per thread, one butterfly reduce-scatter per warp,
+//               written to a small fp32 scratch, published with release increments of the
+//               group's counter)
 //       expand  y[t][c] = y0[t][c] + s * sum_j u[t][j] * B[j][c]
-//               (B row segments per 8-row tile; waits, with a time limit, until every
-//               shrink item of its group has been published)
+//               (8 B row segments per tile; waits, with a time limit, until every shrink
+//               item of its group has been published)
 //     Each used adapter page row is read from HBM once per token chunk of its group (the
 //     repeats of hot adapters hit L2).  Ranks 1..1024 run in the same launch: the last
 //     rank chunk of an adapter simply has fewer rows; nothing in the pool is padded.
@@ -30,6 +35,8 @@
 // Per-token arithmetic is fixed by the thread layout (which K elements a thread sums,
 // the butterfly order, the row order of the expand), never by how tokens are grouped,
 // so results do not depend on the batch, its order, or the physical pages.
+#include <type_traits>
+
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -39,46 +46,44 @@
 namespace slora {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
+constexpr int kDT = 128;                 // threads of the delta kernel
+constexpr int kDW = kDT / 32;            // its warps
 constexpr int RS = 8;       // A^T rows per shrink item
 constexpr int TS = 4;       // tokens per shrink item
 constexpr int TE = 4;       // tokens per expand item
 constexpr int RB = 8;       // B rows per expand tile
-constexpr int KC = 2048;    // K elements per shrink tile (= 8 * kThreads)
-constexpr int CE = 2048;    // output columns per expand item (= 8 * kThreads)
-constexpr int NS = 4;       // pipeline stages
-constexpr int kStageBytes = (RS + TS) * KC * 2;       // 48 KiB
+constexpr int VC = 8 * kDT; // elements of a row segment: K per shrink tile, columns per expand item
+constexpr int NST = 4;      // depth of each thread's cp.async ring (tiles)
 constexpr int kMaxRank = 1024;
-constexpr int kUBytes = TE * kMaxRank * 4;            // 16 KiB
-constexpr int kSmemBytes = NS * kStageBytes + kUBytes + kWarps * 32 * 4;
+constexpr int kBatchItems = 32;          // item metadata a CTA holds at once
+constexpr int kBatchPages = 2048;        // page indices a CTA holds at once
 
 constexpr int kPlanThreads = 1024;
-constexpr int kMaxPlanTokens = 4096;                  // token-index range per plan
-constexpr int kMaxHash = 2 * kMaxPlanTokens;
+constexpr int kMaxPlanTokens = 16384;   // token-index range per plan when groups fit
+constexpr int kMaxPlanGroups = 2048;    // distinct adapters per plan
+constexpr int kMaxHash = 2 * kMaxPlanGroups;
 
-static_assert(KC == 8 * kThreads && CE == 8 * kThreads, "one 16-byte vector per thread per row");
-static_assert(RB * CE * 2 <= kStageBytes, "expand tile fits a stage");
 static_assert(RS * TS == 32, "shrink item partials = one value per lane after the butterfly");
+static_assert(RB <= RS + TS, "expand rows fit the tile slots");
+static_assert(kBatchPages >= kMaxRank, "one expand item's pages always fit a batch");
 
 struct PlanHeader {
     int32_t n_groups, n_shrink, n_expand, claim;
     int32_t seg_lo, seg_hi, pad0, pad1;
 };
-struct GroupRec {
-    int32_t adapter, tok_begin, n_tok, rank;
+// One work item, with the fields of its group copied in.
+struct alignas(16) Item {
+    int32_t g, a, t0, nt;           // group, first rank row (shrink) or column chunk (expand), tokens
+    int32_t rank, tok_begin, u_off, adapter;
+    int32_t n_tok;
     float scaling;
-    int32_t u_off;
-    int64_t pt_base;  // arena index of this projection's page table
+    int64_t pt_base;                // arena index of this projection's page table
 };
-struct Item {
-    int32_t g, a, t0, nt;  // a = first rank row (shrink) or column chunk (expand)
-};
+static_assert(sizeof(Item) == 48, "Item layout");
 
 struct PlanLayout {
     PlanHeader *hdr;
     int32_t *tok_order;
-    GroupRec *groups;
     int32_t *done;
     Item *items;
     float *u;
@@ -89,9 +94,16 @@ struct PlanLayout {
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 // Number of column chunks of the expand.
-__host__ __device__ inline int n_col_chunks(int d) { return ceil_div(d, CE); }
+__host__ __device__ inline int n_col_chunks(int d) { return ceil_div(d, VC); }
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Tokens one plan covers: the whole range up to kMaxPlanTokens when every adapter id fits
+// the plan's group tables, otherwise chunks of kMaxPlanGroups tokens.
+inline int32_t plan_chunk(int32_t max_adapters)
+{
+    return max_adapters <= kMaxPlanGroups ? kMaxPlanTokens : kMaxPlanGroups;
+}
 
 PlanLayout carve(void *base, int32_t cap_tokens, int32_t max_rank, int32_t hidden, size_t *total)
 {
@@ -104,10 +116,9 @@ PlanLayout carve(void *base, int32_t cap_tokens, int32_t max_rank, int32_t hidde
     };
     const int64_t cap = cap_tokens;
     L.cap_items = cap * (ceil_div(max_rank, RS) + n_col_chunks(hidden));
-    L.cap_u = cap * (int64_t)max_rank;
+    L.cap_u = cap * ((int64_t)max_rank + 4) + 16;   // per-group offsets padded to 4 floats
     L.hdr = (PlanHeader *)take(sizeof(PlanHeader));
     L.tok_order = (int32_t *)take(cap * 4);
-    L.groups = (GroupRec *)take(cap * sizeof(GroupRec));
     L.done = (int32_t *)take(cap * 4);
     L.items = (Item *)take(L.cap_items * sizeof(Item));
     L.u = (float *)take(L.cap_u * 4);
@@ -155,23 +166,50 @@ struct PlanArgs {
     const int32_t *seg_indptr;
     int32_t n_seg;
     int32_t t_begin, t_end;
-    int32_t hash_size;  // power of two >= 2 * (t_end - t_begin)
+    int32_t hash_size;  // power of two >= 2 * min(t_end - t_begin, max_adapters), <= kMaxHash
     PlanLayout L;
 };
+
+constexpr int kRankBuckets = 11;        // floor(log2(rank)) for ranks 1..1024
+
+constexpr size_t plan_smem_bytes(int hs)
+{
+    return (size_t)hs * 4 + (size_t)kMaxPlanTokens * 2 + (size_t)13 * kMaxPlanGroups * 4;
+}
+
+__device__ __forceinline__ void plan_refuse(const PlanArgs &a)
+{
+    set_status(a.pv.status, SLORA_DEV_BAD_SEGMENT);
+    a.L.hdr->n_groups = 0;
+    a.L.hdr->n_shrink = 0;
+    a.L.hdr->n_expand = 0;
+    a.L.hdr->claim = 0;
+}
 
 __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const __grid_constant__ PlanArgs a)
 {
     extern __shared__ int plan_smem[];
     const int HS = a.hash_size;
     const int Tc = a.t_end - a.t_begin;
-    int *keys = plan_smem;            // [HS] adapter id or -1
-    int *gid = keys + HS;             // [HS] group id of an occupied slot
-    int *garr = gid + HS;             // [Tc] adapter of group g
-    int *cnt = garr + kMaxPlanTokens; // [Tc] tokens per group, then the placement cursor
-    short *tslot = reinterpret_cast<short *>(cnt + kMaxPlanTokens);  // [Tc] slot of token
+    int *keys = plan_smem;                                  // [HS] adapter id / -1, then group id
+    short *tslot = reinterpret_cast<short *>(keys + HS);     // [Tc] hash slot, then group id
+    int *gad = reinterpret_cast<int *>(tslot + kMaxPlanTokens);  // [G] adapter
+    int *gn = gad + kMaxPlanGroups;                         // [G] tokens
+    int *gtok = gn + kMaxPlanGroups;                        // [G] first token position
+    int *gsh = gtok + kMaxPlanGroups;                       // [G] token placement cursor
+    int *psh = gsh + kMaxPlanGroups;                        // [position] first shrink item
+    int *pex = psh + kMaxPlanGroups;                        // [position] first expand item
+    int *gu = pex + kMaxPlanGroups;                         // [G] first u float (multiple of 4)
+    int *grank = gu + kMaxPlanGroups;                       // [G] rank
+    float *gscale = reinterpret_cast<float *>(grank + kMaxPlanGroups);   // [G] scaling
+    int *gperm = reinterpret_cast<int *>(gscale + kMaxPlanGroups);       // [position] group, by rank descending
+    long long *gpt = reinterpret_cast<long long *>(gperm + kMaxPlanGroups);  // [G] page-table offset
     __shared__ int warp_tot[33];
-    __shared__ int s_lo, s_hi, s_G, s_nsh, s_nex;
+    __shared__ int s_lo, s_hi, s_G, s_nsh, s_nex, s_bad;
+    __shared__ int s_bucket[kRankBuckets + 1];
     const int tid = threadIdx.x;
+    const int d = a.pv.hidden;
+    const int nch = n_col_chunks(d);
 
     griddep_launch_dependents();
     griddep_wait();
@@ -188,47 +226,51 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const __grid_cons
         }
         s_lo = lo;
         s_hi = hi;
+        s_bad = 0;
     }
+    if (tid <= kRankBuckets)
+        s_bucket[tid] = 0;
     for (int h = tid; h < HS; h += kPlanThreads)
         keys[h] = -1;
-    for (int g = tid; g < Tc; g += kPlanThreads)
-        cnt[g] = 0;
+    for (int g = tid; g < kMaxPlanGroups; g += kPlanThreads)
+        gn[g] = 0;
     __syncthreads();
     const int lo = s_lo, hi = s_hi;
 
-    // insert the decode tokens of [t_begin, t_end)
+    // 1. hash the decode tokens of [t_begin, t_end) by adapter
     for (int i = tid; i < Tc; i += kPlanThreads) {
         const int t = a.t_begin + i;
         int slot = -1;
         const bool in_seg = t >= lo && t < hi;
         const int ad = a.idx[t];
-        // segment tokens run on the tensor cores unless their adapter's rank is too large
-        // for that path; segment errors are reported there
-        const bool mine = !in_seg || (ad >= 0 && ad < a.pv.max_adapters && a.pv.dir[ad].pt_off >= 0 &&
-                                      a.pv.dir[ad].rank > kMaxPrefillRank);
-        if (mine) {
-            if (ad >= 0 && ad < a.pv.max_adapters) {
-                const DirEntry e = a.pv.dir[ad];
-                if (e.pt_off >= 0 && e.rank > 0 && e.rank <= kMaxRank) {
+        if (ad >= 0 && ad < a.pv.max_adapters) {
+            const DirEntry e = a.pv.dir[ad];
+            const bool resident = e.pt_off >= 0 && e.rank > 0 && e.rank <= kMaxRank;
+            // segment tokens run on the tensor cores unless their adapter's rank is too
+            // large for that path; errors of segment tokens are reported there
+            const bool mine = !in_seg || (resident && e.rank > kMaxPrefillRank);
+            if (mine) {
+                if (resident) {
                     int h = (int)(((uint32_t)ad * 2654435761u) & (uint32_t)(HS - 1));
-                    for (;;) {
-                        int k = atomicCAS(&keys[h], -1, ad);
-                        if (k == -1 || k == ad) break;
+                    for (int probe = 0; probe < HS; ++probe) {
+                        const int k = atomicCAS(&keys[h], -1, ad);
+                        if (k == -1 || k == ad) { slot = h; break; }
                         h = (h + 1) & (HS - 1);
                     }
-                    slot = h;
+                    if (slot < 0) s_bad = 1;   // more distinct adapters than the table holds
                 } else {
                     set_status(a.pv.status, SLORA_DEV_NOT_RESIDENT);
                 }
-            } else if (ad != -1) {
-                set_status(a.pv.status, SLORA_DEV_BAD_ADAPTER);
             }
+        } else if (ad != -1 && !in_seg) {
+            set_status(a.pv.status, SLORA_DEV_BAD_ADAPTER);
         }
         tslot[i] = (short)slot;
     }
     __syncthreads();
 
-    // groups = occupied slots, numbered in slot order
+    // 2. groups = occupied slots, numbered in slot order; keys[h] becomes the group id;
+    //    each group's directory entry is cached and its rank bucket counted
     {
         const int per = HS / kPlanThreads;
         const int h0 = tid * per;
@@ -238,90 +280,138 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const __grid_cons
         int total;
         int base = block_excl_scan(c, warp_tot, &total);
         for (int h = h0; h < h0 + per; ++h) {
-            if (keys[h] != -1) {
-                gid[h] = base;
-                garr[base] = keys[h];
+            const int k = keys[h];
+            if (k != -1) {
+                if (base < kMaxPlanGroups) {
+                    const DirEntry e = a.pv.dir[k];
+                    gad[base] = k;
+                    grank[base] = e.rank;
+                    gscale[base] = e.scaling;
+                    gpt[base] = e.pt_off + (long long)a.proj * 2 * e.rank;
+                    atomicAdd(&s_bucket[31 - __clz(e.rank)], 1);
+                }
+                keys[h] = base;
                 ++base;
             }
         }
+        if (tid == 0 && total > kMaxPlanGroups) s_bad = 1;
         if (tid == 0) s_G = total;
     }
     __syncthreads();
+    if (s_bad) {
+        // cannot happen with the host's chunking; refuse the batch rather than overrun
+        if (tid == 0) plan_refuse(a);
+        return;
+    }
     const int G = s_G;
-    for (int i = tid; i < Tc; i += kPlanThreads)
-        if (tslot[i] >= 0)
-            atomicAdd(&cnt[gid[tslot[i]]], 1);
+    if (tid == 0) {   // bucket starts, largest ranks first
+        int acc = 0;
+        for (int b = kRankBuckets - 1; b >= 0; --b) {
+            const int n = s_bucket[b];
+            s_bucket[b] = acc;
+            acc += n;
+        }
+    }
+    for (int i = tid; i < Tc; i += kPlanThreads) {
+        const int h = tslot[i];
+        if (h >= 0) {
+            const int g = keys[h];
+            tslot[i] = (short)g;
+            atomicAdd(&gn[g], 1);
+        }
+    }
+    __syncthreads();
+    for (int g = tid; g < G; g += kPlanThreads)
+        gperm[atomicAdd(&s_bucket[31 - __clz(grank[g])], 1)] = g;
     __syncthreads();
 
-    // per-group totals: tokens, shrink items, expand items, u floats
-    const int d = a.pv.hidden;
-    const int nch = n_col_chunks(d);
-    const int per_g = ceil_div(G > 0 ? G : 1, kPlanThreads);
-    const int g0 = tid * per_g;
+    // 3. per-group offsets (tokens, shrink items, expand items, u floats), laid out in
+    //    descending-rank order so the costliest items are claimed first
+    const int per_g = ceil_div(G > 0 ? G : 1, kPlanThreads);   // <= 2
+    const int p0 = tid * per_g;
     int my_tok = 0, my_sh = 0, my_ex = 0, my_u = 0;
-    for (int g = g0; g < g0 + per_g && g < G; ++g) {
-        const int r = a.pv.dir[garr[g]].rank;
-        const int n = cnt[g];
+    for (int q = 0; q < per_g && p0 + q < G; ++q) {
+        const int g = gperm[p0 + q];
+        const int r = grank[g], n = gn[g];
         my_tok += n;
         my_sh += ceil_div(r, RS) * ceil_div(n, TS);
         my_ex += nch * ceil_div(n, TE);
-        my_u += n * r;
+        my_u += (n * r + 3) & ~3;
     }
     int tot_tok, tot_sh, tot_ex, tot_u;
     int off_tok = block_excl_scan(my_tok, warp_tot, &tot_tok);
     int off_sh = block_excl_scan(my_sh, warp_tot, &tot_sh);
     int off_ex = block_excl_scan(my_ex, warp_tot, &tot_ex);
     int off_u = block_excl_scan(my_u, warp_tot, &tot_u);
+    for (int q = 0; q < per_g && p0 + q < G; ++q) {
+        const int g = gperm[p0 + q];
+        const int r = grank[g], n = gn[g];
+        gtok[g] = off_tok;
+        gu[g] = off_u;
+        psh[p0 + q] = off_sh;
+        pex[p0 + q] = off_ex;
+        off_tok += n;
+        off_sh += ceil_div(r, RS) * ceil_div(n, TS);
+        off_ex += nch * ceil_div(n, TE);
+        off_u += (n * r + 3) & ~3;
+    }
     if (tid == 0) {
         s_nsh = tot_sh;
         s_nex = tot_ex;
     }
     __syncthreads();
-    if ((int64_t)tot_sh + tot_ex > a.L.cap_items || (int64_t)tot_u > a.L.cap_u) {
-        // cannot happen with the host's sizing; refuse the batch rather than overrun
-        if (tid == 0) {
-            set_status(a.pv.status, SLORA_DEV_BAD_SEGMENT);
-            a.L.hdr->n_groups = 0;
-            a.L.hdr->n_shrink = 0;
-            a.L.hdr->n_expand = 0;
-            a.L.hdr->claim = 0;
-        }
+    if ((int64_t)tot_sh + tot_ex > a.L.cap_items || (int64_t)tot_u + 4 > a.L.cap_u) {
+        if (tid == 0) plan_refuse(a);
         return;
     }
-    for (int g = g0; g < g0 + per_g && g < G; ++g) {
-        const int ad = garr[g];
-        const DirEntry e = a.pv.dir[ad];
-        const int r = e.rank, n = cnt[g];
-        GroupRec rec;
-        rec.adapter = ad;
-        rec.tok_begin = off_tok;
-        rec.n_tok = n;
-        rec.rank = r;
-        rec.scaling = e.scaling;
-        rec.u_off = off_u;
-        rec.pt_base = e.pt_off + (int64_t)a.proj * 2 * r;
-        a.L.groups[g] = rec;
-        a.L.done[g] = 0;
-        const int ntc_s = ceil_div(n, TS), ntc_e = ceil_div(n, TE);
-        for (int jc = 0; jc < ceil_div(r, RS); ++jc)
-            for (int tc = 0; tc < ntc_s; ++tc)
-                a.L.items[off_sh++] = Item{g, jc * RS, tc * TS, min(TS, n - tc * TS)};
-        for (int c = 0; c < nch; ++c)
-            for (int tc = 0; tc < ntc_e; ++tc)
-                a.L.items[tot_sh + off_ex++] = Item{g, c, tc * TE, min(TE, n - tc * TE)};
-        off_tok += n;
-        off_u += n * r;
+
+    // 4. items, in parallel over items: each finds its group position by binary search over
+    //    the (strictly increasing) first-item offsets
+    for (int i = tid; i < tot_sh + tot_ex; i += kPlanThreads) {
+        const bool sh = i < tot_sh;
+        const int rel = sh ? i : i - tot_sh;
+        const int *off = sh ? psh : pex;
+        int lo_p = 0, hi_p = G - 1;
+        while (lo_p < hi_p) {
+            const int mid = (lo_p + hi_p + 1) >> 1;
+            if (off[mid] <= rel) lo_p = mid; else hi_p = mid - 1;
+        }
+        const int g = gperm[lo_p];
+        const int local = rel - off[lo_p];
+        const int r = grank[g], n = gn[g];
+        Item it;
+        it.g = g;
+        it.rank = r;
+        it.tok_begin = gtok[g];
+        it.u_off = gu[g];
+        it.adapter = gad[g];
+        it.n_tok = n;
+        it.scaling = gscale[g];
+        it.pt_base = gpt[g];
+        if (sh) {
+            const int ntc = ceil_div(n, TS), jc = local / ntc, tc = local - jc * ntc;
+            it.a = jc * RS;
+            it.t0 = tc * TS;
+            it.nt = min(TS, n - tc * TS);
+        } else {
+            const int ntc = ceil_div(n, TE), c = local / ntc, tc = local - c * ntc;
+            it.a = c;
+            it.t0 = tc * TE;
+            it.nt = min(TE, n - tc * TE);
+        }
+        a.L.items[i] = it;
     }
-    __syncthreads();
-    // token placement: cnt becomes the cursor
     for (int g = tid; g < G; g += kPlanThreads)
-        cnt[g] = 0;
+        a.L.done[g] = 0;
+    __syncthreads();
+    // 5. token placement: gsh becomes the cursor
+    for (int g = tid; g < G; g += kPlanThreads)
+        gsh[g] = 0;
     __syncthreads();
     for (int i = tid; i < Tc; i += kPlanThreads) {
-        const int h = tslot[i];
-        if (h >= 0) {
-            const int g = gid[h];
-            const int pos = __ldcg(&a.L.groups[g].tok_begin) + atomicAdd(&cnt[g], 1);
+        const int g = tslot[i];
+        if (g >= 0) {
+            const int pos = gtok[g] + atomicAdd(&gsh[g], 1);
             a.L.tok_order[pos] = a.t_begin + i;
         }
     }
@@ -341,6 +431,7 @@ struct DeltaArgs {
     __half *y;
     const float *scaling;   // optional override [max_adapters]
     PlanLayout L;
+    int32_t ustride;        // u row stride in shared memory: the largest rank rounded up to 8
 };
 
 __device__ __forceinline__ void h8_to_f(const uint4 &raw, float *f)
@@ -382,179 +473,254 @@ __device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32])
     return v[0];
 }
 
-__device__ __forceinline__ int item_tiles(const GroupRec &g, bool shrink, int d)
+// acc += x.lo * a.lo, then acc += x.hi * a.hi: fp16 operands, exact widening, one fp32
+// rounding per product-add (the same value as widening both and using fmaf).
+__device__ __forceinline__ float fma_h2(uint32_t x, uint32_t a, float acc)
 {
-    return shrink ? ceil_div(d, KC) : ceil_div(g.rank, RB);
+    asm("{\n\t.reg .f16 xl, xh, al, ah;\n\tmov.b32 {xl, xh}, %1;\n\tmov.b32 {al, ah}, %2;\n\t"
+        "fma.rn.f32.f16 %0, xl, al, %0;\n\tfma.rn.f32.f16 %0, xh, ah, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(x), "r"(a));
+    return acc;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constant__ DeltaArgs a)
-{
-    extern __shared__ __align__(1024) uint8_t smem[];
-    uint8_t *stages = smem;
-    float *u_s = reinterpret_cast<float *>(smem + NS * kStageBytes);
-    float *red = u_s + TE * kMaxRank;
-    __shared__ __align__(8) uint64_t full[NS];
-    __shared__ int tile_item[NS], tile_sub[NS];
-    __shared__ int s_flag;
+// A tile is up to kSlots row segments of VC elements; every thread owns the same 16-byte
+// piece (8 elements) of each segment.  Shrink tiles: 8 A^T rows then 4 token rows;
+// expand tiles: 8 B rows.
+constexpr int kSlots = RS + TS;
 
+// acc[t][j] += x[t] . At[j] over the thread's 8 elements.  Rows past the adapter's rank
+// are never loaded; their accumulators are never published.
+template <int NT>
+__device__ __forceinline__ void shrink_tile(const uint4 (&v)[kSlots], float (&acc)[TS][RS])
+{
+#pragma unroll
+    for (int j = 0; j < RS; ++j) {
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            float s = acc[t][j];
+            s = fma_h2(v[RS + t].x, v[j].x, s);
+            s = fma_h2(v[RS + t].y, v[j].y, s);
+            s = fma_h2(v[RS + t].z, v[j].z, s);
+            s = fma_h2(v[RS + t].w, v[j].w, s);
+            acc[t][j] = s;
+        }
+    }
+}
+
+// acc[t][0..7] += u[t][j] * B[j][the thread's 8 columns], rows in order.  FULL: all 8 rows
+// exist; otherwise rows past the rank contribute exactly zero.
+template <int NT, bool FULL>
+__device__ __forceinline__ void expand_tile(const uint4 (&v)[kSlots], const float *u_s, int ustride, int j0,
+                                            int nrows, float (&acc)[TS][RS])
+{
+    float uu[NT][RB];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        if (FULL) {
+            const float4 u0 = *reinterpret_cast<const float4 *>(u_s + t * ustride + j0);
+            const float4 u1 = *reinterpret_cast<const float4 *>(u_s + t * ustride + j0 + 4);
+            uu[t][0] = u0.x; uu[t][1] = u0.y; uu[t][2] = u0.z; uu[t][3] = u0.w;
+            uu[t][4] = u1.x; uu[t][5] = u1.y; uu[t][6] = u1.z; uu[t][7] = u1.w;
+        } else {
+#pragma unroll
+            for (int j = 0; j < RB; ++j)
+                uu[t][j] = j < nrows ? u_s[t * ustride + j0 + j] : 0.f;
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < RB; ++j) {
+        float bf[8];
+        h8_to_f((FULL || j < nrows) ? v[j] : make_uint4(0, 0, 0, 0), bf);
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                acc[t][e] = fmaf(uu[t][j], bf[e], acc[t][e]);
+    }
+}
+
+// Item index of this CTA's k-th item: rounds of gridDim.x items, walked in alternating
+// direction so that the costliest items (the list is ordered by rank, descending) spread
+// evenly over the CTAs.  Every CTA's items are increasing, so all its shrink items (which
+// never wait) come before its expand items (which wait only on shrink items).
+__device__ __forceinline__ int my_item(int k)
+{
+    const int G = (int)gridDim.x, b = (int)blockIdx.x;
+    return k * G + ((k & 1) ? (G - 1 - b) : b);
+}
+
+__device__ __forceinline__ int item_pages(const Item &it, bool shrink)
+{
+    return shrink ? min(RS, it.rank - it.a) : it.rank;
+}
+
+template <bool V>
+using bool_c = std::integral_constant<bool, V>;
+template <int V>
+using int_c = std::integral_constant<int, V>;
+
+__global__ void __launch_bounds__(kDT, 2) delta_kernel(const __grid_constant__ DeltaArgs a)
+{
+    extern __shared__ __align__(16) uint8_t smem[];
+    uint4 *stg = reinterpret_cast<uint4 *>(smem);                                   // [NST][kSlots][kDT]
+    float *u_s = reinterpret_cast<float *>(smem + NST * kSlots * kDT * 16);       // [TE][ustride]
+    float *red = u_s + TE * a.ustride;                                             // [2][kDW][32]
+    Item *mit = reinterpret_cast<Item *>(red + 2 * kDW * 32);                      // [kBatchItems]
+    int *mpo = reinterpret_cast<int *>(mit + kBatchItems);                         // [kBatchItems + 1]
+    int *mpg = mpo + kBatchItems + 1;                                              // [kBatchPages]
+    int *mtk = mpg + kBatchPages;                                                  // [kBatchItems][TE]
+    __shared__ int s_nb, s_flag;
+
+    constexpr uint32_t kSlotB = kDT * 16;          // one row segment of the CTA
+    constexpr uint32_t kStageB = kSlots * kSlotB;  // one tile
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int d = a.pv.hidden;
+    const int nkt = ceil_div(d, VC);               // K tiles of a shrink item
     const __half *pool = reinterpret_cast<const __half *>(a.pv.pool);
+    const uint32_t sbase = smem_u32(stg) + (uint32_t)tid * 16;
 
-    if (tid == 0) {
-        for (int s = 0; s < NS; ++s)
-            mbar_init(&full[s], 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
     griddep_wait();   // the plan of this batch is complete and visible
     griddep_launch_dependents();
-
     const int n_sh = a.L.hdr->n_shrink;
     const int n_tot = n_sh + a.L.hdr->n_expand;
 
-    // ---- producer state (warp 0; lane 0 authoritative) ----
-    int p_item = -1, p_sub = 0, p_nsub = 0;
+    float acc[TS][RS];
+    int n_red = 0;
+    for (int k0 = 0;;) {
+        // ---- metadata of the next batch of this CTA's items, into shared memory ----
+        if (tid < kBatchItems) {
+            const int i = my_item(k0 + tid);
+            if (i < n_tot)
+                mit[tid] = a.L.items[i];
+        }
+        __syncthreads();
+        if (tid == 0) {
+            int nb = 0, np = 0;
+            while (nb < kBatchItems && my_item(k0 + nb) < n_tot) {
+                const int need = item_pages(mit[nb], my_item(k0 + nb) < n_sh);
+                if (np + need > kBatchPages) break;
+                mpo[nb] = np;
+                np += need;
+                ++nb;
+            }
+            mpo[nb] = np;
+            s_nb = nb;
+        }
+        __syncthreads();
+        const int nb = s_nb;
+        if (nb == 0)
+            break;
+        for (int q = 0; q < nb; ++q) {
+            const bool sh = my_item(k0 + q) < n_sh;
+            const Item &it = mit[q];
+            const int np = mpo[q + 1] - mpo[q];
+            const int64_t base = it.pt_base + (sh ? it.a : it.rank);
+            for (int j = tid; j < np; j += kDT) {
+                int32_t pg = a.pv.pt_arena[base + j];
+                if (pg < 0 || pg >= a.pv.num_pages) {
+                    set_status(a.pv.status, SLORA_DEV_BAD_PAGE);
+                    pg = -1;
+                }
+                mpg[mpo[q] + j] = pg;
+            }
+        }
+        for (int e = tid; e < nb * TE; e += kDT) {
+            const int q = e / TE, t = e - q * TE;
+            const Item &it = mit[q];
+            mtk[e] = t < it.nt ? a.L.tok_order[it.tok_begin + it.t0 + t] : -1;
+        }
+        __syncthreads();
 
-    auto produce = [&](int s) {
-        int item = 0, sub = 0;
-        if (lane == 0) {
-            if (p_item < 0 || (p_item < n_tot && p_sub >= p_nsub)) {
-                p_item = atomicAdd(&a.L.hdr->claim, 1);
-                if (p_item > n_tot) p_item = n_tot;
-                p_sub = 0;
-                if (p_item < n_tot) {
-                    const Item it = a.L.items[p_item];
-                    p_nsub = item_tiles(a.L.groups[it.g], p_item < n_sh, d);
-                }
-            }
-            item = p_item;
-            sub = p_sub;
-            if (p_item < n_tot) ++p_sub;
-        }
-        item = __shfl_sync(0xffffffffu, item, 0);
-        sub = __shfl_sync(0xffffffffu, sub, 0);
-        if (item >= n_tot) {
-            if (lane == 0) {
-                tile_item[s] = -1;
-                mbar_arrive(&full[s]);
-            }
-            return;
-        }
-        const Item it = a.L.items[item];
-        const GroupRec g = a.L.groups[it.g];
-        uint8_t *st = stages + s * kStageBytes;
-        const __half *src = nullptr;
-        uint32_t bytes = 0;
-        void *dst = nullptr;
-        if (item < n_sh) {
-            const int k0 = sub * KC;
-            const int kc = min(KC, d - k0);
-            const int nrows = min(RS, g.rank - it.a);
-            if (lane < nrows) {
-                const int32_t page = a.pv.pt_arena[g.pt_base + it.a + lane];
-                if (page >= 0 && page < a.pv.num_pages) {
-                    src = pool + (int64_t)page * d + k0;
-                    bytes = kc * 2;
-                    dst = st + lane * (KC * 2);
-                } else {
-                    set_status(a.pv.status, SLORA_DEV_BAD_PAGE);
-                }
-            } else if (lane >= RS && lane < RS + it.nt) {
-                const int tok = a.L.tok_order[g.tok_begin + it.t0 + (lane - RS)];
-                src = a.x + (int64_t)tok * d + k0;
-                bytes = kc * 2;
-                dst = st + lane * (KC * 2);
-            }
-        } else {
-            const int c0 = it.a * CE;
-            const int ce = min(CE, d - c0);
-            const int j0 = sub * RB;
-            const int nrows = min(RB, g.rank - j0);
-            if (lane < nrows) {
-                const int32_t page = a.pv.pt_arena[g.pt_base + g.rank + j0 + lane];
-                if (page >= 0 && page < a.pv.num_pages) {
-                    src = pool + (int64_t)page * d + c0;
-                    bytes = ce * 2;
-                    dst = st + lane * (CE * 2);
-                } else {
-                    set_status(a.pv.status, SLORA_DEV_BAD_PAGE);
-                }
-            }
-        }
-        uint32_t total = bytes;
+        // ---- copy stream: every thread copies its own 16-byte piece of each row segment
+        //      into an NST-deep ring, NST-1 tiles ahead of its arithmetic ----
+        int is_q = 0, is_sub = 0, is_ntiles = 0, is_rank = 0, is_col = 0;
+        bool is_sh = true;
+        const int *is_pg = mpg;
+        const __half *is_src[kSlots];
+        auto load_issue_item = [&]() {
+            if (is_q >= nb)
+                return;
+            const Item &it = mit[is_q];
+            is_sh = my_item(k0 + is_q) < n_sh;
+            is_pg = mpg + mpo[is_q];
+            if (is_sh) {
+                is_ntiles = nkt;
+                const int nrows = min(RS, it.rank - it.a);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            total += __shfl_xor_sync(0xffffffffu, total, o);
-        if (lane == 0) {
-            tile_item[s] = item;
-            tile_sub[s] = sub;
-            if (total > 0)
-                mbar_arrive_expect_tx(&full[s], total);
-            else
-                mbar_arrive(&full[s]);
-        }
-        __syncwarp();
-        if (bytes > 0)
-            bulk_g2s(dst, src, bytes, &full[s]);
-    };
+                for (int j = 0; j < RS; ++j)
+                    is_src[j] = (j < nrows && is_pg[j] >= 0) ? pool + (int64_t)is_pg[j] * d + 8 * tid : nullptr;
+#pragma unroll
+                for (int t = 0; t < TS; ++t)
+                    is_src[RS + t] = t < it.nt ? a.x + (int64_t)mtk[is_q * TE + t] * d + 8 * tid : nullptr;
+            } else {
+                is_ntiles = ceil_div(it.rank, RB);
+                is_rank = it.rank;
+                is_col = it.a * VC + 8 * tid;
+            }
+        };
+        auto issue_tile = [&](int stage) {
+            if (is_q < nb) {
+                const uint32_t sd = sbase + (uint32_t)stage * kStageB;
+                if (is_sh) {
+                    const int off = is_sub * VC;
+                    if (off + 8 * tid < d) {
+#pragma unroll
+                        for (int j = 0; j < kSlots; ++j)
+                            if (is_src[j])
+                                cp_async16_s(sd + j * kSlotB, is_src[j] + off);
+                    }
+                } else if (is_col < d) {
+                    const int j0 = is_sub * RB;
+#pragma unroll
+                    for (int j = 0; j < RB; ++j)
+                        if (j0 + j < is_rank && is_pg[j0 + j] >= 0)
+                            cp_async16_s(sd + j * kSlotB, pool + (int64_t)is_pg[j0 + j] * d + is_col);
+                }
+                if (++is_sub == is_ntiles) {
+                    is_sub = 0;
+                    ++is_q;
+                    load_issue_item();
+                }
+            }
+            cp_async_commit();   // one group per tile, possibly empty
+        };
+        load_issue_item();
+#pragma unroll 1
+        for (int p = 0; p < NST - 1; ++p)
+            issue_tile(p);
 
-    if (warp == 0)
-        for (int s = 0; s < NS; ++s)
-            produce(s);
-
-    float acc[TS][RS];   // shrink: [token][row]; expand: [token][column of the vector]
-    uint4 yv[TE];
-    int cur_item = -1;
-    GroupRec cg;
-    Item cit;
-    bool ok = true;
-    int c = 0;
-    bool timed_out = false;
-
-    for (;; ++c) {
-        const int s = c % NS;
-        const uint32_t parity = (uint32_t)(c / NS) & 1u;
-        if (!mbar_wait_bounded(&full[s], parity, a.pv.status)) {
-            timed_out = true;
-            break;
-        }
-        const int item = tile_item[s];
-        const int sub = tile_sub[s];
-        if (item < 0)
-            break;
-        const uint8_t *st = stages + s * kStageBytes;
-        const bool shrink = item < n_sh;
-        if (item != cur_item) {
-            // ---- item start ----
-            cur_item = item;
-            cit = a.L.items[item];
-            cg = a.L.groups[cit.g];
+        int ct = 0;   // tiles consumed in this batch
+        // One item's tiles, with the item kind and token count fixed at compile time.
+        auto run_item = [&](int q, auto sh_c, auto nt_c) {
+            constexpr bool SH = decltype(sh_c)::value;
+            constexpr int NT = decltype(nt_c)::value;
+            const Item it = mit[q];
+            const int ntiles = SH ? nkt : ceil_div(it.rank, RB);
+            const int col = it.a * VC + 8 * tid;
 #pragma unroll
             for (int t = 0; t < TS; ++t)
 #pragma unroll
                 for (int j = 0; j < RS; ++j)
                     acc[t][j] = 0.f;
-            ok = true;
-            if (!shrink) {
-                const int c0 = cit.a * CE;
-                const bool active = c0 + 8 * tid < d;
+            uint4 yv[NT];
+            bool ok = true;
+            if (!SH) {
+                if (col < d) {
 #pragma unroll
-                for (int t = 0; t < TE; ++t) {
-                    if (t < cit.nt && active) {
-                        const int tok = a.L.tok_order[cg.tok_begin + cit.t0 + t];
-                        yv[t] = *reinterpret_cast<const uint4 *>(a.y + (int64_t)tok * d + c0 + 8 * tid);
-                    }
+                    for (int t = 0; t < NT; ++t)
+                        yv[t] = *reinterpret_cast<const uint4 *>(a.y + (int64_t)mtk[q * TE + t] * d + col);
                 }
-                // wait until every shrink item of the group has published its u values
+                __syncthreads();   // every thread is done with the previous item's u_s
                 if (tid == 0) {
-                    const int need = ceil_div(cg.rank, RS) * ceil_div(cg.n_tok, TS);
+                    // every shrink item of the group has published its u values?
+                    const int need = 32 * ceil_div(it.rank, RS) * ceil_div(it.n_tok, TS);
                     int flag = 1;
-                    if (ld_acquire_gpu(&a.L.done[cit.g]) < need) {
+                    if (ld_acquire_gpu(&a.L.done[it.g]) < need) {
                         const uint64_t t0 = global_timer_ns();
                         for (;;) {
-                            __nanosleep(64);
-                            if (ld_acquire_gpu(&a.L.done[cit.g]) >= need) break;
+                            __nanosleep(32);
+                            if (ld_acquire_gpu(&a.L.done[it.g]) >= need) break;
                             if (global_timer_ns() - t0 > kWaitLimitNs) {
                                 set_status(a.pv.status, SLORA_DEV_TIMEOUT);
                                 flag = 0;
@@ -566,134 +732,121 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
                 }
                 __syncthreads();
                 ok = s_flag != 0;
-                const int r = cg.rank;
-                const int nu = cit.nt * r;
-                const float *ug = a.L.u + cg.u_off + (int64_t)cit.t0 * r;
-                for (int i = tid; i < nu; i += kThreads)
-                    u_s[i] = __ldcg(ug + i);
+                const int r = it.rank;
+                const float *ug = a.L.u + it.u_off + (int64_t)it.t0 * r;
+                for (int e = tid; e < NT * r; e += kDT) {
+                    const int t = e / r, j = e - t * r;
+                    u_s[t * a.ustride + j] = __ldcg(ug + e);
+                }
                 __syncthreads();
             }
-        }
-        // ---- tile compute ----
-        if (shrink) {
-            const int k0 = sub * KC;
-            const int nrows = min(RS, cg.rank - cit.a);
-            if (k0 + 8 * tid < d) {
-                float xf[TS][8];
+#pragma unroll 1
+            for (int sub = 0; sub < ntiles; ++sub) {
+                issue_tile((ct + NST - 1) % NST);
+                cp_async_wait<NST - 1>();   // this thread's copies of tile ct have landed
+                const uint4 *slot = stg + (ct % NST) * (kSlots * kDT) + tid;
+                if (SH) {
+                    if (sub * VC + 8 * tid < d) {
+                        uint4 v[kSlots];
 #pragma unroll
-                for (int t = 0; t < TS; ++t)
-                    if (t < cit.nt)
-                        h8_to_f(lds128(st + (RS + t) * (KC * 2) + 16 * tid), xf[t]);
+                        for (int i = 0; i < RS + NT; ++i)
+                            v[i] = slot[i * kDT];
+                        shrink_tile<NT>(v, acc);
+                    }
+                } else if (col < d) {
+                    const int j0 = sub * RB;
+                    const int nrows = min(RB, it.rank - j0);
+                    uint4 v[kSlots];
+                    if (nrows == RB) {
 #pragma unroll
-                for (int j = 0; j < RS; ++j) {
-                    if (j < nrows) {
-                        float af[8];
-                        h8_to_f(lds128(st + j * (KC * 2) + 16 * tid), af);
+                        for (int i = 0; i < RB; ++i)
+                            v[i] = slot[i * kDT];
+                        expand_tile<NT, true>(v, u_s, a.ustride, j0, nrows, acc);
+                    } else {
 #pragma unroll
-                        for (int t = 0; t < TS; ++t) {
-                            if (t < cit.nt) {
-                                float v = acc[t][j];
-#pragma unroll
-                                for (int e = 0; e < 8; ++e)
-                                    v = fmaf(xf[t][e], af[e], v);
-                                acc[t][j] = v;
-                            }
-                        }
+                        for (int i = 0; i < RB; ++i)
+                            v[i] = i < nrows ? slot[i * kDT] : make_uint4(0, 0, 0, 0);
+                        expand_tile<NT, false>(v, u_s, a.ustride, j0, nrows, acc);
                     }
                 }
+                ++ct;
             }
-        } else {
-            const int c0 = cit.a * CE;
-            const int j0 = sub * RB;
-            const int nrows = min(RB, cg.rank - j0);
-            const int r = cg.rank;
-            if (c0 + 8 * tid < d) {
-#pragma unroll
-                for (int j = 0; j < RB; ++j) {
-                    if (j < nrows) {
-                        float bf[8];
-                        h8_to_f(lds128(st + j * (CE * 2) + 16 * tid), bf);
-#pragma unroll
-                        for (int t = 0; t < TE; ++t) {
-                            if (t < cit.nt) {
-                                const float uu = u_s[t * r + j0 + j];
-#pragma unroll
-                                for (int e = 0; e < 8; ++e)
-                                    acc[t][e] = fmaf(uu, bf[e], acc[t][e]);
-                            }
-                        }
-                    }
-                }
-            }
-        }
-        const bool last = sub == item_tiles(cg, shrink, d) - 1;
-        if (last) {
-            if (shrink) {
+            if (SH) {
                 // ---- reduce the 32 partials over the CTA, publish u ----
-                float v[32];
+                float vv[32];
 #pragma unroll
                 for (int t = 0; t < TS; ++t)
 #pragma unroll
                     for (int j = 0; j < RS; ++j)
-                        v[t * RS + j] = acc[t][j];
-                const float ws = warp_reduce_scatter32(v);
-                red[warp * 32 + lane] = ws;
+                        vv[t * RS + j] = acc[t][j];
+                const float ws = warp_reduce_scatter32(vv);
+                float *rb = red + (n_red & 1) * (kDW * 32);
+                ++n_red;
+                rb[warp * 32 + lane] = ws;
                 __syncthreads();
                 if (tid < 32) {
                     float tot = 0.f;
 #pragma unroll
-                    for (int w = 0; w < kWarps; ++w)
-                        tot += red[w * 32 + tid];
+                    for (int w = 0; w < kDW; ++w)
+                        tot += rb[w * 32 + tid];
                     const int t = tid / RS, j = tid % RS;
-                    if (t < cit.nt && cit.a + j < cg.rank)
-                        __stcg(a.L.u + cg.u_off + (int64_t)(cit.t0 + t) * cg.rank + cit.a + j, tot);
+                    if (t < it.nt && it.a + j < it.rank)
+                        __stcg(a.L.u + it.u_off + (int64_t)(it.t0 + t) * it.rank + it.a + j, tot);
+                    red_release_add1(&a.L.done[it.g]);   // 32 per shrink item
                 }
-                __syncthreads();
-                if (tid == 0) {
-                    __threadfence();
-                    atomicAdd(&a.L.done[cit.g], 1);
+            } else if (ok && col < d) {
+                const float sc = a.scaling ? a.scaling[it.adapter] : it.scaling;
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    float y0f[8], out[8];
+                    h8_to_f(yv[t], y0f);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        out[e] = fmaf(sc, acc[t][e], y0f[e]);
+                    *reinterpret_cast<uint4 *>(a.y + (int64_t)mtk[q * TE + t] * d + col) = f_to_h8(out);
                 }
-            } else if (ok) {
-                const int c0 = cit.a * CE;
-                if (c0 + 8 * tid < d) {
-                    const float sc = a.scaling ? a.scaling[cg.adapter] : cg.scaling;
-#pragma unroll
-                    for (int t = 0; t < TE; ++t) {
-                        if (t < cit.nt) {
-                            const int tok = a.L.tok_order[cg.tok_begin + cit.t0 + t];
-                            float y0f[8], out[8];
-                            h8_to_f(yv[t], y0f);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                out[e] = fmaf(sc, acc[t][e], y0f[e]);
-                            *reinterpret_cast<uint4 *>(a.y + (int64_t)tok * d + c0 + 8 * tid) = f_to_h8(out);
-                        }
-                    }
+            }
+        };
+        for (int q = 0; q < nb; ++q) {
+            const bool sh = my_item(k0 + q) < n_sh;
+            const int nt = mit[q].nt;
+            if (sh) {
+                switch (nt) {
+                case 1: run_item(q, bool_c<true>(), int_c<1>()); break;
+                case 2: run_item(q, bool_c<true>(), int_c<2>()); break;
+                case 3: run_item(q, bool_c<true>(), int_c<3>()); break;
+                default: run_item(q, bool_c<true>(), int_c<4>()); break;
+                }
+            } else {
+                switch (nt) {
+                case 1: run_item(q, bool_c<false>(), int_c<1>()); break;
+                case 2: run_item(q, bool_c<false>(), int_c<2>()); break;
+                case 3: run_item(q, bool_c<false>(), int_c<3>()); break;
+                default: run_item(q, bool_c<false>(), int_c<4>()); break;
                 }
             }
         }
-        __syncthreads();   // stage s and the item scratch are free
-        if (warp == 0)
-            produce(s);
-    }
-    if (timed_out) {
-        // Copies of this CTA may still be in flight into the stages ahead: wait for each
-        // (bounded) before the CTA's shared memory is released.
-        for (int k = 1; k < NS; ++k) {
-            const int cc = c + k;
-            mbar_wait_bounded(&full[cc % NS], (uint32_t)(cc / NS) & 1u, a.pv.status);
-        }
+        cp_async_wait<0>();
+        __syncthreads();   // the batch's metadata is about to be replaced
+        k0 += nb;
     }
 }
 
 }  // namespace
 
-size_t plan_scratch_bytes(int32_t T, int32_t max_rank, int32_t hidden)
+size_t plan_scratch_bytes(int32_t T, int32_t max_rank, int32_t hidden, int32_t max_adapters)
 {
     size_t total = 0;
-    const int32_t cap = T < kMaxPlanTokens ? T : kMaxPlanTokens;
+    const int32_t chunk = plan_chunk(max_adapters);
+    const int32_t cap = T < chunk ? T : chunk;
     carve(nullptr, cap, max_rank, hidden, &total);
     return total;
+}
+
+inline size_t delta_smem_bytes(int ustride)
+{
+    return (size_t)NST * kSlots * kDT * 16 + (size_t)TE * ustride * 4 + 2 * kDW * 32 * 4 +
+           kBatchItems * sizeof(Item) + (kBatchItems + 1) * 4 + kBatchPages * 4 + kBatchItems * TE * 4;
 }
 
 cudaError_t launch_lora_apply(const PoolView &pv, int32_t proj, const uint16_t *x, uint16_t *y,
@@ -702,30 +855,43 @@ cudaError_t launch_lora_apply(const PoolView &pv, int32_t proj, const uint16_t *
                               int num_sms, cudaStream_t stream, int *launches)
 {
     static bool attrs_set = false;
+    static int occ_ustride = -1, occ_blocks = 1;
     if (!attrs_set) {
-        cudaError_t e = cudaFuncSetAttribute(delta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(delta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)delta_smem_bytes(kMaxRank));
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (2 * kMaxHash + 2 * kMaxPlanTokens) * 4 + kMaxPlanTokens * 2);
+                                 (int)plan_smem_bytes(kMaxHash));
         if (e != cudaSuccess) return e;
         attrs_set = true;
     }
-    const int32_t cap = scratch.cap_tokens < kMaxPlanTokens ? scratch.cap_tokens : kMaxPlanTokens;
+    const int ustride = (scratch.max_rank + 7) & ~7;
+    const size_t dsmem = delta_smem_bytes(ustride);
+    if (ustride != occ_ustride) {
+        int nb = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, delta_kernel, kDT, dsmem);
+        if (e != cudaSuccess) return e;
+        occ_blocks = nb > 0 ? nb : 1;
+        occ_ustride = ustride;
+    }
+    const int32_t chunk = plan_chunk(pv.max_adapters);
+    const int32_t cap = scratch.cap_tokens < chunk ? scratch.cap_tokens : chunk;
     PlanLayout L = carve(scratch.base, cap, scratch.max_rank, pv.hidden, nullptr);
 
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
 
-    for (int32_t tb = 0; tb < T; tb += kMaxPlanTokens) {
-        const int32_t te = tb + kMaxPlanTokens < T ? tb + kMaxPlanTokens : T;
+    for (int32_t tb = 0; tb < T; tb += chunk) {
+        const int32_t te = tb + chunk < T ? tb + chunk : T;
+        const int32_t groups = (te - tb) < pv.max_adapters ? (te - tb) : pv.max_adapters;
         int hs = 1024;
-        while (hs < 2 * (te - tb)) hs <<= 1;
+        while (hs < 2 * groups && hs < kMaxHash) hs <<= 1;
         PlanArgs pa{pv, proj, idx, T, seg_indptr, n_seg, tb, te, hs, L};
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(1);
         cfg.blockDim = dim3(kPlanThreads);
-        cfg.dynamicSmemBytes = (size_t)(2 * hs + 2 * kMaxPlanTokens) * 4 + kMaxPlanTokens * 2;
+        cfg.dynamicSmemBytes = plan_smem_bytes(hs);
         cfg.stream = stream;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
@@ -733,11 +899,11 @@ cudaError_t launch_lora_apply(const PoolView &pv, int32_t proj, const uint16_t *
         if (e != cudaSuccess) return e;
         *launches += 1;
 
-        DeltaArgs da{pv, reinterpret_cast<const __half *>(x), reinterpret_cast<__half *>(y), scaling, L};
+        DeltaArgs da{pv, reinterpret_cast<const __half *>(x), reinterpret_cast<__half *>(y), scaling, L, ustride};
         cudaLaunchConfig_t cfg2 = {};
-        cfg2.gridDim = dim3(num_sms);
-        cfg2.blockDim = dim3(kThreads);
-        cfg2.dynamicSmemBytes = kSmemBytes;
+        cfg2.gridDim = dim3(num_sms * occ_blocks);
+        cfg2.blockDim = dim3(kDT);
+        cfg2.dynamicSmemBytes = dsmem;
         cfg2.stream = stream;
         cfg2.attrs = attr;
         cfg2.numAttrs = 1;

@@ -73,7 +73,7 @@ struct PlanScratch {
     int32_t cap_tokens = 0;   // tokens the layout was carved for
     int32_t max_rank = 0;     // largest adapter rank the layout was carved for
 };
-size_t plan_scratch_bytes(int32_t T, int32_t max_rank, int32_t hidden);
+size_t plan_scratch_bytes(int32_t T, int32_t max_rank, int32_t hidden, int32_t max_adapters);
 
 // Segments whose adapter rank is at most this run on the tensor cores (prefill.cu);
 // larger ranks take the decode path.  At most kMaxSegments segments per call.

@@ -77,7 +77,7 @@ extern "C" slora_status slora_lora_apply_noalloc(slora_pool_t pool, int32_t proj
         return fail(SLORA_ERR_INVALID_ARG, "lora_apply_noalloc: n_seg=%d (at most min(T, %d))", n_seg,
                     kMaxSegments);
     const int32_t max_rank = hp.max_rank > 0 ? hp.max_rank : 1;
-    const size_t need = plan_scratch_bytes(T, max_rank, hp.pv.hidden);
+    const size_t need = plan_scratch_bytes(T, max_rank, hp.pv.hidden, hp.pv.max_adapters);
     if (need > kNoAllocScratchBytes)
         return fail(SLORA_ERR_UNSUPPORTED,
                     "lora_apply_noalloc: this batch needs %zu bytes of plan scratch (T=%d, largest registered "

@@ -563,7 +563,7 @@ slora_status slora_lora_apply(slora_pool_t p, int32_t proj, const void *x, void 
     const int32_t want_rank = std::max(p->max_rank, 1);
     if (T > p->plan.cap_tokens || want_rank > p->plan.max_rank) {
         int32_t cap = std::max(T, std::max(p->plan.cap_tokens, 256));
-        size_t bytes = plan_scratch_bytes(cap, want_rank, p->hidden);
+        size_t bytes = plan_scratch_bytes(cap, want_rank, p->hidden, p->max_adapters);
         CUDA_TRY(cudaDeviceSynchronize());
         if (p->plan.base)
             cudaFree(p->plan.base);

@@ -106,10 +106,46 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
                  : "memory");
 }
 
+// Order this thread's earlier generic-proxy accesses (e.g. an acquire of data that other
+// threads wrote with plain stores) before its later async-proxy (bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// ---- cp.async (16 bytes, zero-fill when src_bytes == 0) --------------------------------
+__device__ __forceinline__ void cp_async16(void *dst_smem, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst_smem)), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+// Same, with the destination given as a shared-memory address.
+__device__ __forceinline__ void cp_async16_s(uint32_t dst_smem, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // ---- loads ----------------------------------------------------------------------------
 __device__ __forceinline__ uint4 lds128(const void *p)
 {
     return *reinterpret_cast<const uint4 *>(p);
+}
+
+// Add 1 with release semantics at GPU scope: this thread's earlier writes become visible
+// to a thread that later observes the sum with an acquire load.
+__device__ __forceinline__ void red_release_add1(int32_t *p)
+{
+    asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(p) : "memory");
 }
 
 __device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t *p)

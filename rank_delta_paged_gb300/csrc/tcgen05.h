@@ -102,21 +102,4 @@ __device__ __forceinline__ void ld_wait()
 
 }  // namespace tc
 
-// ---- cp.async (16 bytes, zero-fill when src_bytes == 0) --------------------------------
-__device__ __forceinline__ void cp_async16(void *dst_smem, const void *src, uint32_t src_bytes)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst_smem)), "l"(src),
-                 "r"(src_bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit()
-{
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait()
-{
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 }  // namespace slora
