@@ -205,6 +205,7 @@ def main():
     import torch.distributed as dist
     import rank_delta_paged_gb300 as rdp
     from rank_delta_paged_gb300.harness import PoolSession
+    from rank_delta_paged_gb300.replicas import job_totals, replica_seed, tokens_per_s_per_layer
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -219,7 +220,7 @@ def main():
         if world > 1:
             dist.barrier()
 
-    w = W.by_name(args.workload, seed=args.seed + rank)
+    w = W.by_name(args.workload, seed=replica_seed(args.seed, rank))
     used = w.used_adapters()
     sess = PoolSession(w, device=local)
     stream = torch.cuda.current_stream()
@@ -274,15 +275,9 @@ def main():
     barrier()
     launches = rdp.slora_pool_launch_count(sess.pool) - launches0
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = float(sum(step_ms))
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    tok = torch.tensor([float(w.T)], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dist.all_reduce(tok, op=dist.ReduceOp.SUM)
-    total_ms = float(t.item())
+    total_ms, job_tokens = job_totals(float(sum(step_ms)), float(w.T), dev, world)
     ms_per_step = total_ms / K
-    value = float(tok.item()) * w.n_layers / (ms_per_step / 1e3)
+    value = tokens_per_s_per_layer(job_tokens, w.n_layers, ms_per_step)
 
     # dominant kernel roofline: the delta kernels are the whole step
     hbm, peak_kind = peaks()
@@ -318,11 +313,8 @@ def main():
         torch.cuda.synchronize()
         if k >= 2:
             e2e_ms.append(1e3 * (time.perf_counter() - t0))
-    e2e_t = torch.tensor([statistics.mean(e2e_ms) if e2e_ms else float("nan")], dtype=torch.float64,
-                         device=dev)
-    if world > 1:
-        dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
-    e2e_value = float(tok.item()) * w.n_layers / (float(e2e_t.item()) / 1e3)
+    e2e_job_ms, _ = job_totals(statistics.mean(e2e_ms) if e2e_ms else float("nan"), float(w.T), dev, world)
+    e2e_value = tokens_per_s_per_layer(job_tokens, w.n_layers, e2e_job_ms)
     status = sess.device_status()
     if status != 0:
         print(f"device status {status} after the run", file=sys.stderr)

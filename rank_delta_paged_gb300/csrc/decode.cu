@@ -158,6 +158,38 @@ __device__ __forceinline__ int block_excl_scan(int v, int *warp_tot, int *total)
     return r;
 }
 
+// Four exclusive scans at once (one set of barriers).  wt: shared int4[33].
+__device__ __forceinline__ int4 block_excl_scan4(int4 v, int4 *wt, int4 *total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int4 incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int nx = __shfl_up_sync(0xffffffffu, incl.x, o), ny = __shfl_up_sync(0xffffffffu, incl.y, o);
+        const int nz = __shfl_up_sync(0xffffffffu, incl.z, o), nw = __shfl_up_sync(0xffffffffu, incl.w, o);
+        if (lane >= o) { incl.x += nx; incl.y += ny; incl.z += nz; incl.w += nw; }
+    }
+    if (lane == 31) wt[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int4 w = (lane < (int)(blockDim.x >> 5)) ? wt[lane] : make_int4(0, 0, 0, 0);
+        int4 wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int nx = __shfl_up_sync(0xffffffffu, wi.x, o), ny = __shfl_up_sync(0xffffffffu, wi.y, o);
+            const int nz = __shfl_up_sync(0xffffffffu, wi.z, o), nw = __shfl_up_sync(0xffffffffu, wi.w, o);
+            if (lane >= o) { wi.x += nx; wi.y += ny; wi.z += nz; wi.w += nw; }
+        }
+        wt[lane] = make_int4(wi.x - w.x, wi.y - w.y, wi.z - w.z, wi.w - w.w);
+        if (lane == 31) wt[32] = wi;
+    }
+    __syncthreads();
+    const int4 b = wt[warp];
+    *total = wt[32];
+    __syncthreads();
+    return make_int4(b.x + incl.x - v.x, b.y + incl.y - v.y, b.z + incl.z - v.z, b.w + incl.w - v.w);
+}
+
 struct PlanArgs {
     PoolView pv;
     int32_t proj;
@@ -205,6 +237,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const __grid_cons
     int *gperm = reinterpret_cast<int *>(gscale + kMaxPlanGroups);       // [position] group, by rank descending
     long long *gpt = reinterpret_cast<long long *>(gperm + kMaxPlanGroups);  // [G] page-table offset
     __shared__ int warp_tot[33];
+    __shared__ int4 warp_tot4[33];
     __shared__ int s_lo, s_hi, s_G, s_nsh, s_nex, s_bad;
     __shared__ int s_bucket[kRankBuckets + 1];
     const int tid = threadIdx.x;
@@ -338,11 +371,10 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const __grid_cons
         my_ex += nch * ceil_div(n, TE);
         my_u += (n * r + 3) & ~3;
     }
-    int tot_tok, tot_sh, tot_ex, tot_u;
-    int off_tok = block_excl_scan(my_tok, warp_tot, &tot_tok);
-    int off_sh = block_excl_scan(my_sh, warp_tot, &tot_sh);
-    int off_ex = block_excl_scan(my_ex, warp_tot, &tot_ex);
-    int off_u = block_excl_scan(my_u, warp_tot, &tot_u);
+    int4 tot4;
+    const int4 off4 = block_excl_scan4(make_int4(my_tok, my_sh, my_ex, my_u), warp_tot4, &tot4);
+    int off_tok = off4.x, off_sh = off4.y, off_ex = off4.z, off_u = off4.w;
+    const int tot_sh = tot4.y, tot_ex = tot4.z, tot_u = tot4.w;
     for (int q = 0; q < per_g && p0 + q < G; ++q) {
         const int g = gperm[p0 + q];
         const int r = grank[g], n = gn[g];
@@ -399,7 +431,11 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const __grid_cons
             it.t0 = tc * TE;
             it.nt = min(TE, n - tc * TE);
         }
-        a.L.items[i] = it;
+        const uint4 *src4 = reinterpret_cast<const uint4 *>(&it);
+        uint4 *dst4 = reinterpret_cast<uint4 *>(a.L.items + i);
+        dst4[0] = src4[0];
+        dst4[1] = src4[1];
+        dst4[2] = src4[2];
     }
     for (int g = tid; g < G; g += kPlanThreads)
         a.L.done[g] = 0;
