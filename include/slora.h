@@ -104,7 +104,8 @@ slora_status slora_pagealloc_num_free(slora_pagealloc_t a, int64_t *out);
 /* ---------------------------------------------------------------------------
  * Pool.
  *   device        CUDA device ordinal (must be compute capability 10.3)
- *   hidden        row length; a multiple of 64, 64 <= hidden <= 16384
+ *   hidden        row length; a multiple of 64, 64 <= hidden <= 8192 (the decode kernel
+ *                 splits a row over a cluster of at most 8 CTAs of 1024 elements each)
  *   num_pages     pool slots, 1 <= num_pages < 2^31; pool bytes = num_pages * hidden * 2
  *   n_proj        projections per adapter (e.g. layers x {q,k,v,o}); >= 1
  *   max_adapters  adapter ids are 0 .. max_adapters-1
@@ -208,13 +209,13 @@ slora_status slora_lora_apply(slora_pool_t pool, int32_t proj, const void *x, vo
  * own plan scratch is allocated on first use and re-allocated when a larger batch or a
  * larger registered rank arrives).
  *
- * Scratch: one fixed 8 MiB device array inside the library, which every GPU that loads
+ * Scratch: one fixed 512 KiB device array inside the library, which every GPU that loads
  * the library holds until the process exits.  The call allocates and frees nothing.
  * Limit: the token plan of the call must fit that array; it needs about
- *   T' * (8 + 48 * (ceil(R / 8) + ceil(hidden / 2048)) + 4 * (R + 4)) bytes,
- * with R the largest rank registered in the pool and T' = min(T, 16384) when
- * max_adapters <= 2048, else min(T, 2048) (about 0.7 MiB for T' = 512, R = 128,
- * hidden = 4096; about 5.4 MiB for T' = 4096).  A call beyond it returns
+ *   T' * 36 + 512 bytes
+ * (a token's slot in the token order and up to one 32-byte work item per token), with
+ * T' = min(T, 16384) when max_adapters <= 2048, else min(T, 2048): a batch of up to about
+ * 14,500 decode tokens fits.  A call beyond it returns
  * SLORA_ERR_UNSUPPORTED with the sizes in slora_last_error() and launches nothing.
  * The first call on a device looks up the array's device address (once per device,
  * with that device current); make that first call before any stream capture.

@@ -11,90 +11,78 @@
 // Two kernels per batch (chained with programmatic dependent launch):
 //
 //   plan_kernel (one CTA): groups the decode tokens by adapter in a shared-memory hash
-//     table and writes the work list: shrink items (adapter, 8 rank rows, <= 4 tokens)
-//     first, then expand items (adapter, 1024 output columns, <= 4 tokens), each list in
-//     descending rank.  Each item carries its group's fields.
+//     table (caching each adapter's directory entry in its slot) and writes the work
+//     list: one item per adapter and chunk of up to 16 of its tokens, in descending rank.
 //
-//   delta_kernel (persistent, 128 threads, two CTAs per SM when ranks are at most 128):
-//     each CTA takes a fixed subset of the items (rounds over the list in alternating
-//     direction), loads their descriptors, page indices and token ids into shared memory,
-//     then streams their page rows with cp.async: every thread copies its own 16-byte piece
-//     of each row segment into a 4-deep per-thread ring, 3 tiles ahead of its arithmetic,
-//     so no barrier guards the ring.  The threads compute
-//       shrink  u[t][j] = sum_k x[t][k] * At[j][k]     (A^T rows + x rows per 1024-element
-//               K tile; fp32 partials per thread, one butterfly reduce-scatter per warp,
-//               written to a small fp32 scratch, published with release increments of the
-//               group's counter)
-//       expand  y[t][c] = y0[t][c] + s * sum_j u[t][j] * B[j][c]
-//               (8 B row segments per tile; waits, with a time limit, until every shrink
-//               item of its group has been published)
-//     Each used adapter page row is read from HBM once per token chunk of its group (the
-//     repeats of hot adapters hit L2).  Ranks 1..1024 run in the same launch: the last
-//     rank chunk of an adapter simply has fewer rows; nothing in the pool is padded.
+//   delta_kernel: persistent clusters of C = ceil(hidden / 1024) CTAs; a cluster takes
+//     whole items, and CTA c of the cluster owns slice c of the hidden dimension (at most
+//     1024 elements): the K range of the shrink and the output columns of the expand.
+//     Per item and per chunk of 128 rank rows:
+//       shrink  partial u[t][j] = sum over the CTA's K slice of x[t][k] * At[j][k]
+//       reduce  every CTA sums the C partials (read from the cluster's shared memory, in
+//               CTA order) and rounds u to fp16 once
+//       expand  acc[t][c] += sum_j u[t][j] * B[j][c] over the CTA's columns
+//     then y[t][c] = y0[t][c] + s * acc[t][c].  One producer warp streams the row slices
+//     (A^T rows, B rows, the tokens' x and y0 rows) with 1-D bulk copies into a ring of
+//     16-row stages; eight consumer warps contract them on the tensor cores with
+//     warp-level mma.sync m16n8k16 (fp16 operands, fp32 accumulators; tokens on M).
+//     Each page row is read once per item; the cluster exchanges only the small fp32
+//     partials.  Every wait is bounded in time.
 //
-// Per-token arithmetic is fixed by the thread layout (which K elements a thread sums,
-// the butterfly order, the row order of the expand), never by how tokens are grouped,
-// so results do not depend on the batch, its order, or the physical pages.
-#include <type_traits>
-
+// A token's arithmetic is fixed by the fragment layout, the slice boundaries and the CTA
+// order of the partial sum, never by the other tokens of its item, so results do not
+// depend on the batch, its order, or the physical pages.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "internal.h"
 #include "ptx.h"
+#include "tcgen05.h"
 
 namespace slora {
 namespace {
 
-constexpr int kDT = 128;                 // threads of the delta kernel
-constexpr int kDW = kDT / 32;            // its warps
-constexpr int RS = 8;       // A^T rows per shrink item
-constexpr int TS = 4;       // tokens per shrink item
-constexpr int TE = 4;       // tokens per expand item
-constexpr int RB = 8;       // B rows per expand tile
-constexpr int VC = 8 * kDT; // elements of a row segment: K per shrink tile, columns per expand item
-constexpr int NST = 4;      // depth of each thread's cp.async ring (tiles)
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = 32 * kConsumerWarps;   // consumer threads
+constexpr int kThreads = kConsumers + 64;         // plus a producer warp and a signal warp
+constexpr int kTok = 16;                          // tokens per item: the MMA's M
+constexpr int kMaxSlice = 1024;                   // elements of hidden per CTA
+constexpr int kMaxCluster = 8;
+constexpr int kRC = 128;                          // rank rows per rank chunk
+constexpr int NST = 4;                            // ring depth (16-row stages)
+constexpr int kUPitch = kRC + 8;                  // halves per token row of the u buffer
 constexpr int kMaxRank = 1024;
-constexpr int kBatchItems = 32;          // item metadata a CTA holds at once
-constexpr int kBatchPages = 2048;        // page indices a CTA holds at once
 
 constexpr int kPlanThreads = 1024;
 constexpr int kMaxPlanTokens = 16384;   // token-index range per plan when groups fit
 constexpr int kMaxPlanGroups = 2048;    // distinct adapters per plan
 constexpr int kMaxHash = 2 * kMaxPlanGroups;
 
-static_assert(RS * TS == 32, "shrink item partials = one value per lane after the butterfly");
-static_assert(RB <= RS + TS, "expand rows fit the tile slots");
-static_assert(kBatchPages >= kMaxRank, "one expand item's pages always fit a batch");
+static_assert(kRC / 16 <= kConsumerWarps, "one shrink block per consumer warp and rank chunk");
 
 struct PlanHeader {
-    int32_t n_groups, n_shrink, n_expand, claim;
-    int32_t seg_lo, seg_hi, pad0, pad1;
+    int32_t n_groups, n_items, pad0, pad1;
+    int32_t seg_lo, seg_hi, pad2, pad3;
 };
-// One work item, with the fields of its group copied in.
+// One work item: an adapter and up to kTok of its tokens, with the group's fields.
 struct alignas(16) Item {
-    int32_t g, a, t0, nt;           // group, first rank row (shrink) or column chunk (expand), tokens
-    int32_t rank, tok_begin, u_off, adapter;
-    int32_t n_tok;
+    int32_t t0, nt;     // first token (position within the group), tokens (<= kTok)
+    int32_t rank;
+    int32_t tok_begin;  // the group's first position in tok_order
+    int32_t adapter;
     float scaling;
-    int64_t pt_base;                // arena index of this projection's page table
+    int64_t pt_base;    // arena index of this projection's page table
 };
-static_assert(sizeof(Item) == 48, "Item layout");
+static_assert(sizeof(Item) == 32, "Item layout");
 
 struct PlanLayout {
     PlanHeader *hdr;
     int32_t *tok_order;
-    int32_t *done;
     Item *items;
-    float *u;
     int64_t cap_items;
-    int64_t cap_u;
 };
 
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
-
-// Number of column chunks of the expand.
-__host__ __device__ inline int n_col_chunks(int d) { return ceil_div(d, VC); }
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -105,7 +93,7 @@ inline int32_t plan_chunk(int32_t max_adapters)
     return max_adapters <= kMaxPlanGroups ? kMaxPlanTokens : kMaxPlanGroups;
 }
 
-PlanLayout carve(void *base, int32_t cap_tokens, int32_t max_rank, int32_t hidden, size_t *total)
+PlanLayout carve(void *base, int32_t cap_tokens, size_t *total)
 {
     PlanLayout L;
     size_t off = 0;
@@ -115,79 +103,67 @@ PlanLayout carve(void *base, int32_t cap_tokens, int32_t max_rank, int32_t hidde
         return (char *)base + o;
     };
     const int64_t cap = cap_tokens;
-    L.cap_items = cap * (ceil_div(max_rank, RS) + n_col_chunks(hidden));
-    L.cap_u = cap * ((int64_t)max_rank + 4) + 16;   // per-group offsets padded to 4 floats
+    L.cap_items = cap;
     L.hdr = (PlanHeader *)take(sizeof(PlanHeader));
     L.tok_order = (int32_t *)take(cap * 4);
-    L.done = (int32_t *)take(cap * 4);
     L.items = (Item *)take(L.cap_items * sizeof(Item));
-    L.u = (float *)take(L.cap_u * 4);
     if (total)
         *total = off;
     return L;
 }
 
-// ---- block-wide exclusive scan of one int per thread --------------------------------
-// warp_tot: shared int[33]; every thread gets the block total in *total.
-__device__ __forceinline__ int block_excl_scan(int v, int *warp_tot, int *total)
+// ---- block-wide exclusive scans -------------------------------------------------------
+// N exclusive scans of one int per thread at once; wt: shared int[33][N]; every thread
+// gets the block totals.
+template <int N>
+__device__ __forceinline__ void block_excl_scan(const int (&v)[N], int (*wt)[N], int (&excl)[N], int (&total)[N])
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int incl = v;
+    int incl[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+        incl[i] = v[i];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        int n = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += n;
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            const int n = __shfl_up_sync(0xffffffffu, incl[i], o);
+            if (lane >= o) incl[i] += n;
+        }
     }
-    if (lane == 31) warp_tot[warp] = incl;
+    if (lane == 31) {
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            wt[warp][i] = incl[i];
+    }
     __syncthreads();
     if (warp == 0) {
-        int w = (lane < (int)(blockDim.x >> 5)) ? warp_tot[lane] : 0;
-        int wi = w;
+        const bool have = lane < (int)(blockDim.x >> 5);
+        int w[N], wi[N];
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            wi[i] = w[i] = have ? wt[lane][i] : 0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            int n = __shfl_up_sync(0xffffffffu, wi, o);
-            if (lane >= o) wi += n;
-        }
-        warp_tot[lane] = wi - w;   // exclusive prefix of warp totals
-        if (lane == 31) warp_tot[32] = wi;
-    }
-    __syncthreads();
-    const int r = warp_tot[warp] + incl - v;
-    *total = warp_tot[32];
-    __syncthreads();
-    return r;
-}
-
-// Four exclusive scans at once (one set of barriers).  wt: shared int4[33].
-__device__ __forceinline__ int4 block_excl_scan4(int4 v, int4 *wt, int4 *total)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int4 incl = v;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int nx = __shfl_up_sync(0xffffffffu, incl.x, o), ny = __shfl_up_sync(0xffffffffu, incl.y, o);
-        const int nz = __shfl_up_sync(0xffffffffu, incl.z, o), nw = __shfl_up_sync(0xffffffffu, incl.w, o);
-        if (lane >= o) { incl.x += nx; incl.y += ny; incl.z += nz; incl.w += nw; }
-    }
-    if (lane == 31) wt[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        const int4 w = (lane < (int)(blockDim.x >> 5)) ? wt[lane] : make_int4(0, 0, 0, 0);
-        int4 wi = w;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int nx = __shfl_up_sync(0xffffffffu, wi.x, o), ny = __shfl_up_sync(0xffffffffu, wi.y, o);
-            const int nz = __shfl_up_sync(0xffffffffu, wi.z, o), nw = __shfl_up_sync(0xffffffffu, wi.w, o);
-            if (lane >= o) { wi.x += nx; wi.y += ny; wi.z += nz; wi.w += nw; }
+            for (int i = 0; i < N; ++i) {
+                const int n = __shfl_up_sync(0xffffffffu, wi[i], o);
+                if (lane >= o) wi[i] += n;
+            }
         }
-        wt[lane] = make_int4(wi.x - w.x, wi.y - w.y, wi.z - w.z, wi.w - w.w);
-        if (lane == 31) wt[32] = wi;
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            wt[lane][i] = wi[i] - w[i];   // exclusive prefix of warp totals
+            if (lane == 31) wt[32][i] = wi[i];
+        }
     }
     __syncthreads();
-    const int4 b = wt[warp];
-    *total = wt[32];
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        excl[i] = wt[warp][i] + incl[i] - v[i];
+        total[i] = wt[32][i];
+    }
     __syncthreads();
-    return make_int4(b.x + incl.x - v.x, b.y + incl.y - v.y, b.z + incl.z - v.z, b.w + incl.w - v.w);
 }
 
 struct PlanArgs {
@@ -204,45 +180,45 @@ struct PlanArgs {
 
 constexpr int kRankBuckets = 11;        // floor(log2(rank)) for ranks 1..1024
 
+// slot page-table bases + group page-table bases + keys, slot ranks and scalings + eight
+// int group tables + token slots
 constexpr size_t plan_smem_bytes(int hs)
 {
-    return (size_t)hs * 4 + (size_t)kMaxPlanTokens * 2 + (size_t)13 * kMaxPlanGroups * 4;
+    return (size_t)hs * 8 + (size_t)kMaxPlanGroups * 8 + (size_t)hs * 12 + (size_t)8 * kMaxPlanGroups * 4 +
+           (size_t)kMaxPlanTokens * 2;
 }
 
 __device__ __forceinline__ void plan_refuse(const PlanArgs &a)
 {
     set_status(a.pv.status, SLORA_DEV_BAD_SEGMENT);
     a.L.hdr->n_groups = 0;
-    a.L.hdr->n_shrink = 0;
-    a.L.hdr->n_expand = 0;
-    a.L.hdr->claim = 0;
+    a.L.hdr->n_items = 0;
 }
 
 __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const __grid_constant__ PlanArgs a)
 {
-    extern __shared__ int plan_smem[];
+    extern __shared__ __align__(16) int plan_smem[];
     const int HS = a.hash_size;
     const int Tc = a.t_end - a.t_begin;
-    int *keys = plan_smem;                                  // [HS] adapter id / -1, then group id
-    short *tslot = reinterpret_cast<short *>(keys + HS);     // [Tc] hash slot, then group id
-    int *gad = reinterpret_cast<int *>(tslot + kMaxPlanTokens);  // [G] adapter
-    int *gn = gad + kMaxPlanGroups;                         // [G] tokens
-    int *gtok = gn + kMaxPlanGroups;                        // [G] first token position
-    int *gsh = gtok + kMaxPlanGroups;                       // [G] token placement cursor
-    int *psh = gsh + kMaxPlanGroups;                        // [position] first shrink item
-    int *pex = psh + kMaxPlanGroups;                        // [position] first expand item
-    int *gu = pex + kMaxPlanGroups;                         // [G] first u float (multiple of 4)
-    int *grank = gu + kMaxPlanGroups;                       // [G] rank
-    float *gscale = reinterpret_cast<float *>(grank + kMaxPlanGroups);   // [G] scaling
-    int *gperm = reinterpret_cast<int *>(gscale + kMaxPlanGroups);       // [position] group, by rank descending
-    long long *gpt = reinterpret_cast<long long *>(gperm + kMaxPlanGroups);  // [G] page-table offset
-    __shared__ int warp_tot[33];
-    __shared__ int4 warp_tot4[33];
-    __shared__ int s_lo, s_hi, s_G, s_nsh, s_nex, s_bad;
+    long long *hpt = reinterpret_cast<long long *>(plan_smem);              // [HS] slot: page-table base
+    long long *gpt = hpt + HS;                                             // [G] page-table base
+    int *keys = reinterpret_cast<int *>(gpt + kMaxPlanGroups);             // [HS] adapter id / -1, then group id
+    int *hrank = keys + HS;                                                // [HS] slot: rank
+    float *hscale = reinterpret_cast<float *>(hrank + HS);                 // [HS] slot: scaling
+    int *gad = reinterpret_cast<int *>(hscale + HS);                       // [G] adapter
+    int *gn = gad + kMaxPlanGroups;                                        // [G] tokens
+    int *gtok = gn + kMaxPlanGroups;                                       // [G] first token position
+    int *gsh = gtok + kMaxPlanGroups;                                      // [G] token placement cursor
+    int *pit = gsh + kMaxPlanGroups;                                       // [position] first item
+    int *grank = pit + kMaxPlanGroups;                                     // [G] rank
+    float *gscale = reinterpret_cast<float *>(grank + kMaxPlanGroups);     // [G] scaling
+    int *gperm = reinterpret_cast<int *>(gscale + kMaxPlanGroups);         // [position] group, by rank descending
+    short *tslot = reinterpret_cast<short *>(gperm + kMaxPlanGroups);      // [Tc] hash slot, then group id
+    __shared__ int warp_tot[33][1];
+    __shared__ int warp_tot2[33][2];
+    __shared__ int s_lo, s_hi, s_G, s_nit, s_bad;
     __shared__ int s_bucket[kRankBuckets + 1];
     const int tid = threadIdx.x;
-    const int d = a.pv.hidden;
-    const int nch = n_col_chunks(d);
 
     griddep_launch_dependents();
     griddep_wait();
@@ -270,7 +246,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const __grid_cons
     __syncthreads();
     const int lo = s_lo, hi = s_hi;
 
-    // 1. hash the decode tokens of [t_begin, t_end) by adapter
+    // 1. hash the decode tokens of [t_begin, t_end) by adapter; the thread that claims a
+    //    slot stores the adapter's directory entry there
     for (int i = tid; i < Tc; i += kPlanThreads) {
         const int t = a.t_begin + i;
         int slot = -1;
@@ -279,14 +256,19 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const __grid_cons
         if (ad >= 0 && ad < a.pv.max_adapters) {
             const DirEntry e = a.pv.dir[ad];
             const bool resident = e.pt_off >= 0 && e.rank > 0 && e.rank <= kMaxRank;
-            // segment tokens run on the tensor cores unless their adapter's rank is too
-            // large for that path; errors of segment tokens are reported there
+            // segment tokens run on the tensor-core prefill path unless their adapter's rank
+            // is too large for it; errors of segment tokens are reported there
             const bool mine = !in_seg || (resident && e.rank > kMaxPrefillRank);
             if (mine) {
                 if (resident) {
                     int h = (int)(((uint32_t)ad * 2654435761u) & (uint32_t)(HS - 1));
                     for (int probe = 0; probe < HS; ++probe) {
                         const int k = atomicCAS(&keys[h], -1, ad);
+                        if (k == -1) {
+                            hrank[h] = e.rank;
+                            hscale[h] = e.scaling;
+                            hpt[h] = e.pt_off + (long long)a.proj * 2 * e.rank;
+                        }
                         if (k == -1 || k == ad) { slot = h; break; }
                         h = (h + 1) & (HS - 1);
                     }
@@ -302,33 +284,33 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const __grid_cons
     }
     __syncthreads();
 
-    // 2. groups = occupied slots, numbered in slot order; keys[h] becomes the group id;
-    //    each group's directory entry is cached and its rank bucket counted
+    // 2. groups = occupied slots, numbered in slot order; keys[h] becomes the group id
     {
         const int per = HS / kPlanThreads;
         const int h0 = tid * per;
-        int c = 0;
+        int c[1] = {0};
         for (int h = h0; h < h0 + per; ++h)
-            c += keys[h] != -1;
-        int total;
-        int base = block_excl_scan(c, warp_tot, &total);
+            c[0] += keys[h] != -1;
+        int base[1], total[1];
+        block_excl_scan<1>(c, warp_tot, base, total);
+        int b = base[0];
         for (int h = h0; h < h0 + per; ++h) {
-            const int k = keys[h];
-            if (k != -1) {
-                if (base < kMaxPlanGroups) {
-                    const DirEntry e = a.pv.dir[k];
-                    gad[base] = k;
-                    grank[base] = e.rank;
-                    gscale[base] = e.scaling;
-                    gpt[base] = e.pt_off + (long long)a.proj * 2 * e.rank;
-                    atomicAdd(&s_bucket[31 - __clz(e.rank)], 1);
+            if (keys[h] != -1) {
+                if (b < kMaxPlanGroups) {
+                    gad[b] = keys[h];
+                    grank[b] = hrank[h];
+                    gscale[b] = hscale[h];
+                    gpt[b] = hpt[h];
+                    atomicAdd(&s_bucket[31 - __clz(hrank[h])], 1);
                 }
-                keys[h] = base;
-                ++base;
+                keys[h] = b;
+                ++b;
             }
         }
-        if (tid == 0 && total > kMaxPlanGroups) s_bad = 1;
-        if (tid == 0) s_G = total;
+        if (tid == 0) {
+            if (total[0] > kMaxPlanGroups) s_bad = 1;
+            s_G = total[0];
+        }
     }
     __syncthreads();
     if (s_bad) {
@@ -358,92 +340,59 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const __grid_cons
         gperm[atomicAdd(&s_bucket[31 - __clz(grank[g])], 1)] = g;
     __syncthreads();
 
-    // 3. per-group offsets (tokens, shrink items, expand items, u floats), laid out in
-    //    descending-rank order so the costliest items are claimed first
+    // 3. per-group offsets (tokens, items), laid out in descending-rank order so the
+    //    costliest items come first
     const int per_g = ceil_div(G > 0 ? G : 1, kPlanThreads);   // <= 2
     const int p0 = tid * per_g;
-    int my_tok = 0, my_sh = 0, my_ex = 0, my_u = 0;
+    int mine[2] = {0, 0};
+    for (int q = 0; q < per_g && p0 + q < G; ++q) {
+        const int n = gn[gperm[p0 + q]];
+        mine[0] += n;
+        mine[1] += ceil_div(n, kTok);
+    }
+    int off[2], tot[2];
+    block_excl_scan<2>(mine, warp_tot2, off, tot);
     for (int q = 0; q < per_g && p0 + q < G; ++q) {
         const int g = gperm[p0 + q];
-        const int r = grank[g], n = gn[g];
-        my_tok += n;
-        my_sh += ceil_div(r, RS) * ceil_div(n, TS);
-        my_ex += nch * ceil_div(n, TE);
-        my_u += (n * r + 3) & ~3;
+        const int n = gn[g];
+        gtok[g] = off[0];
+        pit[p0 + q] = off[1];
+        gsh[g] = 0;
+        off[0] += n;
+        off[1] += ceil_div(n, kTok);
     }
-    int4 tot4;
-    const int4 off4 = block_excl_scan4(make_int4(my_tok, my_sh, my_ex, my_u), warp_tot4, &tot4);
-    int off_tok = off4.x, off_sh = off4.y, off_ex = off4.z, off_u = off4.w;
-    const int tot_sh = tot4.y, tot_ex = tot4.z, tot_u = tot4.w;
-    for (int q = 0; q < per_g && p0 + q < G; ++q) {
-        const int g = gperm[p0 + q];
-        const int r = grank[g], n = gn[g];
-        gtok[g] = off_tok;
-        gu[g] = off_u;
-        psh[p0 + q] = off_sh;
-        pex[p0 + q] = off_ex;
-        off_tok += n;
-        off_sh += ceil_div(r, RS) * ceil_div(n, TS);
-        off_ex += nch * ceil_div(n, TE);
-        off_u += (n * r + 3) & ~3;
-    }
-    if (tid == 0) {
-        s_nsh = tot_sh;
-        s_nex = tot_ex;
-    }
+    if (tid == 0) s_nit = tot[1];
     __syncthreads();
-    if ((int64_t)tot_sh + tot_ex > a.L.cap_items || (int64_t)tot_u + 4 > a.L.cap_u) {
+    const int n_items = s_nit;
+    if ((int64_t)n_items > a.L.cap_items) {
         if (tid == 0) plan_refuse(a);
         return;
     }
 
     // 4. items, in parallel over items: each finds its group position by binary search over
     //    the (strictly increasing) first-item offsets
-    for (int i = tid; i < tot_sh + tot_ex; i += kPlanThreads) {
-        const bool sh = i < tot_sh;
-        const int rel = sh ? i : i - tot_sh;
-        const int *off = sh ? psh : pex;
+    for (int i = tid; i < n_items; i += kPlanThreads) {
         int lo_p = 0, hi_p = G - 1;
         while (lo_p < hi_p) {
             const int mid = (lo_p + hi_p + 1) >> 1;
-            if (off[mid] <= rel) lo_p = mid; else hi_p = mid - 1;
+            if (pit[mid] <= i) lo_p = mid; else hi_p = mid - 1;
         }
         const int g = gperm[lo_p];
-        const int local = rel - off[lo_p];
-        const int r = grank[g], n = gn[g];
+        const int tc = i - pit[lo_p];
         Item it;
-        it.g = g;
-        it.rank = r;
+        it.t0 = tc * kTok;
+        it.nt = min(kTok, gn[g] - it.t0);
+        it.rank = grank[g];
         it.tok_begin = gtok[g];
-        it.u_off = gu[g];
         it.adapter = gad[g];
-        it.n_tok = n;
         it.scaling = gscale[g];
         it.pt_base = gpt[g];
-        if (sh) {
-            const int ntc = ceil_div(n, TS), jc = local / ntc, tc = local - jc * ntc;
-            it.a = jc * RS;
-            it.t0 = tc * TS;
-            it.nt = min(TS, n - tc * TS);
-        } else {
-            const int ntc = ceil_div(n, TE), c = local / ntc, tc = local - c * ntc;
-            it.a = c;
-            it.t0 = tc * TE;
-            it.nt = min(TE, n - tc * TE);
-        }
         const uint4 *src4 = reinterpret_cast<const uint4 *>(&it);
         uint4 *dst4 = reinterpret_cast<uint4 *>(a.L.items + i);
         dst4[0] = src4[0];
         dst4[1] = src4[1];
-        dst4[2] = src4[2];
     }
-    for (int g = tid; g < G; g += kPlanThreads)
-        a.L.done[g] = 0;
-    __syncthreads();
-    // 5. token placement: gsh becomes the cursor
-    for (int g = tid; g < G; g += kPlanThreads)
-        gsh[g] = 0;
-    __syncthreads();
+    // 5. token placement (gsh, the cursors, were zeroed before the last barrier)
     for (int i = tid; i < Tc; i += kPlanThreads) {
         const int g = tslot[i];
         if (g >= 0) {
@@ -453,13 +402,14 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const __grid_cons
     }
     if (tid == 0) {
         a.L.hdr->n_groups = G;
-        a.L.hdr->n_shrink = s_nsh;
-        a.L.hdr->n_expand = s_nex;
-        a.L.hdr->claim = 0;
+        a.L.hdr->n_items = n_items;
         a.L.hdr->seg_lo = lo;
         a.L.hdr->seg_hi = hi;
     }
 }
+
+// ---------------------------------------------------------------------------------------
+// delta kernel
 
 struct DeltaArgs {
     PoolView pv;
@@ -467,422 +417,608 @@ struct DeltaArgs {
     __half *y;
     const float *scaling;   // optional override [max_adapters]
     PlanLayout L;
-    int32_t ustride;        // u row stride in shared memory: the largest rank rounded up to 8
+    int32_t pitch;          // bytes per row of a stage / x / y0 buffer: 2 * largest slice + 16
 };
 
-__device__ __forceinline__ void h8_to_f(const uint4 &raw, float *f)
+// ---- cluster and tensor-core helpers (inline PTX) -------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank()
 {
-    const __half2 *h = reinterpret_cast<const __half2 *>(&raw);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        float2 v = __half22float2(h[i]);
-        f[2 * i] = v.x;
-        f[2 * i + 1] = v.y;
-    }
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t ncluster_x()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t caddr)
+{
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(caddr) : "memory");
+    return v;
+}
+// Arrive (release, cluster scope) on an mbarrier in another CTA of the cluster.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t caddr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(smem_u32(bar)), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void consumers_sync()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+// d += a * b for one 16x8x16 tile: fp16 operands, fp32 accumulators.
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint4 f_to_h8(const float *f)
+// Bounded wait on an mbarrier phase.  After the first timeout anywhere in the CTA
+// (recorded in *abort and as SLORA_DEV_TIMEOUT) every wait returns at once, so the
+// kernel runs to its end without further waiting.
+template <bool kCluster>
+__device__ __forceinline__ void wait_phase(uint64_t *bar, uint32_t parity, volatile int *abort, int32_t *status)
 {
-    uint4 raw;
-    __half2 *h = reinterpret_cast<__half2 *>(&raw);
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-        h[i] = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
-    return raw;
-}
-
-// Butterfly reduce-scatter of 32 per-lane values: afterwards lane L holds the warp sum
-// of value L.
-__device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32])
-{
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int o = 16, n = 32; o >= 1; o >>= 1, n >>= 1) {
-        const bool upper = (lane & o) != 0;
-#pragma unroll
-        for (int i = 0; i < n / 2; ++i) {
-            float send = upper ? v[i] : v[i + n / 2];
-            float keep = upper ? v[i + n / 2] : v[i];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    auto probe = [&]() { return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+    if (probe())
+        return;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (probe())
+            return;
+        if ((it & 63u) == 0) {
+            if (*abort)
+                return;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                set_status(status, SLORA_DEV_TIMEOUT);
+                *abort = 1;
+                return;
+            }
         }
     }
-    return v[0];
 }
 
-// acc += x.lo * a.lo, then acc += x.hi * a.hi: fp16 operands, exact widening, one fp32
-// rounding per product-add (the same value as widening both and using fmaf).
-__device__ __forceinline__ float fma_h2(uint32_t x, uint32_t a, float acc)
+// The k-th item of this cluster: rounds of ncl items, walked in alternating direction so
+// that the costliest items (the list is ordered by rank, descending) spread evenly over
+// the clusters.
+__device__ __forceinline__ int cluster_item(int k, int cl, int ncl)
 {
-    asm("{\n\t.reg .f16 xl, xh, al, ah;\n\tmov.b32 {xl, xh}, %1;\n\tmov.b32 {al, ah}, %2;\n\t"
-        "fma.rn.f32.f16 %0, xl, al, %0;\n\tfma.rn.f32.f16 %0, xh, ah, %0;\n\t}"
-        : "+f"(acc)
-        : "r"(x), "r"(a));
-    return acc;
+    return k * ncl + ((k & 1) ? (ncl - 1 - cl) : cl);
 }
 
-// A tile is up to kSlots row segments of VC elements; every thread owns the same 16-byte
-// piece (8 elements) of each segment.  Shrink tiles: 8 A^T rows then 4 token rows;
-// expand tiles: 8 B rows.
-constexpr int kSlots = RS + TS;
-
-// acc[t][j] += x[t] . At[j] over the thread's 8 elements.  Rows past the adapter's rank
-// are never loaded; their accumulators are never published.
-template <int NT>
-__device__ __forceinline__ void shrink_tile(const uint4 (&v)[kSlots], float (&acc)[TS][RS])
+__device__ __forceinline__ Item load_item(const Item *p)
 {
-#pragma unroll
-    for (int j = 0; j < RS; ++j) {
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            float s = acc[t][j];
-            s = fma_h2(v[RS + t].x, v[j].x, s);
-            s = fma_h2(v[RS + t].y, v[j].y, s);
-            s = fma_h2(v[RS + t].z, v[j].z, s);
-            s = fma_h2(v[RS + t].w, v[j].w, s);
-            acc[t][j] = s;
-        }
-    }
+    const uint4 *s = reinterpret_cast<const uint4 *>(p);
+    const uint4 w0 = __ldcg(s), w1 = __ldcg(s + 1);
+    Item it;
+    it.t0 = (int32_t)w0.x;
+    it.nt = (int32_t)w0.y;
+    it.rank = (int32_t)w0.z;
+    it.tok_begin = (int32_t)w0.w;
+    it.adapter = (int32_t)w1.x;
+    it.scaling = __uint_as_float(w1.y);
+    it.pt_base = (int64_t)(((uint64_t)w1.w << 32) | w1.z);
+    return it;
 }
 
-// acc[t][0..7] += u[t][j] * B[j][the thread's 8 columns], rows in order.  FULL: all 8 rows
-// exist; otherwise rows past the rank contribute exactly zero.
-template <int NT, bool FULL>
-__device__ __forceinline__ void expand_tile(const uint4 (&v)[kSlots], const float *u_s, int ustride, int j0,
-                                            int nrows, float (&acc)[TS][RS])
+__global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constant__ DeltaArgs a)
 {
-    float uu[NT][RB];
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-        if (FULL) {
-            const float4 u0 = *reinterpret_cast<const float4 *>(u_s + t * ustride + j0);
-            const float4 u1 = *reinterpret_cast<const float4 *>(u_s + t * ustride + j0 + 4);
-            uu[t][0] = u0.x; uu[t][1] = u0.y; uu[t][2] = u0.z; uu[t][3] = u0.w;
-            uu[t][4] = u1.x; uu[t][5] = u1.y; uu[t][6] = u1.z; uu[t][7] = u1.w;
-        } else {
-#pragma unroll
-            for (int j = 0; j < RB; ++j)
-                uu[t][j] = j < nrows ? u_s[t * ustride + j0 + j] : 0.f;
-        }
-    }
-#pragma unroll
-    for (int j = 0; j < RB; ++j) {
-        float bf[8];
-        h8_to_f((FULL || j < nrows) ? v[j] : make_uint4(0, 0, 0, 0), bf);
-#pragma unroll
-        for (int t = 0; t < NT; ++t)
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                acc[t][e] = fmaf(uu[t][j], bf[e], acc[t][e]);
-    }
-}
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int P = a.pitch;
+    const int stageB = kTok * P;                                                 // one 16-row stage
+    uint8_t *ring = smem;                                                        // [NST][16][P]
+    uint8_t *xbuf = ring + NST * stageB;                                         // [2][16][P] x rows, by item parity
+    float *part = reinterpret_cast<float *>(xbuf + 2 * stageB);                  // [2][16][kRC] partial u, by unit parity
+    float *ptmp = part + 2 * kTok * kRC;                                         // [ksplit][16][16 nb] per-warp partials
+    __half *ubuf = reinterpret_cast<__half *>(ptmp + kTok * kRC);                // [16][kUPitch] u (fp16)
+    Item *rec_it = reinterpret_cast<Item *>(ubuf + kTok * kUPitch);              // [2] item, by item parity
+    int32_t *rec_tok = reinterpret_cast<int32_t *>(rec_it + 2);                 // [2][kTok] token ids
+    uint64_t *bars = reinterpret_cast<uint64_t *>(rec_tok + 2 * kTok);
+    uint64_t *full = bars, *empty = bars + NST;
+    uint64_t *full_x = bars + 2 * NST;   // [2] an item's x rows (and record) landed
+    uint64_t *xfree = full_x + 2;        // [2] an item's shrink no longer reads its x rows
+    uint64_t *ready = full_x + 4;        // [2] every CTA of the cluster wrote its partials of a unit
+    uint64_t *consumed = full_x + 6;     // [2] every CTA of the cluster has read the partials of a unit
+    uint64_t *done = full_x + 8;         // every CTA of the cluster is finished with the others' memory
+    uint64_t *pwrit = full_x + 9;        // [2] this CTA's partials of a unit are written (local)
+    uint64_t *rdone = full_x + 11;       // [2] this CTA has read the cluster's partials of a unit (local)
+    __shared__ int s_abort;
 
-// Item index of this CTA's k-th item: rounds of gridDim.x items, walked in alternating
-// direction so that the costliest items (the list is ordered by rank, descending) spread
-// evenly over the CTAs.  Every CTA's items are increasing, so all its shrink items (which
-// never wait) come before its expand items (which wait only on shrink items).
-__device__ __forceinline__ int my_item(int k)
-{
-    const int G = (int)gridDim.x, b = (int)blockIdx.x;
-    return k * G + ((k & 1) ? (G - 1 - b) : b);
-}
-
-__device__ __forceinline__ int item_pages(const Item &it, bool shrink)
-{
-    return shrink ? min(RS, it.rank - it.a) : it.rank;
-}
-
-template <bool V>
-using bool_c = std::integral_constant<bool, V>;
-template <int V>
-using int_c = std::integral_constant<int, V>;
-
-__global__ void __launch_bounds__(kDT, 2) delta_kernel(const __grid_constant__ DeltaArgs a)
-{
-    extern __shared__ __align__(16) uint8_t smem[];
-    uint4 *stg = reinterpret_cast<uint4 *>(smem);                                   // [NST][kSlots][kDT]
-    float *u_s = reinterpret_cast<float *>(smem + NST * kSlots * kDT * 16);       // [TE][ustride]
-    float *red = u_s + TE * a.ustride;                                             // [2][kDW][32]
-    Item *mit = reinterpret_cast<Item *>(red + 2 * kDW * 32);                      // [kBatchItems]
-    int *mpo = reinterpret_cast<int *>(mit + kBatchItems);                         // [kBatchItems + 1]
-    int *mpg = mpo + kBatchItems + 1;                                              // [kBatchPages]
-    int *mtk = mpg + kBatchPages;                                                  // [kBatchItems][TE]
-    __shared__ int s_nb, s_flag;
-
-    constexpr uint32_t kSlotB = kDT * 16;          // one row segment of the CTA
-    constexpr uint32_t kStageB = kSlots * kSlotB;  // one tile
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int d = a.pv.hidden;
-    const int nkt = ceil_div(d, VC);               // K tiles of a shrink item
-    const __half *pool = reinterpret_cast<const __half *>(a.pv.pool);
-    const uint32_t sbase = smem_u32(stg) + (uint32_t)tid * 16;
+    const uint32_t crank = cluster_ctarank(), C = cluster_nctarank();
+    const int cl = (int)cluster_id_x(), ncl = (int)ncluster_x();
+    // this CTA's slice of the hidden dimension, in whole 16-element steps
+    const int nk16 = d / 16;
+    const int kb = 16 * (int)((crank * (uint32_t)nk16) / C);
+    const int KS = 16 * (int)(((crank + 1) * (uint32_t)nk16) / C) - kb;
+    const uint32_t sliceB = (uint32_t)KS * 2;
+    int32_t *status = a.pv.status;
+    volatile int *abort = &s_abort;
+    const uint32_t ring_s = smem_u32(ring), xbuf_s = smem_u32(xbuf);
+    const uint32_t ubuf_s = smem_u32(ubuf);
 
-    griddep_wait();   // the plan of this batch is complete and visible
+    if (tid == 0) {
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&full_x[b], 1);
+            mbar_init(&xfree[b], 1);
+            mbar_init(&ready[b], C);
+            mbar_init(&consumed[b], C);
+        }
+        mbar_init(done, C);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&pwrit[b], 1);
+            mbar_init(&rdone[b], 1);
+        }
+        s_abort = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    cluster_sync_all();   // every CTA's barriers exist before any remote arrival
+    griddep_wait();       // the plan of this batch is complete and visible
     griddep_launch_dependents();
-    const int n_sh = a.L.hdr->n_shrink;
-    const int n_tot = n_sh + a.L.hdr->n_expand;
+    const int n_items = a.L.hdr->n_items;
 
-    float acc[TS][RS];
-    int n_red = 0;
-    for (int k0 = 0;;) {
-        // ---- metadata of the next batch of this CTA's items, into shared memory ----
-        if (tid < kBatchItems) {
-            const int i = my_item(k0 + tid);
-            if (i < n_tot)
-                mit[tid] = a.L.items[i];
-        }
-        __syncthreads();
-        if (tid == 0) {
-            int nb = 0, np = 0;
-            while (nb < kBatchItems && my_item(k0 + nb) < n_tot) {
-                const int need = item_pages(mit[nb], my_item(k0 + nb) < n_sh);
-                if (np + need > kBatchPages) break;
-                mpo[nb] = np;
-                np += need;
-                ++nb;
-            }
-            mpo[nb] = np;
-            s_nb = nb;
-        }
-        __syncthreads();
-        const int nb = s_nb;
-        if (nb == 0)
-            break;
-        for (int q = 0; q < nb; ++q) {
-            const bool sh = my_item(k0 + q) < n_sh;
-            const Item &it = mit[q];
-            const int np = mpo[q + 1] - mpo[q];
-            const int64_t base = it.pt_base + (sh ? it.a : it.rank);
-            for (int j = tid; j < np; j += kDT) {
-                int32_t pg = a.pv.pt_arena[base + j];
-                if (pg < 0 || pg >= a.pv.num_pages) {
-                    set_status(a.pv.status, SLORA_DEV_BAD_PAGE);
-                    pg = -1;
+    // Work runs in units: one chunk of at most kRC rank rows of an item.  Both sides walk
+    // the units in the same order and interleave them one unit apart (the shrink of unit
+    // u, then the expand of unit u-1), so the wait for the cluster's partials of a unit
+    // overlaps the next unit's shrink.
+
+    if (warp == kConsumerWarps + 1) {
+        // ================================ signal warp ================================
+        // Relays this CTA's "partials written" and "partials read" events of every unit to
+        // the cluster (lane c arrives, release at cluster scope, on CTA c's barrier).  The
+        // warp writes no global memory, so its releases only order the shared-memory
+        // writes it has observed through the local barriers.
+        int k = -1, c = 0, nch = 0;
+        uint32_t u = 0;
+        for (;;) {
+            bool have = true;
+            if (c == nch) {
+                ++k;
+                const int i = cluster_item(k, cl, ncl);
+                if (i >= n_items) {
+                    have = false;
+                } else {
+                    c = 0;
+                    nch = ceil_div(__ldcg(&a.L.items[i].rank), kRC);
                 }
-                mpg[mpo[q] + j] = pg;
             }
+            if (have) {
+                wait_phase<false>(&pwrit[u & 1], (u >> 1) & 1, abort, status);
+                if (lane < (int)C) mbar_arrive_remote(mapa(smem_u32(&ready[u & 1]), lane));
+            }
+            if (u >= 1) {
+                const uint32_t pu = u - 1;
+                wait_phase<false>(&rdone[pu & 1], (pu >> 1) & 1, abort, status);
+                if (lane < (int)C) mbar_arrive_remote(mapa(smem_u32(&consumed[pu & 1]), lane));
+            }
+            if (!have) break;
+            ++c;
+            ++u;
         }
-        for (int e = tid; e < nb * TE; e += kDT) {
-            const int q = e / TE, t = e - q * TE;
-            const Item &it = mit[q];
-            mtk[e] = t < it.nt ? a.L.tok_order[it.tok_begin + it.t0 + t] : -1;
-        }
-        __syncthreads();
+        // the CTA is done reading the others' partials once its last unit was reduced
+        if (lane < (int)C) mbar_arrive_remote(mapa(smem_u32(done), lane));
+        if (lane == 0) wait_phase<true>(done, 0, abort, status);
+        return;
+    }
 
-        // ---- copy stream: every thread copies its own 16-byte piece of each row segment
-        //      into an NST-deep ring, NST-1 tiles ahead of its arithmetic ----
-        int is_q = 0, is_sub = 0, is_ntiles = 0, is_rank = 0, is_col = 0;
-        bool is_sh = true;
-        const int *is_pg = mpg;
-        const __half *is_src[kSlots];
-        auto load_issue_item = [&]() {
-            if (is_q >= nb)
-                return;
-            const Item &it = mit[is_q];
-            is_sh = my_item(k0 + is_q) < n_sh;
-            is_pg = mpg + mpo[is_q];
-            if (is_sh) {
-                is_ntiles = nkt;
-                const int nrows = min(RS, it.rank - it.a);
+    if (warp == kConsumerWarps) {
+        // ===================================== producer =====================================
+        const __half *pool = reinterpret_cast<const __half *>(a.pv.pool);
+        uint32_t sc = 0;   // stages issued
+        // Lane r < 16 copies the CTA's slice of row r from src_r (when ok_r) into a 16-row
+        // buffer at dst; rows not copied are zero-filled when zero_rest.  Completion on *bar.
+        auto fill16 = [&](uint32_t dst, uint64_t *bar, const __half *src_r, bool ok_r, bool zero_rest) {
+            const bool mine = ok_r && lane < 16;
+            const uint32_t m = __ballot_sync(0xffffffffu, mine);
+            if (mine && !*abort)
+                bulk_g2s_s(dst + lane * P, src_r + kb, sliceB, bar);
+            if (zero_rest && m != 0xffffu) {
+                for (int r = 0; r < 16; ++r) {
+                    if ((m >> r) & 1u) continue;
+                    for (uint32_t o = lane * 16; o < sliceB; o += 32 * 16)
+                        *reinterpret_cast<uint4 *>(smem + (dst - ring_s) + r * P + o) = make_uint4(0, 0, 0, 0);
+                }
+                tc::fence_proxy_async_smem();   // before later bulk copies land in the same rows
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_expect_tx(bar, *abort ? 0u : (uint32_t)__popc(m) * sliceB);
+        };
+        auto next_slot = [&]() -> uint32_t {
+            const uint32_t slot = sc % NST;
+            if (sc >= NST) wait_phase<false>(&empty[slot], ((sc / NST) - 1) & 1, abort, status);
+            return slot;
+        };
+        auto page_ok = [&](int32_t pg) -> bool {
+            if (pg >= 0 && pg < a.pv.num_pages) return true;
+            set_status(status, SLORA_DEV_BAD_PAGE);
+            return false;
+        };
+        // the 16-row blocks of a unit: rows rc0 .. rc0+rows-1 of A^T (ab 0) or B (ab 1);
+        // lane l holds the page indices of the unit's rows l + 32m in pg4[m]
+        auto emit_blocks = [&](int rows, const int32_t (&pg4)[4], bool zero_rest) {
+            const int nb = ceil_div(rows, 16);
+            for (int b = 0; b < nb; ++b) {
+                const uint32_t slot = next_slot();
+                const int src_lane = 16 * (b & 1) + (lane & 15);   // rows 16b+l live in lane 16(b&1)+l, word b/2
+                int32_t pg = -1;
 #pragma unroll
-                for (int j = 0; j < RS; ++j)
-                    is_src[j] = (j < nrows && is_pg[j] >= 0) ? pool + (int64_t)is_pg[j] * d + 8 * tid : nullptr;
-#pragma unroll
-                for (int t = 0; t < TS; ++t)
-                    is_src[RS + t] = t < it.nt ? a.x + (int64_t)mtk[is_q * TE + t] * d + 8 * tid : nullptr;
-            } else {
-                is_ntiles = ceil_div(it.rank, RB);
-                is_rank = it.rank;
-                is_col = it.a * VC + 8 * tid;
+                for (int m = 0; m < 4; ++m) {
+                    const int v = __shfl_sync(0xffffffffu, pg4[m], src_lane);
+                    if (m == (b >> 1)) pg = v;
+                }
+                const bool ok = 16 * b + (lane & 15) < rows && pg >= 0 && page_ok(pg);
+                fill16(ring_s + slot * stageB, &full[slot], pool + (int64_t)(ok ? pg : 0) * d, ok, zero_rest);
+                ++sc;
             }
         };
-        auto issue_tile = [&](int stage) {
-            if (is_q < nb) {
-                const uint32_t sd = sbase + (uint32_t)stage * kStageB;
-                if (is_sh) {
-                    const int off = is_sub * VC;
-                    if (off + 8 * tid < d) {
+        int k = -1, c = 0, nch = 0;      // current unit: item ordinal, rank chunk, chunks of the item
+        Item it{};
+        int tl = 0;                      // lane l: token id of the item's token l & 15
+        bool tv = false;
+        bool have_prev = false;          // previous unit, whose expand data follows
+        Item pit{};
+        int pc = 0, ptl = 0;
+        bool ptv = false;
+        int32_t ppb[4] = {-1, -1, -1, -1};
+        for (;;) {
+            bool have = true;
+            if (c == nch) {
+                ++k;
+                const int i = cluster_item(k, cl, ncl);
+                if (i >= n_items) {
+                    have = false;
+                } else {
+                    it = load_item(a.L.items + i);
+                    const int tok = lane < it.nt ? __ldcg(a.L.tok_order + it.tok_begin + it.t0 + lane) : 0;
+                    tl = __shfl_sync(0xffffffffu, tok, lane & 15);
+                    tv = (lane & 15) < it.nt;
+                    c = 0;
+                    nch = ceil_div(it.rank, kRC);
+                    // the item's record and x rows, once item k-2's shrink is done with buffer k&1
+                    if (k >= 2) wait_phase<false>(&xfree[k & 1], ((k >> 1) - 1) & 1, abort, status);
+                    if (lane == 0) rec_it[k & 1] = it;
+                    if (lane < kTok) rec_tok[(k & 1) * kTok + lane] = tok;
+                    fill16(xbuf_s + (k & 1) * stageB, &full_x[k & 1], a.x + (int64_t)tl * d, tv, false);
+                }
+            }
+            int32_t pb[4] = {-1, -1, -1, -1};
+            if (have) {
+                // shrink data of the unit: its A^T rows
+                const int rc0 = c * kRC, rows = min(kRC, it.rank - rc0);
+                int32_t pa[4];
 #pragma unroll
-                        for (int j = 0; j < kSlots; ++j)
-                            if (is_src[j])
-                                cp_async16_s(sd + j * kSlotB, is_src[j] + off);
+                for (int m = 0; m < 4; ++m) {
+                    const int r = lane + 32 * m;
+                    pa[m] = -1;
+                    if (r < rows) {
+                        pa[m] = __ldcg(a.pv.pt_arena + it.pt_base + rc0 + r);
+                        pb[m] = __ldcg(a.pv.pt_arena + it.pt_base + it.rank + rc0 + r);
                     }
-                } else if (is_col < d) {
-                    const int j0 = is_sub * RB;
-#pragma unroll
-                    for (int j = 0; j < RB; ++j)
-                        if (j0 + j < is_rank && is_pg[j0 + j] >= 0)
-                            cp_async16_s(sd + j * kSlotB, pool + (int64_t)is_pg[j0 + j] * d + is_col);
                 }
-                if (++is_sub == is_ntiles) {
-                    is_sub = 0;
-                    ++is_q;
-                    load_issue_item();
-                }
+                emit_blocks(rows, pa, false);
             }
-            cp_async_commit();   // one group per tile, possibly empty
-        };
-        load_issue_item();
-#pragma unroll 1
-        for (int p = 0; p < NST - 1; ++p)
-            issue_tile(p);
-
-        int ct = 0;   // tiles consumed in this batch
-        // One item's tiles, with the item kind and token count fixed at compile time.
-        auto run_item = [&](int q, auto sh_c, auto nt_c) {
-            constexpr bool SH = decltype(sh_c)::value;
-            constexpr int NT = decltype(nt_c)::value;
-            const Item it = mit[q];
-            const int ntiles = SH ? nkt : ceil_div(it.rank, RB);
-            const int col = it.a * VC + 8 * tid;
-#pragma unroll
-            for (int t = 0; t < TS; ++t)
-#pragma unroll
-                for (int j = 0; j < RS; ++j)
-                    acc[t][j] = 0.f;
-            uint4 yv[NT];
-            bool ok = true;
-            if (!SH) {
-                if (col < d) {
-#pragma unroll
-                    for (int t = 0; t < NT; ++t)
-                        yv[t] = *reinterpret_cast<const uint4 *>(a.y + (int64_t)mtk[q * TE + t] * d + col);
+            if (have_prev) {
+                // expand data of the previous unit: the item's y0 rows (first unit) and B rows
+                if (pc == 0) {
+                    const uint32_t slot = next_slot();
+                    fill16(ring_s + slot * stageB, &full[slot], a.y + (int64_t)ptl * d, ptv, false);
+                    ++sc;
                 }
-                __syncthreads();   // every thread is done with the previous item's u_s
-                if (tid == 0) {
-                    // every shrink item of the group has published its u values?
-                    const int need = 32 * ceil_div(it.rank, RS) * ceil_div(it.n_tok, TS);
-                    int flag = 1;
-                    if (ld_acquire_gpu(&a.L.done[it.g]) < need) {
-                        const uint64_t t0 = global_timer_ns();
-                        for (;;) {
-                            __nanosleep(32);
-                            if (ld_acquire_gpu(&a.L.done[it.g]) >= need) break;
-                            if (global_timer_ns() - t0 > kWaitLimitNs) {
-                                set_status(a.pv.status, SLORA_DEV_TIMEOUT);
-                                flag = 0;
-                                break;
+                emit_blocks(min(kRC, pit.rank - pc * kRC), ppb, true);
+            }
+            if (!have) break;
+            have_prev = true;
+            pit = it;
+            pc = c;
+            ptl = tl;
+            ptv = tv;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) ppb[m] = pb[m];
+            ++c;
+        }
+        return;
+    }
+
+    // ===================================== consumers =====================================
+    const int w = warp;
+    const int q = lane >> 3, rr = lane & 7, gid = lane >> 2, tig = lane & 3;
+    // this warp's output columns in the expand: column pairs [pp0, pp1) of 16 columns
+    const int npair = KS / 16;
+    const int pp0 = (w * npair) / kConsumerWarps, pp1 = ((w + 1) * npair) / kConsumerWarps;
+    uint32_t sc = 0;    // stages consumed
+    uint32_t un = 0;    // units shrunk
+    int k = -1, c = 0, nch = 0;
+    Item it{};
+    int tk[2] = {0, 0};                 // token ids of rows gid, gid+8 of the current item
+    bool have_prev = false;
+    Item pit{};
+    int pc = 0, ptk[2] = {0, 0};
+    float acc[16][4];
+    uint32_t yv[2][16];                 // y0 of the item being expanded: [token half][n-block], half2 bits
+#pragma unroll
+    for (int n8 = 0; n8 < 16; ++n8)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            acc[n8][e] = 0.f;
+    for (;;) {
+        bool have = true;
+        if (c == nch) {
+            ++k;
+            const int i = cluster_item(k, cl, ncl);
+            if (i >= n_items) {
+                have = false;
+            } else {
+                wait_phase<false>(&full_x[k & 1], (k >> 1) & 1, abort, status);
+                it = rec_it[k & 1];
+                tk[0] = rec_tok[(k & 1) * kTok + gid];
+                tk[1] = rec_tok[(k & 1) * kTok + gid + 8];
+                c = 0;
+                nch = ceil_div(it.rank, kRC);
+            }
+        }
+        if (have) {
+            // ---- shrink of unit un: block b (16 rank rows) of the unit goes to warps
+            //      b + nb*g, which split the CTA's K slice into ksplit = 8/nb parts ----
+            const uint32_t par = un & 1;
+            if (un >= 2) wait_phase<true>(&consumed[par], ((un >> 1) - 1) & 1, abort, status);
+            float *mypart = part + par * (kTok * kRC);
+            const uint32_t xs = xbuf_s + (k & 1) * stageB;
+            const int rows = min(kRC, it.rank - c * kRC), nb = ceil_div(rows, 16);
+            const int ksplit = kConsumerWarps / nb, wb = w % nb, wg = w / nb;
+            const int nsteps = KS / 16;
+            const int ks0 = (wg * nsteps) / ksplit, ks1 = ((wg + 1) * nsteps) / ksplit;
+            for (int b = 0; b < nb; ++b) {
+                const uint32_t s = sc + b, slot = s % NST;
+                wait_phase<false>(&full[slot], (s / NST) & 1, abort, status);
+                if (b == wb && wg < ksplit) {
+                    // two accumulators per n-block (even / odd K steps) halve the MMA chains
+                    float pacc[2][2][4] = {};
+                    const uint32_t sb = ring_s + slot * stageB;
+                    for (int st = ks0; st < ks1; st += 2) {
+#pragma unroll
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            if (st + h2 < ks1) {
+                                const int k16 = 16 * (st + h2);
+                                uint32_t af[4], bf[4];
+                                ldsm_x4(xs + (rr + 8 * (q & 1)) * P + (k16 + 8 * (q >> 1)) * 2, af);   // token rows
+                                ldsm_x4(sb + (rr + 8 * (q >> 1)) * P + (k16 + 8 * (q & 1)) * 2, bf);   // A^T rows
+                                mma16816(pacc[h2][0], af, bf[0], bf[1]);
+                                mma16816(pacc[h2][1], af, bf[2], bf[3]);
                             }
                         }
                     }
-                    s_flag = flag;
-                }
-                __syncthreads();
-                ok = s_flag != 0;
-                const int r = it.rank;
-                const float *ug = a.L.u + it.u_off + (int64_t)it.t0 * r;
-                for (int e = tid; e < NT * r; e += kDT) {
-                    const int t = e / r, j = e - t * r;
-                    u_s[t * a.ustride + j] = __ldcg(ug + e);
-                }
-                __syncthreads();
-            }
-#pragma unroll 1
-            for (int sub = 0; sub < ntiles; ++sub) {
-                issue_tile((ct + NST - 1) % NST);
-                cp_async_wait<NST - 1>();   // this thread's copies of tile ct have landed
-                const uint4 *slot = stg + (ct % NST) * (kSlots * kDT) + tid;
-                if (SH) {
-                    if (sub * VC + 8 * tid < d) {
-                        uint4 v[kSlots];
+                    const int ld = 16 * nb;
 #pragma unroll
-                        for (int i = 0; i < RS + NT; ++i)
-                            v[i] = slot[i * kDT];
-                        shrink_tile<NT>(v, acc);
+                    for (int nb8 = 0; nb8 < 2; ++nb8)
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+                            *reinterpret_cast<float2 *>(ptmp + (wg * kTok + gid + 8 * h) * ld + 16 * b + 8 * nb8 + 2 * tig) =
+                                make_float2(pacc[0][nb8][2 * h] + pacc[1][nb8][2 * h],
+                                            pacc[0][nb8][2 * h + 1] + pacc[1][nb8][2 * h + 1]);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[slot]);
+            }
+            sc += nb;
+            consumers_sync();   // every warp's partials are written
+            {
+                // this CTA's partial: the ksplit parts summed in order
+                const int ld = 16 * nb;
+                for (int e = tid; e < kTok * ld; e += kConsumers) {
+                    const int t = e / ld, j = e - t * ld;
+                    float v = 0.f;
+                    for (int g = 0; g < ksplit; ++g)
+                        v += ptmp[(g * kTok + t) * ld + j];
+                    mypart[t * kRC + j] = v;
+                }
+            }
+            consumers_sync();   // this CTA's partials of the unit are written
+            if (tid == 0) {
+                if (c == nch - 1) mbar_arrive(&xfree[k & 1]);   // the item's x rows are no longer read
+                mbar_arrive(&pwrit[par]);                       // relayed to the cluster by the signal warp
+            }
+        }
+        if (have_prev) {
+            // ---- expand of unit un-1 ----
+            const uint32_t pu = un - 1, ppar = pu & 1;
+            const int rows = min(kRC, pit.rank - pc * kRC), nb = ceil_div(rows, 16);
+            wait_phase<true>(&ready[ppar], (pu >> 1) & 1, abort, status);
+            consumers_sync();   // the previous expand is done reading u
+            {
+                // u = sum of the C partials in CTA order, rounded to fp16 once; all the
+                // remote loads of a thread are issued before the sums
+                const uint32_t pbase = smem_u32(part + ppar * (kTok * kRC));
+                constexpr int kPer = kTok * kRC / kConsumers;   // elements per thread at most
+                constexpr int kBatch = 2;                        // elements whose loads are in flight together
+                const int ne = kTok * 16 * nb;
+                for (int m0 = 0; m0 < kPer; m0 += kBatch) {
+                    if (tid + m0 * kConsumers >= ne) break;
+                    float v[kBatch][kMaxCluster];
+#pragma unroll
+                    for (int m = 0; m < kBatch; ++m) {
+                        const int e = tid + (m0 + m) * kConsumers;
+                        const int t = e / (16 * nb), j = e - t * (16 * nb);
+                        const uint32_t off = (uint32_t)(t * kRC + j) * 4;
+#pragma unroll
+                        for (int cc = 0; cc < kMaxCluster; ++cc)
+                            v[m][cc] = (e < ne && cc < (int)C) ? ld_cluster_f32(mapa(pbase + off, cc)) : 0.f;
                     }
-                } else if (col < d) {
-                    const int j0 = sub * RB;
-                    const int nrows = min(RB, it.rank - j0);
-                    uint4 v[kSlots];
-                    if (nrows == RB) {
 #pragma unroll
-                        for (int i = 0; i < RB; ++i)
-                            v[i] = slot[i * kDT];
-                        expand_tile<NT, true>(v, u_s, a.ustride, j0, nrows, acc);
-                    } else {
+                    for (int m = 0; m < kBatch; ++m) {
+                        const int e = tid + (m0 + m) * kConsumers;
+                        if (e < ne) {
+                            const int t = e / (16 * nb), j = e - t * (16 * nb);
+                            float sum = 0.f;
 #pragma unroll
-                        for (int i = 0; i < RB; ++i)
-                            v[i] = i < nrows ? slot[i * kDT] : make_uint4(0, 0, 0, 0);
-                        expand_tile<NT, false>(v, u_s, a.ustride, j0, nrows, acc);
+                            for (int cc = 0; cc < kMaxCluster; ++cc)
+                                sum += v[m][cc];   // CTA order; absent CTAs add zero
+                            ubuf[t * kUPitch + j] = __float2half_rn(j < rows ? sum : 0.f);
+                        }
                     }
                 }
-                ++ct;
             }
-            if (SH) {
-                // ---- reduce the 32 partials over the CTA, publish u ----
-                float vv[32];
+            consumers_sync();   // u of the unit is in place; the partials have been read
+            if (tid == 0) mbar_arrive(&rdone[ppar]);   // relayed to the cluster by the signal warp
+            if (pc == 0) {
+                // the item's y0 rows: into registers, and a fresh accumulator
+                const uint32_t slot = sc % NST;
+                wait_phase<false>(&full[slot], (sc / NST) & 1, abort, status);
+                const uint8_t *st = ring + slot * stageB;
 #pragma unroll
-                for (int t = 0; t < TS; ++t)
+                for (int h = 0; h < 2; ++h)
 #pragma unroll
-                    for (int j = 0; j < RS; ++j)
-                        vv[t * RS + j] = acc[t][j];
-                const float ws = warp_reduce_scatter32(vv);
-                float *rb = red + (n_red & 1) * (kDW * 32);
-                ++n_red;
-                rb[warp * 32 + lane] = ws;
-                __syncthreads();
-                if (tid < 32) {
-                    float tot = 0.f;
+                    for (int p = 0; p < 8; ++p)
 #pragma unroll
-                    for (int w = 0; w < kDW; ++w)
-                        tot += rb[w * 32 + tid];
-                    const int t = tid / RS, j = tid % RS;
-                    if (t < it.nt && it.a + j < it.rank)
-                        __stcg(a.L.u + it.u_off + (int64_t)(it.t0 + t) * it.rank + it.a + j, tot);
-                    red_release_add1(&a.L.done[it.g]);   // 32 per shrink item
-                }
-            } else if (ok && col < d) {
-                const float sc = a.scaling ? a.scaling[it.adapter] : it.scaling;
+                        for (int n2 = 0; n2 < 2; ++n2)
+                            yv[h][2 * p + n2] = pp0 + p < pp1 ? *reinterpret_cast<const uint32_t *>(
+                                                                    st + (gid + 8 * h) * P + (16 * (pp0 + p) + 8 * n2 + 2 * tig) * 2)
+                                                              : 0u;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[slot]);
+                ++sc;
 #pragma unroll
-                for (int t = 0; t < NT; ++t) {
-                    float y0f[8], out[8];
-                    h8_to_f(yv[t], y0f);
+                for (int n8 = 0; n8 < 16; ++n8)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        out[e] = fmaf(sc, acc[t][e], y0f[e]);
-                    *reinterpret_cast<uint4 *>(a.y + (int64_t)mtk[q * TE + t] * d + col) = f_to_h8(out);
-                }
+                    for (int e = 0; e < 4; ++e)
+                        acc[n8][e] = 0.f;
             }
-        };
-        for (int q = 0; q < nb; ++q) {
-            const bool sh = my_item(k0 + q) < n_sh;
-            const int nt = mit[q].nt;
-            if (sh) {
-                switch (nt) {
-                case 1: run_item(q, bool_c<true>(), int_c<1>()); break;
-                case 2: run_item(q, bool_c<true>(), int_c<2>()); break;
-                case 3: run_item(q, bool_c<true>(), int_c<3>()); break;
-                default: run_item(q, bool_c<true>(), int_c<4>()); break;
+            // every warp its column pairs, over the unit's B blocks
+            for (int b = 0; b < nb; ++b) {
+                const uint32_t s = sc + b, slot = s % NST;
+                wait_phase<false>(&full[slot], (s / NST) & 1, abort, status);
+                const uint32_t sb = ring_s + slot * stageB;
+                uint32_t af[4];
+                ldsm_x4(ubuf_s + ((rr + 8 * (q & 1)) * kUPitch + 16 * b + 8 * (q >> 1)) * 2, af);   // u rows
+#pragma unroll
+                for (int p = 0; p < 8; ++p) {
+                    if (pp0 + p < pp1) {
+                        uint32_t bf[4];
+                        ldsm_x4_t(sb + (rr + 8 * (q & 1)) * P + (16 * (pp0 + p) + 8 * (q >> 1)) * 2, bf);   // B rows
+                        mma16816(acc[2 * p], af, bf[0], bf[1]);
+                        mma16816(acc[2 * p + 1], af, bf[2], bf[3]);
+                    }
                 }
-            } else {
-                switch (nt) {
-                case 1: run_item(q, bool_c<false>(), int_c<1>()); break;
-                case 2: run_item(q, bool_c<false>(), int_c<2>()); break;
-                case 3: run_item(q, bool_c<false>(), int_c<3>()); break;
-                default: run_item(q, bool_c<false>(), int_c<4>()); break;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[slot]);
+            }
+            sc += nb;
+            if (pc == ceil_div(pit.rank, kRC) - 1 && !*abort) {
+                // ---- epilogue of the item: y = y0 + s * acc over this CTA's columns ----
+                const float scl = a.scaling ? a.scaling[pit.adapter] : pit.scaling;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int t = gid + 8 * h;
+                    if (t < pit.nt) {
+                        __half *yrow = a.y + (int64_t)ptk[h] * d + kb;
+#pragma unroll
+                        for (int p = 0; p < 8; ++p) {
+                            if (pp0 + p < pp1) {
+#pragma unroll
+                                for (int n2 = 0; n2 < 2; ++n2) {
+                                    const int col = 16 * (pp0 + p) + 8 * n2 + 2 * tig;
+                                    const float2 y0 = __half22float2(*reinterpret_cast<const __half2 *>(&yv[h][2 * p + n2]));
+                                    const float *ac = acc[2 * p + n2];
+                                    *reinterpret_cast<__half2 *>(yrow + col) =
+                                        __floats2half2_rn(fmaf(scl, ac[2 * h], y0.x), fmaf(scl, ac[2 * h + 1], y0.y));
+                                }
+                            }
+                        }
+                    }
                 }
             }
         }
-        cp_async_wait<0>();
-        __syncthreads();   // the batch's metadata is about to be replaced
-        k0 += nb;
+        if (!have) break;
+        have_prev = true;
+        pit = it;
+        pc = c;
+        ptk[0] = tk[0];
+        ptk[1] = tk[1];
+        ++c;
+        ++un;
     }
+    // the signal warp keeps the CTA alive until no other CTA may still read its partials
 }
 
 }  // namespace
 
 size_t plan_scratch_bytes(int32_t T, int32_t max_rank, int32_t hidden, int32_t max_adapters)
 {
+    (void)max_rank;
+    (void)hidden;
     size_t total = 0;
     const int32_t chunk = plan_chunk(max_adapters);
     const int32_t cap = T < chunk ? T : chunk;
-    carve(nullptr, cap, max_rank, hidden, &total);
+    carve(nullptr, cap, &total);
     return total;
 }
 
-inline size_t delta_smem_bytes(int ustride)
+// CTAs per cluster for a hidden size: slices of at most kMaxSlice elements.
+inline int delta_cluster(int hidden) { return ceil_div(hidden, kMaxSlice); }
+inline int delta_pitch(int hidden)
 {
-    return (size_t)NST * kSlots * kDT * 16 + (size_t)TE * ustride * 4 + 2 * kDW * 32 * 4 +
-           kBatchItems * sizeof(Item) + (kBatchItems + 1) * 4 + kBatchPages * 4 + kBatchItems * TE * 4;
+    const int C = delta_cluster(hidden);
+    return 2 * 16 * ceil_div(hidden / 16, C) + 16;
+}
+inline size_t delta_smem_bytes(int hidden)
+{
+    const size_t stage = (size_t)kTok * delta_pitch(hidden);
+    return (NST + 2) * stage + 3 * (size_t)kTok * kRC * 4 + (size_t)kTok * kUPitch * 2 + 2 * sizeof(Item) +
+           2 * kTok * 4 + (2 * NST + 13) * 8;
 }
 
 cudaError_t launch_lora_apply(const PoolView &pv, int32_t proj, const uint16_t *x, uint16_t *y,
@@ -891,32 +1027,47 @@ cudaError_t launch_lora_apply(const PoolView &pv, int32_t proj, const uint16_t *
                               int num_sms, cudaStream_t stream, int *launches)
 {
     static bool attrs_set = false;
-    static int occ_ustride = -1, occ_blocks = 1;
+    static int occ_hidden = -1, occ_clusters = 1;
+    if (pv.hidden > kMaxCluster * kMaxSlice) return cudaErrorInvalidValue;
     if (!attrs_set) {
         cudaError_t e = cudaFuncSetAttribute(delta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)delta_smem_bytes(kMaxRank));
+                                             (int)delta_smem_bytes(kMaxSlice));
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)plan_smem_bytes(kMaxHash));
         if (e != cudaSuccess) return e;
         attrs_set = true;
     }
-    const int ustride = (scratch.max_rank + 7) & ~7;
-    const size_t dsmem = delta_smem_bytes(ustride);
-    if (ustride != occ_ustride) {
-        int nb = 0;
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, delta_kernel, kDT, dsmem);
-        if (e != cudaSuccess) return e;
-        occ_blocks = nb > 0 ? nb : 1;
-        occ_ustride = ustride;
-    }
-    const int32_t chunk = plan_chunk(pv.max_adapters);
-    const int32_t cap = scratch.cap_tokens < chunk ? scratch.cap_tokens : chunk;
-    PlanLayout L = carve(scratch.base, cap, scratch.max_rank, pv.hidden, nullptr);
+    const int C = delta_cluster(pv.hidden);
+    const size_t dsmem = delta_smem_bytes(pv.hidden);
 
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = C;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+
+    cudaLaunchConfig_t cfg2 = {};
+    cfg2.blockDim = dim3(kThreads);
+    cfg2.dynamicSmemBytes = dsmem;
+    cfg2.stream = stream;
+    cfg2.attrs = attr;
+    cfg2.numAttrs = 2;
+    if (pv.hidden != occ_hidden) {
+        cfg2.gridDim = dim3(C * num_sms);
+        int ncl = 0;
+        cudaError_t e = cudaOccupancyMaxActiveClusters(&ncl, delta_kernel, &cfg2);
+        if (e != cudaSuccess) return e;
+        occ_clusters = ncl > 0 ? ncl : 1;
+        occ_hidden = pv.hidden;
+    }
+    cfg2.gridDim = dim3(C * occ_clusters);
+
+    const int32_t chunk = plan_chunk(pv.max_adapters);
+    const int32_t cap = scratch.cap_tokens < chunk ? scratch.cap_tokens : chunk;
+    PlanLayout L = carve(scratch.base, cap, nullptr);
 
     for (int32_t tb = 0; tb < T; tb += chunk) {
         const int32_t te = tb + chunk < T ? tb + chunk : T;
@@ -935,14 +1086,8 @@ cudaError_t launch_lora_apply(const PoolView &pv, int32_t proj, const uint16_t *
         if (e != cudaSuccess) return e;
         *launches += 1;
 
-        DeltaArgs da{pv, reinterpret_cast<const __half *>(x), reinterpret_cast<__half *>(y), scaling, L, ustride};
-        cudaLaunchConfig_t cfg2 = {};
-        cfg2.gridDim = dim3(num_sms * occ_blocks);
-        cfg2.blockDim = dim3(kDT);
-        cfg2.dynamicSmemBytes = dsmem;
-        cfg2.stream = stream;
-        cfg2.attrs = attr;
-        cfg2.numAttrs = 1;
+        DeltaArgs da{pv, reinterpret_cast<const __half *>(x), reinterpret_cast<__half *>(y), scaling, L,
+                     delta_pitch(pv.hidden)};
         e = cudaLaunchKernelEx(&cfg2, delta_kernel, da);
         if (e != cudaSuccess) return e;
         *launches += 1;

@@ -21,7 +21,7 @@
 namespace slora {
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = 8u << 20;   // 8 MiB
+constexpr size_t kNoAllocScratchBytes = 512u << 10;   // 512 KiB
 constexpr int kMaxDevices = 64;
 
 // Shared by every call of the entry point on a device; holds the last call's plan.

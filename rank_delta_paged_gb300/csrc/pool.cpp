@@ -139,8 +139,8 @@ slora_status slora_pool_create(int device, int32_t hidden, int64_t num_pages, in
     if (!out)
         return fail(SLORA_ERR_INVALID_ARG, "pool_create: out is NULL");
     *out = nullptr;
-    if (hidden < 64 || hidden > 16384 || hidden % 64 != 0)
-        return fail(SLORA_ERR_INVALID_ARG, "pool_create: hidden=%d (multiple of 64 in [64, 16384])", hidden);
+    if (hidden < 64 || hidden > 8192 || hidden % 64 != 0)
+        return fail(SLORA_ERR_INVALID_ARG, "pool_create: hidden=%d (multiple of 64 in [64, 8192])", hidden);
     if (num_pages < 1 || num_pages >= (int64_t)INT32_MAX)
         return fail(SLORA_ERR_INVALID_ARG, "pool_create: num_pages=%lld", (long long)num_pages);
     if (n_proj < 1 || max_adapters < 1 || max_adapters > (1 << 24))

@@ -106,6 +106,14 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
                  : "memory");
 }
 
+// Same, with the destination given as a shared-memory address.
+__device__ __forceinline__ void bulk_g2s_s(uint32_t dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
 // Order this thread's earlier generic-proxy accesses (e.g. an acquire of data that other
 // threads wrote with plain stores) before its later async-proxy (bulk copy) accesses.
 __device__ __forceinline__ void fence_proxy_async_global()

@@ -74,9 +74,9 @@ def test_noalloc_matches_apply_twice(make):
 
 
 def test_noalloc_refuses_batch_beyond_its_scratch():
-    # 4096 tokens with a rank-1024 adapter registered needs 16 MiB of u alone
-    ranks = np.array([1024, 8], np.int32)
-    idx = (np.arange(4096) % 2).astype(np.int32)
+    # 16384 decode tokens need about 36 * 16384 bytes of plan: more than the 512 KiB array
+    ranks = np.array([16, 8], np.int32)
+    idx = (np.arange(16384) % 2).astype(np.int32)
     w = W.Workload("noalloc_big", 256, 1, ranks, idx, None, num_pages=2 * int(ranks.sum()) + 8,
                    kv_pages=0, shuffle_seed=1, seed=3)
     with PoolSession(w) as s:
