@@ -53,7 +53,8 @@ constexpr int NST = 4;                            // ring depth (16-row stages)
 constexpr int kUPitch = kRC + 8;                  // halves per token row of the u buffer
 constexpr int kMaxRank = 1024;
 
-constexpr int kPlanThreads = 1024;
+constexpr int kPlanThreads = 1024;       // threads of the plan kernel (256 for batches of <= 256 tokens)
+constexpr int kPlanThreadsSmall = 256;
 constexpr int kMaxPlanTokens = 16384;   // token-index range per plan when groups fit
 constexpr int kMaxPlanGroups = 2048;    // distinct adapters per plan
 constexpr int kMaxHash = 2 * kMaxPlanGroups;
@@ -180,12 +181,11 @@ struct PlanArgs {
 
 constexpr int kRankBuckets = 11;        // floor(log2(rank)) for ranks 1..1024
 
-// slot page-table bases + group page-table bases + keys, slot ranks and scalings + eight
-// int group tables + token slots
+// group page-table bases + three int hash tables + seven int group tables + two short
+// token tables
 constexpr size_t plan_smem_bytes(int hs)
 {
-    return (size_t)hs * 8 + (size_t)kMaxPlanGroups * 8 + (size_t)hs * 12 + (size_t)8 * kMaxPlanGroups * 4 +
-           (size_t)kMaxPlanTokens * 2;
+    return (size_t)kMaxPlanGroups * 8 + (size_t)hs * 12 + (size_t)7 * kMaxPlanGroups * 4 + (size_t)kMaxPlanTokens * 4;
 }
 
 __device__ __forceinline__ void plan_refuse(const PlanArgs &a)
@@ -195,30 +195,29 @@ __device__ __forceinline__ void plan_refuse(const PlanArgs &a)
     a.L.hdr->n_items = 0;
 }
 
-__global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const __grid_constant__ PlanArgs a)
+template <int NT>
+__global__ void __launch_bounds__(NT, 1) plan_kernel(const __grid_constant__ PlanArgs a)
 {
     extern __shared__ __align__(16) int plan_smem[];
     const int HS = a.hash_size;
     const int Tc = a.t_end - a.t_begin;
-    long long *hpt = reinterpret_cast<long long *>(plan_smem);              // [HS] slot: page-table base
-    long long *gpt = hpt + HS;                                             // [G] page-table base
-    int *keys = reinterpret_cast<int *>(gpt + kMaxPlanGroups);             // [HS] adapter id / -1, then group id
-    int *hrank = keys + HS;                                                // [HS] slot: rank
-    float *hscale = reinterpret_cast<float *>(hrank + HS);                 // [HS] slot: scaling
-    int *gad = reinterpret_cast<int *>(hscale + HS);                       // [G] adapter
-    int *gn = gad + kMaxPlanGroups;                                        // [G] tokens
-    int *gtok = gn + kMaxPlanGroups;                                       // [G] first token position
-    int *gsh = gtok + kMaxPlanGroups;                                      // [G] token placement cursor
-    int *pit = gsh + kMaxPlanGroups;                                       // [position] first item
-    int *grank = pit + kMaxPlanGroups;                                     // [G] rank
+    long long *gpt = reinterpret_cast<long long *>(plan_smem);              // [G] page-table base
+    int *keys = reinterpret_cast<int *>(gpt + kMaxPlanGroups);             // [HS] adapter id / -1
+    int *hgrp = keys + HS;                                                 // [HS] group of the slot
+    int *hcnt = hgrp + HS;                                                 // [HS] tokens of the slot
+    int *gad = hcnt + HS;                                                  // [G] adapter
+    int *grank = gad + kMaxPlanGroups;                                     // [G] rank
     float *gscale = reinterpret_cast<float *>(grank + kMaxPlanGroups);     // [G] scaling
-    int *gperm = reinterpret_cast<int *>(gscale + kMaxPlanGroups);         // [position] group, by rank descending
-    short *tslot = reinterpret_cast<short *>(gperm + kMaxPlanGroups);      // [Tc] hash slot, then group id
-    __shared__ int warp_tot[33][1];
+    int *gslot = reinterpret_cast<int *>(gscale + kMaxPlanGroups);         // [G] hash slot
+    int *gtok = gslot + kMaxPlanGroups;                                    // [G] first token position
+    int *pit = gtok + kMaxPlanGroups;                                      // [position] first item
+    int *gperm = pit + kMaxPlanGroups;                                     // [position] group, by rank descending
+    short *tslot = reinterpret_cast<short *>(gperm + kMaxPlanGroups);      // [Tc] hash slot of the token (-1: none)
+    short *tpos = tslot + kMaxPlanTokens;                                  // [Tc] the token's place within its group
     __shared__ int warp_tot2[33][2];
-    __shared__ int s_lo, s_hi, s_G, s_nit, s_bad;
-    __shared__ int s_bucket[kRankBuckets + 1];
-    const int tid = threadIdx.x;
+    __shared__ int s_lo, s_hi, s_G, s_nit;
+    __shared__ int s_bucket[kRankBuckets + 1], s_bcur[kRankBuckets + 1];
+    const int tid = threadIdx.x, lane = tid & 31;
 
     griddep_launch_dependents();
     griddep_wait();
@@ -235,118 +234,109 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const __grid_cons
         }
         s_lo = lo;
         s_hi = hi;
-        s_bad = 0;
+        s_G = 0;
     }
-    if (tid <= kRankBuckets)
+    if (tid <= kRankBuckets) {
         s_bucket[tid] = 0;
-    for (int h = tid; h < HS; h += kPlanThreads)
+        s_bcur[tid] = 0;
+    }
+    for (int h = tid; h < HS; h += NT) {
         keys[h] = -1;
-    for (int g = tid; g < kMaxPlanGroups; g += kPlanThreads)
-        gn[g] = 0;
+        hcnt[h] = 0;
+    }
     __syncthreads();
     const int lo = s_lo, hi = s_hi;
 
-    // 1. hash the decode tokens of [t_begin, t_end) by adapter; the thread that claims a
-    //    slot stores the adapter's directory entry there
-    for (int i = tid; i < Tc; i += kPlanThreads) {
-        const int t = a.t_begin + i;
+    // 1. hash the decode tokens of [t_begin, t_end) by adapter.  The thread that claims a
+    //    slot numbers the group and fills its fields from the adapter's directory entry;
+    //    every token learns its place within its group (one atomic per warp and group).
+    for (int i0 = 0; i0 < Tc; i0 += NT) {
+        const int i = i0 + tid;
         int slot = -1;
-        const bool in_seg = t >= lo && t < hi;
-        const int ad = a.idx[t];
-        if (ad >= 0 && ad < a.pv.max_adapters) {
-            const DirEntry e = a.pv.dir[ad];
-            const bool resident = e.pt_off >= 0 && e.rank > 0 && e.rank <= kMaxRank;
-            // segment tokens run on the tensor-core prefill path unless their adapter's rank
-            // is too large for it; errors of segment tokens are reported there
-            const bool mine = !in_seg || (resident && e.rank > kMaxPrefillRank);
-            if (mine) {
-                if (resident) {
-                    int h = (int)(((uint32_t)ad * 2654435761u) & (uint32_t)(HS - 1));
-                    for (int probe = 0; probe < HS; ++probe) {
-                        const int k = atomicCAS(&keys[h], -1, ad);
-                        if (k == -1) {
-                            hrank[h] = e.rank;
-                            hscale[h] = e.scaling;
-                            hpt[h] = e.pt_off + (long long)a.proj * 2 * e.rank;
+        if (i < Tc) {
+            const int t = a.t_begin + i;
+            const bool in_seg = t >= lo && t < hi;
+            const int ad = a.idx[t];
+            if (ad >= 0 && ad < a.pv.max_adapters) {
+                const DirEntry e = a.pv.dir[ad];
+                const bool resident = e.pt_off >= 0 && e.rank > 0 && e.rank <= kMaxRank;
+                // segment tokens run on the tensor-core prefill path unless their adapter's
+                // rank is too large for it; errors of segment tokens are reported there
+                const bool mine = !in_seg || (resident && e.rank > kMaxPrefillRank);
+                if (mine) {
+                    if (resident) {
+                        int h = (int)(((uint32_t)ad * 2654435761u) & (uint32_t)(HS - 1));
+                        for (int probe = 0; probe < HS; ++probe) {
+                            const int k = atomicCAS(&keys[h], -1, ad);
+                            if (k == -1) {
+                                const int g = atomicAdd(&s_G, 1);
+                                hgrp[h] = g;
+                                if (g < kMaxPlanGroups) {
+                                    gad[g] = ad;
+                                    grank[g] = e.rank;
+                                    gscale[g] = e.scaling;
+                                    gpt[g] = e.pt_off + (long long)a.proj * 2 * e.rank;
+                                    gslot[g] = h;
+                                    atomicAdd(&s_bucket[31 - __clz(e.rank)], 1);
+                                }
+                            }
+                            if (k == -1 || k == ad) { slot = h; break; }
+                            h = (h + 1) & (HS - 1);
                         }
-                        if (k == -1 || k == ad) { slot = h; break; }
-                        h = (h + 1) & (HS - 1);
+                        // a full table cannot happen with the host's chunking (HS >= 2 x groups)
+                    } else {
+                        set_status(a.pv.status, SLORA_DEV_NOT_RESIDENT);
                     }
-                    if (slot < 0) s_bad = 1;   // more distinct adapters than the table holds
-                } else {
-                    set_status(a.pv.status, SLORA_DEV_NOT_RESIDENT);
                 }
-            }
-        } else if (ad != -1 && !in_seg) {
-            set_status(a.pv.status, SLORA_DEV_BAD_ADAPTER);
-        }
-        tslot[i] = (short)slot;
-    }
-    __syncthreads();
-
-    // 2. groups = occupied slots, numbered in slot order; keys[h] becomes the group id
-    {
-        const int per = HS / kPlanThreads;
-        const int h0 = tid * per;
-        int c[1] = {0};
-        for (int h = h0; h < h0 + per; ++h)
-            c[0] += keys[h] != -1;
-        int base[1], total[1];
-        block_excl_scan<1>(c, warp_tot, base, total);
-        int b = base[0];
-        for (int h = h0; h < h0 + per; ++h) {
-            if (keys[h] != -1) {
-                if (b < kMaxPlanGroups) {
-                    gad[b] = keys[h];
-                    grank[b] = hrank[h];
-                    gscale[b] = hscale[h];
-                    gpt[b] = hpt[h];
-                    atomicAdd(&s_bucket[31 - __clz(hrank[h])], 1);
-                }
-                keys[h] = b;
-                ++b;
+            } else if (ad != -1 && !in_seg) {
+                set_status(a.pv.status, SLORA_DEV_BAD_ADAPTER);
             }
         }
-        if (tid == 0) {
-            if (total[0] > kMaxPlanGroups) s_bad = 1;
-            s_G = total[0];
+        // the token's place within its group: lanes with the same slot share one atomic
+        const uint32_t same = __match_any_sync(0xffffffffu, slot);
+        const int leader = __ffs(same) - 1;
+        int base = 0;
+        if (slot >= 0 && lane == leader) base = atomicAdd(&hcnt[slot], __popc(same));
+        base = __shfl_sync(0xffffffffu, base, leader);
+        if (i < Tc) {
+            tslot[i] = (short)slot;
+            tpos[i] = (short)(base + __popc(same & ((1u << lane) - 1u)));
         }
     }
     __syncthreads();
-    if (s_bad) {
+    const int G = s_G;
+    if (G > kMaxPlanGroups) {
         // cannot happen with the host's chunking; refuse the batch rather than overrun
         if (tid == 0) plan_refuse(a);
         return;
     }
-    const int G = s_G;
-    if (tid == 0) {   // bucket starts, largest ranks first
+
+    // 2. groups in descending-rank order (a counting sort on floor(log2(rank)))
+    {
+        int start[kRankBuckets];
         int acc = 0;
+#pragma unroll
         for (int b = kRankBuckets - 1; b >= 0; --b) {
-            const int n = s_bucket[b];
-            s_bucket[b] = acc;
-            acc += n;
+            start[b] = acc;
+            acc += s_bucket[b];
+        }
+        for (int g = tid; g < G; g += NT) {
+            const int b = 31 - __clz(grank[g]);
+            int st = 0;
+#pragma unroll
+            for (int bb = 0; bb < kRankBuckets; ++bb)
+                if (bb == b) st = start[bb];
+            gperm[st + atomicAdd(&s_bcur[b], 1)] = g;
         }
     }
-    for (int i = tid; i < Tc; i += kPlanThreads) {
-        const int h = tslot[i];
-        if (h >= 0) {
-            const int g = keys[h];
-            tslot[i] = (short)g;
-            atomicAdd(&gn[g], 1);
-        }
-    }
-    __syncthreads();
-    for (int g = tid; g < G; g += kPlanThreads)
-        gperm[atomicAdd(&s_bucket[31 - __clz(grank[g])], 1)] = g;
     __syncthreads();
 
-    // 3. per-group offsets (tokens, items), laid out in descending-rank order so the
-    //    costliest items come first
-    const int per_g = ceil_div(G > 0 ? G : 1, kPlanThreads);   // <= 2
+    // 3. per-group offsets (tokens, items) in that order
+    const int per_g = ceil_div(G > 0 ? G : 1, NT);
     const int p0 = tid * per_g;
     int mine[2] = {0, 0};
     for (int q = 0; q < per_g && p0 + q < G; ++q) {
-        const int n = gn[gperm[p0 + q]];
+        const int n = hcnt[gslot[gperm[p0 + q]]];
         mine[0] += n;
         mine[1] += ceil_div(n, kTok);
     }
@@ -354,10 +344,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const __grid_cons
     block_excl_scan<2>(mine, warp_tot2, off, tot);
     for (int q = 0; q < per_g && p0 + q < G; ++q) {
         const int g = gperm[p0 + q];
-        const int n = gn[g];
+        const int n = hcnt[gslot[g]];
         gtok[g] = off[0];
         pit[p0 + q] = off[1];
-        gsh[g] = 0;
         off[0] += n;
         off[1] += ceil_div(n, kTok);
     }
@@ -369,9 +358,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const __grid_cons
         return;
     }
 
-    // 4. items, in parallel over items: each finds its group position by binary search over
-    //    the (strictly increasing) first-item offsets
-    for (int i = tid; i < n_items; i += kPlanThreads) {
+    // 4. items, in parallel over items (each finds its group position by binary search over
+    //    the strictly increasing first-item offsets), and the token order
+    for (int i = tid; i < n_items; i += NT) {
         int lo_p = 0, hi_p = G - 1;
         while (lo_p < hi_p) {
             const int mid = (lo_p + hi_p + 1) >> 1;
@@ -381,7 +370,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const __grid_cons
         const int tc = i - pit[lo_p];
         Item it;
         it.t0 = tc * kTok;
-        it.nt = min(kTok, gn[g] - it.t0);
+        it.nt = min(kTok, hcnt[gslot[g]] - it.t0);
         it.rank = grank[g];
         it.tok_begin = gtok[g];
         it.adapter = gad[g];
@@ -392,13 +381,10 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const __grid_cons
         dst4[0] = src4[0];
         dst4[1] = src4[1];
     }
-    // 5. token placement (gsh, the cursors, were zeroed before the last barrier)
-    for (int i = tid; i < Tc; i += kPlanThreads) {
-        const int g = tslot[i];
-        if (g >= 0) {
-            const int pos = gtok[g] + atomicAdd(&gsh[g], 1);
-            a.L.tok_order[pos] = a.t_begin + i;
-        }
+    for (int i = tid; i < Tc; i += NT) {
+        const int h = tslot[i];
+        if (h >= 0)
+            a.L.tok_order[gtok[hgrp[h]] + tpos[i]] = a.t_begin + i;
     }
     if (tid == 0) {
         a.L.hdr->n_groups = G;
@@ -1033,7 +1019,10 @@ cudaError_t launch_lora_apply(const PoolView &pv, int32_t proj, const uint16_t *
         cudaError_t e = cudaFuncSetAttribute(delta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)delta_smem_bytes(kMaxSlice));
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(plan_kernel<kPlanThreads>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)plan_smem_bytes(kMaxHash));
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(plan_kernel<kPlanThreadsSmall>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)plan_smem_bytes(kMaxHash));
         if (e != cudaSuccess) return e;
         attrs_set = true;
@@ -1077,12 +1066,14 @@ cudaError_t launch_lora_apply(const PoolView &pv, int32_t proj, const uint16_t *
         PlanArgs pa{pv, proj, idx, T, seg_indptr, n_seg, tb, te, hs, L};
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(1);
-        cfg.blockDim = dim3(kPlanThreads);
+        const bool small = te - tb <= kPlanThreadsSmall;
+        cfg.blockDim = dim3(small ? kPlanThreadsSmall : kPlanThreads);
         cfg.dynamicSmemBytes = plan_smem_bytes(hs);
         cfg.stream = stream;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        cudaError_t e = cudaLaunchKernelEx(&cfg, plan_kernel, pa);
+        cudaError_t e = small ? cudaLaunchKernelEx(&cfg, plan_kernel<kPlanThreadsSmall>, pa)
+                              : cudaLaunchKernelEx(&cfg, plan_kernel<kPlanThreads>, pa);
         if (e != cudaSuccess) return e;
         *launches += 1;
 
