@@ -52,6 +52,12 @@ def parse():
     return ap.parse_args()
 
 
+# DRAM bytes (read + write) per launch of the delta kernel, from one ncu capture of the
+# current kernel on the workload (profiles/delta_kernel_<workload>.md gives the command);
+# a workload without a capture of the current kernel reports null.
+TRAFFIC = {"decode_7b_h4096_a100_t256_zipf1": 41897984}
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -279,10 +285,32 @@ def main():
     ms_per_step = total_ms / K
     value = tokens_per_s_per_layer(job_tokens, w.n_layers, ms_per_step)
 
-    # dominant kernel roofline: the delta kernels are the whole step
+    # dominant kernel roofline: the delta kernel of one projection, timed on its own
+    # (the pool records an event between the plan and the delta; that record serialises
+    # the two kernels, so this pass is separate from the timed steps above)
     hbm, peak_kind = peaks()
     alg_bytes = algorithmic_bytes(w)
-    achieved = alg_bytes / (ms_per_step / 1e3) / 1e9
+    alg_bytes_launch = alg_bytes / w.n_proj
+    Kd = min(K, 200)
+    d0 = [torch.cuda.Event(enable_timing=True) for _ in range(Kd)]
+    d1 = [torch.cuda.Event(enable_timing=True) for _ in range(Kd)]
+    for ev in d0 + d1:
+        ev.record(stream)   # creates the events
+    torch.cuda.synchronize()
+    for k in range(Kd):
+        flush.zero_()
+        rdp.slora_pool_set_stage_event(sess.pool, d0[k])
+        rdp.slora_lora_apply(sess.pool, 0, xs[0], ys[0], w.T, idx, seg, n_seg, None, stream)
+        d1[k].record(stream)
+    torch.cuda.synchronize()
+    rdp.slora_pool_set_stage_event(sess.pool, None)
+    delta_ms = statistics.median(a.elapsed_time(b) for a, b in zip(d0, d1))
+    t_d = torch.tensor([delta_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t_d, op=dist.ReduceOp.MAX)
+    delta_ms = float(t_d.item())
+    achieved = alg_bytes_launch / (delta_ms / 1e3) / 1e9
+    step_achieved = alg_bytes / (ms_per_step / 1e3) / 1e9
     kernel_stats = rdp.slora_pool_kernel_stats(sess.pool) if hasattr(rdp, "slora_pool_kernel_stats") else None
 
     # ---- end to end through the C ABI from pinned host buffers --------------------
@@ -329,10 +357,13 @@ def main():
                                "per-step CUDA-event intervals"),
         "gpu_launches": int(launches),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": None,
-                     "kernel": "whole delta step (plan + delta kernels)",
+                     "frac": achieved / hbm, "traffic": TRAFFIC.get(w.name),
+                     "kernel": "delta_kernel" + (" + prefill_kernel" if n_seg else "") +
+                               " (one projection; median CUDA-event time between the plan and the end of the call)",
+                     "launch_ms": delta_ms, "algorithmic_bytes_per_launch": alg_bytes_launch,
                      "peak_kind": f"{peak_kind} HBM copy bandwidth",
-                     "algorithmic_bytes_per_step": alg_bytes},
+                     "step": {"achieved": step_achieved, "frac": step_achieved / hbm,
+                              "algorithmic_bytes": alg_bytes, "includes": "plan + delta kernels"}},
         "e2e": {"value": e2e_value, "unit": "tokens/s/layer", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h),
                 "includes": "H2D of x, y0, token map; cold load of the batch's adapters from the "

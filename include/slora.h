@@ -246,6 +246,14 @@ slora_status slora_get_device_status(slora_pool_t pool, int32_t *status);
 /* Number of kernels this pool has launched so far (scatter, directory, plan and delta
  * kernels), counted on the host at each launch. */
 slora_status slora_pool_launch_count(slora_pool_t pool, int64_t *out);
+/* Measurement hook.  event: a cudaEvent_t created by the caller on the pool's device, or
+ * NULL to clear.  While set, every slora_lora_apply call of the pool records it on the
+ * call's stream between the token plan and the first delta kernel, so the caller can time
+ * the delta kernels alone.  The record breaks the launch overlap of the plan and the
+ * delta, so a timing loop that wants the overlapped step leaves it unset.  The pool does
+ * not take ownership; clear it before destroying the event.  The S-LoRA pages have no
+ * counterpart for it. */
+slora_status slora_pool_set_stage_event(slora_pool_t pool, void *event);
 
 #ifdef __cplusplus
 }

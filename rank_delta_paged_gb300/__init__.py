@@ -29,6 +29,7 @@ __all__ = [
     "slora_lora_apply", "slora_lora_apply_noalloc",
     "slora_adapter_pages", "slora_adapter_rank", "slora_page_read", "slora_get_device_status",
     "slora_pool_launch_count",
+    "slora_pool_set_stage_event",
 ]
 
 _I32, _I64, _U64, _F32, _P = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float, ctypes.c_void_p
@@ -63,6 +64,7 @@ _SIGS = {
     "slora_page_read": [_P, _I32, _P],
     "slora_get_device_status": [_P, _P],
     "slora_pool_launch_count": [_P, _P],
+    "slora_pool_set_stage_event": [_P, _P],
 }
 _RESTYPE = {"slora_status_str": ctypes.c_char_p, "slora_last_error": ctypes.c_char_p,
             "slora_version": _I32}
@@ -261,3 +263,10 @@ def slora_pool_launch_count(pool: int) -> int:
     v = ctypes.c_int64()
     _call("slora_pool_launch_count", pool, ctypes.byref(v))
     return v.value
+
+
+def slora_pool_set_stage_event(pool: int, event) -> None:
+    """Record `event` (a torch.cuda.Event, a raw cudaEvent_t as int, or None) between the
+    plan and the delta kernels of every apply of the pool; None clears it."""
+    handle = 0 if event is None else int(getattr(event, "cuda_event", event))
+    _call("slora_pool_set_stage_event", pool, ctypes.c_void_p(handle))

@@ -1010,7 +1010,7 @@ inline size_t delta_smem_bytes(int hidden)
 cudaError_t launch_lora_apply(const PoolView &pv, int32_t proj, const uint16_t *x, uint16_t *y,
                               int32_t T, const int32_t *idx, const int32_t *seg_indptr,
                               int32_t n_seg, const float *scaling, const PlanScratch &scratch,
-                              int num_sms, cudaStream_t stream, int *launches)
+                              int num_sms, cudaStream_t stream, int *launches, cudaEvent_t after_plan)
 {
     static bool attrs_set = false;
     static int occ_hidden = -1, occ_clusters = 1;
@@ -1077,6 +1077,10 @@ cudaError_t launch_lora_apply(const PoolView &pv, int32_t proj, const uint16_t *
         if (e != cudaSuccess) return e;
         *launches += 1;
 
+        if (after_plan && tb == 0) {
+            e = cudaEventRecord(after_plan, stream);
+            if (e != cudaSuccess) return e;
+        }
         DeltaArgs da{pv, reinterpret_cast<const __half *>(x), reinterpret_cast<__half *>(y), scaling, L,
                      delta_pitch(pv.hidden)};
         e = cudaLaunchKernelEx(&cfg2, delta_kernel, da);

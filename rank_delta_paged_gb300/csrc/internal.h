@@ -88,7 +88,8 @@ cudaError_t launch_prefill(const PoolView &pv, int32_t proj, const uint16_t *x, 
 cudaError_t launch_lora_apply(const PoolView &pv, int32_t proj, const uint16_t *x, uint16_t *y,
                               int32_t T, const int32_t *idx, const int32_t *seg_indptr,
                               int32_t n_seg, const float *scaling, const PlanScratch &scratch,
-                              int num_sms, cudaStream_t stream, int *launches);
+                              int num_sms, cudaStream_t stream, int *launches,
+                              cudaEvent_t after_plan = nullptr);
 
 // What the hot path needs to know about a pool, for entry points defined outside
 // pool.cpp (pool.cpp).  *launches points at the pool's kernel-launch counter.

@@ -61,6 +61,7 @@ struct slora_pool {
     PlanScratch plan;
     std::vector<AdapterRec> adapters;
     int64_t launches = 0;  // kernels launched by this pool
+    cudaEvent_t stage_event = nullptr;   // measurement hook: recorded between plan and delta
     int32_t max_rank = 0;  // largest registered rank (sizes the plan scratch)
 };
 
@@ -578,10 +579,19 @@ slora_status slora_lora_apply(slora_pool_t p, int32_t proj, const void *x, void 
                 p->max_adapters, p->status_dev};
     int launched = 0;
     cudaError_t e = launch_lora_apply(pv, proj, (const uint16_t *)x, (uint16_t *)y, T, idx, seg_indptr,
-                                      n_seg, scaling, p->plan, p->num_sms, (cudaStream_t)stream, &launched);
+                                      n_seg, scaling, p->plan, p->num_sms, (cudaStream_t)stream, &launched,
+                                      p->stage_event);
     p->launches += launched;
     if (e != cudaSuccess)
         return fail(SLORA_ERR_CUDA, "lora_apply: launch failed: %s", cudaGetErrorString(e));
+    return SLORA_OK;
+}
+
+slora_status slora_pool_set_stage_event(slora_pool_t p, void *event)
+{
+    if (!p)
+        return fail(SLORA_ERR_INVALID_ARG, "pool_set_stage_event: null pool");
+    p->stage_event = (cudaEvent_t)event;
     return SLORA_OK;
 }
 
