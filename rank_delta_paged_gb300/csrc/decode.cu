@@ -17,17 +17,19 @@
 //   delta_kernel: persistent clusters of C = ceil(hidden / 1024) CTAs; a cluster takes
 //     whole items, and CTA c of the cluster owns slice c of the hidden dimension (at most
 //     1024 elements): the K range of the shrink and the output columns of the expand.
-//     Per item and per chunk of 128 rank rows:
+//     An item runs in units of 128 rank rows:
 //       shrink  partial u[t][j] = sum over the CTA's K slice of x[t][k] * At[j][k]
 //       reduce  every CTA sums the C partials (read from the cluster's shared memory, in
 //               CTA order) and rounds u to fp16 once
 //       expand  acc[t][c] += sum_j u[t][j] * B[j][c] over the CTA's columns
-//     then y[t][c] = y0[t][c] + s * acc[t][c].  One producer warp streams the row slices
-//     (A^T rows, B rows, the tokens' x and y0 rows) with 1-D bulk copies into a ring of
+//     then y[t][c] = y0[t][c] + s * acc[t][c].  A producer warp streams the row slices
+//     (the tokens' x rows, A^T rows, y0 rows, B rows) with 1-D bulk copies into a ring of
 //     16-row stages; eight consumer warps contract them on the tensor cores with
-//     warp-level mma.sync m16n8k16 (fp16 operands, fp32 accumulators; tokens on M).
-//     Each page row is read once per item; the cluster exchanges only the small fp32
-//     partials.  Every wait is bounded in time.
+//     warp-level mma.sync m16n8k16 (fp16 operands, fp32 accumulators; tokens on M),
+//     running the shrink of unit u before the expand of unit u-1 so that the wait for the
+//     cluster's partials overlaps useful work; a signal warp relays the "partials
+//     written / read" events to the cluster.  Each page row is read once per item; the
+//     cluster exchanges only the small fp32 partials.  Every wait is bounded in time.
 //
 // A token's arithmetic is fixed by the fragment layout, the slice boundaries and the CTA
 // order of the partial sum, never by the other tokens of its item, so results do not
