@@ -253,12 +253,16 @@ def main():
     if args.steps > 0:
         K = args.steps
     else:
-        t0 = time.perf_counter()
+        # device time of one flush + step, so that the timed region lasts about 2 s
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
         for _ in range(5):
             flush.zero_()
             step()
+        g1.record(stream)
         torch.cuda.synchronize()
-        per = (time.perf_counter() - t0) / 5
+        per = g0.elapsed_time(g1) / 5 / 1e3
         K = int(min(20000, max(10, 2.0 / max(per, 1e-6))))
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
