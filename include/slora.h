@@ -163,11 +163,16 @@ slora_status slora_adapter_unregister(slora_pool_t pool, int32_t adapter_id,
  * SLORA_ERR_POOL_FULL is returned.
  * evict() enqueues on `stream` the clearing of the directory entry, returns the
  * adapter's pages to the free list and records the release event on `stream`.
+ * adapters_evict() does the same for a list with one directory update for all of it:
+ * ids that are not resident (or repeated) are skipped; an id that is not registered
+ * returns SLORA_ERR_NOT_REGISTERED before anything is evicted.
  * ------------------------------------------------------------------------- */
 slora_status slora_adapter_load(slora_pool_t pool, int32_t adapter_id, slora_stream_t stream);
 slora_status slora_adapters_load(slora_pool_t pool, int32_t n, const int32_t *adapter_ids /*host*/,
                                  slora_stream_t stream);
 slora_status slora_adapter_evict(slora_pool_t pool, int32_t adapter_id, slora_stream_t stream);
+slora_status slora_adapters_evict(slora_pool_t pool, int32_t n, const int32_t *adapter_ids /*host*/,
+                                  slora_stream_t stream);
 slora_status slora_adapter_is_resident(slora_pool_t pool, int32_t adapter_id, int32_t *out);
 
 /* ---------------------------------------------------------------------------

@@ -30,6 +30,7 @@ __all__ = [
     "slora_adapter_pages", "slora_adapter_rank", "slora_page_read", "slora_get_device_status",
     "slora_pool_launch_count",
     "slora_pool_set_stage_event",
+    "slora_adapters_evict",
 ]
 
 _I32, _I64, _U64, _F32, _P = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float, ctypes.c_void_p
@@ -65,6 +66,7 @@ _SIGS = {
     "slora_get_device_status": [_P, _P],
     "slora_pool_launch_count": [_P, _P],
     "slora_pool_set_stage_event": [_P, _P],
+    "slora_adapters_evict": [_P, _I32, _P, _P],
 }
 _RESTYPE = {"slora_status_str": ctypes.c_char_p, "slora_last_error": ctypes.c_char_p,
             "slora_version": _I32}
@@ -217,6 +219,10 @@ def slora_adapters_load(pool: int, n: int, adapter_ids, stream=None) -> None:
 
 def slora_adapter_evict(pool: int, adapter_id: int, stream=None) -> None:
     _call("slora_adapter_evict", pool, adapter_id, _stream(stream))
+
+
+def slora_adapters_evict(pool: int, n: int, adapter_ids, stream=None) -> None:
+    _call("slora_adapters_evict", pool, n, _ptr(adapter_ids), _stream(stream))
 
 
 def slora_adapter_is_resident(pool: int, adapter_id: int) -> bool:

@@ -481,6 +481,53 @@ slora_status slora_adapter_evict(slora_pool_t p, int32_t id, slora_stream_t stre
     return SLORA_OK;
 }
 
+slora_status slora_adapters_evict(slora_pool_t p, int32_t n, const int32_t *ids, slora_stream_t stream)
+{
+    if (!p || n < 0 || (n > 0 && !ids))
+        return fail(SLORA_ERR_INVALID_ARG, "adapters_evict: n=%d", n);
+    std::vector<int32_t> todo;
+    std::unordered_set<int32_t> seen;
+    for (int32_t i = 0; i < n; ++i) {
+        const int32_t id = ids[i];
+        if (!valid_id(p, id))
+            return fail(SLORA_ERR_INVALID_ARG, "adapters_evict: id=%d", id);
+        const AdapterRec &a = p->adapters[(size_t)id];
+        if (!a.registered)
+            return fail(SLORA_ERR_NOT_REGISTERED, "adapters_evict: id=%d", id);
+        if (a.resident && seen.insert(id).second)
+            todo.push_back(id);
+    }
+    if (todo.empty())
+        return SLORA_OK;
+    slora_status st = set_device(p);
+    if (st != SLORA_OK)
+        return st;
+    DirArgs dargs;
+    dargs.n = 0;
+    for (size_t i = 0; i < todo.size(); ++i) {
+        const AdapterRec &a = p->adapters[(size_t)todo[i]];
+        dargs.upd[dargs.n++] = DirUpdate{todo[i], a.rank, a.scaling, 0, -1};
+        if (dargs.n == kMaxDirUpdatesPerLaunch || i + 1 == todo.size()) {
+            CUDA_TRY(launch_dir_update(p->dir_dev, dargs, (cudaStream_t)stream));
+            p->launches += 1;
+            dargs.n = 0;
+        }
+    }
+    for (int32_t id : todo) {
+        AdapterRec &a = p->adapters[(size_t)id];
+        const int64_t rows = adapter_rows(p, a);
+        // pt_host still holds the pages handed out at load time
+        if ((st = p->pages.release(rows, a.pt_host)) != SLORA_OK)
+            return st;
+        p->arena.release(a.pt_off, rows);
+        a.pt_off = -1;
+        a.resident = false;
+    }
+    CUDA_TRY(cudaEventRecord(p->release_event, (cudaStream_t)stream));
+    p->release_pending = true;
+    return SLORA_OK;
+}
+
 slora_status slora_adapter_is_resident(slora_pool_t p, int32_t id, int32_t *out)
 {
     if (!p || !valid_id(p, id) || !out)

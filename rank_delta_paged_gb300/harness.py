@@ -12,7 +12,7 @@ from typing import Iterable, Optional
 import numpy as np
 import torch
 
-from . import (slora_adapter_register, slora_adapters_load, slora_adapter_evict,
+from . import (slora_adapter_register, slora_adapters_load, slora_adapters_evict,
                slora_get_device_status, slora_lora_apply, slora_pages_alloc, slora_pool_create,
                slora_pool_destroy, slora_adapter_is_resident)
 from .workloads import Workload
@@ -45,9 +45,8 @@ class PoolSession:
         slora_adapters_load(self.pool, int(ids.shape[0]), ids, stream)
 
     def evict(self, ids: Iterable[int], stream=None) -> None:
-        for a in ids:
-            if slora_adapter_is_resident(self.pool, int(a)):
-                slora_adapter_evict(self.pool, int(a), stream)
+        ids = np.ascontiguousarray(np.asarray(list(ids), dtype=np.int32))
+        slora_adapters_evict(self.pool, int(ids.shape[0]), ids, stream)
 
     # ---- device inputs ------------------------------------------------------------
     def device_inputs(self, p: int = 0):
