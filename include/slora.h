@@ -259,6 +259,14 @@ slora_status slora_pool_launch_count(slora_pool_t pool, int64_t *out);
  * not take ownership; clear it before destroying the event.  The S-LoRA pages have no
  * counterpart for it. */
 slora_status slora_pool_set_stage_event(slora_pool_t pool, void *event);
+/* Test hook.  Forces the number of CTAs per thread-block cluster of the prefill
+ * (segment) kernel for every later call in the process: 1, 2, 4 or 8, or 0 to let each
+ * call choose from its batch size (the default).  The result does not depend on it up to
+ * the summation order of the cluster's partial products.  A cluster size whose hidden
+ * slices would leave a CTA without columns makes slora_lora_apply fail with
+ * SLORA_ERR_CUDA.  Other values return SLORA_ERR_INVALID_ARG.  The S-LoRA pages have no
+ * counterpart for it. */
+slora_status slora_debug_set_prefill_cluster(int32_t ctas);
 
 #ifdef __cplusplus
 }

@@ -31,6 +31,7 @@ __all__ = [
     "slora_pool_launch_count",
     "slora_pool_set_stage_event",
     "slora_adapters_evict",
+    "slora_debug_set_prefill_cluster",
 ]
 
 _I32, _I64, _U64, _F32, _P = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float, ctypes.c_void_p
@@ -67,6 +68,7 @@ _SIGS = {
     "slora_pool_launch_count": [_P, _P],
     "slora_pool_set_stage_event": [_P, _P],
     "slora_adapters_evict": [_P, _I32, _P, _P],
+    "slora_debug_set_prefill_cluster": [_I32],
 }
 _RESTYPE = {"slora_status_str": ctypes.c_char_p, "slora_last_error": ctypes.c_char_p,
             "slora_version": _I32}
@@ -269,6 +271,11 @@ def slora_pool_launch_count(pool: int) -> int:
     v = ctypes.c_int64()
     _call("slora_pool_launch_count", pool, ctypes.byref(v))
     return v.value
+
+
+def slora_debug_set_prefill_cluster(ctas: int) -> None:
+    """Force the prefill kernel's CTAs per cluster (1, 2, 4, 8) for later calls; 0 = auto."""
+    _call("slora_debug_set_prefill_cluster", int(ctas))
 
 
 def slora_pool_set_stage_event(pool: int, event) -> None:

@@ -408,63 +408,7 @@ struct DeltaArgs {
     int32_t pitch;          // bytes per row of a stage / x / y0 buffer: 2 * largest slice + 16
 };
 
-// ---- cluster and tensor-core helpers (inline PTX) -------------------------------------
-__device__ __forceinline__ uint32_t cluster_ctarank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ uint32_t cluster_nctarank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ uint32_t cluster_id_x()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ uint32_t ncluster_x()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-    return r;
-}
-// Address of the same shared-memory location in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank)
-{
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-    return r;
-}
-__device__ __forceinline__ float ld_cluster_f32(uint32_t caddr)
-{
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(caddr) : "memory");
-    return v;
-}
-// Arrive (release, cluster scope) on an mbarrier in another CTA of the cluster.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t caddr)
-{
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-                 "selp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(ok)
-                 : "r"(smem_u32(bar)), "r"(parity)
-                 : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ void cluster_sync_all()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
+// ---- decode-specific helpers (inline PTX) ---------------------------------------------
 __device__ __forceinline__ void consumers_sync()
 {
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
@@ -488,31 +432,6 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
         "{%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// Bounded wait on an mbarrier phase.  After the first timeout anywhere in the CTA
-// (recorded in *abort and as SLORA_DEV_TIMEOUT) every wait returns at once, so the
-// kernel runs to its end without further waiting.
-template <bool kCluster>
-__device__ __forceinline__ void wait_phase(uint64_t *bar, uint32_t parity, volatile int *abort, int32_t *status)
-{
-    auto probe = [&]() { return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
-    if (probe())
-        return;
-    const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (probe())
-            return;
-        if ((it & 63u) == 0) {
-            if (*abort)
-                return;
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
-                set_status(status, SLORA_DEV_TIMEOUT);
-                *abort = 1;
-                return;
-            }
-        }
-    }
 }
 
 // The k-th item of this cluster: rounds of ncl items, walked in alternating direction so

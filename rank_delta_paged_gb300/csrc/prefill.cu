@@ -10,18 +10,45 @@
 // segment is the one place where the delta is a real GEMM: U = X_s A (T_s x r), then
 // Y_s = Y0_s + s * U B.
 //
-// One persistent CTA per SM walks units (segment, 128-token M tile, column part):
-//   shrink   K loop over hidden in 64-element blocks, 4-stage cp.async pipeline into
-//            128-byte-swizzled K-major shared memory (X rows and the adapter's A^T page
-//            rows, gathered through the page table), tcgen05.mma M=128, N=r (padded to a
-//            multiple of 16 with zero rows in shared memory, never in the pool), K=16 per
-//            instruction, accumulating in TMEM.
-//   U        TMEM -> registers -> fp16 -> K-major swizzled shared memory (the A operand
-//            of the expand).  This rounding of x A to fp16 is the only extra rounding.
-//   expand   256-column tiles of B's page rows as the MN-major operand, double-buffered,
-//            tcgen05.mma M=128, N=256, K=r; epilogue y = y0 + s * acc, one fp16 rounding.
-// Every mbarrier wait is bounded; a unit whose tokens disagree on their adapter, or whose
-// adapter is not resident, is skipped with a device status code.
+// Work unit: one 128-token tile of one segment.  Persistent clusters of C CTAs (C = 1,
+// 2, 4 or 8, chosen on the host from the batch size so that the units fill the SMs)
+// take units in turn; CTA c of a cluster owns hidden slice c: the K range of its part
+// of the shrink and the N range of its part of the expand, so every byte of x, y0, y and
+// of the adapter's pages is moved by exactly one CTA.
+//
+// Warp roles (384 threads, one CTA per SM):
+//   warp 3      scheduler and token loader: maps the cluster's next unit to (segment,
+//               tile), checks the tile's tokens agree on the adapter, reads the directory
+//               and the page table (invalid pages read as zeros) and publishes a unit
+//               descriptor with the unit's page ids through a two-slot ring; then one lane
+//               streams the unit's token tiles (128 x 64 of x for the shrink, then of y0
+//               for the expand) by TMA tensor-tile loads with the 128-byte swizzle into a
+//               ring of 16 KiB slots, as many as shared memory holds (5 to 8), as fast as
+//               slots free up.
+//   warps 0-1, 8-11  page-row gather: the adapter's page rows for each stage (64-element
+//               pieces of the A^T rows, or of the B rows) go through the page table into a
+//               three-slot ring in the same swizzled layout, 16 bytes per cp.async, spread
+//               over 192 threads (a gather runs at about 10 GB/s per issuing warp).  The
+//               copies signal the slot's mbarrier as they land
+//               (cp.async.mbarrier.arrive.noinc), so no thread waits for data.  The token
+//               stream runs up to a whole ring ahead; the page rows, mostly L2 hits, follow
+//               just in time, so a slot of either ring is held only as long as it must be.
+//   warp 2      one thread issues tcgen05.mma: the shrink M=128, N=r (padded to a
+//               multiple of 16 with zero rows), K=16 per instruction into TMEM columns
+//               0..127; the expand M=128, N=64, K=r into four 64-column TMEM buffers.
+//   warps 4-7   exchange and epilogue (warp 4 + q reads TMEM lanes 32q..32q+31).  After
+//               the shrink, the partial U of each CTA is reduced over the cluster: rows
+//               are owned round the cluster, partial rows go to their owner's shared memory
+//               (st.shared::cluster), the owner sums the C partials in CTA order, rounds
+//               to fp16 once (the only extra rounding) and writes the row into every CTA's
+//               U operand.  Then, tile by tile, each warp forms y = y0 + s * acc for its 32
+//               rows in place in the y0 slot and writes them back with its own TMA
+//               tensor-tile store (a ragged last tile of a segment is stored row by row, so
+//               no token of another segment is touched); the last warp done with a slot
+//               returns it to the ring, so the four warps never wait for one another there.
+// Every wait is bounded; a unit whose tokens disagree on their adapter, or whose adapter
+// is not resident, is skipped with a device status code.
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -32,364 +59,647 @@
 namespace slora {
 namespace {
 
-constexpr int kPThreads = 256;
-constexpr int MT = 128;            // tokens per M tile
-constexpr int KBLK = 64;           // K elements per stage (one 128-byte swizzle atom row)
-constexpr int NSTG = 4;
-constexpr int NT = 256;            // expand N tile
-constexpr int kXBytes = MT * 128;                  // 16 KiB
-constexpr int kABytes = kMaxPrefillRank * 128;     // 16 KiB
-constexpr int kStage = kXBytes + kABytes;          // 32 KiB
-constexpr int kUBytes = (kMaxPrefillRank / 64) * MT * 128;   // 32 KiB
-constexpr int kBBuf = kMaxPrefillRank * NT * 2;    // 64 KiB (two fit in the stage area)
-constexpr uint32_t kTmemCols = 512;
-constexpr int kSegSmem = (kMaxSegments + 1) * 4;
-constexpr int kSmemBytes = 1024 /*align slack*/ + NSTG * kStage + kUBytes + kSegSmem + 2 * kMaxPrefillRank * 4;
+constexpr int kWarps = 12;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kMmaWarp = 2;
+constexpr int kSchedWarp = 3;
+constexpr int kEpiWarp0 = 4;                  // warps 4-7: one per TMEM lane quarter
+constexpr int kEpiWarps = 4;
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kProdWarps = 6;                 // warps 0-1 and 8-11 gather page rows
+constexpr int kProdThreads = 32 * kProdWarps;
+constexpr int MT = 128;                       // tokens per unit
+constexpr int KBLK = 64;                      // K elements (shrink) or columns (expand) per stage
+constexpr int kTileBytes = MT * 128;          // 128 rows x 64 fp16, 128-byte rows
+constexpr int kUBytes = 2 * kTileBytes;       // U operand: 128 x 128 fp16, two 64-column atoms
+constexpr int NB = 4;                         // expand accumulator buffers in TMEM
+constexpr uint32_t kTmemCols = 512;           // U at 0..127, expand buffer b at 128 + 64 b
+constexpr int kXPitchMax = kMaxPrefillRank * 4 + 16;
+constexpr int kMaxClusterP = 8;
+constexpr int kPSlots = 3;                    // page-row ring
+constexpr int kMaxTSlots = 8;                 // token-tile ring (as many as shared memory holds)
+constexpr size_t kSmemLimit = 227 * 1024;     // dynamic + static shared memory of one CTA
+constexpr size_t kStaticReserve = 512;        // the kernel's static shared memory, rounded up
 
-static_assert(2 * kBBuf <= NSTG * kStage, "B double buffer reuses the shrink stages");
-
-struct PrefillArgs {
-    PoolView pv;
-    int32_t proj;
-    const __half *x;
-    __half *y;
-    int32_t T;
-    const int32_t *idx;
-    const int32_t *seg_indptr;
-    int32_t n_seg;
-    const float *scaling;
+constexpr int kCompute = 0, kSkip = 1, kEnd = 2;
+struct alignas(64) UnitDesc {
+    int32_t m0, mlen, rank, r_pad;
+    float sc;
+    int32_t flag;
+    int32_t pad[2];
+    int32_t pg[2 * kMaxPrefillRank];   // pool pages of the A^T rows, then of the B rows; -1 reads zeros
 };
 
-__device__ __forceinline__ uint4 pack_h8(const uint32_t *v)
+struct PrefillArgs {
+    CUtensorMap tmap_x;   // x [T][hidden], box 64 x 128, 128-byte swizzle
+    CUtensorMap tmap_y;   // y likewise (y0 loads)
+    CUtensorMap tmap_ys;  // y with 64 x 32 boxes: each epilogue warp stores its own 32 rows
+    PoolView pv;
+    __half *y;
+    const int32_t *idx;
+    const int32_t *seg_indptr;
+    const float *scaling;
+    int32_t proj;
+    int32_t T;
+    int32_t n_seg;
+    int32_t C;       // CTAs per cluster
+    int32_t slice;   // hidden elements per CTA, a multiple of 64
+    int32_t nt;      // token-tile slots
+};
+
+// Shared memory: token-tile ring, page-row ring, the U operand, two unit descriptors,
+// and the buffer that receives other CTAs' partial rows.
+constexpr size_t xbuf_bytes(int C) { return (size_t)(C - 1) * (MT / C) * kXPitchMax; }
+constexpr size_t fixed_bytes(int C)
+{
+    return 1024 + (size_t)kPSlots * kTileBytes + kUBytes + 2 * sizeof(UnitDesc) + xbuf_bytes(C);
+}
+constexpr int tslots_for(int C)
+{
+    const size_t n = (kSmemLimit - kStaticReserve - fixed_bytes(C)) / kTileBytes;
+    return n > (size_t)kMaxTSlots ? kMaxTSlots : (int)n;
+}
+constexpr size_t smem_bytes_for(int C) { return fixed_bytes(C) + (size_t)tslots_for(C) * kTileBytes; }
+static_assert(tslots_for(8) >= 5 && tslots_for(2) >= 6, "token ring depth");
+
+// When every cp.async this thread issued so far has landed, arrive on the mbarrier (the
+// arrival counts toward the barrier's expected count).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// Barrier of the epilogue warps that also ORs a flag over them.
+__device__ __forceinline__ bool epi_sync_or(bool v)
+{
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, %2, p;\n\t"
+                 "selp.u32 %0, 1, 0, q;\n\t}"
+                 : "=r"(r)
+                 : "r"((uint32_t)v), "n"(kEpiThreads)
+                 : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ uint4 pack_h8(const float *f)
 {
     uint4 r;
     __half2 *h = reinterpret_cast<__half2 *>(&r);
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-        h[i] = __floats2half2_rn(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+        h[i] = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
     return r;
 }
 
-__global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_constant__ PrefillArgs a)
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *stages = smem;                                  // NSTG x (X 16K | A 16K)
-    uint8_t *Us = smem + NSTG * kStage;                      // 2 K blocks x 16K
-    int32_t *segp = reinterpret_cast<int32_t *>(Us + kUBytes);   // [n_seg + 1] tile prefix
-    int32_t *pa = segp + (kMaxSegments + 1);                 // A^T pages of the unit
-    int32_t *pb = pa + kMaxPrefillRank;                      // B pages
-    __shared__ __align__(8) uint64_t mma_bar[NSTG];
-    __shared__ __align__(8) uint64_t acc_bar[2];
+    const int nts = a.nt;
+    uint8_t *tring = smem;                                  // nts x 16 KiB: x or y0 tiles
+    uint8_t *pring = tring + nts * kTileBytes;              // kPSlots x 16 KiB: page rows
+    uint8_t *Us = pring + kPSlots * kTileBytes;
+    UnitDesc *desc = reinterpret_cast<UnitDesc *>(Us + kUBytes);
+    uint8_t *xbuf = reinterpret_cast<uint8_t *>(desc + 2);
+
+    __shared__ __align__(8) uint64_t fullT[kMaxTSlots], emptyT[kMaxTSlots], fullP[kPSlots], emptyP[kPSlots];
+    __shared__ __align__(8) uint64_t dfull[2], dempty[2], accfull[NB], accempty[NB];
+    __shared__ __align__(8) uint64_t ubar, ufull, ufree, xfull, fin;
     __shared__ uint32_t s_tmem;
-    __shared__ int warp_sum[kPThreads / 32 + 1];
-    __shared__ int s_flag;
+    __shared__ int s_abort;
+    __shared__ int s_stored[kMaxTSlots];   // epilogue warps done with an expand slot
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int d = a.pv.hidden;
-    const __half *pool = reinterpret_cast<const __half *>(a.pv.pool);
+    const int C = a.C;
+    const uint32_t crank = cluster_ctarank();
+    volatile int *abort = &s_abort;
+    int32_t *status = a.pv.status;
 
     griddep_wait();
     griddep_launch_dependents();
 
-    if (warp == 0) {
+    if (warp == kMmaWarp) {
         tc::tmem_alloc(&s_tmem, kTmemCols);
         tc::tmem_relinquish();
     }
     if (tid == 0) {
-        for (int i = 0; i < NSTG; ++i) mbar_init(&mma_bar[i], 1);
-        for (int i = 0; i < 2; ++i) mbar_init(&acc_bar[i], 1);
+        for (int i = 0; i < nts; ++i) {
+            mbar_init(&fullT[i], 1);
+            mbar_init(&emptyT[i], 1);
+        }
+        for (int i = 0; i < kPSlots; ++i) {
+            mbar_init(&fullP[i], kProdThreads);
+            mbar_init(&emptyP[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&dfull[i], 1);
+            mbar_init(&dempty[i], kProdWarps + 1 + kEpiWarps);
+        }
+        for (int i = 0; i < NB; ++i) {
+            mbar_init(&accfull[i], 1);
+            mbar_init(&accempty[i], kEpiWarps);
+        }
+        mbar_init(&ubar, 1);
+        mbar_init(&ufull, C);
+        mbar_init(&ufree, C);
+        mbar_init(&xfull, C > 1 ? C - 1 : 1);
+        mbar_init(&fin, 1);
+        s_abort = 0;
+        for (int i = 0; i < kMaxTSlots; ++i) s_stored[i] = 0;
         fence_mbar_init();
-        s_flag = 0;
+    }
+    // every segment well formed?
+    int bad = 0;
+    for (int i = tid; i < a.n_seg; i += kThreads) {
+        const int lo = a.seg_indptr[i], hi = a.seg_indptr[i + 1];
+        if (lo < 0 || hi < lo || hi > a.T) bad = 1;
     }
     tc::fence_before_sync();
-    __syncthreads();
+    bad = __syncthreads_or(bad);
     tc::fence_after_sync();
+    if (C > 1) cluster_sync_all();   // every CTA's barriers exist before any remote access
     const uint32_t tmem = s_tmem;
-    // segment tile prefix: segp[i] = M tiles before segment i
-    {
-        const int ns = a.n_seg;
-        const int per = (ns + kPThreads - 1) / kPThreads;
-        const int i0 = tid * per;
-        int my = 0;
-        for (int i = i0; i < i0 + per && i < ns; ++i) {
-            const int lo = a.seg_indptr[i], hi = a.seg_indptr[i + 1];
-            if (lo < 0 || hi < lo || hi > a.T) s_flag = 1;
-            else my += (hi - lo + MT - 1) / MT;
-        }
-        int incl = my;
+    if (bad && tid == 0) set_status(status, SLORA_DEV_BAD_SEGMENT);
+
+    const int d = a.pv.hidden;
+    const int k_lo = (int)crank * a.slice;
+    const int k_hi = min(d, k_lo + a.slice);
+    const int nkb = (k_hi - k_lo) / KBLK;   // shrink K blocks = expand column tiles
+
+    if (bad) {
+        // nothing to do
+    } else if (warp == kSchedWarp) {
+        // ---------------------------------------------------------------- scheduler
+        const uint32_t cl = cluster_id_x(), ncl = ncluster_x();
+        int s0 = 0, base = 0;   // window of 32 segments and the tiles before it
+        uint32_t gT = 0;        // token tiles issued
+        for (uint32_t i = 0;; ++i) {
+            const int mt = (int)(cl + i * ncl);
+            int tile = -1, lo = 0, hi = 0;
+            while (s0 < a.n_seg) {
+                const int j = s0 + lane;
+                int l = 0, h = 0;
+                if (j < a.n_seg) {
+                    l = a.seg_indptr[j];
+                    h = a.seg_indptr[j + 1];
+                }
+                const int t = (h - l + MT - 1) / MT;
+                int incl = t;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            int n = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += n;
-        }
-        if (lane == 31) warp_sum[warp] = incl;
-        __syncthreads();
-        if (tid == 0) {
-            int acc = 0;
-            for (int w = 0; w < kPThreads / 32; ++w) {
-                int v = warp_sum[w];
-                warp_sum[w] = acc;
-                acc += v;
-            }
-            warp_sum[kPThreads / 32] = acc;
-        }
-        __syncthreads();
-        int base = warp_sum[warp] + incl - my;
-        for (int i = i0; i < i0 + per && i < ns; ++i) {
-            segp[i] = base;
-            const int lo = a.seg_indptr[i], hi = a.seg_indptr[i + 1];
-            if (!(lo < 0 || hi < lo || hi > a.T)) base += (hi - lo + MT - 1) / MT;
-        }
-        if (tid == 0) segp[ns] = warp_sum[kPThreads / 32];
-        __syncthreads();
-    }
-    if (s_flag) {
-        if (tid == 0) set_status(a.pv.status, SLORA_DEV_BAD_SEGMENT);
-    } else {
-        const int total_mt = segp[a.n_seg];
-        int S = (int)gridDim.x / (total_mt > 0 ? total_mt : 1);
-        S = S < 1 ? 1 : (S > 4 ? 4 : S);
-        const int cols_per = ((d + S - 1) / S + 63) / 64 * 64;
-        const int S_eff = (d + cols_per - 1) / cols_per;
-        const int units = total_mt * S_eff;
-        uint32_t g_kb = 0;   // global K-block sequence (stage / phase bookkeeping)
-        uint32_t g_nt = 0;   // global expand-tile sequence
-        bool alive = true;
-
-        for (int u = blockIdx.x; u < units && alive; u += gridDim.x) {
-            const int mt = u / S_eff, part = u % S_eff;
-            int lo_s = 0, hi_s = a.n_seg - 1;      // last segment with segp[i] <= mt
-            while (lo_s < hi_s) {
-                const int mid = (lo_s + hi_s + 1) >> 1;
-                if (segp[mid] <= mt) lo_s = mid; else hi_s = mid - 1;
-            }
-            const int sg = lo_s;
-            const int seg_lo = a.seg_indptr[sg], seg_hi = a.seg_indptr[sg + 1];
-            const int m0 = seg_lo + (mt - segp[sg]) * MT;
-            const int mlen = min(MT, seg_hi - m0);
-            const int c_lo = part * cols_per;
-            const int c_hi = min(d, c_lo + cols_per);
-
-            // ---- adapter of the unit, checks ----
-            const int ad = a.idx[m0];
-            if (tid == 0) s_flag = 0;
-            __syncthreads();
-            for (int i = tid; i < mlen; i += kPThreads)
-                if (a.idx[m0 + i] != ad) s_flag = 1;
-            __syncthreads();
-            if (s_flag) {
-                if (tid == 0) set_status(a.pv.status, SLORA_DEV_BAD_SEGMENT);
-                continue;
-            }
-            if (ad == -1)
-                continue;   // base only
-            if (ad < -1 || ad >= a.pv.max_adapters) {
-                if (tid == 0) set_status(a.pv.status, SLORA_DEV_BAD_ADAPTER);
-                continue;
-            }
-            const DirEntry e = a.pv.dir[ad];
-            if (e.pt_off < 0 || e.rank <= 0) {
-                if (tid == 0) set_status(a.pv.status, SLORA_DEV_NOT_RESIDENT);
-                continue;
-            }
-            const int r = e.rank;
-            if (r > kMaxPrefillRank)
-                continue;   // such segments take the decode path (the plan routes them there)
-            const int r_pad = (r + 15) / 16 * 16;
-            const float sc = a.scaling ? a.scaling[ad] : e.scaling;
-            const int32_t *pt = a.pv.pt_arena + e.pt_off + (int64_t)a.proj * 2 * r;
-            if (tid == 0) s_flag = 0;
-            __syncthreads();
-            for (int j = tid; j < r; j += kPThreads) {
-                const int32_t p0 = pt[j], p1 = pt[r + j];
-                if (p0 < 0 || p0 >= a.pv.num_pages || p1 < 0 || p1 >= a.pv.num_pages) s_flag = 1;
-                pa[j] = p0;
-                pb[j] = p1;
-            }
-            __syncthreads();
-            if (s_flag) {
-                if (tid == 0) set_status(a.pv.status, SLORA_DEV_BAD_PAGE);
-                continue;
-            }
-
-            // ---- shrink: U = X A over K = d ----
-            const int nkb = d / KBLK;
-            auto issue = [&](int kb) {
-                uint8_t *st = stages + ((g_kb + kb) % NSTG) * kStage;
-                uint8_t *Xs = st, *As = st + kXBytes;
-                for (int q = tid; q < MT * 8; q += kPThreads) {
-                    const int m = q >> 3, ch = q & 7;
-                    void *dst = Xs + m * 128 + ((ch ^ (m & 7)) << 4);
-                    if (m < mlen)
-                        cp_async16(dst, a.x + (int64_t)(m0 + m) * d + kb * KBLK + ch * 8, 16);
-                    else
-                        cp_async16(dst, a.x, 0);
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += n;
                 }
-                for (int q = tid; q < r_pad * 8; q += kPThreads) {
-                    const int j = q >> 3, ch = q & 7;
-                    void *dst = As + j * 128 + ((ch ^ (j & 7)) << 4);
-                    if (j < r)
-                        cp_async16(dst, pool + (int64_t)pa[j] * d + kb * KBLK + ch * 8, 16);
-                    else
-                        cp_async16(dst, a.x, 0);
+                const int tot = __shfl_sync(0xffffffffu, incl, 31);
+                if (base + tot <= mt) {
+                    base += tot;
+                    s0 += 32;
+                    continue;
                 }
-                cp_async_commit();
-            };
-            for (int kb = 0; kb < NSTG - 1; ++kb) {
-                if (kb < nkb) issue(kb);
-                else cp_async_commit();
+                const int f = __ffs(__ballot_sync(0xffffffffu, base + incl > mt)) - 1;
+                tile = mt - (base + __shfl_sync(0xffffffffu, incl - t, f));
+                lo = __shfl_sync(0xffffffffu, l, f);
+                hi = __shfl_sync(0xffffffffu, h, f);
+                break;
             }
-            const uint32_t idesc_s = tc::idesc_f16_f32(MT, r_pad, 0, 0);
-            for (int kb = 0; kb < nkb; ++kb) {
-                const int nxt = kb + NSTG - 1;
-                bool ok = true;
-                if (nxt < nkb) {
-                    if (kb >= 1) {   // the stage of block nxt was read by the MMAs of block kb-1
-                        const uint32_t gq = g_kb + kb - 1;
-                        ok = mbar_wait_bounded(&mma_bar[gq % NSTG], (gq / NSTG) & 1u, a.pv.status);
-                    }
-                    if (ok) issue(nxt);
-                    else cp_async_commit();
+            int flag = kEnd, m0 = 0, mlen = 0, rank = 0;
+            float sc = 0.f;
+            int64_t pt = 0;
+            if (tile >= 0) {
+                flag = kSkip;
+                m0 = lo + tile * MT;
+                mlen = min(MT, hi - m0);
+                const int ad = a.idx[m0];
+                bool mixed = false;
+                for (int q = lane; q < mlen; q += 32) mixed |= a.idx[m0 + q] != ad;
+                if (__any_sync(0xffffffffu, mixed)) {
+                    if (lane == 0) set_status(status, SLORA_DEV_BAD_SEGMENT);
+                } else if (ad == -1) {
+                    // base model only
+                } else if (ad < -1 || ad >= a.pv.max_adapters) {
+                    if (lane == 0) set_status(status, SLORA_DEV_BAD_ADAPTER);
                 } else {
-                    cp_async_commit();
-                }
-                cp_async_wait<NSTG - 1>();
-                tc::fence_proxy_async_smem();
-                if (__syncthreads_or(!ok)) { alive = false; break; }
-                if (tid == 0) {
-                    tc::fence_after_sync();
-                    const uint32_t gq = g_kb + kb;
-                    const uint8_t *st = stages + (gq % NSTG) * kStage;
-                    const uint32_t xa = smem_u32(st), aa = smem_u32(st + kXBytes);
-#pragma unroll
-                    for (int kk = 0; kk < KBLK / 16; ++kk) {
-                        tc::mma_f16(tmem, tc::smem_desc_sw128(xa + kk * 32, 16, 1024),
-                                    tc::smem_desc_sw128(aa + kk * 32, 16, 1024), idesc_s,
-                                    (kb | kk) != 0);
+                    const DirEntry e = a.pv.dir[ad];
+                    if (e.pt_off < 0 || e.rank <= 0) {
+                        if (lane == 0) set_status(status, SLORA_DEV_NOT_RESIDENT);
+                    } else if (e.rank <= kMaxPrefillRank) {   // larger ranks take the decode path
+                        flag = kCompute;
+                        rank = e.rank;
+                        sc = a.scaling ? a.scaling[ad] : e.scaling;
+                        pt = e.pt_off + (int64_t)a.proj * 2 * e.rank;
                     }
-                    tc::commit(&mma_bar[gq % NSTG]);
                 }
             }
-            cp_async_wait<0>();
-            if (!alive) break;
-            {
-                const uint32_t gq = g_kb + nkb - 1;
-                const bool ok = mbar_wait_bounded(&mma_bar[gq % NSTG], (gq / NSTG) & 1u, a.pv.status);
-                g_kb += nkb;
-                if (__syncthreads_or(!ok)) { alive = false; break; }
-            }
-            tc::fence_after_sync();
-
-            // ---- U: TMEM -> fp16 K-major swizzled shared memory ----
-            if (warp < 4) {
-                const int m = 32 * warp + lane;
-                for (int cb = 0; cb < r_pad / 16; ++cb) {
-                    uint32_t v[16];
-                    tc::ld_32x32b_x16(tmem + ((uint32_t)(32 * warp) << 16) + cb * 16, v);
-                    tc::ld_wait();
-                    const int k = cb * 16;
-                    uint8_t *row = Us + (k / 64) * (MT * 128) + m * 128;
-                    const int ch0 = (k % 64) / 8;
-                    *reinterpret_cast<uint4 *>(row + ((ch0 ^ (m & 7)) << 4)) = pack_h8(v);
-                    *reinterpret_cast<uint4 *>(row + (((ch0 + 1) ^ (m & 7)) << 4)) = pack_h8(v + 8);
-                }
-            }
-            tc::fence_proxy_async_smem();
-            tc::fence_before_sync();
-            __syncthreads();
-
-            // ---- expand: Y = Y0 + s * U B over this unit's columns ----
-            const int ntiles = (c_hi - c_lo + NT - 1) / NT;
-            auto load_b = [&](int n, int buf) {
-                const int n0 = c_lo + n * NT;
-                const int nt = min(NT, c_hi - n0);
-                const int cpr = nt / 8;   // 16-byte chunks per row
-                uint8_t *Bs = stages + buf * kBBuf;
-                for (int q = tid; q < r_pad * cpr; q += kPThreads) {
-                    const int j = q / cpr, c = q % cpr;
-                    const int col = c * 8;
-                    void *dst = Bs + (j >> 3) * (4 * 1024) + (col >> 6) * 1024 + (j & 7) * 128 +
-                                ((((col & 63) >> 3) ^ (j & 7)) << 4);
-                    if (j < r)
-                        cp_async16(dst, pool + (int64_t)pb[j] * d + n0 + col, 16);
-                    else
-                        cp_async16(dst, a.x, 0);
-                }
-                cp_async_commit();
-            };
-            load_b(0, 0);
-            for (int n = 0; n < ntiles; ++n) {
-                if (n + 1 < ntiles) load_b(n + 1, (n + 1) & 1);
-                else cp_async_commit();
-                cp_async_wait<1>();
-                tc::fence_proxy_async_smem();
-                __syncthreads();
-                const int n0 = c_lo + n * NT;
-                const int nt = min(NT, c_hi - n0);
-                const uint32_t tb = g_nt & 1u;
-                if (tid == 0) {
-                    tc::fence_after_sync();
-                    const uint32_t idesc_e = tc::idesc_f16_f32(MT, nt, 0, 1);
-                    const uint32_t ua = smem_u32(Us);
-                    const uint32_t ba = smem_u32(stages + (n & 1) * kBBuf);
-                    for (int ks = 0; ks < r_pad / 16; ++ks) {
-                        const int k = ks * 16;
-                        const uint32_t a_addr = ua + (k / 64) * (MT * 128) + ((k % 64) / 16) * 32;
-                        const uint32_t b_addr = ba + ks * 2 * (4 * 1024);
-                        tc::mma_f16(tmem + tb * NT, tc::smem_desc_sw128(a_addr, 16, 1024),
-                                    tc::smem_desc_sw128(b_addr, 1024, 4 * 1024), idesc_e, ks != 0);
+            wait_phase<false>(&dempty[i & 1], ((i >> 1) & 1) ^ 1, abort, status);
+            if (__any_sync(0xffffffffu, *abort)) break;
+            UnitDesc *u = &desc[i & 1];
+            if (flag == kCompute) {
+                bool badp = false;
+                for (int j = lane; j < 2 * rank; j += 32) {
+                    int32_t p = a.pv.pt_arena[pt + j];
+                    if (p < 0 || p >= a.pv.num_pages) {
+                        badp = true;   // the row reads as zeros
+                        p = -1;
                     }
-                    tc::commit(&acc_bar[tb]);
+                    u->pg[j < rank ? j : kMaxPrefillRank + j - rank] = p;
                 }
-                const bool ok = mbar_wait_bounded(&acc_bar[tb], (g_nt >> 1) & 1u, a.pv.status);
-                ++g_nt;
-                if (__syncthreads_or(!ok)) { alive = false; break; }
-                tc::fence_after_sync();
-                // epilogue: warps w and w+4 share TMEM lanes 32*(w%4).. and split the columns
-                const int sub = warp & 3, half = warp >> 2;
-                const int m = 32 * sub + lane;
-                const bool valid = m < mlen;
-                const int64_t yrow = (int64_t)(m0 + m) * d;
-                const int cols_half = nt / 2;
-                for (int cc = 0; cc < cols_half; cc += 16) {
-                    const int col = half * cols_half + cc;
-                    uint32_t v[16];
-                    tc::ld_32x32b_x16(tmem + tb * NT + ((uint32_t)(32 * sub) << 16) + col, v);
-                    tc::ld_wait();
-                    if (valid) {
-                        uint4 *yp = reinterpret_cast<uint4 *>(a.y + yrow + n0 + col);
-                        uint4 y0a = yp[0], y0b = yp[1];
-                        const __half2 *ha = reinterpret_cast<const __half2 *>(&y0a);
-                        const __half2 *hb = reinterpret_cast<const __half2 *>(&y0b);
-                        uint32_t o[16];
+                if (__any_sync(0xffffffffu, badp) && lane == 0) set_status(status, SLORA_DEV_BAD_PAGE);
+            }
+            if (lane == 0) {
+                u->m0 = m0;
+                u->mlen = mlen;
+                u->rank = rank;
+                u->r_pad = (rank + 15) / 16 * 16;
+                u->sc = sc;
+                u->flag = flag;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&dfull[i & 1]);
+            if (flag == kEnd) break;
+            // the unit's token tiles: x for the shrink, then y0 for the expand, as slots free up
+            if (flag == kCompute && lane == 0) {
+                for (int st = 0; st < 2 * nkb; ++st) {
+                    const bool shrink = st < nkb;
+                    const int col = k_lo + (shrink ? st : st - nkb) * KBLK;
+                    const uint32_t sT = gT % nts;
+                    wait_phase<false>(&emptyT[sT], ((gT / nts) & 1) ^ 1, abort, status);
+                    if (*abort) break;
+                    mbar_arrive_expect_tx(&fullT[sT], kTileBytes);
+                    tma_load_2d(smem_u32(tring + sT * kTileBytes),
+                                shrink ? (const void *)&a.tmap_x : (const void *)&a.tmap_y, col, m0, &fullT[sT]);
+                    ++gT;
+                }
+            }
+            __syncwarp();
+        }
+        // the CTA stays until its last tensor-tile loads have landed
+        if (lane == 0)
+            for (uint32_t q = gT > (uint32_t)nts ? gT - nts : 0; q < gT; ++q)
+                mbar_wait_bounded(&fullT[q % nts], (q / nts) & 1, status);
+    } else if (warp < kMmaWarp || warp >= kEpiWarp0 + kEpiWarps) {
+        // ---------------------------------------------------------------- producer
+        // 192 threads; thread pt copies 16-byte chunks pt, pt + 192, ... of the stage's page
+        // rows (chunk q: row q / 8, column chunk q % 8)
+        const int pt = warp < kMmaWarp ? tid : tid - 32 * (kEpiWarp0 + kEpiWarps) + 32 * kMmaWarp;
+        const __half *pool = reinterpret_cast<const __half *>(a.pv.pool);
+        uint32_t g = 0;
+        for (uint32_t i = 0;; ++i) {
+            wait_phase<false>(&dfull[i & 1], (i >> 1) & 1, abort, status);
+            if (__any_sync(0xffffffffu, *abort)) break;
+            const UnitDesc *u = &desc[i & 1];
+            const int flag = u->flag, r_pad = u->r_pad;
+            if (flag == kEnd) break;
+            bool ab = false;
+            if (flag == kCompute) {
+                for (int st = 0; st < 2 * nkb; ++st) {
+                    const bool shrink = st < nkb;
+                    const int col = k_lo + (shrink ? st : st - nkb) * KBLK;
+                    const uint32_t sP = g % kPSlots;
+                    wait_phase<false>(&emptyP[sP], ((g / kPSlots) & 1) ^ 1, abort, status);
+                    if (__any_sync(0xffffffffu, *abort)) {
+                        ab = true;
+                        break;
+                    }
+                    uint8_t *rows = pring + sP * kTileBytes;
+                    const int32_t *pg = u->pg + (shrink ? 0 : kMaxPrefillRank);
+                    const int rank = u->rank;
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            float2 f = __half22float2(ha[i]);
-                            o[2 * i] = __float_as_uint(fmaf(sc, __uint_as_float(v[2 * i]), f.x));
-                            o[2 * i + 1] = __float_as_uint(fmaf(sc, __uint_as_float(v[2 * i + 1]), f.y));
-                            float2 g = __half22float2(hb[i]);
-                            o[8 + 2 * i] = __float_as_uint(fmaf(sc, __uint_as_float(v[8 + 2 * i]), g.x));
-                            o[8 + 2 * i + 1] = __float_as_uint(fmaf(sc, __uint_as_float(v[8 + 2 * i + 1]), g.y));
+                    for (int k = 0; k < (kMaxPrefillRank * 8 + kProdThreads - 1) / kProdThreads; ++k) {
+                        const int q = pt + kProdThreads * k;
+                        const int j = q >> 3, ch = q & 7;
+                        if (j < r_pad) {
+                            const int32_t p = pg[j];   // rows r..r_pad-1 were never written: masked below
+                            const bool v = j < rank && p >= 0;
+                            const __half *src = v ? pool + (int64_t)p * d + col + ch * 8 : pool;
+                            cp_async16(rows + j * 128 + ((ch ^ (j & 7)) << 4), src, v ? 16u : 0u);
                         }
-                        yp[0] = pack_h8(o);
-                        yp[1] = pack_h8(o + 8);
+                    }
+                    cp_async_arrive_noinc(&fullP[sP]);   // the stage's consumer fences the proxies
+                    ++g;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&dempty[i & 1]);   // done with the descriptor
+            if (ab) break;
+        }
+        cp_async_wait_all();
+    } else if (warp == kMmaWarp) {
+        // ---------------------------------------------------------------- MMA issue
+        if (lane == 0) {
+            uint32_t g = 0, e = 0, ui = 0;
+            const uint32_t ua = smem_u32(Us);
+            for (uint32_t i = 0;; ++i) {
+                wait_phase<false>(&dfull[i & 1], (i >> 1) & 1, abort, status);
+                if (*abort) break;
+                const int flag = desc[i & 1].flag, r_pad = desc[i & 1].r_pad;
+                mbar_arrive(&dempty[i & 1]);
+                if (flag == kEnd) break;
+                if (flag != kCompute) continue;
+                const uint32_t idesc_s = tc::idesc_f16_f32(MT, r_pad, 0, 0);
+                for (int kb = 0; kb < nkb && !*abort; ++kb) {
+                    const uint32_t sT = g % nts, sP = g % kPSlots;
+                    wait_phase<false>(&fullT[sT], (g / nts) & 1, abort, status);
+                    wait_phase<false>(&fullP[sP], (g / kPSlots) & 1, abort, status);
+                    if (*abort) break;
+                    tc::fence_proxy_async_smem();   // the cp.async page rows, for the tensor core
+                    tc::fence_after_sync();
+                    const uint32_t xa = smem_u32(tring + sT * kTileBytes), aa = smem_u32(pring + sP * kTileBytes);
+#pragma unroll
+                    for (int kk = 0; kk < KBLK / 16; ++kk)
+                        tc::mma_f16(tmem, tc::smem_desc_sw128(xa + kk * 32, 16, 1024),
+                                    tc::smem_desc_sw128(aa + kk * 32, 16, 1024), idesc_s, (kb | kk) != 0);
+                    tc::commit(&emptyT[sT]);
+                    tc::commit(&emptyP[sP]);
+                    ++g;
+                }
+                if (*abort) break;
+                tc::commit(&ubar);
+                wait_phase<true>(&ufull, ui & 1, abort, status);
+                if (*abort) break;
+                tc::fence_after_sync();
+                fence_proxy_async_all();
+                const uint32_t idesc_e = tc::idesc_f16_f32(MT, KBLK, 0, 1);
+                for (int nt = 0; nt < nkb; ++nt) {
+                    const uint32_t sP = g % kPSlots, b = e % NB;
+                    wait_phase<false>(&fullP[sP], (g / kPSlots) & 1, abort, status);
+                    if (e >= (uint32_t)NB) wait_phase<false>(&accempty[b], ((e / NB) - 1) & 1, abort, status);
+                    if (*abort) break;
+                    tc::fence_proxy_async_smem();
+                    tc::fence_after_sync();
+                    const uint32_t ba = smem_u32(pring + sP * kTileBytes);
+                    for (int ks = 0; ks < r_pad / 16; ++ks) {
+                        const uint32_t a_addr = ua + (ks >> 2) * kTileBytes + (ks & 3) * 32;
+                        tc::mma_f16(tmem + 128 + b * 64, tc::smem_desc_sw128(a_addr, 16, 1024),
+                                    tc::smem_desc_sw128(ba + ks * 2048, 8192, 1024), idesc_e, ks != 0);
+                    }
+                    tc::commit(&emptyP[sP]);
+                    tc::commit(&accfull[b]);
+                    ++g;
+                    ++e;
+                }
+                if (*abort) break;
+                ++ui;
+            }
+            // every MMA issued has completed before tensor memory is released
+            tc::commit(&fin);
+            mbar_wait_bounded(&fin, 0, status);
+        }
+    } else {
+        // ---------------------------------------------------------------- exchange + epilogue
+        const int qd = warp & 3;           // TMEM lane quarter this warp may access
+        const int m = 32 * qd + lane;      // the tile row (token) of this thread
+        const int et = tid - 32 * kEpiWarp0;
+        const uint32_t lane_base = (uint32_t)(32 * qd) << 16;
+        const uint32_t ua = smem_u32(Us);
+        uint32_t g = 0, e = 0, ui = 0;
+        int pend = -1;   // (lane 0) token slot this warp's last tensor-tile store may still be reading
+        for (uint32_t i = 0;; ++i) {
+            wait_phase<false>(&dfull[i & 1], (i >> 1) & 1, abort, status);
+            if (epi_sync_or(*abort)) break;
+            const UnitDesc *ud = &desc[i & 1];
+            const int flag = ud->flag, m0 = ud->m0, mlen = ud->mlen, r_pad = ud->r_pad;
+            const float sc = ud->sc;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&dempty[i & 1]);
+            if (flag == kEnd) break;
+            if (flag != kCompute) continue;
+            const int nkc = r_pad / 16;
+
+            // ---- U = the cluster's partial products summed, rounded to fp16 ----
+            wait_phase<false>(&ubar, ui & 1, abort, status);
+            tc::fence_after_sync();
+            auto u_off = [&](int kc, int half) -> uint32_t {
+                return (uint32_t)((kc >> 2) * kTileBytes + m * 128 + (((2 * (kc & 3) + half) ^ (m & 7)) << 4));
+            };
+            if (C == 1) {
+                for (int kc = 0; kc < nkc; ++kc) {
+                    uint32_t v[16];
+                    tc::ld_32x32b_x16(tmem + lane_base + kc * 16, v);
+                    tc::ld_wait();
+                    float f[16];
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) f[t] = __uint_as_float(v[t]);
+                    *reinterpret_cast<uint4 *>(Us + u_off(kc, 0)) = pack_h8(f);
+                    *reinterpret_cast<uint4 *>(Us + u_off(kc, 1)) = pack_h8(f + 8);
+                }
+                tc::fence_proxy_async_smem();
+            } else {
+                // rows are owned in blocks of R; with R = 16 the two halves of a warp have
+                // different owners, so the (warp-wide) TMEM loads run in every lane
+                const int R = MT / C, owner = m / R, rl = m - owner * R;
+                const bool mine = owner == (int)crank;
+                const int xpitch = r_pad * 4 + 16;
+                if (__any_sync(0xffffffffu, !mine)) {
+                    // the owner has read its buffer for the previous unit (it signalled ufull)
+                    if (ui >= 1) wait_phase<true>(&ufull, (ui - 1) & 1, abort, status);
+                    const int slot = (int)crank < owner ? (int)crank : (int)crank - 1;
+                    const uint32_t dst = mapa(smem_u32(xbuf + (slot * R + rl) * xpitch), (uint32_t)owner);
+                    for (int kc = 0; kc < nkc; ++kc) {
+                        uint32_t v[16];
+                        __syncwarp();
+                        tc::ld_32x32b_x16(tmem + lane_base + kc * 16, v);
+                        tc::ld_wait();
+                        if (!mine) {
+#pragma unroll
+                            for (int w4 = 0; w4 < 4; ++w4)
+                                st_cluster_v4(dst + kc * 64 + w4 * 16,
+                                              make_uint4(v[4 * w4], v[4 * w4 + 1], v[4 * w4 + 2], v[4 * w4 + 3]));
+                        }
                     }
                 }
                 tc::fence_before_sync();
-                __syncthreads();
+                if (epi_sync_or(*abort)) break;
+                if (et == 0)
+                    for (int q = 0; q < C; ++q)
+                        if (q != (int)crank) mbar_arrive_remote(mapa(smem_u32(&xfull), (uint32_t)q));
+                if (__any_sync(0xffffffffu, mine)) {
+                    wait_phase<true>(&xfull, ui & 1, abort, status);
+                    // every CTA's expand of the previous unit is done with its U operand
+                    if (ui >= 1) wait_phase<true>(&ufree, (ui - 1) & 1, abort, status);
+                    tc::fence_after_sync();
+                    for (int kc = 0; kc < nkc; ++kc) {
+                        uint32_t v[16];
+                        __syncwarp();
+                        tc::ld_32x32b_x16(tmem + lane_base + kc * 16, v);
+                        tc::ld_wait();
+                        if (!mine) continue;
+                        float f[16];
+                        for (int src = 0; src < C; ++src) {
+                            float p[16];
+                            if (src == (int)crank) {
+#pragma unroll
+                                for (int t = 0; t < 16; ++t) p[t] = __uint_as_float(v[t]);
+                            } else {
+                                const int slot = src < (int)crank ? src : src - 1;
+                                const float4 *xp =
+                                    reinterpret_cast<const float4 *>(xbuf + (slot * R + rl) * xpitch + kc * 64);
+#pragma unroll
+                                for (int w4 = 0; w4 < 4; ++w4) {
+                                    const float4 x4 = xp[w4];
+                                    p[4 * w4] = x4.x;
+                                    p[4 * w4 + 1] = x4.y;
+                                    p[4 * w4 + 2] = x4.z;
+                                    p[4 * w4 + 3] = x4.w;
+                                }
+                            }
+#pragma unroll
+                            for (int t = 0; t < 16; ++t) f[t] = src == 0 ? p[t] : f[t] + p[t];
+                        }
+                        const uint4 lo4 = pack_h8(f), hi4 = pack_h8(f + 8);
+                        const uint32_t o0 = ua + u_off(kc, 0), o1 = ua + u_off(kc, 1);
+                        for (int q = 0; q < C; ++q) {
+                            st_cluster_v4(mapa(o0, (uint32_t)q), lo4);
+                            st_cluster_v4(mapa(o1, (uint32_t)q), hi4);
+                        }
+                    }
+                    fence_proxy_async_all();
+                }
             }
-            cp_async_wait<0>();
-            __syncthreads();
+            tc::fence_before_sync();
+            if (epi_sync_or(*abort)) break;
+            if (et == 0)
+                for (int q = 0; q < C; ++q) mbar_arrive_remote(mapa(smem_u32(&ufull), (uint32_t)q));
+            g += nkb;
+
+            // ---- y = y0 + s * (U B), one 64-column tile at a time, in place in the y0 slot ----
+            // Each warp forms and stores its own 32 rows; the last warp done with a slot
+            // returns it to the ring, so the warps never wait for one another here.
+            const bool full_tile = mlen == MT;
+            bool ab = false;
+            auto release = [&](int slot) {
+                if (atomicAdd(&s_stored[slot], 1) == kEpiWarps - 1) {
+                    atomicExch(&s_stored[slot], 0);
+                    mbar_arrive(&emptyT[slot]);
+                }
+            };
+            for (int nt = 0; nt < nkb; ++nt) {
+                const uint32_t sT = g % nts, b = e % NB;
+                wait_phase<false>(&accfull[b], (e / NB) & 1, abort, status);
+                tc::fence_after_sync();
+                uint32_t v[64];
+                tc::ld_32x32b_x32(tmem + lane_base + 128 + b * 64, *reinterpret_cast<uint32_t(*)[32]>(v));
+                tc::ld_32x32b_x32(tmem + lane_base + 128 + b * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+                tc::ld_wait();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&accempty[b]);
+                wait_phase<false>(&fullT[sT], (g / nts) & 1, abort, status);   // the y0 tile has landed
+                if (__any_sync(0xffffffffu, *abort)) {
+                    ab = true;
+                    break;
+                }
+                uint8_t *yt = tring + sT * kTileBytes;
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) {
+                    uint4 *yp = reinterpret_cast<uint4 *>(yt + m * 128 + ((cc ^ (m & 7)) << 4));
+                    const uint4 y0 = *yp;
+                    const __half2 *h2 = reinterpret_cast<const __half2 *>(&y0);
+                    float o[8];
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const float2 f2 = __half22float2(h2[t]);
+                        o[2 * t] = fmaf(sc, __uint_as_float(v[8 * cc + 2 * t]), f2.x);
+                        o[2 * t + 1] = fmaf(sc, __uint_as_float(v[8 * cc + 2 * t + 1]), f2.y);
+                    }
+                    *yp = pack_h8(o);
+                }
+                const int n0 = k_lo + nt * KBLK;
+                if (full_tile) {
+                    tc::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&a.tmap_ys, n0, m0 + 32 * qd, smem_u32(yt + 32 * qd * 128));
+                        bulk_commit();
+                        if (pend >= 0) {   // this warp's store of the previous tile has read its slot
+                            bulk_wait_read<1>();
+                            release(pend);
+                        }
+                        pend = (int)sT;
+                    }
+                } else {
+                    __syncwarp();
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int qq = lane + 32 * k;
+                        const int row = 32 * qd + (qq >> 3), c8 = qq & 7;
+                        if (row < mlen) {
+                            const uint4 val = *reinterpret_cast<const uint4 *>(yt + row * 128 + ((c8 ^ (row & 7)) << 4));
+                            *reinterpret_cast<uint4 *>(a.y + (int64_t)(m0 + row) * d + n0 + c8 * 8) = val;
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) release((int)sT);
+                }
+                ++g;
+                ++e;
+            }
+            // the unit's last slot is released before the next unit's shrink needs the ring
+            if (lane == 0 && pend >= 0) {
+                bulk_wait_read<0>();
+                release(pend);
+                pend = -1;
+            }
+            if (epi_sync_or(ab || *abort)) break;
+            if (C > 1 && et == 0)
+                for (int q = 0; q < C; ++q) mbar_arrive_remote(mapa(smem_u32(&ufree), (uint32_t)q));
+            ++ui;
         }
+        if (lane == 0) bulk_wait<0>();
     }
+
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) {
+    if (C > 1) cluster_sync_all();   // no CTA of the cluster still touches this one's shared memory
+    if (warp == kMmaWarp) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, kTmemCols);
     }
 }
+
+// ---- host side ------------------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled()
+{
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// [T][hidden] fp16, 64 x box_rows boxes with the 128-byte swizzle; rows past T read as
+// zeros and are not written.
+cudaError_t token_map(CUtensorMap *m, const void *base, int hidden, int T, int box_rows = MT)
+{
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)hidden, (cuuint64_t)T};
+    const cuuint64_t strides[1] = {(cuuint64_t)hidden * 2};
+    const cuuint32_t box[2] = {KBLK, (cuuint32_t)box_rows};
+    const cuuint32_t es[2] = {1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+int g_forced_cluster = 0;
+
+inline int slice_for(int hidden, int C) { return (hidden / 64 + C - 1) / C * 64; }
 
 }  // namespace
 
@@ -398,24 +708,96 @@ cudaError_t launch_prefill(const PoolView &pv, int32_t proj, const uint16_t *x, 
                            const float *scaling, int num_sms, cudaStream_t stream)
 {
     static bool attr_set = false;
+    static int ncl_cache[4] = {0, 0, 0, 0};   // resident clusters for C = 1, 2, 4, 8
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        size_t most = 0;
+        for (int c = 1; c <= kMaxClusterP; c *= 2) most = smem_bytes_for(c) > most ? smem_bytes_for(c) : most;
+        cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    PrefillArgs pa{pv, proj, reinterpret_cast<const __half *>(x), reinterpret_cast<__half *>(y), T, idx,
-                   seg_indptr, n_seg, scaling};
-    cudaLaunchAttribute attr[1];
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) return cudaErrorInvalidValue;
+
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(num_sms);
-    cfg.blockDim = dim3(kPThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.blockDim = dim3(kThreads);
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
+
+    auto clusters = [&](int C, int lg) -> int {
+        if (ncl_cache[lg] == 0) {
+            attr[1].val.clusterDim.x = C;
+            cfg.gridDim = dim3(C * num_sms);
+            cfg.dynamicSmemBytes = smem_bytes_for(C);
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, prefill_kernel, &cfg) != cudaSuccess) n = 0;
+            ncl_cache[lg] = n > 0 ? n : -1;
+        }
+        return ncl_cache[lg];
+    };
+
+    // CTAs per cluster: the largest C whose resident clusters still cover the units
+    // (128-token tiles; the host does not read the segments, so T bounds their number).
+    const int units = (T + MT - 1) / MT;
+    int C = 1, lgC = 0;
+    for (int lg = 1; lg <= 3; ++lg) {
+        const int c = 1 << lg;
+        const int sl = slice_for(pv.hidden, c);
+        if (sl < 256 || (c - 1) * sl >= pv.hidden) break;
+        const int n = clusters(c, lg);
+        if (n > 0 && units <= n) {
+            C = c;
+            lgC = lg;
+        }
+    }
+    if (g_forced_cluster > 0) {
+        for (lgC = 0; (1 << lgC) < g_forced_cluster; ++lgC) {
+        }
+        C = 1 << lgC;
+        const int sl = slice_for(pv.hidden, C);
+        if (C > kMaxClusterP || (C - 1) * sl >= pv.hidden) return cudaErrorInvalidValue;
+    }
+    int ncl = clusters(C, lgC);
+    if (ncl <= 0) ncl = C == 1 ? num_sms : 1;
+
+    PrefillArgs pa;
+    cudaError_t e = token_map(&pa.tmap_x, x, pv.hidden, T);
+    if (e != cudaSuccess) return e;
+    e = token_map(&pa.tmap_y, y, pv.hidden, T);
+    if (e != cudaSuccess) return e;
+    e = token_map(&pa.tmap_ys, y, pv.hidden, T, 32);
+    if (e != cudaSuccess) return e;
+    pa.pv = pv;
+    pa.y = reinterpret_cast<__half *>(y);
+    pa.idx = idx;
+    pa.seg_indptr = seg_indptr;
+    pa.scaling = scaling;
+    pa.proj = proj;
+    pa.T = T;
+    pa.n_seg = n_seg;
+    pa.C = C;
+    pa.slice = slice_for(pv.hidden, C);
+    pa.nt = tslots_for(C);
+
+    attr[1].val.clusterDim.x = C;
+    cfg.gridDim = dim3(C * ncl);
+    cfg.dynamicSmemBytes = smem_bytes_for(C);
     return cudaLaunchKernelEx(&cfg, prefill_kernel, pa);
 }
 
 }  // namespace slora
+
+// Test hook: force the prefill kernel's cluster size (1, 2, 4 or 8; 0 = chosen from the
+// batch).
+extern "C" slora_status slora_debug_set_prefill_cluster(int32_t ctas)
+{
+    if (ctas != 0 && ctas != 1 && ctas != 2 && ctas != 4 && ctas != 8) return SLORA_ERR_INVALID_ARG;
+    slora::g_forced_cluster = ctas;
+    return SLORA_OK;
+}

@@ -358,3 +358,41 @@ def test_prefill_exact_all_ranks_bit_exact():
         assert s.device_status() == 0
     ref = oracle.workload_reference(w)
     assert np.array_equal(got.view(np.uint16), ref.astype(np.float16).view(np.uint16))
+
+
+@pytest.mark.parametrize("ctas", [1, 2, 4, 8])
+def test_prefill_every_cluster_size_bit_exact(ctas):
+    """The segment kernel with 1, 2, 4 and 8 CTAs per cluster on exact-arithmetic inputs
+    (every partial sum an integer, so the cross-CTA sum of the shrink partials is exact in
+    any order): hidden slices, the partial-product exchange, full tiles stored by tensor
+    map and ragged last tiles stored row by row, next to decode tokens."""
+    ranks = np.array([8, 16, 24, 32, 64, 100, 128], np.int32)
+    lens = [128, 129, 64, 200, 17, 256, 300]
+    idx = np.concatenate([np.full(L, i) for i, L in enumerate(lens)] +
+                         [np.array([3, -1, 6, 0], np.int32)]).astype(np.int32)
+    indptr = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    w = W.Workload("prefill_clusters", 4096, 1, ranks, idx, indptr, num_pages=2 * 2 * int(ranks.sum()),
+                   kv_pages=int(ranks.sum()), shuffle_seed=4, seed=6, values="exact")
+    rdp.slora_debug_set_prefill_cluster(ctas)
+    try:
+        with session_all_loaded(w) as s:
+            got = run(s)
+            assert s.device_status() == 0
+    finally:
+        rdp.slora_debug_set_prefill_cluster(0)
+    ref = oracle.workload_reference(w)
+    assert np.array_equal(got.view(np.uint16), ref.astype(np.float16).view(np.uint16))
+
+
+@pytest.mark.parametrize("ctas", [2, 8])
+def test_prefill_cluster_normal_values(ctas):
+    """Normal-valued inputs at a forced cluster size: within the fp16 tolerance."""
+    w = W.prefill_7b(n_seg=5, seg_len=200)
+    rdp.slora_debug_set_prefill_cluster(ctas)
+    try:
+        with session_all_loaded(w) as s:
+            got = run(s)
+            assert s.device_status() == 0
+    finally:
+        rdp.slora_debug_set_prefill_cluster(0)
+    assert_close(got, oracle.workload_reference(w), f"prefill, {ctas} CTAs per cluster")
