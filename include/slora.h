@@ -196,8 +196,11 @@ slora_status slora_adapter_is_resident(slora_pool_t pool, int32_t adapter_id, in
  *   stream             work is enqueued on this stream; nothing waits
  *
  * Tokens with a non-resident or out-of-range adapter are skipped (y unchanged) and
- * set a device status code.  Each token's result does not depend on the other tokens
- * in the batch, their order, or which pages hold its adapter.
+ * set a device status code.  A decode token's result does not depend on the other
+ * tokens in the batch, their order, or which pages hold its adapter.  A segment token's
+ * result is the same up to the order of the fp32 partial sums of x A: the segment
+ * kernel splits hidden over 1, 2, 4 or 8 CTAs, chosen from T, and adds their partial
+ * products in CTA order.
  * Scratch: the pool keeps device scratch for the token plan, sized on first use and
  * grown when a larger T arrives (a growth synchronises the pool's device).
  * ------------------------------------------------------------------------- */

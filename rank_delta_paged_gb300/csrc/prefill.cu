@@ -27,8 +27,10 @@
 //               slots free up.
 //   warps 0-1, 8-11  page-row gather: the adapter's page rows for each stage (64-element
 //               pieces of the A^T rows, or of the B rows) go through the page table into a
-//               three-slot ring in the same swizzled layout, 16 bytes per cp.async, spread
-//               over 192 threads (a gather runs at about 10 GB/s per issuing warp).  The
+//               48 KiB ring in the same swizzled layout, 16 bytes per cp.async, spread over
+//               192 threads (a gather runs at about 10 GB/s per issuing warp).  Its slots
+//               hold r_pad rows of 128 bytes, so a small rank keeps more stages in flight
+//               (16 slots at rank 8 or 16, 3 at rank 128).  The
 //               copies signal the slot's mbarrier as they land
 //               (cp.async.mbarrier.arrive.noinc), so no thread waits for data.  The token
 //               stream runs up to a whole ring ahead; the page rows, mostly L2 hits, follow
@@ -76,10 +78,11 @@ constexpr int NB = 4;                         // expand accumulator buffers in T
 constexpr uint32_t kTmemCols = 512;           // U at 0..127, expand buffer b at 128 + 64 b
 constexpr int kXPitchMax = kMaxPrefillRank * 4 + 16;
 constexpr int kMaxClusterP = 8;
-constexpr int kPSlots = 3;                    // page-row ring
+constexpr int kPRingBytes = 3 * kTileBytes;   // page-row ring: slots of r_pad * 128 bytes
+constexpr int kMaxPSlots = 16;
 constexpr int kMaxTSlots = 8;                 // token-tile ring (as many as shared memory holds)
 constexpr size_t kSmemLimit = 227 * 1024;     // dynamic + static shared memory of one CTA
-constexpr size_t kStaticReserve = 512;        // the kernel's static shared memory, rounded up
+constexpr size_t kStaticReserve = 1024;       // the kernel's static shared memory, rounded up
 
 constexpr int kCompute = 0, kSkip = 1, kEnd = 2;
 struct alignas(64) UnitDesc {
@@ -112,7 +115,7 @@ struct PrefillArgs {
 constexpr size_t xbuf_bytes(int C) { return (size_t)(C - 1) * (MT / C) * kXPitchMax; }
 constexpr size_t fixed_bytes(int C)
 {
-    return 1024 + (size_t)kPSlots * kTileBytes + kUBytes + 2 * sizeof(UnitDesc) + xbuf_bytes(C);
+    return 1024 + (size_t)kPRingBytes + kUBytes + 2 * sizeof(UnitDesc) + xbuf_bytes(C);
 }
 constexpr int tslots_for(int C)
 {
@@ -145,6 +148,14 @@ __device__ __forceinline__ bool epi_sync_or(bool v)
     return r != 0;
 }
 
+// Page-row slots for a unit of padded rank r_pad: each holds r_pad rows of 128 bytes, so a
+// small rank keeps many stages in flight (16 at rank 8 or 16, 3 at rank 128).
+__device__ __forceinline__ int pslots_for(int r_pad)
+{
+    const int n = kPRingBytes / (r_pad * 128);
+    return n > kMaxPSlots ? kMaxPSlots : n;
+}
+
 __device__ __forceinline__ uint4 pack_h8(const float *f)
 {
     uint4 r;
@@ -161,12 +172,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int nts = a.nt;
     uint8_t *tring = smem;                                  // nts x 16 KiB: x or y0 tiles
-    uint8_t *pring = tring + nts * kTileBytes;              // kPSlots x 16 KiB: page rows
-    uint8_t *Us = pring + kPSlots * kTileBytes;
+    uint8_t *pring = tring + nts * kTileBytes;              // page rows
+    uint8_t *Us = pring + kPRingBytes;
     UnitDesc *desc = reinterpret_cast<UnitDesc *>(Us + kUBytes);
     uint8_t *xbuf = reinterpret_cast<uint8_t *>(desc + 2);
 
-    __shared__ __align__(8) uint64_t fullT[kMaxTSlots], emptyT[kMaxTSlots], fullP[kPSlots], emptyP[kPSlots];
+    __shared__ __align__(8) uint64_t fullT[kMaxTSlots], emptyT[kMaxTSlots], fullP[kMaxPSlots], emptyP[kMaxPSlots];
     __shared__ __align__(8) uint64_t dfull[2], dempty[2], accfull[NB], accempty[NB];
     __shared__ __align__(8) uint64_t ubar, ufull, ufree, xfull, fin;
     __shared__ uint32_t s_tmem;
@@ -191,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             mbar_init(&fullT[i], 1);
             mbar_init(&emptyT[i], 1);
         }
-        for (int i = 0; i < kPSlots; ++i) {
+        for (int i = 0; i < kMaxPSlots; ++i) {
             mbar_init(&fullP[i], kProdThreads);
             mbar_init(&emptyP[i], 1);
         }
@@ -346,7 +357,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         // rows (chunk q: row q / 8, column chunk q % 8)
         const int pt = warp < kMmaWarp ? tid : tid - 32 * (kEpiWarp0 + kEpiWarps) + 32 * kMmaWarp;
         const __half *pool = reinterpret_cast<const __half *>(a.pv.pool);
-        uint32_t g = 0;
+        uint32_t pfill = 0;         // bit s: parity of the number of fills of page slot s
+        int cur_np = 0, cur_sz = 0;  // the page ring's current slot count and size
         for (uint32_t i = 0;; ++i) {
             wait_phase<false>(&dfull[i & 1], (i >> 1) & 1, abort, status);
             if (__any_sync(0xffffffffu, *abort)) break;
@@ -355,16 +367,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             if (flag == kEnd) break;
             bool ab = false;
             if (flag == kCompute) {
+                const int np = pslots_for(r_pad), psz = r_pad * 128;
+                if (psz != cur_sz) {   // new slot size: every slot of the old layout must be free
+                    for (int q = 0; q < cur_np; ++q)
+                        wait_phase<false>(&emptyP[q], ((pfill >> q) & 1) ^ 1, abort, status);
+                    cur_np = np;
+                    cur_sz = psz;
+                }
+                int sP = 0;
                 for (int st = 0; st < 2 * nkb; ++st) {
                     const bool shrink = st < nkb;
                     const int col = k_lo + (shrink ? st : st - nkb) * KBLK;
-                    const uint32_t sP = g % kPSlots;
-                    wait_phase<false>(&emptyP[sP], ((g / kPSlots) & 1) ^ 1, abort, status);
+                    wait_phase<false>(&emptyP[sP], ((pfill >> sP) & 1) ^ 1, abort, status);
                     if (__any_sync(0xffffffffu, *abort)) {
                         ab = true;
                         break;
                     }
-                    uint8_t *rows = pring + sP * kTileBytes;
+                    uint8_t *rows = pring + sP * psz;
                     const int32_t *pg = u->pg + (shrink ? 0 : kMaxPrefillRank);
                     const int rank = u->rank;
 #pragma unroll
@@ -379,7 +398,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                         }
                     }
                     cp_async_arrive_noinc(&fullP[sP]);   // the stage's consumer fences the proxies
-                    ++g;
+                    pfill ^= 1u << sP;
+                    sP = sP + 1 == np ? 0 : sP + 1;
                 }
             }
             __syncwarp();
@@ -391,6 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         // ---------------------------------------------------------------- MMA issue
         if (lane == 0) {
             uint32_t g = 0, e = 0, ui = 0;
+            uint32_t pcons = 0;   // bit s: parity of the number of times page slot s was consumed
             const uint32_t ua = smem_u32(Us);
             for (uint32_t i = 0;; ++i) {
                 wait_phase<false>(&dfull[i & 1], (i >> 1) & 1, abort, status);
@@ -400,20 +421,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 if (flag == kEnd) break;
                 if (flag != kCompute) continue;
                 const uint32_t idesc_s = tc::idesc_f16_f32(MT, r_pad, 0, 0);
+                const int np = pslots_for(r_pad), psz = r_pad * 128;
+                int sP = 0;
                 for (int kb = 0; kb < nkb && !*abort; ++kb) {
-                    const uint32_t sT = g % nts, sP = g % kPSlots;
+                    const uint32_t sT = g % nts;
                     wait_phase<false>(&fullT[sT], (g / nts) & 1, abort, status);
-                    wait_phase<false>(&fullP[sP], (g / kPSlots) & 1, abort, status);
+                    wait_phase<false>(&fullP[sP], (pcons >> sP) & 1, abort, status);
                     if (*abort) break;
                     tc::fence_proxy_async_smem();   // the cp.async page rows, for the tensor core
                     tc::fence_after_sync();
-                    const uint32_t xa = smem_u32(tring + sT * kTileBytes), aa = smem_u32(pring + sP * kTileBytes);
+                    const uint32_t xa = smem_u32(tring + sT * kTileBytes), aa = smem_u32(pring + sP * psz);
 #pragma unroll
                     for (int kk = 0; kk < KBLK / 16; ++kk)
                         tc::mma_f16(tmem, tc::smem_desc_sw128(xa + kk * 32, 16, 1024),
                                     tc::smem_desc_sw128(aa + kk * 32, 16, 1024), idesc_s, (kb | kk) != 0);
                     tc::commit(&emptyT[sT]);
                     tc::commit(&emptyP[sP]);
+                    pcons ^= 1u << sP;
+                    sP = sP + 1 == np ? 0 : sP + 1;
                     ++g;
                 }
                 if (*abort) break;
@@ -424,13 +449,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 fence_proxy_async_all();
                 const uint32_t idesc_e = tc::idesc_f16_f32(MT, KBLK, 0, 1);
                 for (int nt = 0; nt < nkb; ++nt) {
-                    const uint32_t sP = g % kPSlots, b = e % NB;
-                    wait_phase<false>(&fullP[sP], (g / kPSlots) & 1, abort, status);
+                    const uint32_t b = e % NB;
+                    wait_phase<false>(&fullP[sP], (pcons >> sP) & 1, abort, status);
                     if (e >= (uint32_t)NB) wait_phase<false>(&accempty[b], ((e / NB) - 1) & 1, abort, status);
                     if (*abort) break;
                     tc::fence_proxy_async_smem();
                     tc::fence_after_sync();
-                    const uint32_t ba = smem_u32(pring + sP * kTileBytes);
+                    const uint32_t ba = smem_u32(pring + sP * psz);
                     for (int ks = 0; ks < r_pad / 16; ++ks) {
                         const uint32_t a_addr = ua + (ks >> 2) * kTileBytes + (ks & 3) * 32;
                         tc::mma_f16(tmem + 128 + b * 64, tc::smem_desc_sw128(a_addr, 16, 1024),
@@ -438,6 +463,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     }
                     tc::commit(&emptyP[sP]);
                     tc::commit(&accfull[b]);
+                    pcons ^= 1u << sP;
+                    sP = sP + 1 == np ? 0 : sP + 1;
                     ++g;
                     ++e;
                 }
@@ -593,11 +620,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     break;
                 }
                 uint8_t *yt = tring + sT * kTileBytes;
+                // the row's eight 16-byte chunks: all loads first, then the arithmetic, then
+                // all stores, so the shared-memory latencies overlap
+                uint4 yrow[8];
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc)
+                    yrow[cc] = *reinterpret_cast<const uint4 *>(yt + m * 128 + ((cc ^ (m & 7)) << 4));
 #pragma unroll
                 for (int cc = 0; cc < 8; ++cc) {
-                    uint4 *yp = reinterpret_cast<uint4 *>(yt + m * 128 + ((cc ^ (m & 7)) << 4));
-                    const uint4 y0 = *yp;
-                    const __half2 *h2 = reinterpret_cast<const __half2 *>(&y0);
+                    const __half2 *h2 = reinterpret_cast<const __half2 *>(&yrow[cc]);
                     float o[8];
 #pragma unroll
                     for (int t = 0; t < 4; ++t) {
@@ -605,8 +636,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                         o[2 * t] = fmaf(sc, __uint_as_float(v[8 * cc + 2 * t]), f2.x);
                         o[2 * t + 1] = fmaf(sc, __uint_as_float(v[8 * cc + 2 * t + 1]), f2.y);
                     }
-                    *yp = pack_h8(o);
+                    yrow[cc] = pack_h8(o);
                 }
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc)
+                    *reinterpret_cast<uint4 *>(yt + m * 128 + ((cc ^ (m & 7)) << 4)) = yrow[cc];
                 const int n0 = k_lo + nt * KBLK;
                 if (full_tile) {
                     tc::fence_proxy_async_smem();
