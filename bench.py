@@ -55,7 +55,7 @@ def parse():
 # DRAM bytes (read + write) per launch of the delta kernel, from one ncu capture of the
 # current kernel on the workload (profiles/delta_kernel_<workload>.md gives the command);
 # a workload without a capture of the current kernel reports null.
-TRAFFIC = {"decode_7b_h4096_a100_t256_zipf1": 41897984}
+TRAFFIC = {"decode_7b_h4096_a100_t256_zipf1": 41897984, "prefill_7b_h4096_s16x512": 155520512}
 
 
 def peaks():
