@@ -52,9 +52,10 @@ def parse():
     return ap.parse_args()
 
 
-# DRAM bytes (read + write) per launch of the delta kernel, from one ncu capture of the
-# current kernel on the workload (profiles/delta_kernel_<workload>.md gives the command);
-# a workload without a capture of the current kernel reports null.
+# DRAM bytes (read + write) per launch of the workload's dominant kernel, from one ncu
+# capture of the current kernel on the workload (profiles/delta_kernel_decode_7b.md and
+# profiles/prefill_kernel_prefill_7b.md give the commands); a workload without a capture
+# of the current kernel reports null.
 TRAFFIC = {"decode_7b_h4096_a100_t256_zipf1": 41897984, "prefill_7b_h4096_s16x512": 155520512}
 
 

@@ -787,35 +787,54 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
             wait_phase<true>(&ready[ppar], (pu >> 1) & 1, abort, status);
             consumers_sync();   // the previous expand is done reading u
             {
-                // u = sum of the C partials in CTA order, rounded to fp16 once; all the
-                // remote loads of a thread are issued before the sums
+                // u = sum of the C partials in CTA order, rounded to fp16 once.  A thread
+                // takes up to two 4-element vectors of the unit and issues the 16-byte
+                // remote loads of four CTAs at once (a second round only for clusters of
+                // more than four), so the exchange costs one or two remote round trips.
                 const uint32_t pbase = smem_u32(part + ppar * (kTok * kRC));
-                constexpr int kPer = kTok * kRC / kConsumers;   // elements per thread at most
-                constexpr int kBatch = 2;                        // elements whose loads are in flight together
-                const int ne = kTok * 16 * nb;
-                for (int m0 = 0; m0 < kPer; m0 += kBatch) {
-                    if (tid + m0 * kConsumers >= ne) break;
-                    float v[kBatch][kMaxCluster];
+                const int vpr = 4 * nb;                 // vectors per token row
+                const int nv = kTok * vpr;
+                static_assert(kTok * kRC / 4 <= 2 * kConsumers, "two vectors per thread");
+                float4 sum[2];
+                int vt[2], vj[2];
 #pragma unroll
-                    for (int m = 0; m < kBatch; ++m) {
-                        const int e = tid + (m0 + m) * kConsumers;
-                        const int t = e / (16 * nb), j = e - t * (16 * nb);
-                        const uint32_t off = (uint32_t)(t * kRC + j) * 4;
+                for (int m = 0; m < 2; ++m) {
+                    const int e = tid + m * kConsumers;
+                    vt[m] = e / vpr;
+                    vj[m] = e - vt[m] * vpr;
+                    sum[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
 #pragma unroll
-                        for (int cc = 0; cc < kMaxCluster; ++cc)
-                            v[m][cc] = (e < ne && cc < (int)C) ? ld_cluster_f32(mapa(pbase + off, cc)) : 0.f;
+                for (int c0 = 0; c0 < kMaxCluster; c0 += 4) {
+                    if (c0 >= (int)C) break;
+                    float4 v[2][4];
+#pragma unroll
+                    for (int m = 0; m < 2; ++m) {
+                        const bool ok = tid + m * kConsumers < nv;
+                        const uint32_t off = (uint32_t)(vt[m] * kRC + vj[m] * 4) * 4;
+#pragma unroll
+                        for (int cc = 0; cc < 4; ++cc)
+                            v[m][cc] = (ok && c0 + cc < (int)C) ? ld_cluster_v4(mapa(pbase + off, c0 + cc))
+                                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
                     }
 #pragma unroll
-                    for (int m = 0; m < kBatch; ++m) {
-                        const int e = tid + (m0 + m) * kConsumers;
-                        if (e < ne) {
-                            const int t = e / (16 * nb), j = e - t * (16 * nb);
-                            float sum = 0.f;
+                    for (int m = 0; m < 2; ++m)
 #pragma unroll
-                            for (int cc = 0; cc < kMaxCluster; ++cc)
-                                sum += v[m][cc];   // CTA order; absent CTAs add zero
-                            ubuf[t * kUPitch + j] = __float2half_rn(j < rows ? sum : 0.f);
+                        for (int cc = 0; cc < 4; ++cc) {   // CTA order; absent CTAs add zero
+                            sum[m].x += v[m][cc].x;
+                            sum[m].y += v[m][cc].y;
+                            sum[m].z += v[m][cc].z;
+                            sum[m].w += v[m][cc].w;
                         }
+                }
+#pragma unroll
+                for (int m = 0; m < 2; ++m) {
+                    if (tid + m * kConsumers < nv) {
+                        const int j = vj[m] * 4;
+                        __half2 h[2];
+                        h[0] = __floats2half2_rn(j < rows ? sum[m].x : 0.f, j + 1 < rows ? sum[m].y : 0.f);
+                        h[1] = __floats2half2_rn(j + 2 < rows ? sum[m].z : 0.f, j + 3 < rows ? sum[m].w : 0.f);
+                        *reinterpret_cast<uint2 *>(ubuf + vt[m] * kUPitch + j) = *reinterpret_cast<const uint2 *>(h);
                     }
                 }
             }

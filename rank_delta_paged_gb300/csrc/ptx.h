@@ -201,6 +201,15 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t caddr)
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(caddr) : "memory");
     return v;
 }
+__device__ __forceinline__ float4 ld_cluster_v4(uint32_t caddr)
+{
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(caddr)
+                 : "memory");
+    return v;
+}
 // Arrive (release, cluster scope) on an mbarrier in another CTA of the cluster.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t caddr)
 {
