@@ -442,6 +442,76 @@ __device__ __forceinline__ int cluster_item(int k, int cl, int ncl)
     return k * ncl + ((k & 1) ? (ncl - 1 - cl) : cl);
 }
 
+// Balanced item order for batches of at most kBalRounds rounds of items over at most 64
+// clusters: round 0 gives item c to cluster c; every later round gives its costliest item
+// to the least loaded cluster, the next to the next least loaded, and so on (cost: the
+// rows of A^T, B, x, y0 and y the item moves).  Every CTA of the grid computes the same
+// order, so each item is still processed by exactly one cluster.
+constexpr int kBalRounds = 4;
+constexpr int kBalClusters = 64;
+
+// Ascending bitonic sort of 64 keys held two per lane (element lane and lane + 32).
+__device__ __forceinline__ void warp_sort64(int &a, int &b, int lane)
+{
+#pragma unroll
+    for (int k = 2; k <= 64; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            if (j == 32) {
+                const int lo = min(a, b), hi = max(a, b);
+                a = lo;
+                b = hi;
+            } else {
+                const int pa = __shfl_xor_sync(0xffffffffu, a, j), pb = __shfl_xor_sync(0xffffffffu, b, j);
+                const bool low = (lane & j) == 0;
+                const bool upa = (lane & k) == 0, upb = ((lane + 32) & k) == 0;
+                a = (low == upa) ? min(a, pa) : max(a, pa);
+                b = (low == upb) ? min(b, pb) : max(b, pb);
+            }
+        }
+    }
+}
+
+// One warp: this cluster's items of rounds 1 .. kBalRounds-1 into seq[] (n_items = none).
+__device__ void balance_items(const Item *items, int n_items, int ncl, int cl, int lane, int *seq, int *cost,
+                              int *load)
+{
+    for (int i = lane; i < kBalRounds * kBalClusters; i += 32) {
+        int c = 0;
+        if (i < n_items) c = 4 * __ldcg(&items[i].rank) + 3 * __ldcg(&items[i].nt);
+        cost[i] = c;
+    }
+    for (int r = lane; r < kBalRounds; r += 32) seq[r] = n_items;
+    __syncwarp();
+    for (int c = lane; c < kBalClusters; c += 32) load[c] = c < ncl && c < n_items ? cost[c] : 0;
+    __syncwarp();
+    for (int r = 1; r < kBalRounds; ++r) {
+        const int base = r * ncl;
+        if (base >= n_items) break;
+        const int nb = min(ncl, n_items - base);
+        // items of the round, costliest first (ties: lower position first)
+        int ia = lane < nb ? -(cost[base + lane] * 1024 + (1023 - lane)) : INT_MAX;
+        int ib = lane + 32 < nb ? -(cost[base + lane + 32] * 1024 + (1023 - lane - 32)) : INT_MAX;
+        warp_sort64(ia, ib, lane);
+        // clusters, least loaded first (ties: lower cluster first)
+        int ca = lane < ncl ? load[lane] * 256 + lane : INT_MAX;
+        int cb = lane + 32 < ncl ? load[lane + 32] * 256 + lane + 32 : INT_MAX;
+        warp_sort64(ca, cb, lane);
+        __syncwarp();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int pos = lane + 32 * h;
+            const int ik = h ? ib : ia, ck = h ? cb : ca;
+            if (pos < nb) {
+                const int key = -ik, c = ck & 255;
+                load[c] += key / 1024;
+                if (c == cl) seq[r] = base + (1023 - key % 1024);
+            }
+        }
+        __syncwarp();
+    }
+}
+
 __device__ __forceinline__ Item load_item(const Item *p)
 {
     const uint4 *s = reinterpret_cast<const uint4 *>(p);
@@ -484,6 +554,8 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
     const int d = a.pv.hidden;
     const uint32_t crank = cluster_ctarank(), C = cluster_nctarank();
     const int cl = (int)cluster_id_x(), ncl = (int)ncluster_x();
+    __shared__ int s_seq[kBalRounds], s_cost[kBalRounds * kBalClusters], s_load[kBalClusters];
+    __shared__ __align__(8) uint64_t seq_bar;
     // this CTA's slice of the hidden dimension, in whole 16-element steps
     const int nk16 = d / 16;
     const int kb = 16 * (int)((crank * (uint32_t)nk16) / C);
@@ -506,6 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
             mbar_init(&consumed[b], C);
         }
         mbar_init(done, C);
+        mbar_init(&seq_bar, 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(&pwrit[b], 1);
             mbar_init(&rdone[b], 1);
@@ -518,6 +591,15 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
     griddep_wait();       // the plan of this batch is complete and visible
     griddep_launch_dependents();
     const int n_items = a.L.hdr->n_items;
+    const bool bal = n_items <= kBalRounds * ncl && ncl <= kBalClusters;
+    // the index of this cluster's k-th item (n_items or more: no more items)
+    auto item_of = [&](int k) -> int {
+        if (!bal) return cluster_item(k, cl, ncl);
+        if (k == 0) return cl;
+        if (k >= kBalRounds || k * ncl >= n_items) return n_items;
+        wait_phase<false>(&seq_bar, 0, abort, status);
+        return s_seq[k];
+    };
 
     // Work runs in units: one chunk of at most kRC rank rows of an item.  Both sides walk
     // the units in the same order and interleave them one unit apart (the shrink of unit
@@ -536,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
             bool have = true;
             if (c == nch) {
                 ++k;
-                const int i = cluster_item(k, cl, ncl);
+                const int i = item_of(k);
                 if (i >= n_items) {
                     have = false;
                 } else {
@@ -626,7 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
             bool have = true;
             if (c == nch) {
                 ++k;
-                const int i = cluster_item(k, cl, ncl);
+                const int i = item_of(k);
                 if (i >= n_items) {
                     have = false;
                 } else {
@@ -683,6 +765,12 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
 
     // ===================================== consumers =====================================
     const int w = warp;
+    if (w == 0 && bal && n_items > ncl) {
+        // while the first data is in flight
+        balance_items(a.L.items, n_items, ncl, cl, lane, s_seq, s_cost, s_load);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&seq_bar);
+    }
     const int q = lane >> 3, rr = lane & 7, gid = lane >> 2, tig = lane & 3;
     // this warp's output columns in the expand: column pairs [pp0, pp1) of 16 columns
     const int npair = KS / 16;
@@ -706,7 +794,7 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
         bool have = true;
         if (c == nch) {
             ++k;
-            const int i = cluster_item(k, cl, ncl);
+            const int i = item_of(k);
             if (i >= n_items) {
                 have = false;
             } else {
