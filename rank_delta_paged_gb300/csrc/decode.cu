@@ -704,20 +704,50 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
         int pc = 0, ptl = 0;
         bool ptv = false;
         int32_t ppb[4] = {-1, -1, -1, -1};
+        // The next item's metadata is fetched ahead in two steps, its record while the
+        // current item's A^T rows go out, then its tokens and the page-table entries of its
+        // first unit after the previous unit's B rows, so an item boundary waits for no load.
+        bool nvalid = false;
+        Item nit{};
+        int ntok = 0;
+        int32_t npa[4] = {-1, -1, -1, -1}, npb[4] = {-1, -1, -1, -1};
+        auto fetch_record = [&](int kk) {
+            const int i = item_of(kk);
+            nvalid = i < n_items;
+            if (nvalid) nit = load_item(a.L.items + i);
+        };
+        auto fetch_rest = [&]() {
+            if (!nvalid) return;
+            ntok = lane < nit.nt ? __ldcg(a.L.tok_order + nit.tok_begin + nit.t0 + lane) : 0;
+            const int rows = min(kRC, nit.rank);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int r = lane + 32 * m;
+                npa[m] = -1;
+                npb[m] = -1;
+                if (r < rows) {
+                    npa[m] = __ldcg(a.pv.pt_arena + nit.pt_base + r);
+                    npb[m] = __ldcg(a.pv.pt_arena + nit.pt_base + nit.rank + r);
+                }
+            }
+        };
+        fetch_record(0);
+        fetch_rest();
         for (;;) {
             bool have = true;
+            bool fresh = false;          // the unit is its item's first: its entries came ahead
             if (c == nch) {
                 ++k;
-                const int i = item_of(k);
-                if (i >= n_items) {
+                if (!nvalid) {
                     have = false;
                 } else {
-                    it = load_item(a.L.items + i);
-                    const int tok = lane < it.nt ? __ldcg(a.L.tok_order + it.tok_begin + it.t0 + lane) : 0;
+                    it = nit;
+                    const int tok = ntok;
                     tl = __shfl_sync(0xffffffffu, tok, lane & 15);
                     tv = (lane & 15) < it.nt;
                     c = 0;
                     nch = ceil_div(it.rank, kRC);
+                    fresh = true;
                     // the item's record and x rows, once item k-2's shrink is done with buffer k&1
                     if (k >= 2) wait_phase<false>(&xfree[k & 1], ((k >> 1) - 1) & 1, abort, status);
                     if (lane == 0) rec_it[k & 1] = it;
@@ -733,13 +763,19 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
                     const int r = lane + 32 * m;
-                    pa[m] = -1;
-                    if (r < rows) {
-                        pa[m] = __ldcg(a.pv.pt_arena + it.pt_base + rc0 + r);
-                        pb[m] = __ldcg(a.pv.pt_arena + it.pt_base + it.rank + rc0 + r);
+                    if (fresh) {
+                        pa[m] = npa[m];
+                        pb[m] = npb[m];
+                    } else {
+                        pa[m] = -1;
+                        if (r < rows) {
+                            pa[m] = __ldcg(a.pv.pt_arena + it.pt_base + rc0 + r);
+                            pb[m] = __ldcg(a.pv.pt_arena + it.pt_base + it.rank + rc0 + r);
+                        }
                     }
                 }
                 emit_blocks(rows, pa, false);
+                if (fresh) fetch_record(k + 1);
             }
             if (have_prev) {
                 // expand data of the previous unit: the item's y0 rows (first unit) and B rows
@@ -750,6 +786,7 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
                 }
                 emit_blocks(min(kRC, pit.rank - pc * kRC), ppb, true);
             }
+            if (have && fresh) fetch_rest();
             if (!have) break;
             have_prev = true;
             pit = it;
