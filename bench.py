@@ -85,7 +85,55 @@ def algorithmic_flops(w: W.Workload) -> float:
 
 
 # ---------------------------------------------------------------- clocks sampling
+class NvmlClocks:
+    """SM clock and clock-event reasons read through NVML (ctypes; reading only), polled
+    from a background thread every 0.5 ms, so that even a timed region of a few
+    milliseconds is sampled while it runs."""
+    # nvmlClocksEventReason bits
+    BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+            "hw_thermal_slowdown": 0x40}
+
+    def __init__(self, uuid: str):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        # the NVML device whose UUID matches the CUDA device's (NVML may list GPUs that
+        # CUDA does not see)
+        norm = lambda t: t.lower().replace("gpu-", "").replace("-", "")
+        want = norm(uuid)
+        n = ctypes.c_uint()
+        self.lib.nvmlDeviceGetCount_v2(ctypes.byref(n))
+        self.h = None
+        for i in range(n.value):
+            h = ctypes.c_void_p()
+            if self.lib.nvmlDeviceGetHandleByIndex_v2(i, ctypes.byref(h)) != 0:
+                continue
+            buf = ctypes.create_string_buffer(96)
+            if self.lib.nvmlDeviceGetUUID(h, buf, 96) == 0 and want and norm(buf.value.decode()) == want:
+                self.h = h
+                break
+        if self.h is None:
+            raise RuntimeError("no NVML device with UUID " + uuid)
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(self.lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        mx = ctypes.c_uint()
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))   # 1: SM clock
+        self.max_mhz = float(mx.value)
+
+    def sample(self):
+        ct = self.ct
+        mhz, mask = ct.c_uint(), ct.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(mhz)) != 0:
+            return None
+        self.reasons_fn(self.h, ct.byref(mask))
+        return float(mhz.value), int(mask.value)
+
+
 class ClockSampler:
+    """Clocks during the timed region: NVML polled every 0.5 ms when the library loads,
+    else nvidia-smi every 100 ms."""
     FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -93,18 +141,43 @@ class ClockSampler:
     def __init__(self, uuid: str):
         self.uuid = uuid
         self.proc = None
+        self.nvml = None
+        self.samples = []
+        self.source = "none"
+
+    def _poll(self):
+        import time
+        while not self._stop.is_set():
+            v = self.nvml.sample()
+            if v is not None:
+                self.samples.append(v)
+            time.sleep(0.0005)
 
     def __enter__(self):
+        try:
+            self.nvml = NvmlClocks(self.uuid)
+            import threading
+            self._stop = threading.Event()
+            self._thr = threading.Thread(target=self._poll, daemon=True)
+            self._thr.start()
+            self.source = "nvml"
+            return self
+        except Exception:
+            self.nvml = None
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi"
         except Exception:
             self.proc = None
         return self
 
     def __exit__(self, *exc):
         self.lines = []
+        if self.nvml is not None:
+            self._stop.set()
+            self._thr.join(timeout=5)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -116,6 +189,13 @@ class ClockSampler:
 
     def summary(self):
         sm, mx, reasons = [], [], set()
+        if self.nvml is not None:
+            for mhz, mask in self.samples:
+                sm.append(mhz)
+                for n, bit in NvmlClocks.BITS.items():
+                    if mask & bit:
+                        reasons.add(n)
+            mx = [self.nvml.max_mhz]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for l in getattr(self, "lines", []):
             f = [x.strip() for x in l.split(",")]
@@ -132,10 +212,10 @@ class ClockSampler:
                 if v.lower() == "active":
                     reasons.add(n)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": self.source}
         loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
         return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "source": self.source}
 
 
 # ---------------------------------------------------------------- CPU oracle timing
@@ -257,13 +337,15 @@ def main():
         # device time of one flush + step, so that the timed region lasts about 2 s
         g0 = torch.cuda.Event(enable_timing=True)
         g1 = torch.cuda.Event(enable_timing=True)
-        g0.record(stream)
-        for _ in range(5):
-            flush.zero_()
-            step()
-        g1.record(stream)
-        torch.cuda.synchronize()
-        per = g0.elapsed_time(g1) / 5 / 1e3
+        per = float("inf")
+        for _ in range(2):   # the faster of two passes: the first can include one-off costs
+            g0.record(stream)
+            for _ in range(5):
+                flush.zero_()
+                step()
+            g1.record(stream)
+            torch.cuda.synchronize()
+            per = min(per, g0.elapsed_time(g1) / 5 / 1e3)
         K = int(min(20000, max(10, 2.0 / max(per, 1e-6))))
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
