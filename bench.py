@@ -416,13 +416,16 @@ def main():
         sess.evict(used, stream)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
+        # the step's inputs go up before the adapter load is enqueued (the load makes the
+        # stream wait for the adapters; the input copies need not)
         idx.copy_(hidx, non_blocking=True)
         if hseg is not None:
             seg.copy_(hseg, non_blocking=True)
-        sess.load(used, stream)
         for p in range(w.n_proj):
             xs[p].copy_(hx[p], non_blocking=True)
             ys[p].copy_(hy0[p], non_blocking=True)
+        sess.load(used, stream)
+        for p in range(w.n_proj):
             rdp.slora_lora_apply(sess.pool, p, xs[p], ys[p], w.T, idx, seg, n_seg, None, stream)
             hy[p].copy_(ys[p], non_blocking=True)
         torch.cuda.synchronize()

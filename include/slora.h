@@ -151,11 +151,14 @@ slora_status slora_adapter_unregister(slora_pool_t pool, int32_t adapter_id,
  * mechanism": unused adapters leave GPU memory and stay on the host).
  *
  * load() takes 2 * rank * n_proj pages from the free list, writes the adapter's page
- * table, and on the pool's side stream: copies the pinned store rows to a device
- * staging buffer (cudaMemcpyAsync), runs the page-scatter kernel (staging row i ->
- * its page, bit for bit), and publishes the directory entry.  `stream` then waits on
- * an event recorded after that work, so kernels enqueued later on `stream` see the
- * adapter; the host call does not wait for the copy.  The side stream first waits for
+ * table into its pinned host copy, and on the pool's side stream runs the load kernel,
+ * which reads the pinned store rows and their page ids straight from host memory
+ * (over the CPU-GPU link: no staging buffer, no copy per adapter) and writes each row
+ * to its page, bit for bit, and the page ids to the device page-table arena; then it
+ * publishes the directory entry.  `stream` then waits on an event recorded after that
+ * work, so kernels enqueued later on `stream` see the adapter; the host call does not
+ * wait for the upload.  The pinned store and page table of an adapter are not
+ * rewritten or freed while a load kernel may still read them.  The side stream first waits for
  * the most recent page release (evict / pages_free), so slots freed by work still in
  * flight are not overwritten early.
  * adapters_load() does the same for a list: ids that are already resident are

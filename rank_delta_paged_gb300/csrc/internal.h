@@ -20,12 +20,16 @@ struct alignas(16) DirEntry {
 };
 static_assert(sizeof(DirEntry) == 16, "DirEntry layout");
 
-// A run of consecutive staging rows that land on consecutive page-table entries.
+// A run of consecutive rows of an adapter's pinned host store that land on the pages of
+// consecutive page-table entries; the kernel reads both the rows and the page ids from
+// host memory and writes the pages and the page-table arena entries.
 struct ScatterRun {
-    int64_t staging_row0;   // first row in the staging buffer
-    int64_t pt_index0;      // first page-table arena entry
+    const void *src;         // device view of the first pinned store row
+    const int32_t *pt_src;   // device view of the rows' page ids (pinned)
+    int64_t pt_index0;       // first page-table arena entry
     int64_t nrows;
 };
+static_assert(sizeof(ScatterRun) == 32, "ScatterRun layout");
 
 // Directory update carried as a kernel argument.
 struct DirUpdate {
@@ -36,7 +40,7 @@ struct DirUpdate {
     int64_t pt_off;
 };
 
-constexpr int kMaxRunsPerLaunch = 512;     // 512 * 24 B fits the 32 KiB parameter space
+constexpr int kMaxRunsPerLaunch = 512;     // 512 * 32 B fits the 32 KiB parameter space
 constexpr int kMaxDirUpdatesPerLaunch = 512;
 
 struct ScatterArgs {
@@ -49,9 +53,8 @@ struct DirArgs {
 };
 
 // Kernel launchers (scatter.cu).
-cudaError_t launch_scatter(const uint16_t *staging, const int32_t *pt_arena, uint16_t *pool,
-                           int64_t num_pages, int32_t hidden, const ScatterArgs &args,
-                           int32_t *status, cudaStream_t stream);
+cudaError_t launch_scatter(int32_t *pt_arena, uint16_t *pool, int64_t num_pages, int32_t hidden,
+                           const ScatterArgs &args, int32_t *status, int num_sms, cudaStream_t stream);
 cudaError_t launch_dir_update(DirEntry *dir, const DirArgs &args, cudaStream_t stream);
 
 // Everything the hot-path kernels read about the pool.

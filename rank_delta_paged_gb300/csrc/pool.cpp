@@ -26,8 +26,9 @@ struct AdapterRec {
     float scaling = 0.f;
     uint16_t *store = nullptr;     // pinned [n_proj][2*rank][hidden]: A^T rows then B rows
     int32_t *pt_host = nullptr;    // pinned [n_proj][2*rank] page table
-    cudaEvent_t pt_event = nullptr;  // recorded after the last copy out of pt_host
-    bool pt_event_pending = false;
+    const void *store_dev = nullptr;      // device views of the two (read by the load kernel)
+    const int32_t *pt_host_dev = nullptr;
+    bool pt_read_pending = false;  // a load kernel may still read pt_host (the pool's load event covers it)
     int64_t pt_off = -1;           // arena offset while resident
 };
 
@@ -55,8 +56,6 @@ struct slora_pool {
     bool release_pending = false;
     cudaEvent_t load_event = nullptr;
 
-    uint16_t *staging = nullptr;
-    int64_t staging_rows = 0;
 
     PlanScratch plan;
     std::vector<AdapterRec> adapters;
@@ -96,14 +95,12 @@ void free_pool_memory(slora_pool *p)
     for (auto &a : p->adapters) {
         if (a.store) cudaFreeHost(a.store);
         if (a.pt_host) cudaFreeHost(a.pt_host);
-        if (a.pt_event) cudaEventDestroy(a.pt_event);
         a = AdapterRec();
     }
     if (p->pool_dev) cudaFree(p->pool_dev);
     if (p->pt_dev) cudaFree(p->pt_dev);
     if (p->dir_dev) cudaFree(p->dir_dev);
     if (p->status_dev) cudaFree(p->status_dev);
-    if (p->staging) cudaFree(p->staging);
     if (p->plan.base) cudaFree(p->plan.base);
     if (p->release_event) cudaEventDestroy(p->release_event);
     if (p->load_event) cudaEventDestroy(p->load_event);
@@ -112,24 +109,6 @@ void free_pool_memory(slora_pool *p)
 
 // Staging rows: enough for the largest registered adapter, at least 64 MiB, at most
 // 512 MiB (loads larger than that are split into several copy + scatter rounds).
-slora_status ensure_staging(slora_pool *p, int64_t want_rows)
-{
-    const int64_t row_bytes = 2ll * p->hidden;
-    int64_t lo = (64ll << 20) / row_bytes, hi = (512ll << 20) / row_bytes;
-    int64_t rows = std::max<int64_t>(lo, std::min<int64_t>(hi, want_rows));
-    if (p->staging && p->staging_rows >= rows)
-        return SLORA_OK;
-    if (p->staging) {
-        CUDA_TRY(cudaStreamSynchronize(p->side));
-        cudaFree(p->staging);
-        p->staging = nullptr;
-        p->staging_rows = 0;
-    }
-    CUDA_TRY(cudaMalloc(&p->staging, (size_t)(rows * row_bytes)));
-    p->staging_rows = rows;
-    return SLORA_OK;
-}
-
 }  // namespace
 
 extern "C" {
@@ -274,12 +253,16 @@ slora_status slora_adapter_register(slora_pool_t p, int32_t id, int32_t rank, fl
         cudaFreeHost(n.store);
         return fail(SLORA_ERR_HOST_ALLOC, "adapter_register: page table");
     }
-    if (cudaEventCreateWithFlags(&n.pt_event, cudaEventDisableTiming) != cudaSuccess) {
+    void *sd = nullptr, *pd = nullptr;
+    if (cudaHostGetDevicePointer(&sd, n.store, 0) != cudaSuccess ||
+        cudaHostGetDevicePointer(&pd, n.pt_host, 0) != cudaSuccess) {
         cudaGetLastError();
         cudaFreeHost(n.store);
         cudaFreeHost(n.pt_host);
-        return fail(SLORA_ERR_CUDA, "adapter_register: event");
+        return fail(SLORA_ERR_CUDA, "adapter_register: no device view of the pinned store");
     }
+    n.store_dev = sd;
+    n.pt_host_dev = static_cast<const int32_t *>(pd);
     // store layout per projection: A^T rows 0..r-1 then B rows 0..r-1, the page-table order
     for (int32_t pr = 0; pr < p->n_proj; ++pr) {
         uint16_t *dst = n.store + (size_t)pr * 2 * rank * row;
@@ -314,7 +297,6 @@ slora_status slora_adapter_unregister(slora_pool_t p, int32_t id, slora_stream_t
     CUDA_TRY(cudaStreamSynchronize(p->side));
     cudaFreeHost(a.store);
     cudaFreeHost(a.pt_host);
-    cudaEventDestroy(a.pt_event);
     a = AdapterRec();
     return SLORA_OK;
 }
@@ -325,7 +307,7 @@ slora_status slora_adapters_load(slora_pool_t p, int32_t n, const int32_t *ids, 
         return fail(SLORA_ERR_INVALID_ARG, "adapters_load: n=%d", n);
     std::vector<int32_t> todo;
     std::unordered_set<int32_t> seen;
-    int64_t need_pages = 0, max_rows = 0;
+    int64_t need_pages = 0;
     for (int32_t i = 0; i < n; ++i) {
         int32_t id = ids[i];
         if (!valid_id(p, id))
@@ -337,7 +319,6 @@ slora_status slora_adapters_load(slora_pool_t p, int32_t n, const int32_t *ids, 
             continue;
         todo.push_back(id);
         need_pages += adapter_rows(p, a);
-        max_rows = std::max(max_rows, adapter_rows(p, a));
     }
     if (todo.empty())
         return SLORA_OK;
@@ -346,8 +327,6 @@ slora_status slora_adapters_load(slora_pool_t p, int32_t n, const int32_t *ids, 
                     (long long)need_pages, (long long)p->pages.num_free());
     slora_status st = set_device(p);
     if (st != SLORA_OK)
-        return st;
-    if ((st = ensure_staging(p, max_rows)) != SLORA_OK)
         return st;
 
     // Host bookkeeping first (pages + arena), with rollback if the arena is too fragmented.
@@ -365,9 +344,9 @@ slora_status slora_adapters_load(slora_pool_t p, int32_t n, const int32_t *ids, 
             }
             return fail(SLORA_ERR_POOL_FULL, "adapters_load: page-table arena fragmented");
         }
-        if (a.pt_event_pending) {  // a previous load may still be copying out of pt_host
-            CUDA_TRY(cudaEventSynchronize(a.pt_event));
-            a.pt_event_pending = false;
+        if (a.pt_read_pending) {   // a previous load kernel may still read pt_host
+            CUDA_TRY(cudaEventSynchronize(p->load_event));   // recorded after every load's work
+            for (int32_t t : todo) p->adapters[(size_t)t].pt_read_pending = false;
         }
         p->pages.alloc(rows, a.pt_host);  // cannot fail: counted above
         a.pt_off = off;
@@ -377,46 +356,33 @@ slora_status slora_adapters_load(slora_pool_t p, int32_t n, const int32_t *ids, 
     cudaStream_t side = p->side;
     if (p->release_pending)
         CUDA_TRY(cudaStreamWaitEvent(side, p->release_event, 0));
-    const int64_t row_elems = p->hidden;
+    // One kernel per 512 adapters reads the rows and their page ids straight from the
+    // pinned store and page table, writes the pages and the page-table arena.
     ScatterArgs sargs;
     sargs.n_runs = 0;
-    int64_t cursor = 0;  // staging rows filled in this round
     auto flush = [&]() -> slora_status {
         if (sargs.n_runs == 0)
             return SLORA_OK;
-        CUDA_TRY(launch_scatter(p->staging, p->pt_dev, p->pool_dev, p->num_pages, p->hidden, sargs,
-                                p->status_dev, side));
+        CUDA_TRY(launch_scatter(p->pt_dev, p->pool_dev, p->num_pages, p->hidden, sargs, p->status_dev,
+                                p->num_sms, side));
         p->launches += 1;
         sargs.n_runs = 0;
-        cursor = 0;
         return SLORA_OK;
     };
     for (int32_t id : todo) {
         AdapterRec &a = p->adapters[(size_t)id];
-        int64_t rows = adapter_rows(p, a);
-        CUDA_TRY(cudaMemcpyAsync(p->pt_dev + a.pt_off, a.pt_host, (size_t)rows * 4,
-                                 cudaMemcpyHostToDevice, side));
-        CUDA_TRY(cudaEventRecord(a.pt_event, side));
-        a.pt_event_pending = true;
-        int64_t r0 = 0;
-        while (r0 < rows) {
-            if (cursor == p->staging_rows || sargs.n_runs == kMaxRunsPerLaunch) {
-                if ((st = flush()) != SLORA_OK)
-                    return st;
-            }
-            int64_t take = std::min(rows - r0, p->staging_rows - cursor);
-            CUDA_TRY(cudaMemcpyAsync(p->staging + cursor * row_elems, a.store + r0 * row_elems,
-                                     (size_t)(take * row_elems * 2), cudaMemcpyHostToDevice, side));
-            ScatterRun &run = sargs.runs[sargs.n_runs++];
-            run.staging_row0 = cursor;
-            run.pt_index0 = a.pt_off + r0;
-            run.nrows = take;
-            cursor += take;
-            r0 += take;
-        }
+        ScatterRun &run = sargs.runs[sargs.n_runs++];
+        run.src = a.store_dev;
+        run.pt_src = a.pt_host_dev;
+        run.pt_index0 = a.pt_off;
+        run.nrows = adapter_rows(p, a);
+        if (sargs.n_runs == kMaxRunsPerLaunch && (st = flush()) != SLORA_OK)
+            return st;
     }
     if ((st = flush()) != SLORA_OK)
         return st;
+    for (int32_t id : todo)   // read by the kernels above until the load event below
+        p->adapters[(size_t)id].pt_read_pending = true;
     DirArgs dargs;
     dargs.n = 0;
     for (size_t i = 0; i < todo.size(); ++i) {

@@ -1,5 +1,7 @@
-// Page-scatter: staging rows (just copied from the pinned host store) -> their pool
-// pages, bit for bit, plus the adapter-directory update that publishes a load.
+// Adapter load: rows of the pinned host store go straight to their pool pages, bit for
+// bit, and the page ids of those rows into the device page-table arena, in one kernel
+// that reads host memory over the CPU-GPU link (no staging buffer, no copy per adapter);
+// plus the adapter-directory update that publishes a load.
 // (S-LoRA: Serving Thousands of Concurrent LoRA Adapters (explainer), "The mechanism":
 // only the adapters the running batch needs are fetched into the paged pool; a block
 // table maps each logical row to its physical page.)
@@ -12,13 +14,16 @@ namespace {
 
 constexpr int kScatterThreads = 256;
 
-// One warp copies one row (hidden * 2 bytes, a multiple of 128 bytes) with 16-byte
-// loads and stores.  Rows are found by a binary search over the runs' row prefix.
+// One warp moves one row (hidden * 2 bytes, a multiple of 128 bytes): its page id from the
+// host page table into the arena, and the row itself with 16-byte loads from host memory.
+// The page id and up to 16 loads per lane (a whole row at hidden 4096) are in flight
+// together, so a row costs about one round trip over the CPU-GPU link.  Rows are found by
+// a binary search over the runs' row prefix.
 __global__ void __launch_bounds__(kScatterThreads)
-scatter_kernel(const uint4 *__restrict__ staging, const int32_t *__restrict__ pt_arena,
-               uint4 *__restrict__ pool, int64_t num_pages, int32_t row_vecs,
+scatter_kernel(int32_t *__restrict__ pt_arena, uint4 *__restrict__ pool, int64_t num_pages, int32_t row_vecs,
                const __grid_constant__ ScatterArgs args, int32_t *status)
 {
+    constexpr int kPer = 16;   // 16-byte loads per lane in flight
     __shared__ int64_t prefix[kMaxRunsPerLaunch + 1];
     if (threadIdx.x == 0) {
         int64_t acc = 0;
@@ -41,15 +46,27 @@ scatter_kernel(const uint4 *__restrict__ staging, const int32_t *__restrict__ pt
         }
         const ScatterRun &run = args.runs[lo];
         const int64_t k = row - prefix[lo];
-        const int32_t page = pt_arena[run.pt_index0 + k];
-        if (page < 0 || page >= num_pages) {
-            if (lane == 0) atomicCAS(status, 0, SLORA_DEV_BAD_PAGE);
-            continue;
+        const uint4 *src = reinterpret_cast<const uint4 *>(run.src) + k * row_vecs;
+        const int32_t page = run.pt_src[k];
+        for (int v0 = 0; v0 < row_vecs; v0 += 32 * kPer) {
+            uint4 buf[kPer];
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) {
+                const int v = v0 + lane + 32 * i;
+                if (v < row_vecs) buf[i] = src[v];
+            }
+            if (v0 == 0 && lane == 0) pt_arena[run.pt_index0 + k] = page;
+            if (page < 0 || page >= num_pages) {
+                if (v0 == 0 && lane == 0) atomicCAS(status, 0, SLORA_DEV_BAD_PAGE);
+                continue;
+            }
+            uint4 *dst = pool + (int64_t)page * row_vecs;
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) {
+                const int v = v0 + lane + 32 * i;
+                if (v < row_vecs) dst[v] = buf[i];
+            }
         }
-        const uint4 *src = staging + (run.staging_row0 + k) * row_vecs;
-        uint4 *dst = pool + (int64_t)page * row_vecs;
-        for (int v = lane; v < row_vecs; v += 32)
-            dst[v] = src[v];
     }
 }
 
@@ -68,9 +85,8 @@ __global__ void dir_update_kernel(DirEntry *dir, const __grid_constant__ DirArgs
 
 }  // namespace
 
-cudaError_t launch_scatter(const uint16_t *staging, const int32_t *pt_arena, uint16_t *pool,
-                           int64_t num_pages, int32_t hidden, const ScatterArgs &args,
-                           int32_t *status, cudaStream_t stream)
+cudaError_t launch_scatter(int32_t *pt_arena, uint16_t *pool, int64_t num_pages, int32_t hidden,
+                           const ScatterArgs &args, int32_t *status, int num_sms, cudaStream_t stream)
 {
     if (args.n_runs <= 0)
         return cudaSuccess;
@@ -79,10 +95,10 @@ cudaError_t launch_scatter(const uint16_t *staging, const int32_t *pt_arena, uin
         rows += args.runs[i].nrows;
     const int warps_per_block = kScatterThreads / 32;
     int64_t blocks = (rows + warps_per_block - 1) / warps_per_block;
-    if (blocks > 152 * 16) blocks = 152 * 16;
-    scatter_kernel<<<(unsigned)blocks, kScatterThreads, 0, stream>>>(
-        reinterpret_cast<const uint4 *>(staging), pt_arena, reinterpret_cast<uint4 *>(pool), num_pages,
-        hidden / 8, args, status);
+    const int64_t cap = (int64_t)(num_sms > 0 ? num_sms : 1) * 8;
+    if (blocks > cap) blocks = cap;
+    scatter_kernel<<<(unsigned)blocks, kScatterThreads, 0, stream>>>(pt_arena, reinterpret_cast<uint4 *>(pool),
+                                                                     num_pages, hidden / 8, args, status);
     return cudaGetLastError();
 }
 
