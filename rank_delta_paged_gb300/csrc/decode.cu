@@ -62,6 +62,9 @@ constexpr int kMaxPlanGroups = 2048;    // distinct adapters per plan
 constexpr int kMaxHash = 2 * kMaxPlanGroups;
 
 static_assert(kRC / 16 <= kConsumerWarps, "one shrink block per consumer warp and rank chunk");
+// per-warp K-split partials of a unit's shrink: ksplit = warps / nb parts of 16 x 16 nb,
+// at most 16 x 16 x (number of warps) floats whatever the unit's size
+constexpr int kPtmpFloats = kTok * 16 * kConsumerWarps;
 
 struct PlanHeader {
     int32_t n_groups, n_items, pad0, pad1;
@@ -536,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
     uint8_t *xbuf = ring + NST * stageB;                                         // [2][16][P] x rows, by item parity
     float *part = reinterpret_cast<float *>(xbuf + 2 * stageB);                  // [2][16][kRC] partial u, by unit parity
     float *ptmp = part + 2 * kTok * kRC;                                         // [ksplit][16][16 nb] per-warp partials
-    __half *ubuf = reinterpret_cast<__half *>(ptmp + kTok * kRC);                // [16][kUPitch] u (fp16)
+    __half *ubuf = reinterpret_cast<__half *>(ptmp + kPtmpFloats);               // [16][kUPitch] u (fp16)
     Item *rec_it = reinterpret_cast<Item *>(ubuf + kTok * kUPitch);              // [2] item, by item parity
     int32_t *rec_tok = reinterpret_cast<int32_t *>(rec_it + 2);                 // [2][kTok] token ids
     uint64_t *bars = reinterpret_cast<uint64_t *>(rec_tok + 2 * kTok);
@@ -1068,7 +1071,7 @@ inline int delta_pitch(int hidden)
 inline size_t delta_smem_bytes(int hidden)
 {
     const size_t stage = (size_t)kTok * delta_pitch(hidden);
-    return (NST + 2) * stage + 3 * (size_t)kTok * kRC * 4 + (size_t)kTok * kUPitch * 2 + 2 * sizeof(Item) +
+    return (NST + 2) * stage + 2 * (size_t)kTok * kRC * 4 + (size_t)kPtmpFloats * 4 + (size_t)kTok * kUPitch * 2 + 2 * sizeof(Item) +
            2 * kTok * 4 + (2 * NST + 13) * 8;
 }
 
