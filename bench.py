@@ -218,6 +218,36 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm), "source": self.source}
 
 
+def graph_timing(step_on, flush, stream, reps):
+    """Median and mean CUDA-event time of one step replayed from a CUDA graph, each replay
+    preceded (outside its events) by a replay of a graph that writes the flush buffer."""
+    import torch
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        gs, gf = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            step_on(side)      # warm the capture stream
+            torch.cuda.current_stream().synchronize()
+            with torch.cuda.graph(gf, stream=side):
+                flush.zero_()
+            with torch.cuda.graph(gs, stream=side):
+                step_on(torch.cuda.current_stream())
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+            for a, b in ev:
+                gf.replay()
+                a.record(side)
+                gs.replay()
+                b.record(side)
+            side.synchronize()
+        stream.wait_stream(side)
+        t = [a.elapsed_time(b) for a, b in ev]
+        return {"ms_per_step": statistics.median(t), "mean_ms": statistics.fmean(t), "replays": reps,
+                "l2": "flush graph replayed before every step replay, outside its events"}
+    except Exception as e:   # a capture the runtime refuses is reported, not fatal
+        return {"unavailable": f"{type(e).__name__}: {e}"[:200]}
+
+
 # ---------------------------------------------------------------- CPU oracle timing
 def oracle_rate(w: W.Workload, seconds: float):
     """Tokens/s per layer of the fp64 oracle on a bounded token sample (projection 0)."""
@@ -372,6 +402,14 @@ def main():
     ms_per_step = total_ms / K
     value = tokens_per_s_per_layer(job_tokens, w.n_layers, ms_per_step)
 
+    # the same step replayed from a CUDA graph (no host launch cost): one graph zeroes the
+    # flush buffer, the other holds the step; CUDA events bracket each step replay
+    def step_on(st):
+        for p in range(w.n_proj):
+            rdp.slora_lora_apply(sess.pool, p, xs[p], ys[p], w.T, idx, seg, n_seg, None, st)
+
+    graph = graph_timing(step_on, flush, stream, max(100, min(K, 2000)))
+
     # dominant kernel roofline: the delta kernel of one projection, timed on its own
     # (the pool records an event between the plan and the delta; that record serialises
     # the two kernels, so this pass is separate from the timed steps above)
@@ -458,6 +496,7 @@ def main():
                 "d2h_bytes_per_step": int(d2h),
                 "includes": "H2D of x, y0, token map; cold load of the batch's adapters from the "
                             "pinned store (copy + page scatter); delta; D2H of y; eviction"},
+        "graph": graph,
         "flops_per_step": algorithmic_flops(w),
         "clocks": clk.summary(),
     }
