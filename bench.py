@@ -469,6 +469,25 @@ def main():
         torch.cuda.synchronize()
         if k >= 2:
             e2e_ms.append(1e3 * (time.perf_counter() - t0))
+    # the load path alone: a cold load of the batch's adapters (host call + device work)
+    load_wall, load_dev = [], []
+    for k in range(5):
+        sess.evict(used, stream)
+        torch.cuda.synchronize()
+        la, lb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        la.record(stream)
+        sess.load(used, stream)
+        lb.record(stream)
+        torch.cuda.synchronize()
+        if k >= 1:
+            load_wall.append(1e3 * (time.perf_counter() - t0))
+            load_dev.append(la.elapsed_time(lb))
+    load = {"adapters": len(used), "bytes": int(adapter_bytes),
+            "wall_ms": statistics.median(load_wall), "stream_ms": statistics.median(load_dev),
+            "gb_per_s": adapter_bytes / (statistics.median(load_wall) * 1e-3) / 1e9,
+            "includes": "host call (page allocation, page tables, launches) and the load kernel reading "
+                        "the pinned store over the CPU-GPU link; the directory update"}
     e2e_job_ms, _ = job_totals(statistics.mean(e2e_ms) if e2e_ms else float("nan"), float(w.T), dev, world)
     e2e_value = tokens_per_s_per_layer(job_tokens, w.n_layers, e2e_job_ms)
     status = sess.device_status()
@@ -497,6 +516,7 @@ def main():
                 "includes": "H2D of x, y0, token map; cold load of the batch's adapters from the "
                             "pinned store (copy + page scatter); delta; D2H of y; eviction"},
         "graph": graph,
+        "load": load,
         "flops_per_step": algorithmic_flops(w),
         "clocks": clk.summary(),
     }
@@ -506,6 +526,11 @@ def main():
         rate, cores, sample = oracle_rate(w, args.cpu_seconds)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s/layer", "cores": cores,
                                 "kind": "oracle", "sample": sample}
+        import oracle
+        oracle.set_threads(1)   # the same oracle on one core, a shorter sample
+        r1, _, s1 = oracle_rate(w, max(1.0, args.cpu_seconds / 3))
+        oracle.set_threads(cores)
+        line["cpu_baseline"]["single_core"] = {"value": r1, "cores": 1, "sample": s1}
     if rank == 0:
         print(json.dumps(line), flush=True)
     sess.close()

@@ -60,6 +60,8 @@ def _load():
             lib.slora_oracle_half_to_double.argtypes = [ctypes.c_uint16]
             lib.slora_oracle_threads.restype = ctypes.c_int
             lib.slora_oracle_threads.argtypes = []
+            lib.slora_oracle_set_threads.restype = None
+            lib.slora_oracle_set_threads.argtypes = [ctypes.c_int]
             P = ctypes.c_void_p
             lib.slora_oracle_delta.restype = ctypes.c_int
             lib.slora_oracle_delta.argtypes = [ctypes.c_int32, ctypes.c_int32, P, P, P,
@@ -72,6 +74,11 @@ def _load():
 def threads() -> int:
     """OpenMP threads the oracle runs on (set OMP_NUM_THREADS before the first call)."""
     return int(_load().slora_oracle_threads())
+
+
+def set_threads(n: int) -> None:
+    """Run later oracle calls on n OpenMP threads (timing only; results do not change)."""
+    _load().slora_oracle_set_threads(int(n))
 
 
 def half_to_double(bits: int) -> float:

@@ -56,6 +56,16 @@ double slora_oracle_half_to_double(uint16_t h)
     return sign ? -v : v;
 }
 
+/* OpenMP threads for later calls (n > 0); the arithmetic does not depend on it. */
+void slora_oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 int slora_oracle_threads(void)
 {
 #ifdef _OPENMP
