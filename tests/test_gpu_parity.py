@@ -396,3 +396,28 @@ def test_prefill_cluster_normal_values(ctas):
     finally:
         rdp.slora_debug_set_prefill_cluster(0)
     assert_close(got, oracle.workload_reference(w), f"prefill, {ctas} CTAs per cluster")
+
+
+def test_load_of_more_adapters_than_one_launch_carries():
+    """600 adapters in one load call: two launches of the load kernel (at most 512 adapters
+    each), which read the pinned store directly; pages bit-exact on both sides of the
+    split, and a batch over all of them matches the oracle."""
+    n = 600
+    ranks = np.full(n, 8, np.int32)
+    rng = np.random.default_rng(5)
+    idx = rng.integers(0, n, size=256).astype(np.int32)
+    w = W.Workload("many_adapters", 256, 1, ranks, idx, None, num_pages=2 * 2 * 8 * n, kv_pages=2 * 8 * n,
+                   shuffle_seed=9, seed=4)
+    with session_all_loaded(w) as s:
+        for a in (0, 1, 511, 512, 513, 599):
+            pt = np.empty(16, np.int32)
+            rdp.slora_adapter_pages(s.pool, a, 0, pt)
+            At, B = w.factors(a)
+            want = np.concatenate([At[0], B[0]]).view(np.uint16)
+            page = np.empty(w.hidden, np.uint16)
+            for j in range(16):
+                rdp.slora_page_read(s.pool, int(pt[j]), page)
+                assert np.array_equal(page, want[j]), (a, j)
+        got = run(s)
+        assert s.device_status() == 0
+    assert_close(got, oracle.workload_reference(w), "600 adapters")
