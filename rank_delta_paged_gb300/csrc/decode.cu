@@ -181,6 +181,7 @@ struct PlanArgs {
     int32_t n_seg;
     int32_t t_begin, t_end;
     int32_t hash_size;  // power of two >= 2 * min(t_end - t_begin, max_adapters), <= kMaxHash
+    int32_t dir_cache;  // the directory (max_adapters entries) is copied into shared memory
     PlanLayout L;
 };
 
@@ -192,6 +193,8 @@ constexpr size_t plan_smem_bytes(int hs)
 {
     return (size_t)kMaxPlanGroups * 8 + (size_t)hs * 12 + (size_t)7 * kMaxPlanGroups * 4 + (size_t)kMaxPlanTokens * 4;
 }
+// directories of at most this many adapters are copied into the plan's shared memory
+constexpr int kPlanDirCache = 2048;
 
 __device__ __forceinline__ void plan_refuse(const PlanArgs &a)
 {
@@ -219,6 +222,7 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const __grid_constant__ Pla
     int *gperm = pit + kMaxPlanGroups;                                     // [position] group, by rank descending
     short *tslot = reinterpret_cast<short *>(gperm + kMaxPlanGroups);      // [Tc] hash slot of the token (-1: none)
     short *tpos = tslot + kMaxPlanTokens;                                  // [Tc] the token's place within its group
+    DirEntry *sdir = reinterpret_cast<DirEntry *>(tpos + kMaxPlanTokens);  // [max_adapters] when dir_cache
     __shared__ int warp_tot2[33][2];
     __shared__ int s_lo, s_hi, s_G, s_nit;
     __shared__ int s_bucket[kRankBuckets + 1], s_bcur[kRankBuckets + 1];
@@ -227,6 +231,14 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const __grid_constant__ Pla
     griddep_launch_dependents();
     griddep_wait();
 
+    // the first NT tokens' adapter ids and (small) directories are fetched at once, beside
+    // the segment bounds, so the hash below waits for one round trip instead of three
+    const int ad_first = tid < Tc ? a.idx[a.t_begin + tid] : -1;
+    if (a.dir_cache) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(a.pv.dir);
+        uint4 *dst = reinterpret_cast<uint4 *>(sdir);
+        for (int i = tid; i < a.pv.max_adapters; i += NT) dst[i] = src[i];
+    }
     if (tid == 0) {
         int lo = 0, hi = 0;
         if (a.n_seg > 0) {
@@ -261,9 +273,9 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const __grid_constant__ Pla
         if (i < Tc) {
             const int t = a.t_begin + i;
             const bool in_seg = t >= lo && t < hi;
-            const int ad = a.idx[t];
+            const int ad = i0 == 0 ? ad_first : a.idx[t];
             if (ad >= 0 && ad < a.pv.max_adapters) {
-                const DirEntry e = a.pv.dir[ad];
+                const DirEntry e = a.dir_cache ? sdir[ad] : a.pv.dir[ad];
                 const bool resident = e.pt_off >= 0 && e.rank > 0 && e.rank <= kMaxRank;
                 // segment tokens run on the tensor-core prefill path unless their adapter's
                 // rank is too large for it; errors of segment tokens are reported there
@@ -1088,10 +1100,10 @@ cudaError_t launch_lora_apply(const PoolView &pv, int32_t proj, const uint16_t *
                                              (int)delta_smem_bytes(kMaxSlice));
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(plan_kernel<kPlanThreads>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)plan_smem_bytes(kMaxHash));
+                                 (int)(plan_smem_bytes(kMaxHash) + kPlanDirCache * sizeof(DirEntry)));
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(plan_kernel<kPlanThreadsSmall>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)plan_smem_bytes(kMaxHash));
+                                 (int)(plan_smem_bytes(kMaxHash) + kPlanDirCache * sizeof(DirEntry)));
         if (e != cudaSuccess) return e;
         attrs_set = true;
     }
@@ -1131,12 +1143,13 @@ cudaError_t launch_lora_apply(const PoolView &pv, int32_t proj, const uint16_t *
         const int32_t groups = (te - tb) < pv.max_adapters ? (te - tb) : pv.max_adapters;
         int hs = 1024;
         while (hs < 2 * groups && hs < kMaxHash) hs <<= 1;
-        PlanArgs pa{pv, proj, idx, T, seg_indptr, n_seg, tb, te, hs, L};
+        const int dcache = pv.max_adapters <= kPlanDirCache ? 1 : 0;
+        PlanArgs pa{pv, proj, idx, T, seg_indptr, n_seg, tb, te, hs, dcache, L};
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(1);
         const bool small = te - tb <= kPlanThreadsSmall;
         cfg.blockDim = dim3(small ? kPlanThreadsSmall : kPlanThreads);
-        cfg.dynamicSmemBytes = plan_smem_bytes(hs);
+        cfg.dynamicSmemBytes = plan_smem_bytes(hs) + (dcache ? (size_t)pv.max_adapters * sizeof(DirEntry) : 0);
         cfg.stream = stream;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
