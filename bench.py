@@ -49,6 +49,9 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--apply", choices=["multi", "single"], default="multi",
+                    help="multi: one slora_lora_apply_multi call per layer (all its projections); "
+                         "single: one slora_lora_apply call per projection")
     return ap.parse_args()
 
 
@@ -353,9 +356,21 @@ def main():
     l2 = int(torch.cuda.get_device_properties(local).L2_cache_size)
     flush = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=dev)
 
+    per_layer = w.n_proj // w.n_layers
+    multi = args.apply == "multi" and per_layer > 1
+
+    def apply_layer(l, st):
+        ps = list(range(l * per_layer, (l + 1) * per_layer))
+        if multi:
+            rdp.slora_lora_apply_multi(sess.pool, ps, [xs[p] for p in ps], [ys[p] for p in ps], w.T, idx, seg,
+                                       n_seg, None, st)
+        else:
+            for p in ps:
+                rdp.slora_lora_apply(sess.pool, p, xs[p], ys[p], w.T, idx, seg, n_seg, None, st)
+
     def step():
-        for p in range(w.n_proj):
-            rdp.slora_lora_apply(sess.pool, p, xs[p], ys[p], w.T, idx, seg, n_seg, None, stream)
+        for l in range(w.n_layers):
+            apply_layer(l, stream)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -405,17 +420,19 @@ def main():
     # the same step replayed from a CUDA graph (no host launch cost): one graph zeroes the
     # flush buffer, the other holds the step; CUDA events bracket each step replay
     def step_on(st):
-        for p in range(w.n_proj):
-            rdp.slora_lora_apply(sess.pool, p, xs[p], ys[p], w.T, idx, seg, n_seg, None, st)
+        for l in range(w.n_layers):
+            apply_layer(l, st)
 
     graph = graph_timing(step_on, flush, stream, max(100, min(K, 2000)))
 
-    # dominant kernel roofline: the delta kernel of one projection, timed on its own
-    # (the pool records an event between the plan and the delta; that record serialises
-    # the two kernels, so this pass is separate from the timed steps above)
+    # dominant kernel roofline: the delta kernel(s) of one call (one projection, or one
+    # layer's projections with --apply multi), timed on their own (the pool records an
+    # event between the plan and the delta; that record serialises the two kernels, so
+    # this pass is separate from the timed steps above)
     hbm, peak_kind = peaks()
     alg_bytes = algorithmic_bytes(w)
-    alg_bytes_launch = alg_bytes / w.n_proj
+    call_projs = per_layer if multi else 1
+    alg_bytes_launch = alg_bytes / w.n_proj * call_projs
     Kd = min(K, 200)
     d0 = [torch.cuda.Event(enable_timing=True) for _ in range(Kd)]
     d1 = [torch.cuda.Event(enable_timing=True) for _ in range(Kd)]
@@ -425,7 +442,10 @@ def main():
     for k in range(Kd):
         flush.zero_()
         rdp.slora_pool_set_stage_event(sess.pool, d0[k])
-        rdp.slora_lora_apply(sess.pool, 0, xs[0], ys[0], w.T, idx, seg, n_seg, None, stream)
+        if multi:
+            apply_layer(0, stream)
+        else:
+            rdp.slora_lora_apply(sess.pool, 0, xs[0], ys[0], w.T, idx, seg, n_seg, None, stream)
         d1[k].record(stream)
     torch.cuda.synchronize()
     rdp.slora_pool_set_stage_event(sess.pool, None)
@@ -463,9 +483,10 @@ def main():
             xs[p].copy_(hx[p], non_blocking=True)
             ys[p].copy_(hy0[p], non_blocking=True)
         sess.load(used, stream)
-        for p in range(w.n_proj):
-            rdp.slora_lora_apply(sess.pool, p, xs[p], ys[p], w.T, idx, seg, n_seg, None, stream)
-            hy[p].copy_(ys[p], non_blocking=True)
+        for l in range(w.n_layers):
+            apply_layer(l, stream)
+            for p in range(l * per_layer, (l + 1) * per_layer):
+                hy[p].copy_(ys[p], non_blocking=True)
         torch.cuda.synchronize()
         if k >= 2:
             e2e_ms.append(1e3 * (time.perf_counter() - t0))
@@ -500,13 +521,16 @@ def main():
         "n_gpus": world, "steps": K, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic (seeded; random-init adapters, no dataset)",
-        "config": config_of(w, "flushed: 2 x L2 written before every timed step, outside the "
-                               "per-step CUDA-event intervals"),
+        "config": dict(config_of(w, "flushed: 2 x L2 written before every timed step, outside the "
+                                    "per-step CUDA-event intervals"),
+                       apply=(f"one slora_lora_apply_multi call per layer ({per_layer} projections)" if multi
+                              else "one slora_lora_apply call per projection")),
         "gpu_launches": int(launches),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": TRAFFIC.get(w.name),
                      "kernel": "delta_kernel" + (" + prefill_kernel" if n_seg else "") +
-                               " (one projection; median CUDA-event time between the plan and the end of the call)",
+                               (f" (one call of {call_projs} projections" if multi else " (one projection") +
+                               "; median CUDA-event time between the plan and the end of the call)",
                      "launch_ms": delta_ms, "algorithmic_bytes_per_launch": alg_bytes_launch,
                      "peak_kind": f"{peak_kind} HBM copy bandwidth",
                      "step": {"achieved": step_achieved, "frac": step_achieved / hbm,

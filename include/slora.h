@@ -212,6 +212,39 @@ slora_status slora_lora_apply(slora_pool_t pool, int32_t proj, const void *x, vo
                               int32_t n_seg, const float *scaling, slora_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * slora_lora_apply_multi: the same computation as n calls of slora_lora_apply that share
+ * the tokens, their adapter ids and segments, one call per entry j with projection
+ * projs[j], input x[j] and in/out y[j] (S-LoRA: Multiplexing Thousands of Fine-Tuned
+ * Adapters on a Single GPU, section 3: the LoRA computation of every projection of a
+ * layer, for a batch of requests with different adapters).  A layer's q, k, v and o
+ * projections use the same batch, so one call makes one token plan and launches one
+ * decode kernel and one segment kernel for all of them, instead of n of each.
+ *
+ *   n       entries, 1 <= n <= 8
+ *   projs   host int32 [n], each 0 <= projs[j] < n_proj; an index may repeat
+ *   x       host array [n] of device pointers, fp16 [T][hidden], 16-byte aligned; entries
+ *           may share one buffer (q, k and v read the same hidden states)
+ *   y       host array [n] of device pointers, fp16 [T][hidden], in/out, 16-byte aligned;
+ *           the y buffers must not overlap each other or any x
+ *   T, token_adapter_idx, seg_indptr, n_seg, scaling, stream: as for slora_lora_apply.
+ *
+ * Every decode token's result is bit for bit that of the separate calls.  A segment
+ * token's result is too when the segment kernel uses the same number of CTAs per
+ * cluster (it is chosen from T * n here, from T in a single call; the test hook
+ * slora_debug_set_prefill_cluster fixes it); otherwise it differs only in the order of
+ * the fp32 partial sums of x A.  The host arrays are read during the call only.
+ * Errors: SLORA_ERR_INVALID_ARG for n out of range, a null array or pointer, a bad
+ * projection index, misalignment, or a y equal to another entry's y or to any x
+ * (checked on the pointers; overlapping ranges are the caller's error); nothing is
+ * launched then.
+ * ------------------------------------------------------------------------- */
+slora_status slora_lora_apply_multi(slora_pool_t pool, int32_t n, const int32_t *projs /*host*/,
+                                    const void *const *x /*host array*/, void *const *y /*host array*/,
+                                    int32_t T, const int32_t *token_adapter_idx,
+                                    const int32_t *seg_indptr, int32_t n_seg, const float *scaling,
+                                    slora_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * slora_lora_apply_noalloc: the same computation as slora_lora_apply, with the same
  * arguments, for callers that must not allocate device memory during the call.  The
  * S-LoRA pages have no counterpart for it; it exists for callers whose device memory

@@ -32,6 +32,7 @@ __all__ = [
     "slora_pool_set_stage_event",
     "slora_adapters_evict",
     "slora_debug_set_prefill_cluster",
+    "slora_lora_apply_multi",
 ]
 
 _I32, _I64, _U64, _F32, _P = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float, ctypes.c_void_p
@@ -69,6 +70,7 @@ _SIGS = {
     "slora_pool_set_stage_event": [_P, _P],
     "slora_adapters_evict": [_P, _I32, _P, _P],
     "slora_debug_set_prefill_cluster": [_I32],
+    "slora_lora_apply_multi": [_P, _I32, _P, _P, _P, _I32, _P, _P, _I32, _P, _P],
 }
 _RESTYPE = {"slora_status_str": ctypes.c_char_p, "slora_last_error": ctypes.c_char_p,
             "slora_version": _I32}
@@ -244,6 +246,20 @@ def slora_lora_apply_noalloc(pool: int, proj: int, x, y, T: int, token_adapter_i
     """slora_lora_apply without device allocation: plan scratch in the library's fixed
     device array (see include/slora.h for the size limit and the sharing rules)."""
     _call("slora_lora_apply_noalloc", pool, proj, _ptr(x), _ptr(y), T, _ptr(token_adapter_idx),
+          _ptr(seg_indptr), n_seg, _ptr(scaling), _stream(stream))
+
+
+def slora_lora_apply_multi(pool: int, projs, xs, ys, T: int, token_adapter_idx, seg_indptr=None,
+                           n_seg: int = 0, scaling=None, stream=None) -> None:
+    """One call for several projections of a layer: projs[j], xs[j], ys[j] per entry (the
+    host arrays of projection indices and device pointers are built here)."""
+    n = len(projs)
+    if len(xs) != n or len(ys) != n:
+        raise ValueError("projs, xs and ys must have the same length")
+    p_arr = (ctypes.c_int32 * max(n, 1))(*[int(v) for v in projs])
+    x_arr = (ctypes.c_void_p * max(n, 1))(*[_ptr(v) for v in xs])
+    y_arr = (ctypes.c_void_p * max(n, 1))(*[_ptr(v) for v in ys])
+    _call("slora_lora_apply_multi", pool, n, p_arr, x_arr, y_arr, T, _ptr(token_adapter_idx),
           _ptr(seg_indptr), n_seg, _ptr(scaling), _stream(stream))
 
 

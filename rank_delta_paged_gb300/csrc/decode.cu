@@ -31,9 +31,16 @@
 //     written / read" events to the cluster.  Each page row is read once per item; the
 //     cluster exchanges only the small fp32 partials.  Every wait is bounded in time.
 //
+// One call may cover several projections of a layer (q, k, v, o: the same tokens and
+// adapters, each projection with its own pages, x and y).  The plan is made once; the
+// delta kernel's work list is every (item, projection) pair, item-major, so the pairs
+// keep the plan's descending-cost order and the clusters share them out as they would
+// the items of one projection.
+//
 // A token's arithmetic is fixed by the fragment layout, the slice boundaries and the CTA
-// order of the partial sum, never by the other tokens of its item, so results do not
-// depend on the batch, its order, or the physical pages.
+// order of the partial sum, never by the other tokens of its item or the other
+// projections of the call, so results do not depend on the batch, its order, the
+// physical pages, or how the projections are grouped into calls.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -77,7 +84,7 @@ struct alignas(16) Item {
     int32_t tok_begin;  // the group's first position in tok_order
     int32_t adapter;
     float scaling;
-    int64_t pt_base;    // arena index of this projection's page table
+    int64_t pt_base;    // arena index of the adapter's page tables (projection 0's)
 };
 static_assert(sizeof(Item) == 32, "Item layout");
 
@@ -174,7 +181,6 @@ __device__ __forceinline__ void block_excl_scan(const int (&v)[N], int (*wt)[N],
 
 struct PlanArgs {
     PoolView pv;
-    int32_t proj;
     const int32_t *idx;
     int32_t T;
     const int32_t *seg_indptr;
@@ -292,7 +298,7 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const __grid_constant__ Pla
                                     gad[g] = ad;
                                     grank[g] = e.rank;
                                     gscale[g] = e.scaling;
-                                    gpt[g] = e.pt_off + (long long)a.proj * 2 * e.rank;
+                                    gpt[g] = e.pt_off;
                                     gslot[g] = h;
                                     atomicAdd(&s_bucket[31 - __clz(e.rank)], 1);
                                 }
@@ -416,8 +422,10 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const __grid_constant__ Pla
 
 struct DeltaArgs {
     PoolView pv;
-    const __half *x;
-    __half *y;
+    const __half *x[kMaxApplyProj];   // per projection of the call
+    __half *y[kMaxApplyProj];
+    int32_t proj[kMaxApplyProj];
+    int32_t n_proj;                   // projections of the call
     const float *scaling;   // optional override [max_adapters]
     PlanLayout L;
     int32_t pitch;          // bytes per row of a stage / x / y0 buffer: 2 * largest slice + 16
@@ -487,13 +495,14 @@ __device__ __forceinline__ void warp_sort64(int &a, int &b, int lane)
     }
 }
 
-// One warp: this cluster's items of rounds 1 .. kBalRounds-1 into seq[] (n_items = none).
-__device__ void balance_items(const Item *items, int n_items, int ncl, int cl, int lane, int *seq, int *cost,
-                              int *load)
+// One warp: this cluster's work entries of rounds 1 .. kBalRounds-1 into seq[] (n_items =
+// none).  Entry i is item i / np of the plan for projection slot i % np.
+__device__ void balance_items(const Item *items, int n_items, int np, int ncl, int cl, int lane, int *seq,
+                              int *cost, int *load)
 {
     for (int i = lane; i < kBalRounds * kBalClusters; i += 32) {
         int c = 0;
-        if (i < n_items) c = 4 * __ldcg(&items[i].rank) + 3 * __ldcg(&items[i].nt);
+        if (i < n_items) c = 4 * __ldcg(&items[i / np].rank) + 3 * __ldcg(&items[i / np].nt);
         cost[i] = c;
     }
     for (int r = lane; r < kBalRounds; r += 32) seq[r] = n_items;
@@ -554,7 +563,8 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
     __half *ubuf = reinterpret_cast<__half *>(ptmp + kPtmpFloats);               // [16][kUPitch] u (fp16)
     Item *rec_it = reinterpret_cast<Item *>(ubuf + kTok * kUPitch);              // [2] item, by item parity
     int32_t *rec_tok = reinterpret_cast<int32_t *>(rec_it + 2);                 // [2][kTok] token ids
-    uint64_t *bars = reinterpret_cast<uint64_t *>(rec_tok + 2 * kTok);
+    int32_t *rec_pj = rec_tok + 2 * kTok;                                        // [2] projection slot
+    uint64_t *bars = reinterpret_cast<uint64_t *>(rec_pj + 2);
     uint64_t *full = bars, *empty = bars + NST;
     uint64_t *full_x = bars + 2 * NST;   // [2] an item's x rows (and record) landed
     uint64_t *xfree = full_x + 2;        // [2] an item's shrink no longer reads its x rows
@@ -605,7 +615,8 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
     cluster_sync_all();   // every CTA's barriers exist before any remote arrival
     griddep_wait();       // the plan of this batch is complete and visible
     griddep_launch_dependents();
-    const int n_items = a.L.hdr->n_items;
+    const int NP = a.n_proj;
+    const int n_items = a.L.hdr->n_items * NP;   // (item, projection) entries
     const bool bal = n_items <= kBalRounds * ncl && ncl <= kBalClusters;
     // the index of this cluster's k-th item (n_items or more: no more items)
     auto item_of = [&](int k) -> int {
@@ -638,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
                     have = false;
                 } else {
                     c = 0;
-                    nch = ceil_div(__ldcg(&a.L.items[i].rank), kRC);
+                    nch = ceil_div(__ldcg(&a.L.items[i / NP].rank), kRC);
                 }
             }
             if (have) {
@@ -712,11 +723,12 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
         };
         int k = -1, c = 0, nch = 0;      // current unit: item ordinal, rank chunk, chunks of the item
         Item it{};
+        int ipj = 0;                     // projection slot of the current item
         int tl = 0;                      // lane l: token id of the item's token l & 15
         bool tv = false;
         bool have_prev = false;          // previous unit, whose expand data follows
         Item pit{};
-        int pc = 0, ptl = 0;
+        int pc = 0, ptl = 0, ppj = 0;
         bool ptv = false;
         int32_t ppb[4] = {-1, -1, -1, -1};
         // The next item's metadata is fetched ahead in two steps, its record while the
@@ -724,12 +736,16 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
         // first unit after the previous unit's B rows, so an item boundary waits for no load.
         bool nvalid = false;
         Item nit{};
-        int ntok = 0;
+        int ntok = 0, npj = 0;
         int32_t npa[4] = {-1, -1, -1, -1}, npb[4] = {-1, -1, -1, -1};
         auto fetch_record = [&](int kk) {
             const int i = item_of(kk);
             nvalid = i < n_items;
-            if (nvalid) nit = load_item(a.L.items + i);
+            if (nvalid) {
+                nit = load_item(a.L.items + i / NP);
+                npj = i % NP;
+                nit.pt_base += (int64_t)a.proj[npj] * 2 * nit.rank;   // this projection's page table
+            }
         };
         auto fetch_rest = [&]() {
             if (!nvalid) return;
@@ -757,6 +773,7 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
                     have = false;
                 } else {
                     it = nit;
+                    ipj = npj;
                     const int tok = ntok;
                     tl = __shfl_sync(0xffffffffu, tok, lane & 15);
                     tv = (lane & 15) < it.nt;
@@ -765,9 +782,12 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
                     fresh = true;
                     // the item's record and x rows, once item k-2's shrink is done with buffer k&1
                     if (k >= 2) wait_phase<false>(&xfree[k & 1], ((k >> 1) - 1) & 1, abort, status);
-                    if (lane == 0) rec_it[k & 1] = it;
+                    if (lane == 0) {
+                        rec_it[k & 1] = it;
+                        rec_pj[k & 1] = ipj;
+                    }
                     if (lane < kTok) rec_tok[(k & 1) * kTok + lane] = tok;
-                    fill16(xbuf_s + (k & 1) * stageB, &full_x[k & 1], a.x + (int64_t)tl * d, tv, false);
+                    fill16(xbuf_s + (k & 1) * stageB, &full_x[k & 1], a.x[ipj] + (int64_t)tl * d, tv, false);
                 }
             }
             int32_t pb[4] = {-1, -1, -1, -1};
@@ -796,7 +816,7 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
                 // expand data of the previous unit: the item's y0 rows (first unit) and B rows
                 if (pc == 0) {
                     const uint32_t slot = next_slot();
-                    fill16(ring_s + slot * stageB, &full[slot], a.y + (int64_t)ptl * d, ptv, false);
+                    fill16(ring_s + slot * stageB, &full[slot], a.y[ppj] + (int64_t)ptl * d, ptv, false);
                     ++sc;
                 }
                 emit_blocks(min(kRC, pit.rank - pc * kRC), ppb, true);
@@ -808,6 +828,7 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
             pc = c;
             ptl = tl;
             ptv = tv;
+            ppj = ipj;
 #pragma unroll
             for (int m = 0; m < 4; ++m) ppb[m] = pb[m];
             ++c;
@@ -819,7 +840,7 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
     const int w = warp;
     if (w == 0 && bal && n_items > ncl) {
         // while the first data is in flight
-        balance_items(a.L.items, n_items, ncl, cl, lane, s_seq, s_cost, s_load);
+        balance_items(a.L.items, n_items, NP, ncl, cl, lane, s_seq, s_cost, s_load);
         __syncwarp();
         if (lane == 0) mbar_arrive(&seq_bar);
     }
@@ -831,10 +852,11 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
     uint32_t un = 0;    // units shrunk
     int k = -1, c = 0, nch = 0;
     Item it{};
+    int ipj = 0;                        // projection slot of the current item
     int tk[2] = {0, 0};                 // token ids of rows gid, gid+8 of the current item
     bool have_prev = false;
     Item pit{};
-    int pc = 0, ptk[2] = {0, 0};
+    int pc = 0, ppj = 0, ptk[2] = {0, 0};
     float acc[16][4];
     uint32_t yv[2][16];                 // y0 of the item being expanded: [token half][n-block], half2 bits
 #pragma unroll
@@ -852,6 +874,7 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
             } else {
                 wait_phase<false>(&full_x[k & 1], (k >> 1) & 1, abort, status);
                 it = rec_it[k & 1];
+                ipj = rec_pj[k & 1];
                 tk[0] = rec_tok[(k & 1) * kTok + gid];
                 tk[1] = rec_tok[(k & 1) * kTok + gid + 8];
                 c = 0;
@@ -1030,7 +1053,7 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
                 for (int h = 0; h < 2; ++h) {
                     const int t = gid + 8 * h;
                     if (t < pit.nt) {
-                        __half *yrow = a.y + (int64_t)ptk[h] * d + kb;
+                        __half *yrow = a.y[ppj] + (int64_t)ptk[h] * d + kb;
 #pragma unroll
                         for (int p = 0; p < 8; ++p) {
                             if (pp0 + p < pp1) {
@@ -1052,6 +1075,7 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
         have_prev = true;
         pit = it;
         pc = c;
+        ppj = ipj;
         ptk[0] = tk[0];
         ptk[1] = tk[1];
         ++c;
@@ -1084,17 +1108,17 @@ inline size_t delta_smem_bytes(int hidden)
 {
     const size_t stage = (size_t)kTok * delta_pitch(hidden);
     return (NST + 2) * stage + 2 * (size_t)kTok * kRC * 4 + (size_t)kPtmpFloats * 4 + (size_t)kTok * kUPitch * 2 + 2 * sizeof(Item) +
-           2 * kTok * 4 + (2 * NST + 13) * 8;
+           2 * kTok * 4 + 2 * 4 + (2 * NST + 13) * 8;
 }
 
-cudaError_t launch_lora_apply(const PoolView &pv, int32_t proj, const uint16_t *x, uint16_t *y,
-                              int32_t T, const int32_t *idx, const int32_t *seg_indptr,
-                              int32_t n_seg, const float *scaling, const PlanScratch &scratch,
-                              int num_sms, cudaStream_t stream, int *launches, cudaEvent_t after_plan)
+cudaError_t launch_lora_apply(const PoolView &pv, const ProjList &pl, int32_t T, const int32_t *idx,
+                              const int32_t *seg_indptr, int32_t n_seg, const float *scaling,
+                              const PlanScratch &scratch, int num_sms, cudaStream_t stream, int *launches,
+                              cudaEvent_t after_plan)
 {
     static bool attrs_set = false;
     static int occ_hidden = -1, occ_clusters = 1;
-    if (pv.hidden > kMaxCluster * kMaxSlice) return cudaErrorInvalidValue;
+    if (pv.hidden > kMaxCluster * kMaxSlice || pl.n < 1 || pl.n > kMaxApplyProj) return cudaErrorInvalidValue;
     if (!attrs_set) {
         cudaError_t e = cudaFuncSetAttribute(delta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)delta_smem_bytes(kMaxSlice));
@@ -1144,7 +1168,7 @@ cudaError_t launch_lora_apply(const PoolView &pv, int32_t proj, const uint16_t *
         int hs = 1024;
         while (hs < 2 * groups && hs < kMaxHash) hs <<= 1;
         const int dcache = pv.max_adapters <= kPlanDirCache ? 1 : 0;
-        PlanArgs pa{pv, proj, idx, T, seg_indptr, n_seg, tb, te, hs, dcache, L};
+        PlanArgs pa{pv, idx, T, seg_indptr, n_seg, tb, te, hs, dcache, L};
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(1);
         const bool small = te - tb <= kPlanThreadsSmall;
@@ -1162,14 +1186,23 @@ cudaError_t launch_lora_apply(const PoolView &pv, int32_t proj, const uint16_t *
             e = cudaEventRecord(after_plan, stream);
             if (e != cudaSuccess) return e;
         }
-        DeltaArgs da{pv, reinterpret_cast<const __half *>(x), reinterpret_cast<__half *>(y), scaling, L,
-                     delta_pitch(pv.hidden)};
+        DeltaArgs da{};
+        da.pv = pv;
+        for (int j = 0; j < pl.n; ++j) {
+            da.x[j] = reinterpret_cast<const __half *>(pl.x[j]);
+            da.y[j] = reinterpret_cast<__half *>(pl.y[j]);
+            da.proj[j] = pl.proj[j];
+        }
+        da.n_proj = pl.n;
+        da.scaling = scaling;
+        da.L = L;
+        da.pitch = delta_pitch(pv.hidden);
         e = cudaLaunchKernelEx(&cfg2, delta_kernel, da);
         if (e != cudaSuccess) return e;
         *launches += 1;
     }
     if (n_seg > 0) {
-        cudaError_t e = launch_prefill(pv, proj, x, y, T, idx, seg_indptr, n_seg, scaling, num_sms, stream);
+        cudaError_t e = launch_prefill(pv, pl, T, idx, seg_indptr, n_seg, scaling, num_sms, stream);
         if (e != cudaSuccess) return e;
         *launches += 1;
     }

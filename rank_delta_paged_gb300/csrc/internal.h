@@ -83,15 +83,32 @@ size_t plan_scratch_bytes(int32_t T, int32_t max_rank, int32_t hidden, int32_t m
 constexpr int kMaxPrefillRank = 128;
 constexpr int kMaxSegments = 4096;
 
-cudaError_t launch_prefill(const PoolView &pv, int32_t proj, const uint16_t *x, uint16_t *y, int32_t T,
-                           const int32_t *idx, const int32_t *seg_indptr, int32_t n_seg,
-                           const float *scaling, int num_sms, cudaStream_t stream);
+// The projections one apply call covers: the same tokens and adapters, each entry with
+// its own projection index, input x and in/out y (fp16 [T][hidden] on the device).  The
+// x of several entries may be one buffer; the y buffers are distinct.
+constexpr int kMaxApplyProj = 8;
+struct ProjList {
+    int32_t n;
+    int32_t proj[kMaxApplyProj];
+    const uint16_t *x[kMaxApplyProj];
+    uint16_t *y[kMaxApplyProj];
+};
 
-// The hot path (decode.cu / prefill.cu).
-cudaError_t launch_lora_apply(const PoolView &pv, int32_t proj, const uint16_t *x, uint16_t *y,
-                              int32_t T, const int32_t *idx, const int32_t *seg_indptr,
-                              int32_t n_seg, const float *scaling, const PlanScratch &scratch,
-                              int num_sms, cudaStream_t stream, int *launches,
+// Checks the projection entries of an apply call (fn names the call in the error text)
+// and fills *out: 1 <= n <= kMaxApplyProj, every projection index in [0, pool_n_proj),
+// x and y non-null and 16-byte aligned, no y equal to another entry's y or to any x.
+slora_status make_proj_list(const char *fn, int32_t pool_n_proj, int32_t n, const int32_t *projs,
+                            const void *const *x, void *const *y, ProjList *out);
+
+cudaError_t launch_prefill(const PoolView &pv, const ProjList &pl, int32_t T, const int32_t *idx,
+                           const int32_t *seg_indptr, int32_t n_seg, const float *scaling, int num_sms,
+                           cudaStream_t stream);
+
+// The hot path (decode.cu / prefill.cu): one token plan, one decode launch and one segment
+// launch for every projection of the list.
+cudaError_t launch_lora_apply(const PoolView &pv, const ProjList &pl, int32_t T, const int32_t *idx,
+                              const int32_t *seg_indptr, int32_t n_seg, const float *scaling,
+                              const PlanScratch &scratch, int num_sms, cudaStream_t stream, int *launches,
                               cudaEvent_t after_plan = nullptr);
 
 // What the hot path needs to know about a pool, for entry points defined outside

@@ -63,16 +63,17 @@ extern "C" slora_status slora_lora_apply_noalloc(slora_pool_t pool, int32_t proj
     slora_status st = pool_hot_path(pool, &hp);
     if (st != SLORA_OK)
         return st;
-    if (proj < 0 || proj >= hp.pv.n_proj)
-        return fail(SLORA_ERR_INVALID_ARG, "lora_apply_noalloc: proj=%d of %d", proj, hp.pv.n_proj);
     if (T < 0 || T > (1 << 20))
         return fail(SLORA_ERR_INVALID_ARG, "lora_apply_noalloc: T=%d", T);
     if (T == 0)
         return SLORA_OK;
-    if (!x || !y || !token_adapter_idx || x == y)
-        return fail(SLORA_ERR_INVALID_ARG, "lora_apply_noalloc: null or aliased x / y / index pointer");
-    if (((uintptr_t)x | (uintptr_t)y) & 15)
-        return fail(SLORA_ERR_INVALID_ARG, "lora_apply_noalloc: x and y must be 16-byte aligned");
+    ProjList pl;
+    const void *xs[1] = {x};
+    void *ys[1] = {y};
+    if ((st = make_proj_list("lora_apply_noalloc", hp.pv.n_proj, 1, &proj, xs, ys, &pl)) != SLORA_OK)
+        return st;
+    if (!token_adapter_idx)
+        return fail(SLORA_ERR_INVALID_ARG, "lora_apply_noalloc: null token index pointer");
     if (n_seg < 0 || (n_seg > 0 && !seg_indptr) || n_seg > T || n_seg > kMaxSegments)
         return fail(SLORA_ERR_INVALID_ARG, "lora_apply_noalloc: n_seg=%d (at most min(T, %d))", n_seg,
                     kMaxSegments);
@@ -97,8 +98,8 @@ extern "C" slora_status slora_lora_apply_noalloc(slora_pool_t pool, int32_t proj
     ps.cap_tokens = T;
     ps.max_rank = max_rank;
     int launched = 0;
-    e = launch_lora_apply(hp.pv, proj, (const uint16_t *)x, (uint16_t *)y, T, token_adapter_idx, seg_indptr,
-                          n_seg, scaling, ps, hp.num_sms, (cudaStream_t)stream, &launched);
+    e = launch_lora_apply(hp.pv, pl, T, token_adapter_idx, seg_indptr, n_seg, scaling, ps, hp.num_sms,
+                          (cudaStream_t)stream, &launched);
     *hp.launches += launched;
     if (e != cudaSuccess)
         return fail(SLORA_ERR_CUDA, "lora_apply_noalloc: launch failed: %s", cudaGetErrorString(e));

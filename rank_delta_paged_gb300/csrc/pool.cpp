@@ -553,24 +553,18 @@ slora_status slora_get_device_status(slora_pool_t p, int32_t *status)
     return SLORA_OK;
 }
 
-slora_status slora_lora_apply(slora_pool_t p, int32_t proj, const void *x, void *y, int32_t T,
-                              const int32_t *idx, const int32_t *seg_indptr, int32_t n_seg,
-                              const float *scaling, slora_stream_t stream)
+static slora_status apply_list(slora_pool_t p, const char *fn, const ProjList &pl, int32_t T,
+                               const int32_t *idx, const int32_t *seg_indptr, int32_t n_seg,
+                               const float *scaling, slora_stream_t stream)
 {
-    if (!p)
-        return fail(SLORA_ERR_INVALID_ARG, "lora_apply: null pool");
-    if (proj < 0 || proj >= p->n_proj)
-        return fail(SLORA_ERR_INVALID_ARG, "lora_apply: proj=%d of %d", proj, p->n_proj);
     if (T < 0 || T > (1 << 20))
-        return fail(SLORA_ERR_INVALID_ARG, "lora_apply: T=%d", T);
+        return fail(SLORA_ERR_INVALID_ARG, "%s: T=%d", fn, T);
     if (T == 0)
         return SLORA_OK;
-    if (!x || !y || !idx || x == y)
-        return fail(SLORA_ERR_INVALID_ARG, "lora_apply: null or aliased x / y / index pointer");
-    if (((uintptr_t)x | (uintptr_t)y) & 15)
-        return fail(SLORA_ERR_INVALID_ARG, "lora_apply: x and y must be 16-byte aligned");
+    if (!idx)
+        return fail(SLORA_ERR_INVALID_ARG, "%s: null token index pointer", fn);
     if (n_seg < 0 || (n_seg > 0 && !seg_indptr) || n_seg > T || n_seg > kMaxSegments)
-        return fail(SLORA_ERR_INVALID_ARG, "lora_apply: n_seg=%d (at most min(T, %d))", n_seg, kMaxSegments);
+        return fail(SLORA_ERR_INVALID_ARG, "%s: n_seg=%d (at most min(T, %d))", fn, n_seg, kMaxSegments);
     slora_status st = set_device(p);
     if (st != SLORA_OK)
         return st;
@@ -591,13 +585,42 @@ slora_status slora_lora_apply(slora_pool_t p, int32_t proj, const void *x, void 
     PoolView pv{p->pool_dev, p->pt_dev, p->dir_dev, p->num_pages, p->hidden, p->n_proj,
                 p->max_adapters, p->status_dev};
     int launched = 0;
-    cudaError_t e = launch_lora_apply(pv, proj, (const uint16_t *)x, (uint16_t *)y, T, idx, seg_indptr,
-                                      n_seg, scaling, p->plan, p->num_sms, (cudaStream_t)stream, &launched,
-                                      p->stage_event);
+    cudaError_t e = launch_lora_apply(pv, pl, T, idx, seg_indptr, n_seg, scaling, p->plan, p->num_sms,
+                                      (cudaStream_t)stream, &launched, p->stage_event);
     p->launches += launched;
     if (e != cudaSuccess)
-        return fail(SLORA_ERR_CUDA, "lora_apply: launch failed: %s", cudaGetErrorString(e));
+        return fail(SLORA_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
     return SLORA_OK;
+}
+
+slora_status slora_lora_apply(slora_pool_t p, int32_t proj, const void *x, void *y, int32_t T,
+                              const int32_t *idx, const int32_t *seg_indptr, int32_t n_seg,
+                              const float *scaling, slora_stream_t stream)
+{
+    if (!p)
+        return fail(SLORA_ERR_INVALID_ARG, "lora_apply: null pool");
+    if (T == 0)
+        return SLORA_OK;
+    ProjList pl;
+    void *ys[1] = {y};
+    const void *xs[1] = {x};
+    slora_status st = make_proj_list("lora_apply", p->n_proj, 1, &proj, xs, ys, &pl);
+    if (st != SLORA_OK)
+        return st;
+    return apply_list(p, "lora_apply", pl, T, idx, seg_indptr, n_seg, scaling, stream);
+}
+
+slora_status slora_lora_apply_multi(slora_pool_t p, int32_t n, const int32_t *projs, const void *const *x,
+                                    void *const *y, int32_t T, const int32_t *idx, const int32_t *seg_indptr,
+                                    int32_t n_seg, const float *scaling, slora_stream_t stream)
+{
+    if (!p)
+        return fail(SLORA_ERR_INVALID_ARG, "lora_apply_multi: null pool");
+    ProjList pl;
+    slora_status st = make_proj_list("lora_apply_multi", p->n_proj, n, projs, x, y, &pl);
+    if (st != SLORA_OK)
+        return st;
+    return apply_list(p, "lora_apply_multi", pl, T, idx, seg_indptr, n_seg, scaling, stream);
 }
 
 slora_status slora_pool_set_stage_event(slora_pool_t p, void *event)
@@ -617,6 +640,31 @@ slora_status slora_pool_launch_count(slora_pool_t p, int64_t *out)
 }
 
 }  // extern "C"
+
+slora_status slora::make_proj_list(const char *fn, int32_t pool_n_proj, int32_t n, const int32_t *projs,
+                                   const void *const *x, void *const *y, ProjList *out)
+{
+    if (n < 1 || n > kMaxApplyProj)
+        return fail(SLORA_ERR_INVALID_ARG, "%s: %d projections (1 to %d per call)", fn, n, kMaxApplyProj);
+    if (!projs || !x || !y)
+        return fail(SLORA_ERR_INVALID_ARG, "%s: null projection, x or y array", fn);
+    out->n = n;
+    for (int j = 0; j < n; ++j) {
+        if (projs[j] < 0 || projs[j] >= pool_n_proj)
+            return fail(SLORA_ERR_INVALID_ARG, "%s: proj=%d of %d", fn, projs[j], pool_n_proj);
+        if (!x[j] || !y[j])
+            return fail(SLORA_ERR_INVALID_ARG, "%s: null x / y pointer (entry %d)", fn, j);
+        if (((uintptr_t)x[j] | (uintptr_t)y[j]) & 15)
+            return fail(SLORA_ERR_INVALID_ARG, "%s: x and y must be 16-byte aligned (entry %d)", fn, j);
+        for (int i = 0; i < n; ++i)
+            if (y[j] == x[i] || (i != j && y[j] == y[i]))
+                return fail(SLORA_ERR_INVALID_ARG, "%s: aliased x / y pointer (entries %d, %d)", fn, j, i);
+        out->proj[j] = projs[j];
+        out->x[j] = (const uint16_t *)x[j];
+        out->y[j] = (uint16_t *)y[j];
+    }
+    return SLORA_OK;
+}
 
 slora_status slora::pool_hot_path(slora_pool_t p, PoolHotPath *out)
 {

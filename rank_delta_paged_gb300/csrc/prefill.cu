@@ -10,8 +10,10 @@
 // segment is the one place where the delta is a real GEMM: U = X_s A (T_s x r), then
 // Y_s = Y0_s + s * U B.
 //
-// Work unit: one 128-token tile of one segment.  Persistent clusters of C CTAs (C = 1,
-// 2, 4 or 8, chosen on the host from the batch size so that the units fill the SMs)
+// Work unit: one 128-token tile of one segment for one projection of the call (a call may
+// cover several projections of a layer; unit u is tile u / n_proj of projection slot
+// u % n_proj).  Persistent clusters of C CTAs (C = 1, 2, 4 or 8, chosen on the host from
+// the number of units so that they fill the SMs)
 // take units in turn; CTA c of a cluster owns hidden slice c: the K range of its part
 // of the shrink and the N range of its part of the expand, so every byte of x, y0, y and
 // of the adapter's pages is moved by exactly one CTA.
@@ -50,6 +52,8 @@
 //               returns it to the ring, so the four warps never wait for one another there.
 // Every wait is bounded; a unit whose tokens disagree on their adapter, or whose adapter
 // is not resident, is skipped with a device status code.
+#include <cstring>
+
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -89,26 +93,30 @@ struct alignas(64) UnitDesc {
     int32_t m0, mlen, rank, r_pad;
     float sc;
     int32_t flag;
-    int32_t pad[2];
+    int32_t pj;        // projection slot of the call
+    int32_t pad;
     int32_t pg[2 * kMaxPrefillRank];   // pool pages of the A^T rows, then of the B rows; -1 reads zeros
 };
 
 struct PrefillArgs {
-    CUtensorMap tmap_x;   // x [T][hidden], box 64 x 128, 128-byte swizzle
-    CUtensorMap tmap_y;   // y likewise (y0 loads)
-    CUtensorMap tmap_ys;  // y with 64 x 32 boxes: each epilogue warp stores its own 32 rows
+    // per projection slot of the call:
+    CUtensorMap tmap_x[kMaxApplyProj];   // x [T][hidden], box 64 x 128, 128-byte swizzle
+    CUtensorMap tmap_y[kMaxApplyProj];   // y likewise (y0 loads)
+    CUtensorMap tmap_ys[kMaxApplyProj];  // y with 64 x 32 boxes: each epilogue warp stores its own 32 rows
+    __half *y[kMaxApplyProj];
+    int32_t proj[kMaxApplyProj];
+    int32_t n_proj;
     PoolView pv;
-    __half *y;
     const int32_t *idx;
     const int32_t *seg_indptr;
     const float *scaling;
-    int32_t proj;
     int32_t T;
     int32_t n_seg;
     int32_t C;       // CTAs per cluster
     int32_t slice;   // hidden elements per CTA, a multiple of 64
     int32_t nt;      // token-tile slots
 };
+static_assert(sizeof(PrefillArgs) <= 4096, "kernel parameters");
 
 // Shared memory: token-tile ring, page-row ring, the U operand, two unit descriptors,
 // and the buffer that receives other CTAs' partial rows.
@@ -249,7 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         int s0 = 0, base = 0;   // window of 32 segments and the tiles before it
         uint32_t gT = 0;        // token tiles issued
         for (uint32_t i = 0;; ++i) {
-            const int mt = (int)(cl + i * ncl);
+            const int vu = (int)(cl + i * ncl);            // unit: (tile mt, projection slot pj)
+            const int mt = vu / a.n_proj, pj = vu - mt * a.n_proj;
             int tile = -1, lo = 0, hi = 0;
             while (s0 < a.n_seg) {
                 const int j = s0 + lane;
@@ -301,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                         flag = kCompute;
                         rank = e.rank;
                         sc = a.scaling ? a.scaling[ad] : e.scaling;
-                        pt = e.pt_off + (int64_t)a.proj * 2 * e.rank;
+                        pt = e.pt_off + (int64_t)a.proj[pj] * 2 * e.rank;
                     }
                 }
             }
@@ -327,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 u->r_pad = (rank + 15) / 16 * 16;
                 u->sc = sc;
                 u->flag = flag;
+                u->pj = pj;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&dfull[i & 1]);
@@ -341,7 +351,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     if (*abort) break;
                     mbar_arrive_expect_tx(&fullT[sT], kTileBytes);
                     tma_load_2d(smem_u32(tring + sT * kTileBytes),
-                                shrink ? (const void *)&a.tmap_x : (const void *)&a.tmap_y, col, m0, &fullT[sT]);
+                                shrink ? (const void *)&a.tmap_x[pj] : (const void *)&a.tmap_y[pj], col, m0,
+                                &fullT[sT]);
                     ++gT;
                 }
             }
@@ -488,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             wait_phase<false>(&dfull[i & 1], (i >> 1) & 1, abort, status);
             if (epi_sync_or(*abort)) break;
             const UnitDesc *ud = &desc[i & 1];
-            const int flag = ud->flag, m0 = ud->m0, mlen = ud->mlen, r_pad = ud->r_pad;
+            const int flag = ud->flag, m0 = ud->m0, mlen = ud->mlen, r_pad = ud->r_pad, pj = ud->pj;
             const float sc = ud->sc;
             __syncwarp();
             if (lane == 0) mbar_arrive(&dempty[i & 1]);
@@ -646,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     tc::fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&a.tmap_ys, n0, m0 + 32 * qd, smem_u32(yt + 32 * qd * 128));
+                        tma_store_2d(&a.tmap_ys[pj], n0, m0 + 32 * qd, smem_u32(yt + 32 * qd * 128));
                         bulk_commit();
                         if (pend >= 0) {   // this warp's store of the previous tile has read its slot
                             bulk_wait_read<1>();
@@ -662,7 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                         const int row = 32 * qd + (qq >> 3), c8 = qq & 7;
                         if (row < mlen) {
                             const uint4 val = *reinterpret_cast<const uint4 *>(yt + row * 128 + ((c8 ^ (row & 7)) << 4));
-                            *reinterpret_cast<uint4 *>(a.y + (int64_t)(m0 + row) * d + n0 + c8 * 8) = val;
+                            *reinterpret_cast<uint4 *>(a.y[pj] + (int64_t)(m0 + row) * d + n0 + c8 * 8) = val;
                         }
                     }
                     __syncwarp();
@@ -737,9 +748,9 @@ inline int slice_for(int hidden, int C) { return (hidden / 64 + C - 1) / C * 64;
 
 }  // namespace
 
-cudaError_t launch_prefill(const PoolView &pv, int32_t proj, const uint16_t *x, uint16_t *y, int32_t T,
-                           const int32_t *idx, const int32_t *seg_indptr, int32_t n_seg,
-                           const float *scaling, int num_sms, cudaStream_t stream)
+cudaError_t launch_prefill(const PoolView &pv, const ProjList &pl, int32_t T, const int32_t *idx,
+                           const int32_t *seg_indptr, int32_t n_seg, const float *scaling, int num_sms,
+                           cudaStream_t stream)
 {
     static bool attr_set = false;
     static int ncl_cache[4] = {0, 0, 0, 0};   // resident clusters for C = 1, 2, 4, 8
@@ -750,7 +761,10 @@ cudaError_t launch_prefill(const PoolView &pv, int32_t proj, const uint16_t *x, 
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) return cudaErrorInvalidValue;
+    if (pl.n < 1 || pl.n > kMaxApplyProj) return cudaErrorInvalidValue;
+    for (int j = 0; j < pl.n; ++j)
+        if ((reinterpret_cast<uintptr_t>(pl.x[j]) | reinterpret_cast<uintptr_t>(pl.y[j])) & 15u)
+            return cudaErrorInvalidValue;
 
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -777,8 +791,9 @@ cudaError_t launch_prefill(const PoolView &pv, int32_t proj, const uint16_t *x, 
     };
 
     // CTAs per cluster: the largest C whose resident clusters still cover the units
-    // (128-token tiles; the host does not read the segments, so T bounds their number).
-    const int units = (T + MT - 1) / MT;
+    // (128-token tiles per projection; the host does not read the segments, so T bounds
+    // their number).
+    const int units = (T + MT - 1) / MT * pl.n;
     int C = 1, lgC = 0;
     for (int lg = 1; lg <= 3; ++lg) {
         const int c = 1 << lg;
@@ -801,18 +816,22 @@ cudaError_t launch_prefill(const PoolView &pv, int32_t proj, const uint16_t *x, 
     if (ncl <= 0) ncl = C == 1 ? num_sms : 1;
 
     PrefillArgs pa;
-    cudaError_t e = token_map(&pa.tmap_x, x, pv.hidden, T);
-    if (e != cudaSuccess) return e;
-    e = token_map(&pa.tmap_y, y, pv.hidden, T);
-    if (e != cudaSuccess) return e;
-    e = token_map(&pa.tmap_ys, y, pv.hidden, T, 32);
-    if (e != cudaSuccess) return e;
+    memset(&pa, 0, sizeof(pa));
+    for (int j = 0; j < pl.n; ++j) {
+        cudaError_t e = token_map(&pa.tmap_x[j], pl.x[j], pv.hidden, T);
+        if (e != cudaSuccess) return e;
+        e = token_map(&pa.tmap_y[j], pl.y[j], pv.hidden, T);
+        if (e != cudaSuccess) return e;
+        e = token_map(&pa.tmap_ys[j], pl.y[j], pv.hidden, T, 32);
+        if (e != cudaSuccess) return e;
+        pa.y[j] = reinterpret_cast<__half *>(pl.y[j]);
+        pa.proj[j] = pl.proj[j];
+    }
+    pa.n_proj = pl.n;
     pa.pv = pv;
-    pa.y = reinterpret_cast<__half *>(y);
     pa.idx = idx;
     pa.seg_indptr = seg_indptr;
     pa.scaling = scaling;
-    pa.proj = proj;
     pa.T = T;
     pa.n_seg = n_seg;
     pa.C = C;
