@@ -742,13 +742,13 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
             const int i = item_of(kk);
             nvalid = i < n_items;
             if (nvalid) {
-                nit = load_item(a.L.items + i / NP);
+                nit = load_item(a.L.items + i / NP);   // not used before fetch_rest: no wait here
                 npj = i % NP;
-                nit.pt_base += (int64_t)a.proj[npj] * 2 * nit.rank;   // this projection's page table
             }
         };
         auto fetch_rest = [&]() {
             if (!nvalid) return;
+            nit.pt_base += (int64_t)a.proj[npj] * 2 * nit.rank;   // this projection's page table
             ntok = lane < nit.nt ? __ldcg(a.L.tok_order + nit.tok_begin + nit.t0 + lane) : 0;
             const int rows = min(kRC, nit.rank);
 #pragma unroll
