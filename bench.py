@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--prefetch", type=int, default=0, metavar="K",
+                    help="also measure K later batches' adapter loads against the deltas (\"prefetch\")")
     ap.add_argument("--apply", choices=["multi", "single"], default="multi",
                     help="multi: one slora_lora_apply_multi call per layer (all its projections); "
                          "single: one slora_lora_apply call per projection")
@@ -59,7 +61,7 @@ def parse():
 # capture of the current kernel on the workload (profiles/delta_kernel_decode_7b.md and
 # profiles/prefill_kernel_prefill_7b.md give the commands); a workload without a capture
 # of the current kernel reports null.
-TRAFFIC = {"decode_7b_h4096_a100_t256_zipf1": 41922816, "prefill_7b_h4096_s16x512": 155520512}
+TRAFFIC = {"decode_7b_h4096_a100_t256_zipf1": 41921024, "prefill_7b_h4096_s16x512": 155184640}
 
 
 def peaks():
@@ -511,6 +513,11 @@ def main():
                         "the pinned store over the CPU-GPU link; the directory update"}
     e2e_job_ms, _ = job_totals(statistics.mean(e2e_ms) if e2e_ms else float("nan"), float(w.T), dev, world)
     e2e_value = tokens_per_s_per_layer(job_tokens, w.n_layers, e2e_job_ms)
+    prefetch = None
+    if args.prefetch > 0 and w.n_seg == 0:
+        from rank_delta_paged_gb300.harness import prefetch_overlap
+        prefetch = prefetch_overlap(sess, args.prefetch, stream)
+        sess.load(used, stream)
     status = sess.device_status()
     if status != 0:
         print(f"device status {status} after the run", file=sys.stderr)
@@ -546,6 +553,8 @@ def main():
     }
     if kernel_stats is not None:
         line["kernels"] = kernel_stats
+    if prefetch is not None:
+        line["prefetch"] = prefetch
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, cores, sample = oracle_rate(w, args.cpu_seconds)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s/layer", "cores": cores,

@@ -75,3 +75,83 @@ class PoolSession:
 
     def __exit__(self, *exc):
         self.close()
+
+
+def prefetch_overlap(sess: PoolSession, K: int = 6, stream=None) -> dict:
+    """How far the adapter loads of later batches hide behind the deltas of earlier ones.
+
+    The pool runs every load on its own side stream and only makes the caller's stream
+    wait for it, so a serving loop that issues load(k), apply(k), load(k+1), apply(k+1), ...
+    on one stream already lets load(k+1) run under apply(k) (S-LoRA: Multiplexing Thousands
+    of Fine-Tuned Adapters on a Single GPU, section 4: the adapters of the next batch are
+    prefetched while the current batch computes).  K decode batches are drawn from the
+    session's zoo (``Workload.later_batch``), starting from an empty pool; each loads the
+    adapters not yet resident.  Timed on the stream with CUDA events:
+
+      loads_ms       the K loads alone
+      applies_ms     the K applies alone (every adapter resident)
+      pipelined_ms   load(k), apply(k) in turn on one stream
+      serialized_ms  the same with the host waiting for the device after every apply, so no
+                     load starts before the previous apply ends
+      overlap_frac   (loads + applies - pipelined) / min(loads, applies)
+      link_gb_per_s  loaded bytes / loads_ms (the load kernel reads the pinned store over
+                     the CPU-GPU link)
+    """
+    from . import slora_lora_apply
+    w = sess.w
+    batches = [w] + [w.later_batch(k) for k in range(1, K)]
+    dev = torch.device("cuda", sess.device)
+    st = stream or torch.cuda.current_stream(dev)
+    x = [torch.from_numpy(w.x(p).view(np.int16)).to(dev).view(torch.float16) for p in range(w.n_proj)]
+    y = [torch.from_numpy(w.y0(p).view(np.int16)).to(dev).view(torch.float16) for p in range(w.n_proj)]
+    idx = [torch.from_numpy(b.token_adapter_idx).to(dev) for b in batches]
+    need, resident = [], set()
+    for b in batches:
+        ids = [a for a in b.used_adapters().tolist() if a not in resident]
+        need.append(ids)
+        resident |= set(ids)
+    union = sorted(resident)
+    sess.register(union)
+    nbytes = sum(4 * int(w.ranks[a]) * w.hidden * w.n_proj for ids in need for a in ids)
+
+    def evict_all():
+        res = [a for a in union if slora_adapter_is_resident(sess.pool, a)]
+        if res:
+            sess.evict(res, st)
+        torch.cuda.synchronize(dev)
+
+    def apply(k):
+        for p in range(w.n_proj):
+            slora_lora_apply(sess.pool, p, x[p], y[p], w.T, idx[k], None, 0, None, st)
+
+    def timed(mode):
+        if mode == "applies":
+            sess.load(union, st)
+        else:
+            evict_all()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for k in range(K):
+            if mode != "applies" and need[k]:
+                sess.load(need[k], st)
+            if mode != "loads":
+                apply(k)
+            if mode == "serialized":
+                torch.cuda.synchronize(dev)
+        e1.record(st)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1)
+
+    best = {}
+    for _ in range(2):   # the faster of two passes of each
+        for mode in ("loads", "applies", "pipelined", "serialized"):
+            t = timed(mode)
+            best[mode] = min(best.get(mode, t), t)
+    evict_all()
+    loads, applies, pipe = best["loads"], best["applies"], best["pipelined"]
+    return {"batches": K, "adapters_loaded": len(union), "bytes": int(nbytes),
+            "loads_ms": loads, "applies_ms": applies, "pipelined_ms": pipe,
+            "serialized_ms": best["serialized"],
+            "overlap_frac": (loads + applies - pipe) / max(1e-9, min(loads, applies)),
+            "link_gb_per_s": nbytes / (loads * 1e-3) / 1e9}

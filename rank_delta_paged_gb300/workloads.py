@@ -66,6 +66,7 @@ class Workload:
     seed: int = 0
     values: str = "normal"
     n_layers: int = 1               # projections per layer = n_proj // n_layers
+    alpha: float = 1.0              # Zipf exponent of the token map's adapter ids
 
     _factor_cache: Dict[int, Tuple[np.ndarray, np.ndarray]] = dataclasses.field(
         default_factory=dict, repr=False)
@@ -93,6 +94,17 @@ class Workload:
 
     def adapter_pages(self, a: int) -> int:
         return 2 * int(self.ranks[a]) * self.n_proj
+
+    def later_batch(self, k: int) -> "Workload":
+        """The k-th later decode batch served from the same adapter zoo and pool: the same
+        ranks, factors and pool geometry, a new token map of as many decode tokens with
+        Zipf(alpha) ids (seeded by the workload's seed and k), the same x and y0."""
+        rng = np.random.default_rng([self.seed, 100 + int(k)])
+        ids = zipf_ids(rng, self.n_adapters, self.T, self.alpha)
+        return Workload(f"{self.name}_next{k}", self.hidden, self.n_proj, self.ranks, ids, None,
+                        num_pages=self.num_pages, kv_pages=self.kv_pages,
+                        shuffle_seed=self.shuffle_seed, seed=self.seed, values=self.values,
+                        n_layers=self.n_layers, alpha=self.alpha)
 
     # ---- factors -------------------------------------------------------
     def factors(self, a: int, cache: bool = True) -> Tuple[np.ndarray, np.ndarray]:
@@ -193,7 +205,7 @@ def decode_7b(seed: int = 0, values: str = "normal", T: int = 256, n_adapters: i
     zoo_pages = int(2 * ranks.sum())
     return Workload(f"decode_7b_h{hidden}_a{n_adapters}_t{T}_zipf{alpha:g}", hidden, 1, ranks,
                     ids, None, num_pages=2 * zoo_pages, kv_pages=zoo_pages,
-                    shuffle_seed=seed * 7919 + 13, seed=seed, values=values)
+                    shuffle_seed=seed * 7919 + 13, seed=seed, values=values, alpha=alpha)
 
 
 def prefill_7b(seed: int = 0, values: str = "normal", n_seg: int = 16, seg_len: int = 512,
@@ -222,7 +234,7 @@ def decode_13b_zoo(seed: int = 0, values: str = "normal", T: int = 512, n_adapte
     zoo_pages = int(2 * ranks.sum())
     return Workload(f"decode_13b_h{hidden}_a{n_adapters}_t{T}_zipf{alpha:g}", hidden, 1, ranks,
                     ids, None, num_pages=2 * zoo_pages, kv_pages=zoo_pages,
-                    shuffle_seed=seed * 7919 + 19, seed=seed, values=values)
+                    shuffle_seed=seed * 7919 + 19, seed=seed, values=values, alpha=alpha)
 
 
 def mixed_iteration(seed: int = 0, values: str = "normal", n_layers: int = 32,
@@ -243,7 +255,7 @@ def mixed_iteration(seed: int = 0, values: str = "normal", n_layers: int = 32,
     return Workload(f"mixed_iteration_h{hidden}_l{n_layers}x4_a{n_adapters}", hidden,
                     4 * n_layers, ranks, ids, indptr, num_pages=int(num_pages),
                     kv_pages=int(num_pages // 2), shuffle_seed=seed * 7919 + 23, seed=seed,
-                    values=values, n_layers=n_layers)
+                    values=values, n_layers=n_layers, alpha=alpha)
 
 
 WORKLOADS = {
