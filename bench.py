@@ -51,6 +51,10 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--prefetch", type=int, default=0, metavar="K",
                     help="also measure K later batches' adapter loads against the deltas (\"prefetch\")")
+    ap.add_argument("--pressure", type=int, default=0, metavar="K",
+                    help="also run K batches of the zoo through acquire / apply / release (\"pressure\")")
+    ap.add_argument("--layers", type=int, default=0, help="mixed_iteration: layers (0 = the default 32)")
+    ap.add_argument("--pool-gib", type=float, default=0.0, help="mixed_iteration: pool size in GiB (0 = 40)")
     ap.add_argument("--apply", choices=["multi", "single"], default="multi",
                     help="multi: one slora_lora_apply_multi call per layer (all its projections); "
                          "single: one slora_lora_apply call per projection")
@@ -342,7 +346,13 @@ def main():
         if world > 1:
             dist.barrier()
 
-    w = W.by_name(args.workload, seed=replica_seed(args.seed, rank))
+    wkw = {}
+    if args.workload == "mixed_iteration":
+        if args.layers > 0:
+            wkw["n_layers"] = args.layers
+        if args.pool_gib > 0:
+            wkw["pool_bytes"] = int(args.pool_gib * (1 << 30))
+    w = W.by_name(args.workload, seed=replica_seed(args.seed, rank), **wkw)
     used = w.used_adapters()
     sess = PoolSession(w, device=local)
     stream = torch.cuda.current_stream()
@@ -518,6 +528,11 @@ def main():
         from rank_delta_paged_gb300.harness import prefetch_overlap
         prefetch = prefetch_overlap(sess, args.prefetch, stream)
         sess.load(used, stream)
+    pressure = None
+    if args.pressure > 0:
+        from rank_delta_paged_gb300.harness import pressure_run
+        sess.evict(used, stream)
+        pressure = pressure_run(sess, args.pressure, stream)
     status = sess.device_status()
     if status != 0:
         print(f"device status {status} after the run", file=sys.stderr)
@@ -555,6 +570,8 @@ def main():
         line["kernels"] = kernel_stats
     if prefetch is not None:
         line["prefetch"] = prefetch
+    if pressure is not None:
+        line["pressure"] = pressure
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, cores, sample = oracle_rate(w, args.cpu_seconds)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s/layer", "cores": cores,

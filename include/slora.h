@@ -102,6 +102,31 @@ slora_status slora_pagealloc_free(slora_pagealloc_t a, int64_t n, const int32_t 
 slora_status slora_pagealloc_num_free(slora_pagealloc_t a, int64_t *out);
 
 /* ---------------------------------------------------------------------------
+ * Host-only recency index of resident adapters: the eviction policy the pool applies
+ * under pressure (slora_adapters_acquire, slora_pages_alloc_evict), exposed like the page
+ * allocator for callers that keep their own residency and for tests without a GPU.
+ * (The explainer's "The mechanism": adapters the running batches do not use can leave
+ * GPU memory; the pages do not name a policy, so this is least-recently-used among the
+ * adapters no running batch holds.)
+ *   insert()  id becomes present, unpinned, most recently used (no-op if present)
+ *   remove()  SLORA_ERR_INVALID_ARG if absent or pinned
+ *   touch()   most recently used; pin() / unpin() count holds (an unpin without a pin is
+ *             SLORA_ERR_INVALID_ARG); absent ids are SLORA_ERR_INVALID_ARG
+ *   victims() up to max_out present, unpinned ids not in exclude[], least recently used
+ *             first, into out_ids (host [max_out]); *out_n = how many
+ * ------------------------------------------------------------------------- */
+typedef struct slora_lru *slora_lru_t;
+slora_status slora_lru_create(slora_lru_t *out);
+slora_status slora_lru_destroy(slora_lru_t l);
+slora_status slora_lru_insert(slora_lru_t l, int32_t id);
+slora_status slora_lru_remove(slora_lru_t l, int32_t id);
+slora_status slora_lru_touch(slora_lru_t l, int32_t id);
+slora_status slora_lru_pin(slora_lru_t l, int32_t id);
+slora_status slora_lru_unpin(slora_lru_t l, int32_t id);
+slora_status slora_lru_victims(slora_lru_t l, int32_t n_exclude, const int32_t *exclude /*host*/,
+                               int32_t max_out, int32_t *out_ids /*host*/, int32_t *out_n);
+
+/* ---------------------------------------------------------------------------
  * Pool.
  *   device        CUDA device ordinal (must be compute capability 10.3)
  *   hidden        row length; a multiple of 64, 64 <= hidden <= 8192 (the decode kernel
@@ -177,6 +202,45 @@ slora_status slora_adapter_evict(slora_pool_t pool, int32_t adapter_id, slora_st
 slora_status slora_adapters_evict(slora_pool_t pool, int32_t n, const int32_t *adapter_ids /*host*/,
                                   slora_stream_t stream);
 slora_status slora_adapter_is_resident(slora_pool_t pool, int32_t adapter_id, int32_t *out);
+
+/* ---------------------------------------------------------------------------
+ * Residency under pool pressure (explainer, "The mechanism": adapters the running
+ * batches do not use leave GPU memory and stay on the host; "What to notice when
+ * reading": KV blocks and adapters share the pool).  The policy is least recently used
+ * among the resident adapters that no running batch holds (see slora_lru_*).
+ *
+ * adapters_acquire(): makes every listed id resident and holds it (a pin count) until
+ *   released.  Missing adapters are loaded as slora_adapters_load does; if the free pages
+ *   do not suffice, the least recently acquired (or loaded) resident adapters that are
+ *   neither held nor listed are evicted first, on `stream`, so their pages are reused only
+ *   after the work enqueued earlier on `stream`.  The listed ids become the most recently
+ *   used, later ones in the list more recent.  If even evicting every such adapter would
+ *   not free enough pages, SLORA_ERR_POOL_FULL is returned and nothing changes.
+ * adapters_release(): drops one hold of each listed id (a repeated id counts once);
+ *   SLORA_ERR_INVALID_ARG, with no change, if an id is not held.  Release after
+ *   enqueuing the batch's work: later evictions on the same stream follow it.
+ * pages_alloc_evict(): slora_pages_alloc for KV blocks that grow into the adapters' share:
+ *   evicts least recently used adapters that no batch holds, on `stream`, until n pages are
+ *   free; SLORA_ERR_POOL_FULL (nothing changes) if the held adapters leave too few.  The
+ *   pages may have held adapter rows until this point of `stream`: write them from work
+ *   enqueued on `stream` after the call.
+ * slora_adapter_evict / slora_adapters_evict refuse a held adapter (SLORA_ERR_INVALID_ARG).
+ * pool_get_stats(): free pages, resident and held adapters, and the adapters loaded and
+ *   evicted since the pool was created.
+ * ------------------------------------------------------------------------- */
+typedef struct slora_pool_stats {
+    int64_t free_pages;
+    int64_t resident_adapters;
+    int64_t pinned_adapters;
+    int64_t adapters_loaded;
+    int64_t adapters_evicted;
+} slora_pool_stats;
+slora_status slora_adapters_acquire(slora_pool_t pool, int32_t n, const int32_t *adapter_ids /*host*/,
+                                    slora_stream_t stream);
+slora_status slora_adapters_release(slora_pool_t pool, int32_t n, const int32_t *adapter_ids /*host*/);
+slora_status slora_pages_alloc_evict(slora_pool_t pool, int64_t n, int32_t *out_pages /*host [n]*/,
+                                     slora_stream_t stream);
+slora_status slora_pool_get_stats(slora_pool_t pool, slora_pool_stats *out);
 
 /* ---------------------------------------------------------------------------
  * The hot path: y += s * (x A) B for a batch of tokens, each with its own adapter.

@@ -33,6 +33,9 @@ __all__ = [
     "slora_adapters_evict",
     "slora_debug_set_prefill_cluster",
     "slora_lora_apply_multi",
+    "slora_lru_create", "slora_lru_destroy", "slora_lru_insert", "slora_lru_remove", "slora_lru_touch",
+    "slora_lru_pin", "slora_lru_unpin", "slora_lru_victims",
+    "slora_adapters_acquire", "slora_adapters_release", "slora_pages_alloc_evict", "slora_pool_get_stats",
 ]
 
 _I32, _I64, _U64, _F32, _P = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float, ctypes.c_void_p
@@ -71,6 +74,18 @@ _SIGS = {
     "slora_adapters_evict": [_P, _I32, _P, _P],
     "slora_debug_set_prefill_cluster": [_I32],
     "slora_lora_apply_multi": [_P, _I32, _P, _P, _P, _I32, _P, _P, _I32, _P, _P],
+    "slora_lru_create": [_PP],
+    "slora_lru_destroy": [_P],
+    "slora_lru_insert": [_P, _I32],
+    "slora_lru_remove": [_P, _I32],
+    "slora_lru_touch": [_P, _I32],
+    "slora_lru_pin": [_P, _I32],
+    "slora_lru_unpin": [_P, _I32],
+    "slora_lru_victims": [_P, _I32, _P, _I32, _P, _P],
+    "slora_adapters_acquire": [_P, _I32, _P, _P],
+    "slora_adapters_release": [_P, _I32, _P],
+    "slora_pages_alloc_evict": [_P, _I64, _P, _P],
+    "slora_pool_get_stats": [_P, _P],
 }
 _RESTYPE = {"slora_status_str": ctypes.c_char_p, "slora_last_error": ctypes.c_char_p,
             "slora_version": _I32}
@@ -261,6 +276,83 @@ def slora_lora_apply_multi(pool: int, projs, xs, ys, T: int, token_adapter_idx, 
     y_arr = (ctypes.c_void_p * max(n, 1))(*[_ptr(v) for v in ys])
     _call("slora_lora_apply_multi", pool, n, p_arr, x_arr, y_arr, T, _ptr(token_adapter_idx),
           _ptr(seg_indptr), n_seg, _ptr(scaling), _stream(stream))
+
+
+# ---- recency index (host only) and residency under pressure ------------------------
+class PoolStats(ctypes.Structure):
+    _fields_ = [("free_pages", ctypes.c_int64), ("resident_adapters", ctypes.c_int64),
+                ("pinned_adapters", ctypes.c_int64), ("adapters_loaded", ctypes.c_int64),
+                ("adapters_evicted", ctypes.c_int64)]
+
+    def as_dict(self) -> dict:
+        return {f: int(getattr(self, f)) for f, _ in self._fields_}
+
+
+def _ids(ids):
+    import numpy as np
+    a = np.ascontiguousarray(np.asarray(list(ids) if not hasattr(ids, "dtype") else ids, dtype=np.int32))
+    return a, int(a.shape[0])
+
+
+def slora_lru_create() -> int:
+    h = ctypes.c_void_p()
+    _call("slora_lru_create", ctypes.byref(h))
+    return h.value
+
+
+def slora_lru_destroy(lru: int) -> None:
+    _call("slora_lru_destroy", lru)
+
+
+def slora_lru_insert(lru: int, adapter_id: int) -> None:
+    _call("slora_lru_insert", lru, adapter_id)
+
+
+def slora_lru_remove(lru: int, adapter_id: int) -> None:
+    _call("slora_lru_remove", lru, adapter_id)
+
+
+def slora_lru_touch(lru: int, adapter_id: int) -> None:
+    _call("slora_lru_touch", lru, adapter_id)
+
+
+def slora_lru_pin(lru: int, adapter_id: int) -> None:
+    _call("slora_lru_pin", lru, adapter_id)
+
+
+def slora_lru_unpin(lru: int, adapter_id: int) -> None:
+    _call("slora_lru_unpin", lru, adapter_id)
+
+
+def slora_lru_victims(lru: int, exclude=(), max_out: int = 1 << 20) -> list:
+    """Up to max_out unpinned ids not in exclude, least recently used first."""
+    import numpy as np
+    ex, n_ex = _ids(exclude)
+    n_all = ctypes.c_int32()
+    out = np.empty(max(1, min(max_out, 1 << 20)), np.int32)
+    _call("slora_lru_victims", lru, n_ex, ex.ctypes.data if n_ex else None, int(out.shape[0]),
+          out.ctypes.data, ctypes.byref(n_all))
+    return out[:n_all.value].tolist()
+
+
+def slora_adapters_acquire(pool: int, adapter_ids, stream=None) -> None:
+    a, n = _ids(adapter_ids)
+    _call("slora_adapters_acquire", pool, n, a.ctypes.data if n else None, _stream(stream))
+
+
+def slora_adapters_release(pool: int, adapter_ids) -> None:
+    a, n = _ids(adapter_ids)
+    _call("slora_adapters_release", pool, n, a.ctypes.data if n else None)
+
+
+def slora_pages_alloc_evict(pool: int, n: int, out_pages, stream=None) -> None:
+    _call("slora_pages_alloc_evict", pool, n, _ptr(out_pages), _stream(stream))
+
+
+def slora_pool_get_stats(pool: int) -> dict:
+    st = PoolStats()
+    _call("slora_pool_get_stats", pool, ctypes.byref(st))
+    return st.as_dict()
 
 
 def slora_adapter_pages(pool: int, adapter_id: int, proj: int, out) -> None:

@@ -62,6 +62,8 @@ struct slora_pool {
     int64_t launches = 0;  // kernels launched by this pool
     cudaEvent_t stage_event = nullptr;   // measurement hook: recorded between plan and delta
     int32_t max_rank = 0;  // largest registered rank (sizes the plan scratch)
+    LruIndex lru;          // resident adapters by last acquire / load; pins of running batches
+    int64_t n_loaded = 0, n_evicted = 0;
 };
 
 namespace {
@@ -401,8 +403,11 @@ slora_status slora_adapters_load(slora_pool_t p, int32_t n, const int32_t *ids, 
     }
     CUDA_TRY(cudaEventRecord(p->load_event, side));
     CUDA_TRY(cudaStreamWaitEvent((cudaStream_t)stream, p->load_event, 0));
-    for (int32_t id : todo)
+    for (int32_t id : todo) {
         p->adapters[(size_t)id].resident = true;
+        p->lru.insert(id);
+    }
+    p->n_loaded += (int64_t)todo.size();
     return SLORA_OK;
 }
 
@@ -427,6 +432,8 @@ slora_status slora_adapter_evict(slora_pool_t p, int32_t id, slora_stream_t stre
         return fail(SLORA_ERR_NOT_REGISTERED, "adapter_evict: id=%d", id);
     if (!a.resident)
         return fail(SLORA_ERR_NOT_RESIDENT, "adapter_evict: id=%d", id);
+    if (p->lru.pins(id) > 0)
+        return fail(SLORA_ERR_INVALID_ARG, "adapter_evict: id=%d is pinned by an acquire", id);
     slora_status st = set_device(p);
     if (st != SLORA_OK)
         return st;
@@ -442,6 +449,8 @@ slora_status slora_adapter_evict(slora_pool_t p, int32_t id, slora_stream_t stre
     p->arena.release(a.pt_off, rows);
     a.pt_off = -1;
     a.resident = false;
+    p->lru.remove(id);
+    p->n_evicted += 1;
     CUDA_TRY(cudaEventRecord(p->release_event, (cudaStream_t)stream));
     p->release_pending = true;
     return SLORA_OK;
@@ -460,6 +469,8 @@ slora_status slora_adapters_evict(slora_pool_t p, int32_t n, const int32_t *ids,
         const AdapterRec &a = p->adapters[(size_t)id];
         if (!a.registered)
             return fail(SLORA_ERR_NOT_REGISTERED, "adapters_evict: id=%d", id);
+        if (a.resident && p->lru.pins(id) > 0)
+            return fail(SLORA_ERR_INVALID_ARG, "adapters_evict: id=%d is pinned by an acquire", id);
         if (a.resident && seen.insert(id).second)
             todo.push_back(id);
     }
@@ -488,9 +499,106 @@ slora_status slora_adapters_evict(slora_pool_t p, int32_t n, const int32_t *ids,
         p->arena.release(a.pt_off, rows);
         a.pt_off = -1;
         a.resident = false;
+        p->lru.remove(id);
     }
+    p->n_evicted += (int64_t)todo.size();
     CUDA_TRY(cudaEventRecord(p->release_event, (cudaStream_t)stream));
     p->release_pending = true;
+    return SLORA_OK;
+}
+
+// Least recently used unpinned adapters outside `exclude` whose pages, added to the free
+// ones, reach `need`; false if even all of them do not.
+static bool lru_victims(slora_pool_t p, const std::unordered_set<int32_t> &exclude, int64_t need,
+                        std::vector<int32_t> *out)
+{
+    int64_t avail = p->pages.num_free();
+    return p->lru.victims(exclude,
+                          [&](const std::vector<int32_t> &v) {
+                              if (!v.empty()) avail += adapter_rows(p, p->adapters[(size_t)v.back()]);
+                              return avail >= need;
+                          },
+                          out);
+}
+
+slora_status slora_adapters_acquire(slora_pool_t p, int32_t n, const int32_t *ids, slora_stream_t stream)
+{
+    if (!p || n < 0 || (n > 0 && !ids))
+        return fail(SLORA_ERR_INVALID_ARG, "adapters_acquire: n=%d", n);
+    std::unordered_set<int32_t> want;
+    std::vector<int32_t> missing;
+    int64_t need = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        const int32_t id = ids[i];
+        if (!valid_id(p, id))
+            return fail(SLORA_ERR_INVALID_ARG, "adapters_acquire: id=%d", id);
+        const AdapterRec &a = p->adapters[(size_t)id];
+        if (!a.registered)
+            return fail(SLORA_ERR_NOT_REGISTERED, "adapters_acquire: id=%d", id);
+        if (!want.insert(id).second)
+            continue;
+        if (!a.resident) {
+            missing.push_back(id);
+            need += adapter_rows(p, a);
+        }
+    }
+    std::vector<int32_t> victims;
+    if (!lru_victims(p, want, need, &victims))
+        return fail(SLORA_ERR_POOL_FULL,
+                    "adapters_acquire: %lld pages needed, %lld free, the rest held by pinned or requested adapters",
+                    (long long)need, (long long)p->pages.num_free());
+    slora_status st;
+    if (!victims.empty() &&
+        (st = slora_adapters_evict(p, (int32_t)victims.size(), victims.data(), stream)) != SLORA_OK)
+        return st;
+    if (!missing.empty() &&
+        (st = slora_adapters_load(p, (int32_t)missing.size(), missing.data(), stream)) != SLORA_OK)
+        return st;
+    for (int32_t i = 0; i < n; ++i) {   // in the caller's order: later ids are more recent
+        p->lru.touch(ids[i]);
+    }
+    for (int32_t id : want)
+        p->lru.pin(id);
+    return SLORA_OK;
+}
+
+slora_status slora_adapters_release(slora_pool_t p, int32_t n, const int32_t *ids)
+{
+    if (!p || n < 0 || (n > 0 && !ids))
+        return fail(SLORA_ERR_INVALID_ARG, "adapters_release: n=%d", n);
+    std::unordered_set<int32_t> seen;
+    for (int32_t i = 0; i < n; ++i)
+        if (seen.insert(ids[i]).second && (!valid_id(p, ids[i]) || p->lru.pins(ids[i]) == 0))
+            return fail(SLORA_ERR_INVALID_ARG, "adapters_release: id=%d is not acquired", ids[i]);
+    for (int32_t id : seen)
+        p->lru.unpin(id);
+    return SLORA_OK;
+}
+
+slora_status slora_pages_alloc_evict(slora_pool_t p, int64_t n, int32_t *out_pages, slora_stream_t stream)
+{
+    if (!p || n < 0 || (n > 0 && !out_pages))
+        return fail(SLORA_ERR_INVALID_ARG, "pages_alloc_evict: n=%lld", (long long)n);
+    std::vector<int32_t> victims;
+    if (!lru_victims(p, {}, n, &victims))
+        return fail(SLORA_ERR_POOL_FULL, "pages_alloc_evict: %lld pages needed, %lld free, the rest pinned",
+                    (long long)n, (long long)p->pages.num_free());
+    slora_status st;
+    if (!victims.empty() &&
+        (st = slora_adapters_evict(p, (int32_t)victims.size(), victims.data(), stream)) != SLORA_OK)
+        return st;
+    return p->pages.alloc(n, out_pages);
+}
+
+slora_status slora_pool_get_stats(slora_pool_t p, slora_pool_stats *out)
+{
+    if (!p || !out)
+        return fail(SLORA_ERR_INVALID_ARG, "pool_get_stats");
+    out->free_pages = p->pages.num_free();
+    out->resident_adapters = (int64_t)p->lru.ents.size();
+    out->pinned_adapters = (int64_t)(p->lru.ents.size() - p->lru.unpinned.size());
+    out->adapters_loaded = p->n_loaded;
+    out->adapters_evicted = p->n_evicted;
     return SLORA_OK;
 }
 

@@ -155,3 +155,57 @@ def prefetch_overlap(sess: PoolSession, K: int = 6, stream=None) -> dict:
             "serialized_ms": best["serialized"],
             "overlap_frac": (loads + applies - pipe) / max(1e-9, min(loads, applies)),
             "link_gb_per_s": nbytes / (loads * 1e-3) / 1e9}
+
+
+def pressure_run(sess: PoolSession, K: int = 6, stream=None) -> dict:
+    """K batches from the session's zoo through a pool too small to keep them all: per
+    batch, acquire its adapters (the pool evicts the least recently used ones that no batch
+    holds), apply every layer (one slora_lora_apply_multi call per layer), release.
+
+    Returns per-batch adapters used / already resident / loaded / evicted, the host time of
+    the acquire call, and the device time from the acquire's first enqueued work to the
+    end of the batch's last layer (CUDA events on the stream).  The explainer's "The
+    mechanism": adapters that the running batches do not use leave GPU memory and stay in
+    host memory; KV and adapters compete for one pool.
+    """
+    import time
+    from . import (slora_adapters_acquire, slora_adapters_release, slora_lora_apply_multi,
+                   slora_pool_get_stats)
+    w = sess.w
+    batches = [w] + [w.later_batch(k) for k in range(1, K)]
+    dev = torch.device("cuda", sess.device)
+    st = stream or torch.cuda.current_stream(dev)
+    per_layer = w.n_proj // w.n_layers
+    x = [torch.from_numpy(w.x(p).view(np.int16)).to(dev).view(torch.float16) for p in range(w.n_proj)]
+    y = [torch.from_numpy(w.y0(p).view(np.int16)).to(dev).view(torch.float16) for p in range(w.n_proj)]
+    seg = None if w.seg_indptr is None else torch.from_numpy(w.seg_indptr).to(dev)
+    n_seg = w.n_seg
+    sess.register(sorted(set().union(*[set(b.used_adapters().tolist()) for b in batches])))
+    rows = []
+    for b in batches:
+        used = b.used_adapters()
+        idx = torch.from_numpy(b.token_adapter_idx).to(dev)
+        before = slora_pool_get_stats(sess.pool)
+        was = sum(1 for a in used.tolist() if slora_adapter_is_resident(sess.pool, a))
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        t0 = time.perf_counter()
+        slora_adapters_acquire(sess.pool, used, st)
+        host_ms = 1e3 * (time.perf_counter() - t0)
+        for l in range(w.n_layers):
+            ps = list(range(l * per_layer, (l + 1) * per_layer))
+            slora_lora_apply_multi(sess.pool, ps, [x[p] for p in ps], [y[p] for p in ps], b.T, idx, seg, n_seg,
+                                   None, st)
+        slora_adapters_release(sess.pool, used)
+        e1.record(st)
+        torch.cuda.synchronize(dev)
+        after = slora_pool_get_stats(sess.pool)
+        rows.append({"used": int(used.size), "resident_before": was,
+                     "loaded": after["adapters_loaded"] - before["adapters_loaded"],
+                     "evicted": after["adapters_evicted"] - before["adapters_evicted"],
+                     "acquire_host_ms": host_ms, "device_ms": e0.elapsed_time(e1)})
+    used = sum(r["used"] for r in rows[1:])
+    return {"batches": K, "pool_adapter_pages": int(w.num_pages - w.kv_pages),
+            "per_batch": rows,
+            "hit_rate_after_first": (sum(r["resident_before"] for r in rows[1:]) / used) if used else None}

@@ -96,12 +96,20 @@ class Workload:
         return 2 * int(self.ranks[a]) * self.n_proj
 
     def later_batch(self, k: int) -> "Workload":
-        """The k-th later decode batch served from the same adapter zoo and pool: the same
-        ranks, factors and pool geometry, a new token map of as many decode tokens with
-        Zipf(alpha) ids (seeded by the workload's seed and k), the same x and y0."""
+        """The k-th later batch served from the same adapter zoo and pool: the same ranks,
+        factors, pool geometry, segment lengths and token count, the same x and y0, and new
+        Zipf(alpha) adapter ids (seeded by the workload's seed and k): one id per prefill
+        segment (all its tokens) and one per decode token."""
         rng = np.random.default_rng([self.seed, 100 + int(k)])
-        ids = zipf_ids(rng, self.n_adapters, self.T, self.alpha)
-        return Workload(f"{self.name}_next{k}", self.hidden, self.n_proj, self.ranks, ids, None,
+        if self.seg_indptr is None or self.n_seg == 0:
+            ids = zipf_ids(rng, self.n_adapters, self.T, self.alpha)
+        else:
+            lo, hi = int(self.seg_indptr[0]), int(self.seg_indptr[-1])
+            req = zipf_ids(rng, self.n_adapters, self.n_seg + self.T - (hi - lo), self.alpha)
+            lens = np.diff(self.seg_indptr)
+            ids = np.concatenate([req[self.n_seg:self.n_seg + lo], np.repeat(req[:self.n_seg], lens),
+                                  req[self.n_seg + lo:]]).astype(np.int32)
+        return Workload(f"{self.name}_next{k}", self.hidden, self.n_proj, self.ranks, ids, self.seg_indptr,
                         num_pages=self.num_pages, kv_pages=self.kv_pages,
                         shuffle_seed=self.shuffle_seed, seed=self.seed, values=self.values,
                         n_layers=self.n_layers, alpha=self.alpha)
