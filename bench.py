@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--prefetch", type=int, default=0, metavar="K",
                     help="also measure K later batches' adapter loads against the deltas (\"prefetch\")")
+    ap.add_argument("--bmm", action="store_true",
+                    help="also time the padded batched-GEMM comparison path (decode-only workloads)")
     ap.add_argument("--pressure", type=int, default=0, metavar="K",
                     help="also run K batches of the zoo through acquire / apply / release (\"pressure\")")
     ap.add_argument("--layers", type=int, default=0, help="mixed_iteration: layers (0 = the default 32)")
@@ -470,6 +472,36 @@ def main():
     step_achieved = alg_bytes / (ms_per_step / 1e3) / 1e9
     kernel_stats = rdp.slora_pool_kernel_stats(sess.pool) if hasattr(rdp, "slora_pool_kernel_stats") else None
 
+    # the padded batched-GEMM comparison path on projection 0 (decode-only batches)
+    bmm = None
+    if args.bmm and n_seg == 0:
+        nb = rdp.slora_bmm_workspace_bytes(sess.pool, w.T)
+        ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+        yb = ys[0].clone()
+        for _ in range(3):
+            rdp.slora_lora_apply_bmm(sess.pool, 0, xs[0], yb, w.T, idx, ws, nb, None, stream)
+        b0 = [torch.cuda.Event(enable_timing=True) for _ in range(Kd)]
+        b1 = [torch.cuda.Event(enable_timing=True) for _ in range(Kd)]
+        c0 = [torch.cuda.Event(enable_timing=True) for _ in range(Kd)]
+        c1 = [torch.cuda.Event(enable_timing=True) for _ in range(Kd)]
+        for k in range(Kd):
+            flush.zero_()
+            b0[k].record(stream)
+            rdp.slora_lora_apply_bmm(sess.pool, 0, xs[0], yb, w.T, idx, ws, nb, None, stream)
+            b1[k].record(stream)
+            flush.zero_()
+            c0[k].record(stream)
+            rdp.slora_lora_apply(sess.pool, 0, xs[0], ys[0], w.T, idx, seg, n_seg, None, stream)
+            c1[k].record(stream)
+        torch.cuda.synchronize()
+        bmm_ms = statistics.median(a.elapsed_time(b) for a, b in zip(b0, b1))
+        cus_ms = statistics.median(a.elapsed_time(b) for a, b in zip(c0, c1))
+        bmm = {"ms": bmm_ms, "custom_ms": cus_ms, "custom_speedup": bmm_ms / cus_ms, "workspace_bytes": int(nb),
+               "padded_rank": int(nb // max(1, w.T * 4 * w.hidden + 2 * w.T)),
+               "includes": "gather of every token's padded A^T and s*B from the pages + two cuBLAS strided "
+                           "batched GEMMs (fp16 in, fp32 accumulation); custom = plan + delta kernels, one "
+                           "projection, each after an L2 flush"}
+
     # ---- end to end through the C ABI from pinned host buffers --------------------
     hx = [torch.from_numpy(w.x(p).view(np.int16)).view(torch.float16).pin_memory() for p in range(w.n_proj)]
     hy0 = [torch.from_numpy(w.y0(p).view(np.int16)).view(torch.float16).pin_memory() for p in range(w.n_proj)]
@@ -572,6 +604,8 @@ def main():
         line["prefetch"] = prefetch
     if pressure is not None:
         line["pressure"] = pressure
+    if bmm is not None:
+        line["bmm"] = bmm
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, cores, sample = oracle_rate(w, args.cpu_seconds)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s/layer", "cores": cores,

@@ -309,6 +309,25 @@ slora_status slora_lora_apply_multi(slora_pool_t pool, int32_t n, const int32_t 
                                     slora_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * slora_lora_apply_bmm: the padded batched-GEMM path, kept as the comparison the S-LoRA
+ * ablation calls the slower BMM path (blog page, section 4; explainer, "Prior limits").
+ * Not the hot path: it exists to be measured against slora_lora_apply.  Decode tokens
+ * only (no segments): every token gets a dense copy of its adapter's factors zero-padded
+ * to R = the pool's largest registered rank rounded up to a multiple of 8 (a gather
+ * kernel writes A^T and s * B into the workspace), then two strided batched GEMMs of the
+ * cuBLAS library (loaded on first use; SLORA_ERR_UNSUPPORTED if it cannot be) form
+ * u_t = fp16(A_t^T x_t) and y_t = y0_t + (s B_t)^T u_t with fp32 accumulation.
+ *   proj, x, y, T, token_adapter_idx, scaling, stream: as slora_lora_apply (n_seg = 0)
+ *   workspace  device buffer, 16-byte aligned, of at least slora_bmm_workspace_bytes()
+ *              bytes (T * R * (4 * hidden + 2), rounded up); owned by the caller
+ * Tokens without a resident adapter keep y and set a device status code.
+ * ------------------------------------------------------------------------- */
+slora_status slora_bmm_workspace_bytes(slora_pool_t pool, int32_t T, size_t *out);
+slora_status slora_lora_apply_bmm(slora_pool_t pool, int32_t proj, const void *x, void *y, int32_t T,
+                                  const int32_t *token_adapter_idx, const float *scaling,
+                                  void *workspace, size_t workspace_bytes, slora_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * slora_lora_apply_noalloc: the same computation as slora_lora_apply, with the same
  * arguments, for callers that must not allocate device memory during the call.  The
  * S-LoRA pages have no counterpart for it; it exists for callers whose device memory

@@ -36,6 +36,7 @@ __all__ = [
     "slora_lru_create", "slora_lru_destroy", "slora_lru_insert", "slora_lru_remove", "slora_lru_touch",
     "slora_lru_pin", "slora_lru_unpin", "slora_lru_victims",
     "slora_adapters_acquire", "slora_adapters_release", "slora_pages_alloc_evict", "slora_pool_get_stats",
+    "slora_bmm_workspace_bytes", "slora_lora_apply_bmm",
 ]
 
 _I32, _I64, _U64, _F32, _P = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float, ctypes.c_void_p
@@ -86,6 +87,8 @@ _SIGS = {
     "slora_adapters_release": [_P, _I32, _P],
     "slora_pages_alloc_evict": [_P, _I64, _P, _P],
     "slora_pool_get_stats": [_P, _P],
+    "slora_bmm_workspace_bytes": [_P, _I32, _P],
+    "slora_lora_apply_bmm": [_P, _I32, _P, _P, _I32, _P, _P, _P, ctypes.c_size_t, _P],
 }
 _RESTYPE = {"slora_status_str": ctypes.c_char_p, "slora_last_error": ctypes.c_char_p,
             "slora_version": _I32}
@@ -353,6 +356,19 @@ def slora_pool_get_stats(pool: int) -> dict:
     st = PoolStats()
     _call("slora_pool_get_stats", pool, ctypes.byref(st))
     return st.as_dict()
+
+
+def slora_bmm_workspace_bytes(pool: int, T: int) -> int:
+    v = ctypes.c_size_t()
+    _call("slora_bmm_workspace_bytes", pool, T, ctypes.byref(v))
+    return v.value
+
+
+def slora_lora_apply_bmm(pool: int, proj: int, x, y, T: int, token_adapter_idx, workspace, workspace_bytes: int,
+                         scaling=None, stream=None) -> None:
+    """The padded batched-GEMM comparison path (see include/slora.h)."""
+    _call("slora_lora_apply_bmm", pool, proj, _ptr(x), _ptr(y), T, _ptr(token_adapter_idx), _ptr(scaling),
+          _ptr(workspace), int(workspace_bytes), _stream(stream))
 
 
 def slora_adapter_pages(pool: int, adapter_id: int, proj: int, out) -> None:
