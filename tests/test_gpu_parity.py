@@ -421,3 +421,20 @@ def test_load_of_more_adapters_than_one_launch_carries():
         got = run(s)
         assert s.device_status() == 0
     assert_close(got, oracle.workload_reference(w), "600 adapters")
+
+
+def test_decode_large_ranks_and_long_groups_bit_exact():
+    """Decode ranks 1 to 1024 (every rank bucket, items of several rank units), an adapter
+    holding 40 tokens (three items), base-only tokens; exact-arithmetic inputs, so the
+    kernel equals the oracle bit for bit."""
+    ranks = np.array([1, 2, 3, 5, 8, 13, 16, 31, 64, 100, 128, 129, 200, 256, 512, 1024], np.int32)
+    rng = np.random.default_rng(3)
+    idx = rng.integers(-1, len(ranks), size=200).astype(np.int32)
+    idx[rng.choice(200, 40, replace=False)] = 6
+    w = W.Workload("decode_ranks", 1024, 1, ranks, idx, None, num_pages=4 * int(ranks.sum()) + 64,
+                   kv_pages=64, shuffle_seed=5, seed=6, values="exact")
+    with session_all_loaded(w) as s:
+        got = run(s)
+        assert s.device_status() == 0
+    ref = oracle.workload_reference(w).astype(np.float16)
+    assert np.array_equal(got.view(np.uint16), ref.view(np.uint16))
