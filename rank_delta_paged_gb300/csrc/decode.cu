@@ -41,6 +41,8 @@
 // order of the partial sum, never by the other tokens of its item or the other
 // projections of the call, so results do not depend on the batch, its order, the
 // physical pages, or how the projections are grouped into calls.
+#include <mutex>
+
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -1111,15 +1113,30 @@ inline size_t delta_smem_bytes(int hidden)
            2 * kTok * 4 + 2 * 4 + (2 * NST + 13) * 8;
 }
 
+// Kernel attributes and the delta grid's resident clusters, per device (the attributes
+// are per-device state; calls may come from several threads).
+struct DeltaLaunchState {
+    bool attrs = false;
+    int occ_hidden = -1;
+    int occ_clusters = 1;
+};
+constexpr int kMaxLaunchDevices = 64;
+std::mutex g_delta_mu;
+DeltaLaunchState g_delta_state[kMaxLaunchDevices];
+
 cudaError_t launch_lora_apply(const PoolView &pv, const ProjList &pl, int32_t T, const int32_t *idx,
                               const int32_t *seg_indptr, int32_t n_seg, const float *scaling,
                               const PlanScratch &scratch, int num_sms, cudaStream_t stream, int *launches,
                               cudaEvent_t after_plan)
 {
-    static bool attrs_set = false;
-    static int occ_hidden = -1, occ_clusters = 1;
     if (pv.hidden > kMaxCluster * kMaxSlice || pl.n < 1 || pl.n > kMaxApplyProj) return cudaErrorInvalidValue;
-    if (!attrs_set) {
+    int device = 0;
+    cudaError_t de = cudaGetDevice(&device);
+    if (de != cudaSuccess) return de;
+    if (device < 0 || device >= kMaxLaunchDevices) return cudaErrorInvalidDevice;
+    std::unique_lock<std::mutex> lk(g_delta_mu);
+    DeltaLaunchState &ls = g_delta_state[device];
+    if (!ls.attrs) {
         cudaError_t e = cudaFuncSetAttribute(delta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)delta_smem_bytes(kMaxSlice));
         if (e != cudaSuccess) return e;
@@ -1129,7 +1146,7 @@ cudaError_t launch_lora_apply(const PoolView &pv, const ProjList &pl, int32_t T,
         e = cudaFuncSetAttribute(plan_kernel<kPlanThreadsSmall>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)(plan_smem_bytes(kMaxHash) + kPlanDirCache * sizeof(DirEntry)));
         if (e != cudaSuccess) return e;
-        attrs_set = true;
+        ls.attrs = true;
     }
     const int C = delta_cluster(pv.hidden);
     const size_t dsmem = delta_smem_bytes(pv.hidden);
@@ -1148,14 +1165,16 @@ cudaError_t launch_lora_apply(const PoolView &pv, const ProjList &pl, int32_t T,
     cfg2.stream = stream;
     cfg2.attrs = attr;
     cfg2.numAttrs = 2;
-    if (pv.hidden != occ_hidden) {
+    if (pv.hidden != ls.occ_hidden) {
         cfg2.gridDim = dim3(C * num_sms);
         int ncl = 0;
         cudaError_t e = cudaOccupancyMaxActiveClusters(&ncl, delta_kernel, &cfg2);
         if (e != cudaSuccess) return e;
-        occ_clusters = ncl > 0 ? ncl : 1;
-        occ_hidden = pv.hidden;
+        ls.occ_clusters = ncl > 0 ? ncl : 1;
+        ls.occ_hidden = pv.hidden;
     }
+    const int occ_clusters = ls.occ_clusters;
+    lk.unlock();
     cfg2.gridDim = dim3(C * occ_clusters);
 
     const int32_t chunk = plan_chunk(pv.max_adapters);

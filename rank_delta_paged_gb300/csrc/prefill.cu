@@ -53,6 +53,7 @@
 // Every wait is bounded; a unit whose tokens disagree on their adapter, or whose adapter
 // is not resident, is skipped with a device status code.
 #include <cstring>
+#include <mutex>
 
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -748,18 +749,33 @@ inline int slice_for(int hidden, int C) { return (hidden / 64 + C - 1) / C * 64;
 
 }  // namespace
 
+// The kernel attribute and the resident clusters for C = 1, 2, 4, 8, per device (the
+// attribute is per-device state; calls may come from several threads).
+struct PrefillLaunchState {
+    bool attr = false;
+    int ncl[4] = {0, 0, 0, 0};
+};
+constexpr int kMaxLaunchDevices = 64;
+std::mutex g_prefill_mu;
+PrefillLaunchState g_prefill_state[kMaxLaunchDevices];
+
 cudaError_t launch_prefill(const PoolView &pv, const ProjList &pl, int32_t T, const int32_t *idx,
                            const int32_t *seg_indptr, int32_t n_seg, const float *scaling, int num_sms,
                            cudaStream_t stream)
 {
-    static bool attr_set = false;
-    static int ncl_cache[4] = {0, 0, 0, 0};   // resident clusters for C = 1, 2, 4, 8
-    if (!attr_set) {
+    int device = 0;
+    cudaError_t de = cudaGetDevice(&device);
+    if (de != cudaSuccess) return de;
+    if (device < 0 || device >= kMaxLaunchDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_prefill_mu);
+    PrefillLaunchState &ls = g_prefill_state[device];
+    int *ncl_cache = ls.ncl;   // resident clusters for C = 1, 2, 4, 8
+    if (!ls.attr) {
         size_t most = 0;
         for (int c = 1; c <= kMaxClusterP; c *= 2) most = smem_bytes_for(c) > most ? smem_bytes_for(c) : most;
         cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        ls.attr = true;
     }
     if (pl.n < 1 || pl.n > kMaxApplyProj) return cudaErrorInvalidValue;
     for (int j = 0; j < pl.n; ++j)
