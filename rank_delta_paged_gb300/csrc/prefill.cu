@@ -13,7 +13,7 @@
 // Work unit: one 128-token tile of one segment for one projection of the call (a call may
 // cover several projections of a layer; unit u is tile u / n_proj of projection slot
 // u % n_proj).  Persistent clusters of C CTAs (C = 1, 2, 4 or 8, chosen on the host from
-// the number of units so that they fill the SMs)
+// the number of units: rounds of units over the resident clusters against bytes per CTA)
 // take units in turn; CTA c of a cluster owns hidden slice c: the K range of its part
 // of the shrink and the N range of its part of the expand, so every byte of x, y0, y and
 // of the adapter's pages is moved by exactly one CTA.
@@ -52,6 +52,7 @@
 //               returns it to the ring, so the four warps never wait for one another there.
 // Every wait is bounded; a unit whose tokens disagree on their adapter, or whose adapter
 // is not resident, is skipped with a device status code.
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -806,17 +807,26 @@ cudaError_t launch_prefill(const PoolView &pv, const ProjList &pl, int32_t T, co
         return ncl_cache[lg];
     };
 
-    // CTAs per cluster: the largest C whose resident clusters still cover the units
-    // (128-token tiles per projection; the host does not read the segments, so T bounds
-    // their number).
+    // CTAs per cluster: the C that minimises the modelled time rounds(C) * (1 + R / C), where
+    // rounds(C) = ceil(units / resident clusters of C) and R is the time one CTA takes to
+    // move a unit's bytes at C = 1 relative to a unit's fixed cost (about 16 at hidden 4096,
+    // in proportion to hidden); ties go to the smaller C.  Units are 128-token tiles per
+    // projection; the host does not read the segments, so T bounds their number.
     const int units = (T + MT - 1) / MT * pl.n;
+    const double R = std::max(2.0, 16.0 * pv.hidden / 4096.0);
     int C = 1, lgC = 0;
-    for (int lg = 1; lg <= 3; ++lg) {
+    double best = 1e300;
+    for (int lg = 0; lg <= 3; ++lg) {
         const int c = 1 << lg;
-        const int sl = slice_for(pv.hidden, c);
-        if (sl < 256 || (c - 1) * sl >= pv.hidden) break;
+        if (lg > 0) {
+            const int sl = slice_for(pv.hidden, c);
+            if (sl < 256 || (c - 1) * sl >= pv.hidden) break;
+        }
         const int n = clusters(c, lg);
-        if (n > 0 && units <= n) {
+        if (n <= 0) continue;
+        const double cost = (double)((units + n - 1) / n) * (1.0 + R / c);
+        if (cost < best - 1e-9) {
+            best = cost;
             C = c;
             lgC = lg;
         }
