@@ -258,11 +258,68 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         const uint32_t cl = cluster_id_x(), ncl = ncluster_x();
         int s0 = 0, base = 0;   // window of 32 segments and the tiles before it
         uint32_t gT = 0;        // token tiles issued
+        // Batches of at most 32 segments deal their units costliest first: lane s holds
+        // segment s; the segments are sorted by their adapter's rank, descending (ties:
+        // lower index first), and the units (tile, projection slot) of the sorted segments
+        // go to the clusters in rounds of one unit per cluster, walked in alternating
+        // direction.  Larger batches take the units in order, cluster c every ncl-th.
+        const bool lpt = a.n_seg <= 32;
+        int s_lo = 0, s_hi = 0, ord = 0, upref = 0, n_units = 0;
+        if (lpt) {
+            int key = 0x7fffffff;
+            if (lane < a.n_seg) {
+                s_lo = a.seg_indptr[lane];
+                s_hi = a.seg_indptr[lane + 1];
+                int rank = 0;
+                if (s_hi > s_lo && s_lo >= 0 && s_lo < a.T) {
+                    const int ad = a.idx[s_lo];
+                    if (ad >= 0 && ad < a.pv.max_adapters) {
+                        const DirEntry e = a.pv.dir[ad];
+                        if (e.pt_off >= 0 && e.rank > 0) rank = min(e.rank, 255);
+                    }
+                }
+                key = ((255 - rank) << 8) | lane;
+            }
+#pragma unroll
+            for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+                for (int j = k >> 1; j > 0; j >>= 1) {
+                    const int o = __shfl_xor_sync(0xffffffffu, key, j);
+                    const bool up = (lane & k) == 0, low = (lane & j) == 0;
+                    key = (low == up) ? min(key, o) : max(key, o);
+                }
+            }
+            const bool valid = key != 0x7fffffff;
+            ord = valid ? (key & 0xff) : 0;   // the segment at sorted place `lane`
+            const int sl = __shfl_sync(0xffffffffu, s_lo, ord), sh = __shfl_sync(0xffffffffu, s_hi, ord);
+            int incl = valid ? (sh - sl + MT - 1) / MT * a.n_proj : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int n = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += n;
+            }
+            upref = incl;   // units of sorted places 0 .. lane
+            n_units = __shfl_sync(0xffffffffu, incl, 31);
+        }
         for (uint32_t i = 0;; ++i) {
+            int tile = -1, lo = 0, hi = 0, pj = 0;
+            if (lpt) {
+                const int p = (int)(i * ncl + ((i & 1) ? (ncl - 1 - cl) : cl));
+                if (p < n_units) {
+                    const int q = __ffs(__ballot_sync(0xffffffffu, upref > p)) - 1;
+                    const int prev = __shfl_sync(0xffffffffu, upref, q > 0 ? q - 1 : 0);
+                    const int o = p - (q > 0 ? prev : 0);
+                    tile = o / a.n_proj;
+                    pj = o - tile * a.n_proj;
+                    const int seg = __shfl_sync(0xffffffffu, ord, q);
+                    lo = __shfl_sync(0xffffffffu, s_lo, seg);
+                    hi = __shfl_sync(0xffffffffu, s_hi, seg);
+                }
+            }
             const int vu = (int)(cl + i * ncl);            // unit: (tile mt, projection slot pj)
-            const int mt = vu / a.n_proj, pj = vu - mt * a.n_proj;
-            int tile = -1, lo = 0, hi = 0;
-            while (s0 < a.n_seg) {
+            const int mt = vu / a.n_proj;
+            if (!lpt) pj = vu - mt * a.n_proj;
+            while (!lpt && s0 < a.n_seg) {
                 const int j = s0 + lane;
                 int l = 0, h = 0;
                 if (j < a.n_seg) {
@@ -809,11 +866,13 @@ cudaError_t launch_prefill(const PoolView &pv, const ProjList &pl, int32_t T, co
 
     // CTAs per cluster: the C that minimises the modelled time rounds(C) * (1 + R / C), where
     // rounds(C) = ceil(units / resident clusters of C) and R is the time one CTA takes to
-    // move a unit's bytes at C = 1 relative to a unit's fixed cost (about 16 at hidden 4096,
-    // in proportion to hidden); ties go to the smaller C.  Units are 128-token tiles per
-    // projection; the host does not read the segments, so T bounds their number.
+    // move a unit's bytes at C = 1 relative to a unit's fixed cost (6 at hidden 4096, in
+    // proportion to hidden: the value that picks the fastest of C = 2, 4 and 8 measured on
+    // 16 x 512-token segments and on a mixed-iteration layer); ties go to the smaller C.
+    // Units are 128-token tiles per projection; the host does not read the segments, so T
+    // bounds their number.
     const int units = (T + MT - 1) / MT * pl.n;
-    const double R = std::max(2.0, 16.0 * pv.hidden / 4096.0);
+    const double R = std::max(2.0, 6.0 * pv.hidden / 4096.0);
     int C = 1, lgC = 0;
     double best = 1e300;
     for (int lg = 0; lg <= 3; ++lg) {
