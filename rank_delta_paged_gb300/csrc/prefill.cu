@@ -200,7 +200,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     volatile int *abort = &s_abort;
     int32_t *status = a.pv.status;
 
-    griddep_wait();
+    // The kernel is launched only right after a decode kernel of the same call, which
+    // starts it (programmatic dependent launch) only once everything enqueued before the
+    // call has completed; it reads nothing the decode kernel writes (segment and decode
+    // tokens are disjoint rows), so it waits for that kernel only at its end: its work
+    // overlaps the decode kernel's tail, and its completion still implies the decode
+    // kernel's, for whatever the stream runs next.
     griddep_launch_dependents();
 
     if (warp == kMmaWarp) {
@@ -755,6 +760,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         if (lane == 0) bulk_wait<0>();
     }
 
+    griddep_wait();   // the decode kernel of the call has completed (see the top)
     tc::fence_before_sync();
     __syncthreads();
     if (C > 1) cluster_sync_all();   // no CTA of the cluster still touches this one's shared memory
