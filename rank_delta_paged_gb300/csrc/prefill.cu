@@ -14,7 +14,9 @@
 // cover several projections of a layer; unit u is tile u / n_proj of projection slot
 // u % n_proj).  Persistent clusters of C CTAs (C = 1, 2, 4 or 8, chosen on the host from
 // the number of units: rounds of units over the resident clusters against bytes per CTA)
-// take units in turn; CTA c of a cluster owns hidden slice c: the K range of its part
+// take units in turn (batches of at most 32 segments deal them costliest first: segments
+// by their adapter's rank, descending, in rounds of alternating direction); CTA c of a
+// cluster owns hidden slice c: the K range of its part
 // of the shrink and the N range of its part of the expand, so every byte of x, y0, y and
 // of the adapter's pages is moved by exactly one CTA.
 //
