@@ -67,7 +67,7 @@ def parse():
 # capture of the current kernel on the workload (profiles/delta_kernel_decode_7b.md and
 # profiles/prefill_kernel_prefill_7b.md give the commands); a workload without a capture
 # of the current kernel reports null.
-TRAFFIC = {"decode_7b_h4096_a100_t256_zipf1": 41921024, "prefill_7b_h4096_s16x512": 155555840}
+TRAFFIC = {"decode_7b_h4096_a100_t256_zipf1": 41918464, "prefill_7b_h4096_s16x512": 155555840}
 
 
 def peaks():

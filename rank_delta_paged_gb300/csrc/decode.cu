@@ -17,7 +17,7 @@
 //   delta_kernel: persistent clusters of C = ceil(hidden / 1024) CTAs; a cluster takes
 //     whole items, and CTA c of the cluster owns slice c of the hidden dimension (at most
 //     1024 elements): the K range of the shrink and the output columns of the expand.
-//     An item runs in units of 128 rank rows:
+//     An item runs in units of 64 rank rows:
 //       shrink  partial u[t][j] = sum over the CTA's K slice of x[t][k] * At[j][k]
 //       reduce  every CTA sums the C partials (read from the cluster's shared memory, in
 //               CTA order) and rounds u to fp16 once
@@ -59,7 +59,7 @@ constexpr int kThreads = kConsumers + 64;         // plus a producer warp and a 
 constexpr int kTok = 16;                          // tokens per item: the MMA's M
 constexpr int kMaxSlice = 1024;                   // elements of hidden per CTA
 constexpr int kMaxCluster = 8;
-constexpr int kRC = 128;                          // rank rows per rank chunk
+constexpr int kRC = 64;                           // rank rows per rank chunk (unit)
 constexpr int NST = 4;                            // ring depth (16-row stages)
 constexpr int kUPitch = kRC + 8;                  // halves per token row of the u buffer
 constexpr int kMaxRank = 1024;
