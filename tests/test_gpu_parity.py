@@ -438,3 +438,23 @@ def test_decode_large_ranks_and_long_groups_bit_exact():
         assert s.device_status() == 0
     ref = oracle.workload_reference(w).astype(np.float16)
     assert np.array_equal(got.view(np.uint16), ref.view(np.uint16))
+
+
+def test_prefill_many_segments_bit_exact():
+    """40 segments (more than the 32 the segment scheduler sorts by rank, so units are
+    dealt in order), ragged lengths and mixed ranks, beside decode tokens; exact inputs,
+    so the result equals the oracle bit for bit."""
+    ranks = np.array([8, 16, 24, 32, 64, 100, 128, 8], np.int32)
+    rng = np.random.default_rng(40)
+    lens = rng.integers(1, 300, size=40)
+    seg_ad = rng.integers(0, len(ranks), size=40)
+    dec = rng.integers(-1, len(ranks), size=64)
+    idx = np.concatenate([np.full(L, a) for a, L in zip(seg_ad, lens)] + [dec]).astype(np.int32)
+    indptr = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    w = W.Workload("many_segments", 1024, 1, ranks, idx, indptr, num_pages=4 * int(ranks.sum()) + 64,
+                   kv_pages=64, shuffle_seed=6, seed=7, values="exact")
+    with session_all_loaded(w) as s:
+        got = run(s)
+        assert s.device_status() == 0
+    ref = oracle.workload_reference(w).astype(np.float16)
+    assert np.array_equal(got.view(np.uint16), ref.view(np.uint16))
