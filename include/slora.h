@@ -82,7 +82,10 @@ const char *slora_status_str(slora_status s);
 /* Message of the calling thread's last failed call ("" if none).  Valid until the
  * thread's next failing call. */
 const char *slora_last_error(void);
-/* Library version as major * 10000 + minor * 100 + patch. */
+/* Library version as major * 10000 + minor * 100 + patch: 200 (0.2.0).  0.2.0 adds
+ * slora_lora_apply_multi, residency under pool pressure (slora_adapters_acquire /
+ * release, slora_pages_alloc_evict, slora_pool_get_stats, slora_lru_*) and the padded
+ * batched-GEMM comparison path (slora_lora_apply_bmm). */
 int32_t slora_version(void);
 
 /* ---------------------------------------------------------------------------

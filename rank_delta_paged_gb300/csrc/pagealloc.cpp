@@ -174,7 +174,7 @@ const char *slora_status_str(slora_status s)
 
 const char *slora_last_error(void) { return g_last_error.c_str(); }
 
-int32_t slora_version(void) { return 100; }
+int32_t slora_version(void) { return 200; }
 
 slora_status slora_pagealloc_create(int64_t num_pages, uint64_t shuffle_seed, slora_pagealloc_t *out)
 {
