@@ -133,7 +133,7 @@ slora_status slora_lru_victims(slora_lru_t l, int32_t n_exclude, const int32_t *
  * Pool.
  *   device        CUDA device ordinal (must be compute capability 10.3)
  *   hidden        row length; a multiple of 64, 64 <= hidden <= 8192 (the decode kernel
- *                 splits a row over a cluster of at most 8 CTAs of 1024 elements each)
+ *                 cuts a row into at most 8 blocks of at most 1024 elements)
  *   num_pages     pool slots, 1 <= num_pages < 2^31; pool bytes = num_pages * hidden * 2
  *   n_proj        projections per adapter (e.g. layers x {q,k,v,o}); >= 1
  *   max_adapters  adapter ids are 0 .. max_adapters-1
@@ -271,8 +271,12 @@ slora_status slora_pool_get_stats(slora_pool_t pool, slora_pool_stats *out);
  * result is the same up to the order of the fp32 partial sums of x A: the segment
  * kernel splits hidden over 1, 2, 4 or 8 CTAs, chosen from T, and adds their partial
  * products in CTA order.
- * Scratch: the pool keeps device scratch for the token plan, sized on first use and
- * grown when a larger T arrives (a growth synchronises the pool's device).
+ * Scratch: the pool keeps device scratch for the token plan, the decode kernel's work list
+ * and the fp32 partial sums of x A its work units exchange, sized on first use and grown
+ * when a larger T, more projections per call or a larger registered rank arrives (a
+ * growth synchronises the pool's device).
+ * Every entry point that works on a pool makes the pool's device current for the call and
+ * gives the calling thread its previous current device back before it returns.
  * ------------------------------------------------------------------------- */
 slora_status slora_lora_apply(slora_pool_t pool, int32_t proj, const void *x, void *y, int32_t T,
                               const int32_t *token_adapter_idx, const int32_t *seg_indptr,
@@ -339,20 +343,28 @@ slora_status slora_lora_apply_bmm(slora_pool_t pool, int32_t proj, const void *x
  * own plan scratch is allocated on first use and re-allocated when a larger batch or a
  * larger registered rank arrives).
  *
- * Scratch: one fixed 512 KiB device array inside the library, which every GPU that loads
+ * Scratch: one fixed 16 MiB device array inside the library, which every GPU that loads
  * the library holds until the process exits.  The call allocates and frees nothing.
- * Limit: the token plan of the call must fit that array; it needs about
- *   T' * 36 + 512 bytes
- * (a token's slot in the token order and up to one 32-byte work item per token), with
- * T' = min(T, 16384) when max_adapters <= 2048, else min(T, 2048): a batch of up to about
- * 14,500 decode tokens fits.  A call beyond it returns
+ * Limit: the call's scratch must fit that array; it needs about
+ *   T' * (4 + NB * (32 * (nch + 1) + 512 * nch)) + 1280 bytes
+ * (per token: its slot in the token order; per hidden block: the 32-byte work units and
+ * the 64 eight-byte tagged partial sums of every 64-row rank chunk), with
+ * NB = ceil(hidden / 1024), nch = ceil(largest registered rank / 64), and
+ * T' = min(T, 16384) when max_adapters <= 2048, else min(T, 2048) (larger batches then run
+ * as several plans of 2048 tokens, each fitting the array on its own).  With ranks up to
+ * 64 that is about 2.3 KB per token at hidden 4096 (a batch of up to about 7,200 tokens
+ * fits) and 2.9 KB at hidden 5120 (about 5,800 tokens).  A call beyond it returns
  * SLORA_ERR_UNSUPPORTED with the sizes in slora_last_error() and launches nothing.
  * The first call on a device looks up the array's device address (once per device,
  * with that device current); make that first call before any stream capture.
- * Every call on a device shares the one array and leaves its plan there; the kernels
- * rewrite every field they read, so nothing needs clearing between calls.  Calls whose
- * kernels overlap on the GPU (other streams, other pools, other threads) race on the
- * array: order them on one stream or synchronise between them.
+ * Every call on a device shares the one array and leaves its plan and partial sums
+ * there; the plan kernel rewrites every plan field the delta kernel reads (counters set
+ * to zero), and every partial sum carries the tag of the launch that wrote it (a new tag
+ * per launch), so stale sums are never taken for new ones.  The first launch on a device,
+ * and the launch after the tag sequence wraps, clear the partial region first with
+ * cudaMemsetAsync on the call's stream.  Calls whose kernels overlap on the
+ * GPU (other streams, other pools, other threads) race on the array: order them on one
+ * stream or synchronise between them.
  * ------------------------------------------------------------------------- */
 slora_status slora_lora_apply_noalloc(slora_pool_t pool, int32_t proj, const void *x, void *y,
                                       int32_t T, const int32_t *token_adapter_idx,

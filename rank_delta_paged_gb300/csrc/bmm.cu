@@ -179,7 +179,8 @@ extern "C" slora_status slora_lora_apply_bmm(slora_pool_t pool, int32_t proj, co
     if (workspace_bytes_ < need)
         return fail(SLORA_ERR_INVALID_ARG, "lora_apply_bmm: workspace of %zu bytes, %zu needed", workspace_bytes_,
                     need);
-    cudaError_t e = cudaSetDevice(hp.device);
+    DeviceScope dev_scope(hp.device);   // the caller's current device comes back on return
+    cudaError_t e = dev_scope.error();
     if (e != cudaSuccess)
         return fail(SLORA_ERR_CUDA, "lora_apply_bmm: cudaSetDevice: %s", cudaGetErrorString(e));
     cublasHandle_t h;

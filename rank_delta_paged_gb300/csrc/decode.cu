@@ -11,35 +11,42 @@
 // Two kernels per batch (chained with programmatic dependent launch):
 //
 //   plan_kernel (one CTA): groups the decode tokens by adapter in a shared-memory hash
-//     table (caching each adapter's directory entry in its slot) and writes the work
-//     list: one item per adapter and chunk of up to 16 of its tokens, in descending rank.
+//     table (caching each adapter's directory entry in its slot), cuts every group into
+//     items of up to 8 tokens, and writes the work list of the delta kernel: for every
+//     item and projection of the call, one shrink unit per (hidden block, 64-row rank
+//     chunk) and one expand unit per hidden block; all shrink units come first, items
+//     in descending rank.
 //
-//   delta_kernel: persistent clusters of C = ceil(hidden / 1024) CTAs; a cluster takes
-//     whole items, and CTA c of the cluster owns slice c of the hidden dimension (at most
-//     1024 elements): the K range of the shrink and the output columns of the expand.
-//     An item runs in units of 64 rank rows:
-//       shrink  partial u[t][j] = sum over the CTA's K slice of x[t][k] * At[j][k]
-//       reduce  every CTA sums the C partials (read from the cluster's shared memory, in
-//               CTA order) and rounds u to fp16 once
-//       expand  acc[t][c] += sum_j u[t][j] * B[j][c] over the CTA's columns
-//     then y[t][c] = y0[t][c] + s * acc[t][c].  A producer warp streams the row slices
-//     (the tokens' x rows, A^T rows, y0 rows, B rows) with 1-D bulk copies into a ring of
-//     16-row stages; eight consumer warps contract them on the tensor cores with
-//     warp-level mma.sync m16n8k16 (fp16 operands, fp32 accumulators; tokens on M),
-//     running the shrink of unit u before the expand of unit u-1 so that the wait for the
-//     cluster's partials overlaps useful work; a signal warp relays the "partials
-//     written / read" events to the cluster.  Each page row is read once per item; the
-//     cluster exchanges only the small fp32 partials.  Every wait is bounded in time.
+//   delta_kernel: one persistent CTA per SM takes units in list order (its first by its
+//     index, then from a counter in the plan), so every SM stays busy until the list ends:
+//       shrink  (item, block b, chunk c): partial u[t][j] = sum over the K slice b of
+//               x[t][k] * At[j][k] for the chunk's rank rows -> fp32 partials in global
+//               scratch (L2), each written as one 64-bit word {value, launch tag}
+//       expand  (item, block b): once every partial word of the item carries this
+//               launch's tag, u = sum of the partials over the hidden blocks in block
+//               order, rounded to fp16 once; acc[t][c] = sum_j u[t][j] * B[j][c] over the
+//               block's columns; y[t][c] = y0[t][c] + s * acc[t][c]
+//     Warp roles: a lead warp fetches the units and publishes each with its token ids and
+//     first page ids; four copy warps stream the row slices (the item's token rows, then
+//     A^T or B rows) into a ring of 8-row stages with 1-D bulk copies; eight consumer
+//     warps contract them on the tensor cores with warp-level mma.sync m16n8k16 (fp16
+//     operands, fp32 accumulators; a shrink puts rank rows on M and tokens on N, an
+//     expand tokens on M and columns on N); a gather warp polls and sums the partials of
+//     the expand units ahead of the consumers, so no consumer waits on a global round
+//     trip.  Every page row is read once per item; the only cross-SM traffic is the small
+//     tagged partials.  Every wait is bounded in time.
+//
+// Expand units only wait for shrink units that precede them in the list, and shrink
+// units never wait on another SM, so the list drains whatever number of CTAs is resident.
 //
 // One call may cover several projections of a layer (q, k, v, o: the same tokens and
-// adapters, each projection with its own pages, x and y).  The plan is made once; the
-// delta kernel's work list is every (item, projection) pair, item-major, so the pairs
-// keep the plan's descending-cost order and the clusters share them out as they would
-// the items of one projection.
+// adapters, each projection with its own pages, x and y): the plan is made once and
+// lists the units of every (item, projection) pair.
 //
-// A token's arithmetic is fixed by the fragment layout, the slice boundaries and the CTA
-// order of the partial sum, never by the other tokens of its item or the other
-// projections of the call, so results do not depend on the batch, its order, the
+// A token's arithmetic is fixed by the fragment layout, the hidden-block boundaries, the
+// fixed split of a block's K steps over the eight consumer warps (summed in warp order)
+// and the block order of the partial sum, never by the other tokens of its item, the other projections of the call
+// or the SM that runs a unit, so results do not depend on the batch, its order, the
 // physical pages, or how the projections are grouped into calls.
 #include <mutex>
 
@@ -53,15 +60,22 @@
 namespace slora {
 namespace {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kConsumers = 32 * kConsumerWarps;   // consumer threads
-constexpr int kThreads = kConsumers + 64;         // plus a producer warp and a signal warp
-constexpr int kTok = 16;                          // tokens per item: the MMA's M
-constexpr int kMaxSlice = 1024;                   // elements of hidden per CTA
-constexpr int kMaxCluster = 8;
-constexpr int kRC = 64;                           // rank rows per rank chunk (unit)
-constexpr int NST = 4;                            // ring depth (16-row stages)
-constexpr int kUPitch = kRC + 8;                  // halves per token row of the u buffer
+constexpr int kConsumerWarps = 8;                 // warps doing the contractions
+constexpr int kConsumers = 32 * kConsumerWarps;
+constexpr int kCopyWarps = 4;                     // warps issuing the bulk copies
+constexpr int kWarpLead = kConsumerWarps;         // fetches and publishes the units
+constexpr int kWarpCopy0 = kConsumerWarps + 1;    // first copy warp
+constexpr int kWarpGather = kWarpCopy0 + kCopyWarps;   // sums the shrink partials of the expand units ahead
+constexpr int kThreads = 32 * (kWarpGather + 1);
+constexpr int kRecReaders = kConsumerWarps + kCopyWarps + 1;   // warps that read every unit record
+constexpr int kTok = 8;                           // tokens per item: one MMA n-tile / one ring stage
+constexpr int kMaxSlice = 1024;                   // elements of a hidden block
+constexpr int kMaxBlocks = 8;                     // hidden blocks (hidden <= 8192)
+constexpr int kRC = 64;                           // rank rows per rank chunk
+constexpr int NST = 12;                           // ring depth (8-row stages)
+constexpr int QD = 8;                             // unit records in flight
+constexpr int QU = 4;                             // u buffers (gather warp -> consumers)
+constexpr int kUPitch = kRC + 8;                  // halves per token row of a u buffer
 constexpr int kMaxRank = 1024;
 
 constexpr int kPlanThreads = 1024;       // threads of the plan kernel (256 for batches of <= 256 tokens)
@@ -70,31 +84,51 @@ constexpr int kMaxPlanTokens = 16384;   // token-index range per plan when group
 constexpr int kMaxPlanGroups = 2048;    // distinct adapters per plan
 constexpr int kMaxHash = 2 * kMaxPlanGroups;
 
-static_assert(kRC / 16 <= kConsumerWarps, "one shrink block per consumer warp and rank chunk");
-// per-warp K-split partials of a unit's shrink: ksplit = warps / nb parts of 16 x 16 nb,
-// at most 16 x 16 x (number of warps) floats whatever the unit's size
-constexpr int kPtmpFloats = kTok * 16 * kConsumerWarps;
+static_assert(kTok == 8, "one ring stage of token rows, one MMA n-tile of tokens");
+static_assert(NST % kCopyWarps == 0, "each ring slot always filled by the same copy warp");
+// Per consumer warp: K steps of a shrink block, 16-column pairs of an expand block at most.
+constexpr int kXs = kMaxSlice / 16 / kConsumerWarps;
+constexpr int kPairs = kMaxSlice / 16 / kConsumerWarps;
+// A consumer warp's own scratch region: a shrink unit's partial (8 tokens x 64 rank rows) or
+// an expand unit's y0 values (2 kPairs n-tiles x 32 lanes, half2 each).
+constexpr int kRegionFloats = 2 * kPairs * 32 > kTok * kRC ? 2 * kPairs * 32 : kTok * kRC;
+constexpr int kPtmpFloats = kRegionFloats * kConsumerWarps;
 
 struct PlanHeader {
-    int32_t n_groups, n_items, pad0, pad1;
-    int32_t seg_lo, seg_hi, pad2, pad3;
+    int32_t n_groups, n_items, n_units, n_shrink;
+    int32_t seg_lo, seg_hi, grab, pad;
 };
-// One work item: an adapter and up to kTok of its tokens, with the group's fields.
-struct alignas(16) Item {
-    int32_t t0, nt;     // first token (position within the group), tokens (<= kTok)
-    int32_t rank;
-    int32_t tok_begin;  // the group's first position in tok_order
-    int32_t adapter;
-    float scaling;
-    int64_t pt_base;    // arena index of the adapter's page tables (projection 0's)
-};
-static_assert(sizeof(Item) == 32, "Item layout");
 
+// One unit of the delta kernel's work list: a shrink or an expand unit of one item (an
+// adapter and up to kTok of its tokens) and one projection of the call.
+//   packed: bits 0-4 tokens - 1, bit 5 expand, bits 6-8 projection slot, bits 9-11 hidden
+//           block, bits 12-15 rank chunk (shrink units)
+struct alignas(16) Unit {
+    int32_t tok_start;  // first position of the item's tokens in tok_order
+    uint32_t packed;
+    int32_t rank;
+    float scaling;      // the adapter's scaling (the call's override applied)
+    int64_t pt_base;    // arena index of the projection's page table (A^T rows, then B rows)
+    int32_t uoff;       // first word of the (item, projection)'s partials
+    int32_t pad;
+};
+static_assert(sizeof(Unit) == 32, "Unit layout");
+
+__host__ __device__ inline uint32_t unit_pack(int nt, int expand, int pj, int b, int c)
+{
+    return (uint32_t)(nt - 1) | ((uint32_t)expand << 5) | ((uint32_t)pj << 6) | ((uint32_t)b << 9) |
+           ((uint32_t)c << 12);
+}
+
+// The shrink units' partial sums: one 64-bit word per value, the fp32 bits in the low half
+// and the launch's tag in the high half, written with one relaxed store, so a reader that
+// sees the tag sees the value (no fence, no counter).
 struct PlanLayout {
     PlanHeader *hdr;
     int32_t *tok_order;
-    Item *items;
-    int64_t cap_items;
+    Unit *units;
+    unsigned long long *upart;
+    int64_t cap_units, cap_words;
 };
 
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -108,7 +142,12 @@ inline int32_t plan_chunk(int32_t max_adapters)
     return max_adapters <= kMaxPlanGroups ? kMaxPlanTokens : kMaxPlanGroups;
 }
 
-PlanLayout carve(void *base, int32_t cap_tokens, size_t *total)
+// Hidden blocks: the K slices of the shrink and the column blocks of the expand.
+inline int n_blocks(int hidden) { return ceil_div(hidden, kMaxSlice); }
+
+// Scratch of one plan: header, token order, units, tagged partials.  Items are at most one
+// per token, so every count is bounded by the tokens of the plan.
+PlanLayout carve(void *base, int32_t cap_tokens, int32_t n_proj, int32_t nblk, int32_t max_rank, size_t *total)
 {
     PlanLayout L;
     size_t off = 0;
@@ -118,10 +157,13 @@ PlanLayout carve(void *base, int32_t cap_tokens, size_t *total)
         return (char *)base + o;
     };
     const int64_t cap = cap_tokens;
-    L.cap_items = cap;
+    const int64_t nch = ceil_div(max_rank < 1 ? 1 : max_rank, kRC);
+    L.cap_units = cap * n_proj * nblk * (nch + 1);
+    L.cap_words = cap * n_proj * nblk * nch * kRC;
     L.hdr = (PlanHeader *)take(sizeof(PlanHeader));
     L.tok_order = (int32_t *)take(cap * 4);
-    L.items = (Item *)take(L.cap_items * sizeof(Item));
+    L.units = (Unit *)take(L.cap_units * sizeof(Unit));
+    L.upart = (unsigned long long *)take(L.cap_words * 8);
     if (total)
         *total = off;
     return L;
@@ -190,6 +232,10 @@ struct PlanArgs {
     int32_t t_begin, t_end;
     int32_t hash_size;  // power of two >= 2 * min(t_end - t_begin, max_adapters), <= kMaxHash
     int32_t dir_cache;  // the directory (max_adapters entries) is copied into shared memory
+    int32_t n_proj;     // projections of the call
+    int32_t nblk;       // hidden blocks
+    int32_t proj[kMaxApplyProj];
+    const float *scaling;   // optional override [max_adapters]
     PlanLayout L;
 };
 
@@ -209,6 +255,9 @@ __device__ __forceinline__ void plan_refuse(const PlanArgs &a)
     set_status(a.pv.status, SLORA_DEV_BAD_SEGMENT);
     a.L.hdr->n_groups = 0;
     a.L.hdr->n_items = 0;
+    a.L.hdr->n_units = 0;
+    a.L.hdr->n_shrink = 0;
+    a.L.hdr->grab = 0;
 }
 
 template <int NT>
@@ -378,33 +427,68 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const __grid_constant__ Pla
     if (tid == 0) s_nit = tot[1];
     __syncthreads();
     const int n_items = s_nit;
-    if ((int64_t)n_items > a.L.cap_items) {
-        if (tid == 0) plan_refuse(a);
-        return;
-    }
+    const int NP = a.n_proj, NB = a.nblk;
 
-    // 4. items, in parallel over items (each finds its group position by binary search over
-    //    the strictly increasing first-item offsets), and the token order
-    for (int i = tid; i < n_items; i += NT) {
+    // 4. the units of every item.  Each thread takes a contiguous run of items, so one scan
+    //    of (shrink units, partial floats) per item gives every item's place in the list.
+    //    An item finds its group position by binary search over the strictly increasing
+    //    first-item offsets.
+    struct ItemInfo {
+        int g, t0, nt, rank, nch;
+    };
+    auto item_info = [&](int i) {
         int lo_p = 0, hi_p = G - 1;
         while (lo_p < hi_p) {
             const int mid = (lo_p + hi_p + 1) >> 1;
             if (pit[mid] <= i) lo_p = mid; else hi_p = mid - 1;
         }
-        const int g = gperm[lo_p];
-        const int tc = i - pit[lo_p];
-        Item it;
-        it.t0 = tc * kTok;
-        it.nt = min(kTok, hcnt[gslot[g]] - it.t0);
-        it.rank = grank[g];
-        it.tok_begin = gtok[g];
-        it.adapter = gad[g];
-        it.scaling = gscale[g];
-        it.pt_base = gpt[g];
-        const uint4 *src4 = reinterpret_cast<const uint4 *>(&it);
-        uint4 *dst4 = reinterpret_cast<uint4 *>(a.L.items + i);
-        dst4[0] = src4[0];
-        dst4[1] = src4[1];
+        ItemInfo f;
+        f.g = gperm[lo_p];
+        f.t0 = (i - pit[lo_p]) * kTok;
+        f.nt = min(kTok, hcnt[gslot[f.g]] - f.t0);
+        f.rank = grank[f.g];
+        f.nch = ceil_div(f.rank, kRC);
+        return f;
+    };
+    const int per_i = ceil_div(n_items > 0 ? n_items : 1, NT);
+    const int i0 = tid * per_i;
+    int cnt[2] = {0, 0};
+    for (int q = 0; q < per_i && i0 + q < n_items; ++q) {
+        const ItemInfo f = item_info(i0 + q);
+        cnt[0] += NP * NB * f.nch;
+        cnt[1] += NP * f.nch * NB * f.nt * kRC;
+    }
+    int uo[2], ut[2];
+    block_excl_scan<2>(cnt, warp_tot2, uo, ut);
+    const int n_shrink = ut[0];
+    const int64_t n_units = (int64_t)n_shrink + (int64_t)n_items * NP * NB;
+    if (n_units > a.L.cap_units || (int64_t)ut[1] > a.L.cap_words) {
+        if (tid == 0) plan_refuse(a);
+        return;
+    }
+    for (int q = 0; q < per_i && i0 + q < n_items; ++q) {
+        const int i = i0 + q;
+        const ItemInfo f = item_info(i);
+        Unit u;
+        u.tok_start = gtok[f.g] + f.t0;
+        u.rank = f.rank;
+        u.scaling = a.scaling ? a.scaling[gad[f.g]] : gscale[f.g];
+        const int per_proj = f.nch * NB * f.nt * kRC;
+        for (int pj = 0; pj < NP; ++pj) {
+            u.pt_base = gpt[f.g] + (int64_t)a.proj[pj] * 2 * f.rank;
+            u.uoff = uo[1] + pj * per_proj;
+            u.pad = 0;
+            for (int b = 0; b < NB; ++b) {
+                for (int c = 0; c < f.nch; ++c) {
+                    u.packed = unit_pack(f.nt, 0, pj, b, c);
+                    a.L.units[uo[0] + (pj * NB + b) * f.nch + c] = u;
+                }
+                u.packed = unit_pack(f.nt, 1, pj, b, 0);
+                a.L.units[n_shrink + (int64_t)i * NP * NB + pj * NB + b] = u;
+            }
+        }
+        uo[0] += NP * NB * f.nch;
+        uo[1] += NP * per_proj;
     }
     for (int i = tid; i < Tc; i += NT) {
         const int h = tslot[i];
@@ -414,8 +498,11 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const __grid_constant__ Pla
     if (tid == 0) {
         a.L.hdr->n_groups = G;
         a.L.hdr->n_items = n_items;
+        a.L.hdr->n_units = (int32_t)n_units;
+        a.L.hdr->n_shrink = n_shrink;
         a.L.hdr->seg_lo = lo;
         a.L.hdr->seg_hi = hi;
+        a.L.hdr->grab = 0;
     }
 }
 
@@ -424,20 +511,26 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const __grid_constant__ Pla
 
 struct DeltaArgs {
     PoolView pv;
-    const __half *x[kMaxApplyProj];   // per projection of the call
+    const __half *x[kMaxApplyProj];   // per projection slot of the call
     __half *y[kMaxApplyProj];
-    int32_t proj[kMaxApplyProj];
-    int32_t n_proj;                   // projections of the call
-    const float *scaling;   // optional override [max_adapters]
     PlanLayout L;
-    int32_t pitch;          // bytes per row of a stage / x / y0 buffer: 2 * largest slice + 16
+    int32_t pitch;          // bytes per row of a ring stage: 2 * largest block + 16
+    int32_t nblk;           // hidden blocks
+    uint32_t tag;           // this launch's partial-sum tag (never 0)
+};
+
+// A unit as the lead warp hands it to the other warps: the descriptor, the item's token
+// ids and the page ids of its first rank chunk (A^T rows of a shrink unit's chunk, B rows
+// of an expand unit's chunk 0).
+struct alignas(16) Rec {
+    Unit u;
+    int32_t tok[kTok];      // token ids of the item's rows (0 past its tokens)
+    int32_t pg[kRC];        // page ids of the first chunk's rows (-1 past the rank)
+    int32_t end;            // no more units
+    int32_t pad[3];
 };
 
 // ---- decode-specific helpers (inline PTX) ---------------------------------------------
-__device__ __forceinline__ void consumers_sync()
-{
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
-}
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4])
 {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -459,666 +552,601 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// The k-th item of this cluster: rounds of ncl items, walked in alternating direction so
-// that the costliest items (the list is ordered by rank, descending) spread evenly over
-// the clusters.
-__device__ __forceinline__ int cluster_item(int k, int cl, int ncl)
-{
-    return k * ncl + ((k & 1) ? (ncl - 1 - cl) : cl);
-}
-
-// Balanced item order for batches of at most kBalRounds rounds of items over at most 64
-// clusters: round 0 gives item c to cluster c; every later round gives its costliest item
-// to the least loaded cluster, the next to the next least loaded, and so on (cost: the
-// rows of A^T, B, x, y0 and y the item moves).  Every CTA of the grid computes the same
-// order, so each item is still processed by exactly one cluster.
-constexpr int kBalRounds = 4;
-constexpr int kBalClusters = 64;
-
-// Ascending bitonic sort of 64 keys held two per lane (element lane and lane + 32).
-__device__ __forceinline__ void warp_sort64(int &a, int &b, int lane)
-{
-#pragma unroll
-    for (int k = 2; k <= 64; k <<= 1) {
-#pragma unroll
-        for (int j = k >> 1; j > 0; j >>= 1) {
-            if (j == 32) {
-                const int lo = min(a, b), hi = max(a, b);
-                a = lo;
-                b = hi;
-            } else {
-                const int pa = __shfl_xor_sync(0xffffffffu, a, j), pb = __shfl_xor_sync(0xffffffffu, b, j);
-                const bool low = (lane & j) == 0;
-                const bool upa = (lane & k) == 0, upb = ((lane + 32) & k) == 0;
-                a = (low == upa) ? min(a, pa) : max(a, pa);
-                b = (low == upb) ? min(b, pb) : max(b, pb);
-            }
-        }
-    }
-}
-
-// One warp: this cluster's work entries of rounds 1 .. kBalRounds-1 into seq[] (n_items =
-// none).  Entry i is item i / np of the plan for projection slot i % np.
-__device__ void balance_items(const Item *items, int n_items, int np, int ncl, int cl, int lane, int *seq,
-                              int *cost, int *load)
-{
-    for (int i = lane; i < kBalRounds * kBalClusters; i += 32) {
-        int c = 0;
-        if (i < n_items) c = 4 * __ldcg(&items[i / np].rank) + 3 * __ldcg(&items[i / np].nt);
-        cost[i] = c;
-    }
-    for (int r = lane; r < kBalRounds; r += 32) seq[r] = n_items;
-    __syncwarp();
-    for (int c = lane; c < kBalClusters; c += 32) load[c] = c < ncl && c < n_items ? cost[c] : 0;
-    __syncwarp();
-    for (int r = 1; r < kBalRounds; ++r) {
-        const int base = r * ncl;
-        if (base >= n_items) break;
-        const int nb = min(ncl, n_items - base);
-        // items of the round, costliest first (ties: lower position first)
-        int ia = lane < nb ? -(cost[base + lane] * 1024 + (1023 - lane)) : INT_MAX;
-        int ib = lane + 32 < nb ? -(cost[base + lane + 32] * 1024 + (1023 - lane - 32)) : INT_MAX;
-        warp_sort64(ia, ib, lane);
-        // clusters, least loaded first (ties: lower cluster first)
-        int ca = lane < ncl ? load[lane] * 256 + lane : INT_MAX;
-        int cb = lane + 32 < ncl ? load[lane + 32] * 256 + lane + 32 : INT_MAX;
-        warp_sort64(ca, cb, lane);
-        __syncwarp();
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int pos = lane + 32 * h;
-            const int ik = h ? ib : ia, ck = h ? cb : ca;
-            if (pos < nb) {
-                const int key = -ik, c = ck & 255;
-                load[c] += key / 1024;
-                if (c == cl) seq[r] = base + (1023 - key % 1024);
-            }
-        }
-        __syncwarp();
-    }
-}
-
-__device__ __forceinline__ Item load_item(const Item *p)
+__device__ __forceinline__ Unit load_unit(const Unit *p)
 {
     const uint4 *s = reinterpret_cast<const uint4 *>(p);
     const uint4 w0 = __ldcg(s), w1 = __ldcg(s + 1);
-    Item it;
-    it.t0 = (int32_t)w0.x;
-    it.nt = (int32_t)w0.y;
-    it.rank = (int32_t)w0.z;
-    it.tok_begin = (int32_t)w0.w;
-    it.adapter = (int32_t)w1.x;
-    it.scaling = __uint_as_float(w1.y);
-    it.pt_base = (int64_t)(((uint64_t)w1.w << 32) | w1.z);
-    return it;
+    Unit u;
+    u.tok_start = (int32_t)w0.x;
+    u.packed = w0.y;
+    u.rank = (int32_t)w0.z;
+    u.scaling = __uint_as_float(w0.w);
+    u.pt_base = (int64_t)(((uint64_t)w1.y << 32) | w1.x);
+    u.uoff = (int32_t)w1.z;
+    u.pad = (int32_t)w1.w;
+    return u;
 }
 
+// Tagged partial words: relaxed 64-bit accesses at GPU scope (single-copy atomic).
+__device__ __forceinline__ void st_word(unsigned long long *p, float v, uint32_t tag)
+{
+    const unsigned long long w = ((unsigned long long)tag << 32) | __float_as_uint(v);
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_word(const unsigned long long *p)
+{
+    unsigned long long w;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+    return w;
+}
+
+// Position in the ring: the slot of the next stage and the parity of its phase.  Walking the
+// ring one stage at a time needs no division.
+struct RingPos {
+    uint32_t slot, phase;
+    __device__ __forceinline__ void next()
+    {
+        if (++slot == NST) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+};
+
+// A unit's fields, unpacked.
+struct UnitShape {
+    int nt, expand, pj, b, c;
+    int nch;         // rank chunks the unit covers (an expand covers every chunk of the rank)
+};
+__device__ __forceinline__ UnitShape unit_shape(const Unit &u)
+{
+    UnitShape s;
+    s.nt = (int)(u.packed & 31u) + 1;
+    s.expand = (int)((u.packed >> 5) & 1u);
+    s.pj = (int)((u.packed >> 6) & 7u);
+    s.b = (int)((u.packed >> 9) & 7u);
+    s.c = (int)((u.packed >> 12) & 15u);
+    s.nch = s.expand ? ceil_div(u.rank, kRC) : 1;
+    return s;
+}
+// rows of the i-th chunk the unit covers
+__device__ __forceinline__ int chunk_rows(const Unit &u, const UnitShape &s, int i)
+{
+    const int c = s.expand ? i : s.c;
+    return min(kRC, u.rank - kRC * c);
+}
+
+// A unit's ring stages: one stage of its token rows (x of a shrink, y0 of an expand), then its
+// rank rows (A^T rows of the shrink's chunk, or B rows of every chunk; 8 per stage).
 __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constant__ DeltaArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     const int P = a.pitch;
-    const int stageB = kTok * P;                                                 // one 16-row stage
-    uint8_t *ring = smem;                                                        // [NST][16][P]
-    uint8_t *xbuf = ring + NST * stageB;                                         // [2][16][P] x rows, by item parity
-    float *part = reinterpret_cast<float *>(xbuf + 2 * stageB);                  // [2][16][kRC] partial u, by unit parity
-    float *ptmp = part + 2 * kTok * kRC;                                         // [ksplit][16][16 nb] per-warp partials
-    __half *ubuf = reinterpret_cast<__half *>(ptmp + kPtmpFloats);               // [16][kUPitch] u (fp16)
-    Item *rec_it = reinterpret_cast<Item *>(ubuf + kTok * kUPitch);              // [2] item, by item parity
-    int32_t *rec_tok = reinterpret_cast<int32_t *>(rec_it + 2);                 // [2][kTok] token ids
-    int32_t *rec_pj = rec_tok + 2 * kTok;                                        // [2] projection slot
-    uint64_t *bars = reinterpret_cast<uint64_t *>(rec_pj + 2);
-    uint64_t *full = bars, *empty = bars + NST;
-    uint64_t *full_x = bars + 2 * NST;   // [2] an item's x rows (and record) landed
-    uint64_t *xfree = full_x + 2;        // [2] an item's shrink no longer reads its x rows
-    uint64_t *ready = full_x + 4;        // [2] every CTA of the cluster wrote its partials of a unit
-    uint64_t *consumed = full_x + 6;     // [2] every CTA of the cluster has read the partials of a unit
-    uint64_t *done = full_x + 8;         // every CTA of the cluster is finished with the others' memory
-    uint64_t *pwrit = full_x + 9;        // [2] this CTA's partials of a unit are written (local)
-    uint64_t *rdone = full_x + 11;       // [2] this CTA has read the cluster's partials of a unit (local)
+    const int stageB = 8 * P;                                                    // one 8-row ring stage
+    uint8_t *ring = smem;                                                        // [NST][8][P]
+    uint8_t *zrow = ring + NST * stageB;                                         // [P] zeros: rows past the rank / tokens
+    float *ptmp = reinterpret_cast<float *>(zrow + P);                           // [8 warps][kRegionFloats] warp scratch
+    __half *ubuf = reinterpret_cast<__half *>(ptmp + kPtmpFloats);               // [QU][8][kUPitch] u (fp16)
+    Rec *recs = reinterpret_cast<Rec *>(ubuf + QU * kTok * kUPitch);             // [QD] units in flight
+    uint64_t *bars = reinterpret_cast<uint64_t *>(recs + QD);
+    uint64_t *full = bars, *empty = bars + NST;              // ring stages
+    uint64_t *rfull = bars + 2 * NST, *rempty = rfull + QD;  // unit records
+    uint64_t *ufull = rempty + QD, *uempty = ufull + QU;     // u buffers
+    uint64_t *cbar = uempty + QU;                            // consumer warps' rendezvous
     __shared__ int s_abort;
+    __shared__ int s_blk[kMaxBlocks + 1];                    // first element of each hidden block
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int d = a.pv.hidden;
-    const uint32_t crank = cluster_ctarank(), C = cluster_nctarank();
-    const int cl = (int)cluster_id_x(), ncl = (int)ncluster_x();
-    __shared__ int s_seq[kBalRounds], s_cost[kBalRounds * kBalClusters], s_load[kBalClusters];
-    __shared__ __align__(8) uint64_t seq_bar;
-    // this CTA's slice of the hidden dimension, in whole 16-element steps
-    const int nk16 = d / 16;
-    const int kb = 16 * (int)((crank * (uint32_t)nk16) / C);
-    const int KS = 16 * (int)(((crank + 1) * (uint32_t)nk16) / C) - kb;
-    const uint32_t sliceB = (uint32_t)KS * 2;
+    const int NB = a.nblk;
     int32_t *status = a.pv.status;
     volatile int *abort = &s_abort;
-    const uint32_t ring_s = smem_u32(ring), xbuf_s = smem_u32(xbuf);
+    const uint32_t ring_s = smem_u32(ring), zrow_s = smem_u32(zrow);
     const uint32_t ubuf_s = smem_u32(ubuf);
 
+    for (int o = tid * 16; o < P; o += kThreads * 16) *reinterpret_cast<uint4 *>(zrow + o) = make_uint4(0, 0, 0, 0);
+    if (tid <= kMaxBlocks) {
+        // hidden block b: whole 16-element steps [s_blk[b], s_blk[b+1])
+        const int nk16 = d / 16;
+        s_blk[tid] = tid <= NB ? 16 * ((tid * nk16) / NB) : d;
+    }
     if (tid == 0) {
         for (int s = 0; s < NST; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kConsumerWarps);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&full_x[b], 1);
-            mbar_init(&xfree[b], 1);
-            mbar_init(&ready[b], C);
-            mbar_init(&consumed[b], C);
+        for (int q = 0; q < QD; ++q) {
+            mbar_init(&rfull[q], 1);
+            mbar_init(&rempty[q], kRecReaders);
         }
-        mbar_init(done, C);
-        mbar_init(&seq_bar, 1);
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&pwrit[b], 1);
-            mbar_init(&rdone[b], 1);
+        for (int q = 0; q < QU; ++q) {
+            mbar_init(&ufull[q], 1);
+            mbar_init(&uempty[q], kConsumerWarps);
         }
+        mbar_init(cbar, kConsumerWarps);
         s_abort = 0;
         fence_mbar_init();
     }
     __syncthreads();
-    cluster_sync_all();   // every CTA's barriers exist before any remote arrival
-    griddep_wait();       // the plan of this batch is complete and visible
+    griddep_wait();   // the plan of this batch is complete and visible
     griddep_launch_dependents();
-    const int NP = a.n_proj;
-    const int n_items = a.L.hdr->n_items * NP;   // (item, projection) entries
-    const bool bal = n_items <= kBalRounds * ncl && ncl <= kBalClusters;
-    // the index of this cluster's k-th item (n_items or more: no more items)
-    auto item_of = [&](int k) -> int {
-        if (!bal) return cluster_item(k, cl, ncl);
-        if (k == 0) return cl;
-        if (k >= kBalRounds || k * ncl >= n_items) return n_items;
-        wait_phase<false>(&seq_bar, 0, abort, status);
-        return s_seq[k];
+    const int n_units = __ldcg(&a.L.hdr->n_units);
+
+    // read record k (every reader walks the records in order); false at the end
+    auto take_record = [&](int k, Unit &u) -> bool {
+        const uint32_t q = k % QD;
+        wait_phase<false>(&rfull[q], (k / QD) & 1, abort, status);
+        if (*abort) return false;
+        const int end = recs[q].end;
+        u = recs[q].u;
+        return !end;
+    };
+    auto release_record = [&](int k) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&rempty[k % QD]);
     };
 
-    // Work runs in units: one chunk of at most kRC rank rows of an item.  Both sides walk
-    // the units in the same order and interleave them one unit apart (the shrink of unit
-    // u, then the expand of unit u-1), so the wait for the cluster's partials of a unit
-    // overlaps the next unit's shrink.
-
-    if (warp == kConsumerWarps + 1) {
-        // ================================ signal warp ================================
-        // Relays this CTA's "partials written" and "partials read" events of every unit to
-        // the cluster (lane c arrives, release at cluster scope, on CTA c's barrier).  The
-        // warp writes no global memory, so its releases only order the shared-memory
-        // writes it has observed through the local barriers.
-        int k = -1, c = 0, nch = 0;
-        uint32_t u = 0;
-        for (;;) {
-            bool have = true;
-            if (c == nch) {
-                ++k;
-                const int i = item_of(k);
-                if (i >= n_items) {
-                    have = false;
-                } else {
-                    c = 0;
-                    nch = ceil_div(__ldcg(&a.L.items[i / NP].rank), kRC);
-                }
+    if (warp == kWarpLead) {
+        // ================================== lead (metadata) ==================================
+        // Takes units in list order (the first by the CTA's index, then from the plan's
+        // counter) and publishes each with its token ids and first chunk's page ids.  The
+        // loads run three units deep: the counter for unit k+2, the descriptor of unit k+1
+        // and the tokens and page ids of unit k are in flight together.
+        const int G = (int)gridDim.x;
+        const int32_t *pt = a.pv.pt_arena;
+        auto fetch_rest = [&](const Unit &u, int &tok, int32_t &p0, int32_t &p1) {
+            const int nt = (int)(u.packed & 31u) + 1;
+            tok = lane < nt ? __ldcg(a.L.tok_order + u.tok_start + lane) : 0;
+            int64_t base;
+            int rows;
+            if (u.packed & 32u) {
+                base = u.pt_base + u.rank;
+                rows = min(kRC, u.rank);
+            } else {
+                const int c = (int)((u.packed >> 12) & 15u);
+                base = u.pt_base + kRC * c;
+                rows = min(kRC, u.rank - kRC * c);
             }
-            if (have) {
-                wait_phase<false>(&pwrit[u & 1], (u >> 1) & 1, abort, status);
-                if (lane < (int)C) mbar_arrive_remote(mapa(smem_u32(&ready[u & 1]), lane));
-            }
-            if (u >= 1) {
-                const uint32_t pu = u - 1;
-                wait_phase<false>(&rdone[pu & 1], (pu >> 1) & 1, abort, status);
-                if (lane < (int)C) mbar_arrive_remote(mapa(smem_u32(&consumed[pu & 1]), lane));
-            }
-            if (!have) break;
-            ++c;
-            ++u;
+            p0 = lane < rows ? __ldcg(pt + base + lane) : -1;
+            p1 = lane + 32 < rows ? __ldcg(pt + base + lane + 32) : -1;
+        };
+        int grab = 0;   // lane 0: index of the unit after `nu`
+        if (lane == 0) grab = G + atomicAdd(&a.L.hdr->grab, 1);
+        bool cvalid = (int)blockIdx.x < n_units;
+        Unit cu{};
+        int ctok = 0;
+        int32_t cp0 = -1, cp1 = -1;
+        if (cvalid) {
+            cu = load_unit(a.L.units + blockIdx.x);
+            fetch_rest(cu, ctok, cp0, cp1);
         }
-        // the CTA is done reading the others' partials once its last unit was reduced
-        if (lane < (int)C) mbar_arrive_remote(mapa(smem_u32(done), lane));
-        if (lane == 0) wait_phase<true>(done, 0, abort, status);
+        int nidx = __shfl_sync(0xffffffffu, grab, 0);
+        bool nvalid = cvalid && nidx < n_units;
+        Unit nu{};
+        if (nvalid) {
+            nu = load_unit(a.L.units + nidx);
+            if (lane == 0) grab = G + atomicAdd(&a.L.hdr->grab, 1);
+        }
+        for (int k = 0;; ++k) {
+            const uint32_t q = k % QD;
+            if (k >= QD) wait_phase<false>(&rempty[q], ((k / QD) - 1) & 1, abort, status);
+            if (!cvalid || *abort) {
+                if (lane == 0) {
+                    recs[q].end = 1;
+                    mbar_arrive(&rfull[q]);
+                }
+                break;
+            }
+            if (lane == 0) {
+                recs[q].u = cu;
+                recs[q].end = 0;
+            }
+            if (lane < kTok) recs[q].tok[lane] = ctok;
+            recs[q].pg[lane] = cp0;
+            recs[q].pg[lane + 32] = cp1;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&rfull[q]);
+            // advance the pipeline
+            cu = nu;
+            cvalid = nvalid;
+            if (cvalid) fetch_rest(cu, ctok, cp0, cp1);
+            nidx = __shfl_sync(0xffffffffu, grab, 0);
+            nvalid = cvalid && nidx < n_units;
+            if (nvalid) {
+                nu = load_unit(a.L.units + nidx);
+                if (lane == 0) grab = G + atomicAdd(&a.L.hdr->grab, 1);
+            }
+        }
         return;
     }
 
-    if (warp == kConsumerWarps) {
-        // ===================================== producer =====================================
+    if (warp >= kWarpCopy0 && warp < kWarpCopy0 + kCopyWarps) {
+        // ==================================== copy warps =====================================
+        // Every copy warp walks every unit's stages; stage g of the CTA goes to copy warp
+        // g % kCopyWarps, which waits for its ring slot, then lanes 0-7 each bulk-copy one
+        // row's slice of the unit's hidden block (several warps keep enough copies in flight).
+        const int cw = warp - kWarpCopy0;
         const __half *pool = reinterpret_cast<const __half *>(a.pv.pool);
-        uint32_t sc = 0;   // stages issued
-        // Lane r < 16 copies the CTA's slice of row r from src_r (when ok_r) into a 16-row
-        // buffer at dst; rows not copied are zero-filled when zero_rest.  Completion on *bar.
-        auto fill16 = [&](uint32_t dst, uint64_t *bar, const __half *src_r, bool ok_r, bool zero_rest) {
-            const bool mine = ok_r && lane < 16;
-            const uint32_t m = __ballot_sync(0xffffffffu, mine);
-            if (mine && !*abort)
-                bulk_g2s_s(dst + lane * P, src_r + kb, sliceB, bar);
-            if (zero_rest && m != 0xffffu) {
-                for (int r = 0; r < 16; ++r) {
-                    if ((m >> r) & 1u) continue;
-                    for (uint32_t o = lane * 16; o < sliceB; o += 32 * 16)
-                        *reinterpret_cast<uint4 *>(smem + (dst - ring_s) + r * P + o) = make_uint4(0, 0, 0, 0);
-                }
-                tc::fence_proxy_async_smem();   // before later bulk copies land in the same rows
+        const int32_t *pt = a.pv.pt_arena;
+        RingPos pos{0, 0};
+        uint32_t sc = 0;   // stages of the CTA so far
+        for (int k = 0;; ++k) {
+            Unit u;
+            const bool have = take_record(k, u);
+            const uint32_t q = k % QD;
+            if (!have) {
+                release_record(k);
+                break;
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive_expect_tx(bar, *abort ? 0u : (uint32_t)__popc(m) * sliceB);
-        };
-        auto next_slot = [&]() -> uint32_t {
-            const uint32_t slot = sc % NST;
-            if (sc >= NST) wait_phase<false>(&empty[slot], ((sc / NST) - 1) & 1, abort, status);
-            return slot;
-        };
-        auto page_ok = [&](int32_t pg) -> bool {
-            if (pg >= 0 && pg < a.pv.num_pages) return true;
-            set_status(status, SLORA_DEV_BAD_PAGE);
-            return false;
-        };
-        // the 16-row blocks of a unit: rows rc0 .. rc0+rows-1 of A^T (ab 0) or B (ab 1);
-        // lane l holds the page indices of the unit's rows l + 32m in pg4[m]
-        auto emit_blocks = [&](int rows, const int32_t (&pg4)[4], bool zero_rest) {
-            const int nb = ceil_div(rows, 16);
-            for (int b = 0; b < nb; ++b) {
-                const uint32_t slot = next_slot();
-                const int src_lane = 16 * (b & 1) + (lane & 15);   // rows 16b+l live in lane 16(b&1)+l, word b/2
-                int32_t pg = -1;
+            const UnitShape sh = unit_shape(u);
+            const int kb = s_blk[sh.b];
+            const uint32_t sliceB = (uint32_t)(s_blk[sh.b + 1] - kb) * 2;
+            const int r8 = lane & 7;
+            const int tok = recs[q].tok[r8];
+            int32_t pg_first[8];
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const int v = __shfl_sync(0xffffffffu, pg4[m], src_lane);
-                    if (m == (b >> 1)) pg = v;
-                }
-                const bool ok = 16 * b + (lane & 15) < rows && pg >= 0 && page_ok(pg);
-                fill16(ring_s + slot * stageB, &full[slot], pool + (int64_t)(ok ? pg : 0) * d, ok, zero_rest);
-                ++sc;
-            }
-        };
-        int k = -1, c = 0, nch = 0;      // current unit: item ordinal, rank chunk, chunks of the item
-        Item it{};
-        int ipj = 0;                     // projection slot of the current item
-        int tl = 0;                      // lane l: token id of the item's token l & 15
-        bool tv = false;
-        bool have_prev = false;          // previous unit, whose expand data follows
-        Item pit{};
-        int pc = 0, ptl = 0, ppj = 0;
-        bool ptv = false;
-        int32_t ppb[4] = {-1, -1, -1, -1};
-        // The next item's metadata is fetched ahead in two steps, its record while the
-        // current item's A^T rows go out, then its tokens and the page-table entries of its
-        // first unit after the previous unit's B rows, so an item boundary waits for no load.
-        bool nvalid = false;
-        Item nit{};
-        int ntok = 0, npj = 0;
-        int32_t npa[4] = {-1, -1, -1, -1}, npb[4] = {-1, -1, -1, -1};
-        auto fetch_record = [&](int kk) {
-            const int i = item_of(kk);
-            nvalid = i < n_items;
-            if (nvalid) {
-                nit = load_item(a.L.items + i / NP);   // not used before fetch_rest: no wait here
-                npj = i % NP;
-            }
-        };
-        auto fetch_rest = [&]() {
-            if (!nvalid) return;
-            nit.pt_base += (int64_t)a.proj[npj] * 2 * nit.rank;   // this projection's page table
-            ntok = lane < nit.nt ? __ldcg(a.L.tok_order + nit.tok_begin + nit.t0 + lane) : 0;
-            const int rows = min(kRC, nit.rank);
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int r = lane + 32 * m;
-                npa[m] = -1;
-                npb[m] = -1;
-                if (r < rows) {
-                    npa[m] = __ldcg(a.pv.pt_arena + nit.pt_base + r);
-                    npb[m] = __ldcg(a.pv.pt_arena + nit.pt_base + nit.rank + r);
-                }
-            }
-        };
-        fetch_record(0);
-        fetch_rest();
-        for (;;) {
-            bool have = true;
-            bool fresh = false;          // the unit is its item's first: its entries came ahead
-            if (c == nch) {
-                ++k;
-                if (!nvalid) {
-                    have = false;
-                } else {
-                    it = nit;
-                    ipj = npj;
-                    const int tok = ntok;
-                    tl = __shfl_sync(0xffffffffu, tok, lane & 15);
-                    tv = (lane & 15) < it.nt;
-                    c = 0;
-                    nch = ceil_div(it.rank, kRC);
-                    fresh = true;
-                    // the item's record and x rows, once item k-2's shrink is done with buffer k&1
-                    if (k >= 2) wait_phase<false>(&xfree[k & 1], ((k >> 1) - 1) & 1, abort, status);
-                    if (lane == 0) {
-                        rec_it[k & 1] = it;
-                        rec_pj[k & 1] = ipj;
+            for (int j = 0; j < 8; ++j) pg_first[j] = recs[q].pg[8 * j + r8];
+            release_record(k);
+            // lane r < 8 copies row r of a stage from src (when ok), rows left out zero-filled
+            // when zero_rest; completion on the slot's full barrier
+            auto issue = [&](const __half *src, bool ok, bool zero_rest) {
+                if (sc >= NST) wait_phase<false>(&empty[pos.slot], pos.phase ^ 1u, abort, status);
+                const uint32_t dst = ring_s + pos.slot * stageB;
+                const bool mine = ok && lane < 8;
+                const uint32_t m = __ballot_sync(0xffffffffu, mine);
+                if (mine && !*abort) bulk_g2s_s(dst + lane * P, src + kb, sliceB, &full[pos.slot]);
+                if (zero_rest && (m & 0xffu) != 0xffu) {
+                    for (int r = 0; r < 8; ++r) {
+                        if ((m >> r) & 1u) continue;
+                        for (uint32_t o = lane * 16; o < sliceB; o += 32 * 16)
+                            *reinterpret_cast<uint4 *>(ring + pos.slot * stageB + r * P + o) = make_uint4(0, 0, 0, 0);
                     }
-                    if (lane < kTok) rec_tok[(k & 1) * kTok + lane] = tok;
-                    fill16(xbuf_s + (k & 1) * stageB, &full_x[k & 1], a.x[ipj] + (int64_t)tl * d, tv, false);
+                    tc::fence_proxy_async_smem();   // before later bulk copies land in the same rows
                 }
-            }
-            int32_t pb[4] = {-1, -1, -1, -1};
-            if (have) {
-                // shrink data of the unit: its A^T rows
-                const int rc0 = c * kRC, rows = min(kRC, it.rank - rc0);
-                int32_t pa[4];
+                __syncwarp();
+                if (lane == 0) mbar_arrive_expect_tx(&full[pos.slot], *abort ? 0u : (uint32_t)__popc(m) * sliceB);
+            };
+            // token stage
+            if ((int)(sc % kCopyWarps) == cw)
+                issue((sh.expand ? a.y[sh.pj] : a.x[sh.pj]) + (int64_t)tok * d, r8 < sh.nt, false);
+            ++sc;
+            pos.next();
+            // rank stages
+#pragma unroll 1
+            for (int i = 0; i < sh.nch; ++i) {
+                const int rows = chunk_rows(u, sh, i);
+                const int ns = ceil_div(rows, 8);
+                const int64_t base = sh.expand ? u.pt_base + u.rank + (int64_t)kRC * i : u.pt_base + (int64_t)kRC * sh.c;
+#pragma unroll 1
+                for (int s = 0; s < ns; ++s, ++sc, pos.next()) {
+                    if ((int)(sc % kCopyWarps) != cw) continue;
+                    const int row = 8 * s + r8;
+                    int32_t pg = -1;
+                    if (row < rows) {
+                        if (i == 0) {
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const int r = lane + 32 * m;
-                    if (fresh) {
-                        pa[m] = npa[m];
-                        pb[m] = npb[m];
-                    } else {
-                        pa[m] = -1;
-                        if (r < rows) {
-                            pa[m] = __ldcg(a.pv.pt_arena + it.pt_base + rc0 + r);
-                            pb[m] = __ldcg(a.pv.pt_arena + it.pt_base + it.rank + rc0 + r);
+                            for (int j = 0; j < 8; ++j)
+                                if (j == s) pg = pg_first[j];
+                        } else {
+                            pg = __ldcg(pt + base + row);
                         }
                     }
+                    bool ok = row < rows && pg >= 0;
+                    if (ok && pg >= a.pv.num_pages) {
+                        set_status(status, SLORA_DEV_BAD_PAGE);
+                        ok = false;
+                    }
+                    if (lane < 8 && row < rows && pg < 0) set_status(status, SLORA_DEV_BAD_PAGE);
+                    issue(pool + (int64_t)(ok ? pg : 0) * d, ok, sh.expand != 0);
                 }
-                emit_blocks(rows, pa, false);
-                if (fresh) fetch_record(k + 1);
             }
-            if (have_prev) {
-                // expand data of the previous unit: the item's y0 rows (first unit) and B rows
-                if (pc == 0) {
-                    const uint32_t slot = next_slot();
-                    fill16(ring_s + slot * stageB, &full[slot], a.y[ppj] + (int64_t)ptl * d, ptv, false);
-                    ++sc;
-                }
-                emit_blocks(min(kRC, pit.rank - pc * kRC), ppb, true);
-            }
-            if (have && fresh) fetch_rest();
+        }
+        // no bulk copy may land after the CTA exits: wait (bounded) for this warp's last ones
+        for (uint32_t i = 0; i < NST && i < sc; ++i) {
+            const uint32_t g = sc - 1 - i;
+            if ((int)(g % kCopyWarps) == cw) mbar_wait_bounded(&full[g % NST], (g / NST) & 1, status);
+        }
+        return;
+    }
+
+    if (warp == kWarpGather) {
+        // ============================ gather (expand units ahead) ===========================
+        // For every expand unit, waits until the partial words of every hidden block carry
+        // this launch's tag, sums them in block order and rounds u to fp16 once, into the
+        // next u buffer.  Lane l covers tokens l>>4 (+2 per round), columns 4 (l & 15) .. +3.
+        const uint32_t tag = a.tag;
+        uint32_t uj = 0;   // u buffers filled
+        for (int k = 0;; ++k) {
+            Unit u;
+            const bool have = take_record(k, u);
+            release_record(k);
             if (!have) break;
-            have_prev = true;
-            pit = it;
-            pc = c;
-            ptl = tl;
-            ptv = tv;
-            ppj = ipj;
+            if (!(u.packed & 32u)) continue;
+            const int nt = (int)(u.packed & 31u) + 1;
+            const int nch = ceil_div(u.rank, kRC);
+            const int j4 = 4 * (lane & 15);
+#pragma unroll 1
+            for (int c = 0; c < nch; ++c) {
+                const uint32_t qu = uj % QU;
+                if (uj >= QU) wait_phase<false>(&uempty[qu], ((uj / QU) - 1) & 1, abort, status);
+                const int rows = min(kRC, u.rank - kRC * c);
+                const unsigned long long *src = a.L.upart + u.uoff + (int64_t)c * NB * nt * kRC;
+                __half *ub = ubuf + qu * kTok * kUPitch;
+#pragma unroll 1
+                for (int t0 = 0; t0 < nt; t0 += 2) {
+                    const int t = t0 + (lane >> 4);
+                    const int nv = (t < nt && j4 < rows) ? min(4, rows - j4) : 0;   // this lane's values
+                    const unsigned long long *sp = src + (int64_t)t * kRC + j4;   // block 0; blocks nt*kRC apart
+                    const int bstride = nt * kRC;
+                    float wv[kMaxBlocks][4];
+                    // poll until every word carries the tag (each was written once, by its
+                    // shrink unit, earlier in the list); bounded in time
+                    uint64_t t_start = 0;
+                    for (uint32_t it = 0;; ++it) {
+                        bool ready = true;
 #pragma unroll
-            for (int m = 0; m < 4; ++m) ppb[m] = pb[m];
-            ++c;
+                        for (int bb = 0; bb < kMaxBlocks; ++bb)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const unsigned long long w = (bb < NB && e < nv) ? ld_word(sp + bb * bstride + e)
+                                                                                 : ((unsigned long long)tag << 32);
+                                ready &= (uint32_t)(w >> 32) == tag;
+                                wv[bb][e] = __uint_as_float((uint32_t)w);
+                            }
+                        if (__all_sync(0xffffffffu, ready)) break;
+                        if (*abort) break;
+                        __nanosleep(128);
+                        if (it == kPollsBeforeTimer) t_start = global_timer_ns();
+                        if (it > kPollsBeforeTimer && (it & 15u) == 0 && global_timer_ns() - t_start > kWaitLimitNs) {
+                            set_status(status, SLORA_DEV_TIMEOUT);
+                            *abort = 1;
+                            break;
+                        }
+                    }
+                    if (t < nt) {
+                        float sm[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            float v = 0.f;
+#pragma unroll
+                            for (int bb = 0; bb < kMaxBlocks; ++bb)
+                                if (bb < NB) v += wv[bb][e];
+                            sm[e] = e < nv ? v : 0.f;
+                        }
+                        __half2 h[2];
+                        h[0] = __floats2half2_rn(sm[0], sm[1]);
+                        h[1] = __floats2half2_rn(sm[2], sm[3]);
+                        *reinterpret_cast<uint2 *>(ub + t * kUPitch + j4) = *reinterpret_cast<const uint2 *>(h);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ufull[qu]);
+                ++uj;
+            }
         }
         return;
     }
 
     // ===================================== consumers =====================================
     const int w = warp;
-    if (w == 0 && bal && n_items > ncl) {
-        // while the first data is in flight
-        balance_items(a.L.items, n_items, NP, ncl, cl, lane, s_seq, s_cost, s_load);
+    const int q4 = lane >> 3, rr = lane & 7, gid = lane >> 2, tig = lane & 3;
+    RingPos cur{0, 0};   // the next stage to consume
+    uint32_t uj = 0;     // u buffers consumed
+    auto wait_at = [&](const RingPos &p) { wait_phase<false>(&full[p.slot], p.phase, abort, status); };
+    // every consumer warp's shared-memory writes before it are visible to all of them after
+    // it; an mbarrier rather than a named barrier so that after an abort no warp waits for
+    // warps that have left
+    uint32_t cph = 0;
+    auto consumers_sync = [&]() {
         __syncwarp();
-        if (lane == 0) mbar_arrive(&seq_bar);
-    }
-    const int q = lane >> 3, rr = lane & 7, gid = lane >> 2, tig = lane & 3;
-    // this warp's output columns in the expand: column pairs [pp0, pp1) of 16 columns
-    const int npair = KS / 16;
-    const int pp0 = (w * npair) / kConsumerWarps, pp1 = ((w + 1) * npair) / kConsumerWarps;
-    uint32_t sc = 0;    // stages consumed
-    uint32_t un = 0;    // units shrunk
-    int k = -1, c = 0, nch = 0;
-    Item it{};
-    int ipj = 0;                        // projection slot of the current item
-    int tk[2] = {0, 0};                 // token ids of rows gid, gid+8 of the current item
-    bool have_prev = false;
-    Item pit{};
-    int pc = 0, ppj = 0, ptk[2] = {0, 0};
-    float acc[16][4];
-    uint32_t yv[2][16];                 // y0 of the item being expanded: [token half][n-block], half2 bits
-#pragma unroll
-    for (int n8 = 0; n8 < 16; ++n8)
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            acc[n8][e] = 0.f;
-    for (;;) {
-        bool have = true;
-        if (c == nch) {
-            ++k;
-            const int i = item_of(k);
-            if (i >= n_items) {
-                have = false;
-            } else {
-                wait_phase<false>(&full_x[k & 1], (k >> 1) & 1, abort, status);
-                it = rec_it[k & 1];
-                ipj = rec_pj[k & 1];
-                tk[0] = rec_tok[(k & 1) * kTok + gid];
-                tk[1] = rec_tok[(k & 1) * kTok + gid + 8];
-                c = 0;
-                nch = ceil_div(it.rank, kRC);
-            }
-        }
-        if (have) {
-            // ---- shrink of unit un: block b (16 rank rows) of the unit goes to warps
-            //      b + nb*g, which split the CTA's K slice into ksplit = 8/nb parts ----
-            const uint32_t par = un & 1;
-            if (un >= 2) wait_phase<true>(&consumed[par], ((un >> 1) - 1) & 1, abort, status);
-            float *mypart = part + par * (kTok * kRC);
-            const uint32_t xs = xbuf_s + (k & 1) * stageB;
-            const int rows = min(kRC, it.rank - c * kRC), nb = ceil_div(rows, 16);
-            const int ksplit = kConsumerWarps / nb, wb = w % nb, wg = w / nb;
+        if (lane == 0) mbar_arrive(cbar);
+        wait_phase<false>(cbar, cph, abort, status);
+        cph ^= 1u;
+    };
+    float *region = ptmp + w * kRegionFloats;   // this warp's scratch: shrink partials or y0 values
+    for (int k = 0;; ++k) {
+        const uint32_t q = k % QD;
+        Unit u;
+        const bool have = take_record(k, u);
+        const int tk = recs[q].tok[gid];
+        release_record(k);
+        if (!have) break;
+        const UnitShape sh_ = unit_shape(u);
+        const int nt = sh_.nt;
+        const int kb = s_blk[sh_.b], KS = s_blk[sh_.b + 1] - kb;
+        const RingPos tpos = cur;   // the token stage
+        cur.next();
+        wait_at(tpos);
+        const uint32_t tstage = ring_s + tpos.slot * stageB;
+
+        if (!sh_.expand) {
+            // ---- shrink: u^T = A^T x^T, rank rows on the MMA's M and tokens on its N.  Warp w
+            //      contracts K steps [w n/8, (w+1) n/8) of the block for every 16-row block of
+            //      the chunk; the 8 warp partials are summed in warp order ----
+            const int rows = chunk_rows(u, sh_, 0), nb = ceil_div(rows, 16), ns = ceil_div(rows, 8);
             const int nsteps = KS / 16;
-            const int ks0 = (wg * nsteps) / ksplit, ks1 = ((wg + 1) * nsteps) / ksplit;
-            for (int b = 0; b < nb; ++b) {
-                const uint32_t s = sc + b, slot = s % NST;
-                wait_phase<false>(&full[slot], (s / NST) & 1, abort, status);
-                if (b == wb && wg < ksplit) {
-                    // two accumulators per n-block (even / odd K steps) halve the MMA chains
-                    float pacc[2][2][4] = {};
-                    const uint32_t sb = ring_s + slot * stageB;
-                    for (int st = ks0; st < ks1; st += 2) {
+            const int ks0 = (w * nsteps) / kConsumerWarps, nks = ((w + 1) * nsteps) / kConsumerWarps - ks0;
+            uint32_t xf[kXs / 2][4];   // this warp's x fragments (the MMA's B operand), two K steps each
+            {
+                const uint32_t trow = tstage + rr * P;
 #pragma unroll
-                        for (int h2 = 0; h2 < 2; ++h2) {
-                            if (st + h2 < ks1) {
-                                const int k16 = 16 * (st + h2);
-                                uint32_t af[4], bf[4];
-                                ldsm_x4(xs + (rr + 8 * (q & 1)) * P + (k16 + 8 * (q >> 1)) * 2, af);   // token rows
-                                ldsm_x4(sb + (rr + 8 * (q >> 1)) * P + (k16 + 8 * (q & 1)) * 2, bf);   // A^T rows
-                                mma16816(pacc[h2][0], af, bf[0], bf[1]);
-                                mma16816(pacc[h2][1], af, bf[2], bf[3]);
-                            }
-                        }
+                for (int i = 0; i < kXs / 2; ++i)
+                    if (2 * i < nks) ldsm_x4(trow + (16 * (ks0 + 2 * i) + 8 * q4) * 2, xf[i]);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[tpos.slot]);
+#pragma unroll 1
+            for (int blk = 0; blk < nb; ++blk) {
+                const RingPos lo = cur;
+                cur.next();
+                const bool has_hi = 2 * blk + 1 < ns;
+                const RingPos hi = cur;
+                if (has_hi) cur.next();
+                wait_at(lo);
+                if (has_hi) wait_at(hi);
+                // A operand rows: 0-7 from stage lo, 8-15 from stage hi (or zeros)
+                const uint32_t arow = (q4 & 1) ? (has_hi ? ring_s + hi.slot * stageB + rr * P : zrow_s)
+                                               : ring_s + lo.slot * stageB + rr * P;
+                float pacc[2][4] = {};   // even / odd K steps: two independent MMA chains
+#pragma unroll
+                for (int i = 0; i < kXs; ++i) {
+                    if (i < nks) {
+                        uint32_t af[4];
+                        ldsm_x4(arow + (16 * (ks0 + i) + 8 * (q4 >> 1)) * 2, af);   // A^T rows
+                        mma16816(pacc[i & 1], af, xf[i >> 1][2 * (i & 1)], xf[i >> 1][2 * (i & 1) + 1]);
                     }
-                    const int ld = 16 * nb;
-#pragma unroll
-                    for (int nb8 = 0; nb8 < 2; ++nb8)
-#pragma unroll
-                        for (int h = 0; h < 2; ++h)
-                            *reinterpret_cast<float2 *>(ptmp + (wg * kTok + gid + 8 * h) * ld + 16 * b + 8 * nb8 + 2 * tig) =
-                                make_float2(pacc[0][nb8][2 * h] + pacc[1][nb8][2 * h],
-                                            pacc[0][nb8][2 * h + 1] + pacc[1][nb8][2 * h + 1]);
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[slot]);
+                if (lane == 0) {
+                    mbar_arrive(&empty[lo.slot]);
+                    if (has_hi) mbar_arrive(&empty[hi.slot]);
+                }
+                // rows gid, gid + 8 of the block; tokens 2 tig, 2 tig + 1
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    region[(2 * tig) * kRC + 16 * blk + gid + 8 * h] = pacc[0][2 * h] + pacc[1][2 * h];
+                    region[(2 * tig + 1) * kRC + 16 * blk + gid + 8 * h] = pacc[0][2 * h + 1] + pacc[1][2 * h + 1];
+                }
             }
-            sc += nb;
             consumers_sync();   // every warp's partials are written
             {
-                // this CTA's partial: the ksplit parts summed in order
+                // the unit's partial (the 8 warp partials summed in order), one tagged word per
+                // value, straight to the scratch the gather warp polls
+                unsigned long long *dst = a.L.upart + u.uoff + ((int64_t)sh_.c * NB + sh_.b) * nt * kRC;
                 const int ld = 16 * nb;
-                for (int e = tid; e < kTok * ld; e += kConsumers) {
+                for (int e = tid; e < nt * ld; e += kConsumers) {
                     const int t = e / ld, j = e - t * ld;
                     float v = 0.f;
-                    for (int g = 0; g < ksplit; ++g)
-                        v += ptmp[(g * kTok + t) * ld + j];
-                    mypart[t * kRC + j] = v;
+#pragma unroll
+                    for (int g = 0; g < kConsumerWarps; ++g)
+                        v += ptmp[g * kRegionFloats + t * kRC + j];
+                    st_word(dst + t * kRC + j, v, a.tag);
                 }
             }
-            consumers_sync();   // this CTA's partials of the unit are written
-            if (tid == 0) {
-                if (c == nch - 1) mbar_arrive(&xfree[k & 1]);   // the item's x rows are no longer read
-                mbar_arrive(&pwrit[par]);                       // relayed to the cluster by the signal warp
-            }
+            consumers_sync();   // the partials are read: the regions are free for the next unit
+            continue;
         }
-        if (have_prev) {
-            // ---- expand of unit un-1 ----
-            const uint32_t pu = un - 1, ppar = pu & 1;
-            const int rows = min(kRC, pit.rank - pc * kRC), nb = ceil_div(rows, 16);
-            wait_phase<true>(&ready[ppar], (pu >> 1) & 1, abort, status);
-            consumers_sync();   // the previous expand is done reading u
-            {
-                // u = sum of the C partials in CTA order, rounded to fp16 once.  A thread
-                // takes up to two 4-element vectors of the unit and issues the 16-byte
-                // remote loads of four CTAs at once (a second round only for clusters of
-                // more than four), so the exchange costs one or two remote round trips.
-                const uint32_t pbase = smem_u32(part + ppar * (kTok * kRC));
-                const int vpr = 4 * nb;                 // vectors per token row
-                const int nv = kTok * vpr;
-                static_assert(kTok * kRC / 4 <= 2 * kConsumers, "two vectors per thread");
-                float4 sum[2];
-                int vt[2], vj[2];
+
+        // ---- expand: y = u B over the block's columns, the item's tokens on the MMA's M (rows
+        //      0-7; rows 8-15 zero) and the columns on its N; warp w takes the column pairs
+        //      [pp0, pp1) (16 columns each), over the rank chunks ----
+        const int npair = KS / 16;
+        const int pp0 = (w * npair) / kConsumerWarps, pp1 = ((w + 1) * npair) / kConsumerWarps;
+        // the y0 values of this lane's outputs (token gid, columns 16 (pp0+p) + 8 n2 + 2 tig, +1),
+        // kept in the warp's region as [value][lane] until the epilogue, so the token stage is
+        // free at once
+        uint32_t *yv = reinterpret_cast<uint32_t *>(region);
+        {
+            const uint8_t *trow = ring + tpos.slot * stageB + gid * P;
 #pragma unroll
-                for (int m = 0; m < 2; ++m) {
-                    const int e = tid + m * kConsumers;
-                    vt[m] = e / vpr;
-                    vj[m] = e - vt[m] * vpr;
-                    sum[m] = make_float4(0.f, 0.f, 0.f, 0.f);
-                }
+            for (int p = 0; p < kPairs; ++p)
 #pragma unroll
-                for (int c0 = 0; c0 < kMaxCluster; c0 += 4) {
-                    if (c0 >= (int)C) break;
-                    float4 v[2][4];
+                for (int n2 = 0; n2 < 2; ++n2)
+                    if (pp0 + p < pp1)
+                        yv[(2 * p + n2) * 32 + lane] =
+                            *reinterpret_cast<const uint32_t *>(trow + (16 * (pp0 + p) + 8 * n2 + 2 * tig) * 2);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[tpos.slot]);
+        }
+        float acc[2 * kPairs][4];
 #pragma unroll
-                    for (int m = 0; m < 2; ++m) {
-                        const bool ok = tid + m * kConsumers < nv;
-                        const uint32_t off = (uint32_t)(vt[m] * kRC + vj[m] * 4) * 4;
+        for (int n8 = 0; n8 < 2 * kPairs; ++n8)
 #pragma unroll
-                        for (int cc = 0; cc < 4; ++cc)
-                            v[m][cc] = (ok && c0 + cc < (int)C) ? ld_cluster_v4(mapa(pbase + off, c0 + cc))
-                                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
-#pragma unroll
-                    for (int m = 0; m < 2; ++m)
-#pragma unroll
-                        for (int cc = 0; cc < 4; ++cc) {   // CTA order; absent CTAs add zero
-                            sum[m].x += v[m][cc].x;
-                            sum[m].y += v[m][cc].y;
-                            sum[m].z += v[m][cc].z;
-                            sum[m].w += v[m][cc].w;
-                        }
-                }
-#pragma unroll
-                for (int m = 0; m < 2; ++m) {
-                    if (tid + m * kConsumers < nv) {
-                        const int j = vj[m] * 4;
-                        __half2 h[2];
-                        h[0] = __floats2half2_rn(j < rows ? sum[m].x : 0.f, j + 1 < rows ? sum[m].y : 0.f);
-                        h[1] = __floats2half2_rn(j + 2 < rows ? sum[m].z : 0.f, j + 3 < rows ? sum[m].w : 0.f);
-                        *reinterpret_cast<uint2 *>(ubuf + vt[m] * kUPitch + j) = *reinterpret_cast<const uint2 *>(h);
-                    }
-                }
-            }
-            consumers_sync();   // u of the unit is in place; the partials have been read
-            if (tid == 0) mbar_arrive(&rdone[ppar]);   // relayed to the cluster by the signal warp
-            if (pc == 0) {
-                // the item's y0 rows: into registers, and a fresh accumulator
-                const uint32_t slot = sc % NST;
-                wait_phase<false>(&full[slot], (sc / NST) & 1, abort, status);
-                const uint8_t *st = ring + slot * stageB;
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
-#pragma unroll
-                    for (int p = 0; p < 8; ++p)
-#pragma unroll
-                        for (int n2 = 0; n2 < 2; ++n2)
-                            yv[h][2 * p + n2] = pp0 + p < pp1 ? *reinterpret_cast<const uint32_t *>(
-                                                                    st + (gid + 8 * h) * P + (16 * (pp0 + p) + 8 * n2 + 2 * tig) * 2)
-                                                              : 0u;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[slot]);
-                ++sc;
-#pragma unroll
-                for (int n8 = 0; n8 < 16; ++n8)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        acc[n8][e] = 0.f;
-            }
-            // every warp its column pairs, over the unit's B blocks
-            for (int b = 0; b < nb; ++b) {
-                const uint32_t s = sc + b, slot = s % NST;
-                wait_phase<false>(&full[slot], (s / NST) & 1, abort, status);
-                const uint32_t sb = ring_s + slot * stageB;
+            for (int e = 0; e < 4; ++e)
+                acc[n8][e] = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < sh_.nch; ++c) {
+            const uint32_t qu = uj % QU;
+            wait_phase<false>(&ufull[qu], (uj / QU) & 1, abort, status);
+            const int rows = chunk_rows(u, sh_, c), nb = ceil_div(rows, 16), ns = ceil_div(rows, 8);
+            const uint32_t ub = ubuf_s + qu * (kTok * kUPitch * 2);
+#pragma unroll 1
+            for (int blk = 0; blk < nb; ++blk) {
+                const RingPos lo = cur;
+                cur.next();
+                const bool has_hi = 2 * blk + 1 < ns;
+                const RingPos hi = cur;
+                if (has_hi) cur.next();
+                wait_at(lo);
+                if (has_hi) wait_at(hi);
+                // u rows (the MMA's A operand): the item's tokens in rows 0-7, zeros in rows 8-15
                 uint32_t af[4];
-                ldsm_x4(ubuf_s + ((rr + 8 * (q & 1)) * kUPitch + 16 * b + 8 * (q >> 1)) * 2, af);   // u rows
+                ldsm_x4((q4 & 1) ? zrow_s + (16 * blk + 8 * (q4 >> 1)) * 2
+                                 : ub + (rr * kUPitch + 16 * blk + 8 * (q4 >> 1)) * 2, af);
+                // B rows (the MMA's B operand, transposed on load): 0-7 from stage lo, 8-15 from hi
+                const uint32_t brow = (q4 & 1) ? (has_hi ? ring_s + hi.slot * stageB + rr * P : zrow_s)
+                                               : ring_s + lo.slot * stageB + rr * P;
 #pragma unroll
-                for (int p = 0; p < 8; ++p) {
+                for (int p = 0; p < kPairs; ++p) {
                     if (pp0 + p < pp1) {
                         uint32_t bf[4];
-                        ldsm_x4_t(sb + (rr + 8 * (q & 1)) * P + (16 * (pp0 + p) + 8 * (q >> 1)) * 2, bf);   // B rows
+                        ldsm_x4_t(brow + (16 * (pp0 + p) + 8 * (q4 >> 1)) * 2, bf);
                         mma16816(acc[2 * p], af, bf[0], bf[1]);
                         mma16816(acc[2 * p + 1], af, bf[2], bf[3]);
                     }
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[slot]);
+                if (lane == 0) {
+                    mbar_arrive(&empty[lo.slot]);
+                    if (has_hi) mbar_arrive(&empty[hi.slot]);
+                }
             }
-            sc += nb;
-            if (pc == ceil_div(pit.rank, kRC) - 1 && !*abort) {
-                // ---- epilogue of the item: y = y0 + s * acc over this CTA's columns ----
-                const float scl = a.scaling ? a.scaling[pit.adapter] : pit.scaling;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&uempty[qu]);
+            ++uj;
+        }
+        if (!*abort && gid < nt) {
+            // ---- epilogue: y = y0 + s * acc for token gid: columns 2 tig, 2 tig + 1 of each n-tile ----
+            const float scl = u.scaling;
+            __half *yrow = a.y[sh_.pj] + (int64_t)tk * d + kb;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int t = gid + 8 * h;
-                    if (t < pit.nt) {
-                        __half *yrow = a.y[ppj] + (int64_t)ptk[h] * d + kb;
+            for (int p = 0; p < kPairs; ++p) {
+                if (pp0 + p < pp1) {
 #pragma unroll
-                        for (int p = 0; p < 8; ++p) {
-                            if (pp0 + p < pp1) {
-#pragma unroll
-                                for (int n2 = 0; n2 < 2; ++n2) {
-                                    const int col = 16 * (pp0 + p) + 8 * n2 + 2 * tig;
-                                    const float2 y0 = __half22float2(*reinterpret_cast<const __half2 *>(&yv[h][2 * p + n2]));
-                                    const float *ac = acc[2 * p + n2];
-                                    *reinterpret_cast<__half2 *>(yrow + col) =
-                                        __floats2half2_rn(fmaf(scl, ac[2 * h], y0.x), fmaf(scl, ac[2 * h + 1], y0.y));
-                                }
-                            }
-                        }
+                    for (int n2 = 0; n2 < 2; ++n2) {
+                        const int col = 16 * (pp0 + p) + 8 * n2 + 2 * tig;
+                        const float2 y0 = __half22float2(*reinterpret_cast<const __half2 *>(&yv[(2 * p + n2) * 32 + lane]));
+                        const float *ac = acc[2 * p + n2];
+                        *reinterpret_cast<__half2 *>(yrow + col) =
+                            __floats2half2_rn(fmaf(scl, ac[0], y0.x), fmaf(scl, ac[1], y0.y));
                     }
                 }
             }
         }
-        if (!have) break;
-        have_prev = true;
-        pit = it;
-        pc = c;
-        ppj = ipj;
-        ptk[0] = tk[0];
-        ptk[1] = tk[1];
-        ++c;
-        ++un;
     }
-    // the signal warp keeps the CTA alive until no other CTA may still read its partials
 }
 
 }  // namespace
 
-size_t plan_scratch_bytes(int32_t T, int32_t max_rank, int32_t hidden, int32_t max_adapters)
+size_t plan_scratch_bytes(int32_t T, int32_t max_rank, int32_t hidden, int32_t max_adapters, int32_t n_proj)
 {
-    (void)max_rank;
-    (void)hidden;
     size_t total = 0;
     const int32_t chunk = plan_chunk(max_adapters);
     const int32_t cap = T < chunk ? T : chunk;
-    carve(nullptr, cap, &total);
+    carve(nullptr, cap, n_proj < 1 ? 1 : n_proj, n_blocks(hidden), max_rank, &total);
     return total;
 }
 
-// CTAs per cluster for a hidden size: slices of at most kMaxSlice elements.
-inline int delta_cluster(int hidden) { return ceil_div(hidden, kMaxSlice); }
+// Bytes per row of a stage or token buffer for a hidden size: the widest block + 16 (the
+// padding keeps the rows' fragment loads free of bank conflicts).
 inline int delta_pitch(int hidden)
 {
-    const int C = delta_cluster(hidden);
-    return 2 * 16 * ceil_div(hidden / 16, C) + 16;
+    const int NB = n_blocks(hidden);
+    return 2 * 16 * ceil_div(hidden / 16, NB) + 16;
 }
 inline size_t delta_smem_bytes(int hidden)
 {
-    const size_t stage = (size_t)kTok * delta_pitch(hidden);
-    return (NST + 2) * stage + 2 * (size_t)kTok * kRC * 4 + (size_t)kPtmpFloats * 4 + (size_t)kTok * kUPitch * 2 + 2 * sizeof(Item) +
-           2 * kTok * 4 + 2 * 4 + (2 * NST + 13) * 8;
+    const size_t P = (size_t)delta_pitch(hidden);
+    return NST * 8 * P + P + (size_t)kPtmpFloats * 4 + (size_t)QU * kTok * kUPitch * 2 + QD * sizeof(Rec) +
+           (2 * NST + 2 * QD + 2 * QU + 1) * 8;
 }
 
-// Kernel attributes and the delta grid's resident clusters, per device (the attributes
-// are per-device state; calls may come from several threads).
+// Kernel attributes and the delta grid's resident CTAs, per device (the attributes are
+// per-device state; calls may come from several threads).
 struct DeltaLaunchState {
     bool attrs = false;
     int occ_hidden = -1;
-    int occ_clusters = 1;
+    int occ_blocks = 1;
 };
 constexpr int kMaxLaunchDevices = 64;
 std::mutex g_delta_mu;
@@ -1126,14 +1154,16 @@ DeltaLaunchState g_delta_state[kMaxLaunchDevices];
 
 cudaError_t launch_lora_apply(const PoolView &pv, const ProjList &pl, int32_t T, const int32_t *idx,
                               const int32_t *seg_indptr, int32_t n_seg, const float *scaling,
-                              const PlanScratch &scratch, int num_sms, cudaStream_t stream, int *launches,
+                              PlanScratch &scratch, int num_sms, cudaStream_t stream, int *launches,
                               cudaEvent_t after_plan)
 {
-    if (pv.hidden > kMaxCluster * kMaxSlice || pl.n < 1 || pl.n > kMaxApplyProj) return cudaErrorInvalidValue;
+    if (pv.hidden > kMaxBlocks * kMaxSlice || pl.n < 1 || pl.n > kMaxApplyProj || pl.n > scratch.cap_proj)
+        return cudaErrorInvalidValue;
     int device = 0;
     cudaError_t de = cudaGetDevice(&device);
     if (de != cudaSuccess) return de;
     if (device < 0 || device >= kMaxLaunchDevices) return cudaErrorInvalidDevice;
+    const size_t dsmem = delta_smem_bytes(pv.hidden);
     std::unique_lock<std::mutex> lk(g_delta_mu);
     DeltaLaunchState &ls = g_delta_state[device];
     if (!ls.attrs) {
@@ -1148,46 +1178,61 @@ cudaError_t launch_lora_apply(const PoolView &pv, const ProjList &pl, int32_t T,
         if (e != cudaSuccess) return e;
         ls.attrs = true;
     }
-    const int C = delta_cluster(pv.hidden);
-    const size_t dsmem = delta_smem_bytes(pv.hidden);
+    if (pv.hidden != ls.occ_hidden) {
+        int nb = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, delta_kernel, kThreads, dsmem);
+        if (e != cudaSuccess) return e;
+        ls.occ_blocks = nb > 0 ? nb : 1;
+        ls.occ_hidden = pv.hidden;
+    }
+    const int occ_blocks = ls.occ_blocks;
+    lk.unlock();
 
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = C;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
 
     cudaLaunchConfig_t cfg2 = {};
+    cfg2.gridDim = dim3(num_sms * occ_blocks);
     cfg2.blockDim = dim3(kThreads);
     cfg2.dynamicSmemBytes = dsmem;
     cfg2.stream = stream;
     cfg2.attrs = attr;
-    cfg2.numAttrs = 2;
-    if (pv.hidden != ls.occ_hidden) {
-        cfg2.gridDim = dim3(C * num_sms);
-        int ncl = 0;
-        cudaError_t e = cudaOccupancyMaxActiveClusters(&ncl, delta_kernel, &cfg2);
-        if (e != cudaSuccess) return e;
-        ls.occ_clusters = ncl > 0 ? ncl : 1;
-        ls.occ_hidden = pv.hidden;
-    }
-    const int occ_clusters = ls.occ_clusters;
-    lk.unlock();
-    cfg2.gridDim = dim3(C * occ_clusters);
+    cfg2.numAttrs = 1;
 
     const int32_t chunk = plan_chunk(pv.max_adapters);
     const int32_t cap = scratch.cap_tokens < chunk ? scratch.cap_tokens : chunk;
-    PlanLayout L = carve(scratch.base, cap, nullptr);
+    const int NB = n_blocks(pv.hidden);
+    PlanLayout L = carve(scratch.base, cap, scratch.cap_proj, NB, scratch.max_rank, nullptr);
 
     for (int32_t tb = 0; tb < T; tb += chunk) {
         const int32_t te = tb + chunk < T ? tb + chunk : T;
+        if (scratch.tag == 0) {
+            // fresh scratch or a wrapped tag sequence: no partial word may carry a tag in use
+            cudaError_t e = cudaMemsetAsync(L.upart, 0, (size_t)L.cap_words * 8, stream);
+            if (e != cudaSuccess) return e;
+        }
+        const uint32_t tag = ++scratch.tag;
+        if (scratch.tag == 0xffffffffu) scratch.tag = 0;
         const int32_t groups = (te - tb) < pv.max_adapters ? (te - tb) : pv.max_adapters;
         int hs = 1024;
         while (hs < 2 * groups && hs < kMaxHash) hs <<= 1;
         const int dcache = pv.max_adapters <= kPlanDirCache ? 1 : 0;
-        PlanArgs pa{pv, idx, T, seg_indptr, n_seg, tb, te, hs, dcache, L};
+        PlanArgs pa{};
+        pa.pv = pv;
+        pa.idx = idx;
+        pa.T = T;
+        pa.seg_indptr = seg_indptr;
+        pa.n_seg = n_seg;
+        pa.t_begin = tb;
+        pa.t_end = te;
+        pa.hash_size = hs;
+        pa.dir_cache = dcache;
+        pa.n_proj = pl.n;
+        pa.nblk = NB;
+        for (int j = 0; j < pl.n; ++j) pa.proj[j] = pl.proj[j];
+        pa.scaling = scaling;
+        pa.L = L;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(1);
         const bool small = te - tb <= kPlanThreadsSmall;
@@ -1210,12 +1255,11 @@ cudaError_t launch_lora_apply(const PoolView &pv, const ProjList &pl, int32_t T,
         for (int j = 0; j < pl.n; ++j) {
             da.x[j] = reinterpret_cast<const __half *>(pl.x[j]);
             da.y[j] = reinterpret_cast<__half *>(pl.y[j]);
-            da.proj[j] = pl.proj[j];
         }
-        da.n_proj = pl.n;
-        da.scaling = scaling;
         da.L = L;
         da.pitch = delta_pitch(pv.hidden);
+        da.nblk = NB;
+        da.tag = tag;
         e = cudaLaunchKernelEx(&cfg2, delta_kernel, da);
         if (e != cudaSuccess) return e;
         *launches += 1;

@@ -10,6 +10,30 @@
 
 namespace slora {
 
+// Makes `device` current for the lifetime of the object, then gives the calling thread
+// back the device it had: every entry point leaves the caller's current device as it
+// found it.
+class DeviceScope {
+public:
+    explicit DeviceScope(int device)
+    {
+        have_prev_ = cudaGetDevice(&prev_) == cudaSuccess;
+        err_ = (have_prev_ && prev_ == device) ? cudaSuccess : cudaSetDevice(device);
+    }
+    ~DeviceScope()
+    {
+        if (have_prev_ && err_ == cudaSuccess) cudaSetDevice(prev_);
+    }
+    DeviceScope(const DeviceScope &) = delete;
+    DeviceScope &operator=(const DeviceScope &) = delete;
+    cudaError_t error() const { return err_; }
+
+private:
+    int prev_ = 0;
+    bool have_prev_ = false;
+    cudaError_t err_ = cudaSuccess;
+};
+
 // One adapter's directory entry on the device, indexed by adapter id.
 // pt_off < 0 means "not resident".  The page table of projection p starts at
 // pt_arena[pt_off + p * 2 * rank]: rank A^T pages, then rank B pages.
@@ -69,14 +93,20 @@ struct PoolView {
     int32_t *status;           // device status word
 };
 
-// Device scratch of the token plan (decode.cu), owned by the pool.
+// Device scratch of the token plan and the decode kernel's partial sums (decode.cu),
+// owned by the pool.
 struct PlanScratch {
     void *base = nullptr;
     size_t bytes = 0;
     int32_t cap_tokens = 0;   // tokens the layout was carved for
     int32_t max_rank = 0;     // largest adapter rank the layout was carved for
+    int32_t cap_proj = 0;     // projections per call the layout was carved for
+    // Tag of the decode kernel's partial sums: each delta launch uses the next value.  0 means
+    // the partial region must be cleared first (fresh scratch, or the sequence wrapped), so a
+    // stale word can never carry a live tag.
+    uint32_t tag = 0;
 };
-size_t plan_scratch_bytes(int32_t T, int32_t max_rank, int32_t hidden, int32_t max_adapters);
+size_t plan_scratch_bytes(int32_t T, int32_t max_rank, int32_t hidden, int32_t max_adapters, int32_t n_proj);
 
 // Segments whose adapter rank is at most this run on the tensor cores (prefill.cu);
 // larger ranks take the decode path.  At most kMaxSegments segments per call.
@@ -108,7 +138,7 @@ cudaError_t launch_prefill(const PoolView &pv, const ProjList &pl, int32_t T, co
 // launch for every projection of the list.
 cudaError_t launch_lora_apply(const PoolView &pv, const ProjList &pl, int32_t T, const int32_t *idx,
                               const int32_t *seg_indptr, int32_t n_seg, const float *scaling,
-                              const PlanScratch &scratch, int num_sms, cudaStream_t stream, int *launches,
+                              PlanScratch &scratch, int num_sms, cudaStream_t stream, int *launches,
                               cudaEvent_t after_plan = nullptr);
 
 // What the hot path needs to know about a pool, for entry points defined outside

@@ -1,8 +1,9 @@
 // slora_lora_apply_noalloc: the batched LoRA delta without any device allocation.
 //
-// slora_lora_apply keeps its token-plan scratch in memory the pool allocates on first
-// use and re-allocates (after a device synchronisation) when a larger batch or a larger
-// adapter rank arrives.  Some callers cannot allow that: code that runs under a host
+// slora_lora_apply keeps its scratch (the token plan, the decode kernel's work list, and
+// the tagged fp32 partial sums of x A that its units exchange) in memory the pool allocates on
+// first use and re-allocates (after a device synchronisation) when a larger batch, more
+// projections per call or a larger adapter rank arrives.  Some callers cannot allow that: code that runs under a host
 // framework whose allocator must own and account for every device byte, or a serving
 // step with a fixed latency budget in which a cudaMalloc / cudaFree (and the device-wide
 // synchronisation around them) is not acceptable.  This entry point serves them: its
@@ -21,14 +22,18 @@
 namespace slora {
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = 512u << 10;   // 512 KiB
+constexpr size_t kNoAllocScratchBytes = 16u << 20;   // 16 MiB
 constexpr int kMaxDevices = 64;
 
-// Shared by every call of the entry point on a device; holds the last call's plan.
+// Shared by every call of the entry point on a device; holds the last call's plan and
+// partial sums.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 std::mutex g_mu;
 void *g_scratch_ptr[kMaxDevices] = {};
+// Per device: the tag sequence of the partial sums in the array (0: clear the array's
+// partial region before the next launch).
+uint32_t g_tag[kMaxDevices] = {};
 
 // Device address of g_noalloc_scratch on `device` (which must be current).  The name of
 // the array in host code is only a host-side stand-in, so the address is fetched once per
@@ -78,28 +83,38 @@ extern "C" slora_status slora_lora_apply_noalloc(slora_pool_t pool, int32_t proj
         return fail(SLORA_ERR_INVALID_ARG, "lora_apply_noalloc: n_seg=%d (at most min(T, %d))", n_seg,
                     kMaxSegments);
     const int32_t max_rank = hp.max_rank > 0 ? hp.max_rank : 1;
-    const size_t need = plan_scratch_bytes(T, max_rank, hp.pv.hidden, hp.pv.max_adapters);
+    const size_t need = plan_scratch_bytes(T, max_rank, hp.pv.hidden, hp.pv.max_adapters, 1);
     if (need > kNoAllocScratchBytes)
         return fail(SLORA_ERR_UNSUPPORTED,
-                    "lora_apply_noalloc: this batch needs %zu bytes of plan scratch (T=%d, largest registered "
+                    "lora_apply_noalloc: this batch needs %zu bytes of scratch (T=%d, largest registered "
                     "rank %d, hidden %d) but the static scratch holds %zu; use slora_lora_apply or a smaller batch",
                     need, T, max_rank, hp.pv.hidden, kNoAllocScratchBytes);
-    cudaError_t e = cudaSetDevice(hp.device);
+    DeviceScope dev_scope(hp.device);   // the caller's current device comes back on return
+    cudaError_t e = dev_scope.error();
     if (e != cudaSuccess)
         return fail(SLORA_ERR_CUDA, "lora_apply_noalloc: cudaSetDevice: %s", cudaGetErrorString(e));
     void *scratch = nullptr;
     if ((st = scratch_for_device(hp.device, &scratch)) != SLORA_OK)
         return st;
-    // The plan kernel writes every scratch field the delta kernel reads (header, claim
-    // counter, per-group counters) before it is read, so nothing needs clearing here.
+    // The plan kernel writes every scratch field the delta kernel reads (the header and its
+    // unit counter, the work list) before the delta kernel starts, and a partial word is
+    // read only once it carries the launch's tag, which no earlier launch used (the
+    // partial region is cleared when the tag sequence starts or wraps; that is a memset on
+    // the stream, not an allocation), so nothing else needs clearing here.
     PlanScratch ps;
     ps.base = scratch;
     ps.bytes = kNoAllocScratchBytes;
     ps.cap_tokens = T;
     ps.max_rank = max_rank;
+    ps.cap_proj = 1;
     int launched = 0;
-    e = launch_lora_apply(hp.pv, pl, T, token_adapter_idx, seg_indptr, n_seg, scaling, ps, hp.num_sms,
-                          (cudaStream_t)stream, &launched);
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        ps.tag = g_tag[hp.device];
+        e = launch_lora_apply(hp.pv, pl, T, token_adapter_idx, seg_indptr, n_seg, scaling, ps, hp.num_sms,
+                              (cudaStream_t)stream, &launched);
+        g_tag[hp.device] = ps.tag;
+    }
     *hp.launches += launched;
     if (e != cudaSuccess)
         return fail(SLORA_ERR_CUDA, "lora_apply_noalloc: launch failed: %s", cudaGetErrorString(e));

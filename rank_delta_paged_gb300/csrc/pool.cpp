@@ -76,11 +76,13 @@ namespace {
                         __FILE__, __LINE__);                                              \
     } while (0)
 
-slora_status set_device(slora_pool *p)
-{
-    CUDA_TRY(cudaSetDevice(p->device));
-    return SLORA_OK;
-}
+// The pool's device is current until the end of the enclosing scope; the caller's
+// current device is restored then.
+#define DEVICE_SCOPE(p)                                                                         \
+    DeviceScope _dev_scope((p)->device);                                                        \
+    if (_dev_scope.error() != cudaSuccess)                                                      \
+        return fail(SLORA_ERR_CUDA, "cudaSetDevice(%d) failed: %s", (p)->device,                 \
+                    cudaGetErrorString(_dev_scope.error()))
 
 bool valid_id(const slora_pool *p, int32_t id) { return id >= 0 && id < p->max_adapters; }
 
@@ -162,8 +164,9 @@ slora_status slora_pool_create(int device, int32_t hidden, int64_t num_pages, in
     auto cuda_fail = [&](cudaError_t e, const char *what) {
         st = fail(SLORA_ERR_CUDA, "pool_create: %s: %s", what, cudaGetErrorString(e));
     };
+    DeviceScope dev_scope(device);
     cudaError_t e;
-    if ((e = cudaSetDevice(device)) != cudaSuccess) cuda_fail(e, "cudaSetDevice");
+    if ((e = dev_scope.error()) != cudaSuccess) cuda_fail(e, "cudaSetDevice");
     else if ((e = cudaMalloc(&p->pool_dev, (size_t)num_pages * (size_t)hidden * 2)) != cudaSuccess) cuda_fail(e, "pool");
     else if ((e = cudaMalloc(&p->pt_dev, (size_t)p->arena_cap * 4)) != cudaSuccess) cuda_fail(e, "page-table arena");
     else if ((e = cudaMalloc(&p->dir_dev, (size_t)max_adapters * sizeof(DirEntry))) != cudaSuccess) cuda_fail(e, "directory");
@@ -187,8 +190,10 @@ slora_status slora_pool_destroy(slora_pool_t p)
 {
     if (!p)
         return SLORA_OK;
-    cudaSetDevice(p->device);
-    free_pool_memory(p);
+    {
+        DeviceScope dev_scope(p->device);
+        free_pool_memory(p);
+    }
     delete p;
     return SLORA_OK;
 }
@@ -223,8 +228,7 @@ slora_status slora_pages_free(slora_pool_t p, int64_t n, const int32_t *pages, s
     slora_status st = p->pages.release(n, pages);
     if (st != SLORA_OK)
         return st;
-    if ((st = set_device(p)) != SLORA_OK)
-        return st;
+    DEVICE_SCOPE(p);
     CUDA_TRY(cudaEventRecord(p->release_event, (cudaStream_t)stream));
     p->release_pending = true;
     return SLORA_OK;
@@ -238,9 +242,8 @@ slora_status slora_adapter_register(slora_pool_t p, int32_t id, int32_t rank, fl
     AdapterRec &a = p->adapters[(size_t)id];
     if (a.registered)
         return fail(SLORA_ERR_ALREADY_REGISTERED, "adapter_register: id=%d", id);
-    slora_status st = set_device(p);
-    if (st != SLORA_OK)
-        return st;
+    DEVICE_SCOPE(p);
+    slora_status st = SLORA_OK;
     const size_t row = (size_t)p->hidden;
     const size_t rows = 2ull * (size_t)rank * (size_t)p->n_proj;
     AdapterRec n;
@@ -292,9 +295,8 @@ slora_status slora_adapter_unregister(slora_pool_t p, int32_t id, slora_stream_t
         if (st != SLORA_OK)
             return st;
     }
-    slora_status st = set_device(p);
-    if (st != SLORA_OK)
-        return st;
+    DEVICE_SCOPE(p);
+    slora_status st = SLORA_OK;
     // the side stream may still copy out of the store
     CUDA_TRY(cudaStreamSynchronize(p->side));
     cudaFreeHost(a.store);
@@ -327,9 +329,8 @@ slora_status slora_adapters_load(slora_pool_t p, int32_t n, const int32_t *ids, 
     if (need_pages > p->pages.num_free())
         return fail(SLORA_ERR_POOL_FULL, "adapters_load: %lld pages needed, %lld free",
                     (long long)need_pages, (long long)p->pages.num_free());
-    slora_status st = set_device(p);
-    if (st != SLORA_OK)
-        return st;
+    DEVICE_SCOPE(p);
+    slora_status st = SLORA_OK;
 
     // Host bookkeeping first (pages + arena), with rollback if the arena is too fragmented.
     std::vector<int32_t> done;
@@ -434,9 +435,8 @@ slora_status slora_adapter_evict(slora_pool_t p, int32_t id, slora_stream_t stre
         return fail(SLORA_ERR_NOT_RESIDENT, "adapter_evict: id=%d", id);
     if (p->lru.pins(id) > 0)
         return fail(SLORA_ERR_INVALID_ARG, "adapter_evict: id=%d is pinned by an acquire", id);
-    slora_status st = set_device(p);
-    if (st != SLORA_OK)
-        return st;
+    DEVICE_SCOPE(p);
+    slora_status st = SLORA_OK;
     DirArgs dargs;
     dargs.n = 1;
     dargs.upd[0] = DirUpdate{id, a.rank, a.scaling, 0, -1};
@@ -476,9 +476,8 @@ slora_status slora_adapters_evict(slora_pool_t p, int32_t n, const int32_t *ids,
     }
     if (todo.empty())
         return SLORA_OK;
-    slora_status st = set_device(p);
-    if (st != SLORA_OK)
-        return st;
+    DEVICE_SCOPE(p);
+    slora_status st = SLORA_OK;
     DirArgs dargs;
     dargs.n = 0;
     for (size_t i = 0; i < todo.size(); ++i) {
@@ -638,9 +637,8 @@ slora_status slora_page_read(slora_pool_t p, int32_t page, uint16_t *host_out)
 {
     if (!p || page < 0 || page >= p->num_pages || !host_out)
         return fail(SLORA_ERR_INVALID_ARG, "page_read: page=%d", page);
-    slora_status st = set_device(p);
-    if (st != SLORA_OK)
-        return st;
+    DEVICE_SCOPE(p);
+    slora_status st = SLORA_OK;
     CUDA_TRY(cudaDeviceSynchronize());
     CUDA_TRY(cudaMemcpy(host_out, p->pool_dev + (size_t)page * p->hidden, (size_t)p->hidden * 2,
                         cudaMemcpyDeviceToHost));
@@ -651,9 +649,8 @@ slora_status slora_get_device_status(slora_pool_t p, int32_t *status)
 {
     if (!p || !status)
         return fail(SLORA_ERR_INVALID_ARG, "get_device_status");
-    slora_status st = set_device(p);
-    if (st != SLORA_OK)
-        return st;
+    DEVICE_SCOPE(p);
+    slora_status st = SLORA_OK;
     CUDA_TRY(cudaDeviceSynchronize());
     CUDA_TRY(cudaMemcpy(status, p->status_dev, 4, cudaMemcpyDeviceToHost));
     CUDA_TRY(cudaMemset(p->status_dev, 0, 4));
@@ -673,13 +670,13 @@ static slora_status apply_list(slora_pool_t p, const char *fn, const ProjList &p
         return fail(SLORA_ERR_INVALID_ARG, "%s: null token index pointer", fn);
     if (n_seg < 0 || (n_seg > 0 && !seg_indptr) || n_seg > T || n_seg > kMaxSegments)
         return fail(SLORA_ERR_INVALID_ARG, "%s: n_seg=%d (at most min(T, %d))", fn, n_seg, kMaxSegments);
-    slora_status st = set_device(p);
-    if (st != SLORA_OK)
-        return st;
+    DEVICE_SCOPE(p);
+    slora_status st = SLORA_OK;
     const int32_t want_rank = std::max(p->max_rank, 1);
-    if (T > p->plan.cap_tokens || want_rank > p->plan.max_rank) {
+    if (T > p->plan.cap_tokens || want_rank > p->plan.max_rank || pl.n > p->plan.cap_proj) {
         int32_t cap = std::max(T, std::max(p->plan.cap_tokens, 256));
-        size_t bytes = plan_scratch_bytes(cap, want_rank, p->hidden, p->max_adapters);
+        const int32_t nproj = std::max(pl.n, p->plan.cap_proj);
+        size_t bytes = plan_scratch_bytes(cap, want_rank, p->hidden, p->max_adapters, nproj);
         CUDA_TRY(cudaDeviceSynchronize());
         if (p->plan.base)
             cudaFree(p->plan.base);
@@ -689,6 +686,7 @@ static slora_status apply_list(slora_pool_t p, const char *fn, const ProjList &p
         p->plan.bytes = bytes;
         p->plan.cap_tokens = cap;
         p->plan.max_rank = want_rank;
+        p->plan.cap_proj = nproj;
     }
     PoolView pv{p->pool_dev, p->pt_dev, p->dir_dev, p->num_pages, p->hidden, p->n_proj,
                 p->max_adapters, p->status_dev};

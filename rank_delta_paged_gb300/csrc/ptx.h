@@ -68,10 +68,26 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
+// Upper bound, in ns, on how long one try_wait may suspend the calling thread: a waiting
+// warp sleeps until the phase completes (or this much time passes) instead of spinning,
+// leaving the issue slots to the warps that have work.
+constexpr uint32_t kSuspendHintNs = 20000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 {
     uint32_t ok;
-    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(smem_u32(bar)), "r"(parity), "n"(kSuspendHintNs)
+                 : "memory");
+    return ok != 0;
+}
+// Non-blocking test of a phase (never suspends).
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
                  "selp.u32 %0, 1, 0, p;\n\t}"
                  : "=r"(ok)
                  : "r"(smem_u32(bar)), "r"(parity)
@@ -79,12 +95,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// Polls of a wait before the wall clock is first read: short waits never touch the timer.
+constexpr uint32_t kPollsBeforeTimer = 64;
+
 // Wait for the phase with the given parity to complete; false (and a status code) after
 // the wall-clock limit.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, int32_t *status)
 {
-    if (mbar_try_wait(bar, parity))
-        return true;
+    for (uint32_t i = 0; i < kPollsBeforeTimer; ++i)
+        if (mbar_try_wait(bar, parity))
+            return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity))
@@ -236,7 +256,10 @@ template <bool kCluster>
 __device__ __forceinline__ void wait_phase(uint64_t *bar, uint32_t parity, volatile int *abort, int32_t *status)
 {
     auto probe = [&]() { return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
-    if (probe())
+    for (uint32_t i = 0; i < kPollsBeforeTimer; ++i)
+        if (probe())
+            return;
+    if (*abort)
         return;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
