@@ -61,7 +61,6 @@ namespace slora {
 namespace {
 
 constexpr int kConsumerWarps = 8;                 // warps doing the contractions
-constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kCopyWarps = 4;                     // warps issuing the bulk copies
 constexpr int kWarpLead = kConsumerWarps;         // fetches and publishes the units
 constexpr int kWarpCopy0 = kConsumerWarps + 1;    // first copy warp
@@ -85,13 +84,19 @@ constexpr int kMaxPlanGroups = 2048;    // distinct adapters per plan
 constexpr int kMaxHash = 2 * kMaxPlanGroups;
 
 static_assert(kTok == 8, "one ring stage of token rows, one MMA n-tile of tokens");
+// Copy warp g % kCopyWarps fills stage g; with NST a multiple of kCopyWarps every ring slot
+// is always filled by the same warp, which saw the release of stage g - 2 NST before it
+// issued stage g - NST, so the parity it waits on for stage g is never one phase behind,
+// whatever order the consumers release stages in (an expand holds its token stage).
 static_assert(NST % kCopyWarps == 0, "each ring slot always filled by the same copy warp");
 // Per consumer warp: K steps of a shrink block, 16-column pairs of an expand block at most.
 constexpr int kXs = kMaxSlice / 16 / kConsumerWarps;
 constexpr int kPairs = kMaxSlice / 16 / kConsumerWarps;
-// A consumer warp's own scratch region: a shrink unit's partial (8 tokens x 64 rank rows) or
-// an expand unit's y0 values (2 kPairs n-tiles x 32 lanes, half2 each).
-constexpr int kRegionFloats = 2 * kPairs * 32 > kTok * kRC ? 2 * kPairs * 32 : kTok * kRC;
+// A consumer warp's scratch region: a shrink unit's partial (8 tokens x 64 rank rows), summed
+// by the gather warp, or the y0 values of an expand unit of more than 64 rank rows (2 kPairs
+// n-tiles x 32 lanes, half2 each).
+constexpr int kRegionFloats = kTok * kRC;
+static_assert(2 * kPairs * 32 <= kRegionFloats, "y0 values fit a region");
 constexpr int kPtmpFloats = kRegionFloats * kConsumerWarps;
 
 struct PlanHeader {
@@ -552,6 +557,15 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// d = a * b for one 16x8x16 tile (zero accumulator input).
+__device__ __forceinline__ void mma16816_zc(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%10, %10, %10, %10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
+}
+
 __device__ __forceinline__ Unit load_unit(const Unit *p)
 {
     const uint4 *s = reinterpret_cast<const uint4 *>(p);
@@ -625,14 +639,14 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
     const int stageB = 8 * P;                                                    // one 8-row ring stage
     uint8_t *ring = smem;                                                        // [NST][8][P]
     uint8_t *zrow = ring + NST * stageB;                                         // [P] zeros: rows past the rank / tokens
-    float *ptmp = reinterpret_cast<float *>(zrow + P);                           // [8 warps][kRegionFloats] warp scratch
-    __half *ubuf = reinterpret_cast<__half *>(ptmp + kPtmpFloats);               // [QU][8][kUPitch] u (fp16)
+    float *pset = reinterpret_cast<float *>(zrow + P);                           // [8 warps][kRegionFloats] partials / y0
+    __half *ubuf = reinterpret_cast<__half *>(pset + kPtmpFloats);               // [QU][8][kUPitch] u (fp16)
     Rec *recs = reinterpret_cast<Rec *>(ubuf + QU * kTok * kUPitch);             // [QD] units in flight
     uint64_t *bars = reinterpret_cast<uint64_t *>(recs + QD);
     uint64_t *full = bars, *empty = bars + NST;              // ring stages
     uint64_t *rfull = bars + 2 * NST, *rempty = rfull + QD;  // unit records
     uint64_t *ufull = rempty + QD, *uempty = ufull + QU;     // u buffers
-    uint64_t *cbar = uempty + QU;                            // consumer warps' rendezvous
+    uint64_t *psfull = uempty + QU, *psempty = psfull + 1;   // shrink partials (consumers -> gather warp)
     __shared__ int s_abort;
     __shared__ int s_blk[kMaxBlocks + 1];                    // first element of each hidden block
 
@@ -663,7 +677,8 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
             mbar_init(&ufull[q], 1);
             mbar_init(&uempty[q], kConsumerWarps);
         }
-        mbar_init(cbar, kConsumerWarps);
+        mbar_init(psfull, kConsumerWarps);
+        mbar_init(psempty, 1);
         s_abort = 0;
         fence_mbar_init();
     }
@@ -710,8 +725,10 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
             p0 = lane < rows ? __ldcg(pt + base + lane) : -1;
             p1 = lane + 32 < rows ? __ldcg(pt + base + lane + 32) : -1;
         };
-        int grab = 0;   // lane 0: index of the unit after `nu`
-        if (lane == 0) grab = G + atomicAdd(&a.L.hdr->grab, 1);
+        // lane 0: the counter's value for the unit after `nu` (its index less G), first read in
+        // the next iteration so that the atomic's round trip overlaps this one
+        int grab = 0;
+        if (lane == 0) grab = atomicAdd(&a.L.hdr->grab, 1);
         bool cvalid = (int)blockIdx.x < n_units;
         Unit cu{};
         int ctok = 0;
@@ -720,12 +737,12 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
             cu = load_unit(a.L.units + blockIdx.x);
             fetch_rest(cu, ctok, cp0, cp1);
         }
-        int nidx = __shfl_sync(0xffffffffu, grab, 0);
+        int nidx = G + __shfl_sync(0xffffffffu, grab, 0);
         bool nvalid = cvalid && nidx < n_units;
         Unit nu{};
         if (nvalid) {
             nu = load_unit(a.L.units + nidx);
-            if (lane == 0) grab = G + atomicAdd(&a.L.hdr->grab, 1);
+            if (lane == 0) grab = atomicAdd(&a.L.hdr->grab, 1);
         }
         for (int k = 0;; ++k) {
             const uint32_t q = k % QD;
@@ -750,11 +767,11 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
             cu = nu;
             cvalid = nvalid;
             if (cvalid) fetch_rest(cu, ctok, cp0, cp1);
-            nidx = __shfl_sync(0xffffffffu, grab, 0);
+            nidx = G + __shfl_sync(0xffffffffu, grab, 0);
             nvalid = cvalid && nidx < n_units;
             if (nvalid) {
                 nu = load_unit(a.L.units + nidx);
-                if (lane == 0) grab = G + atomicAdd(&a.L.hdr->grab, 1);
+                if (lane == 0) grab = atomicAdd(&a.L.hdr->grab, 1);
             }
         }
         return;
@@ -791,10 +808,11 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
             // when zero_rest; completion on the slot's full barrier
             auto issue = [&](const __half *src, bool ok, bool zero_rest) {
                 if (sc >= NST) wait_phase<false>(&empty[pos.slot], pos.phase ^ 1u, abort, status);
+                if (__any_sync(0xffffffffu, *abort != 0)) return;   // after an abort nothing more is issued
                 const uint32_t dst = ring_s + pos.slot * stageB;
                 const bool mine = ok && lane < 8;
                 const uint32_t m = __ballot_sync(0xffffffffu, mine);
-                if (mine && !*abort) bulk_g2s_s(dst + lane * P, src + kb, sliceB, &full[pos.slot]);
+                if (mine) bulk_g2s_s(dst + lane * P, src + kb, sliceB, &full[pos.slot]);
                 if (zero_rest && (m & 0xffu) != 0xffu) {
                     for (int r = 0; r < 8; ++r) {
                         if ((m >> r) & 1u) continue;
@@ -804,7 +822,7 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
                     tc::fence_proxy_async_smem();   // before later bulk copies land in the same rows
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive_expect_tx(&full[pos.slot], *abort ? 0u : (uint32_t)__popc(m) * sliceB);
+                if (lane == 0) mbar_arrive_expect_tx(&full[pos.slot], (uint32_t)__popc(m) * sliceB);
             };
             // token stage
             if ((int)(sc % kCopyWarps) == cw)
@@ -850,18 +868,49 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
     }
 
     if (warp == kWarpGather) {
-        // ============================ gather (expand units ahead) ===========================
-        // For every expand unit, waits until the partial words of every hidden block carry
-        // this launch's tag, sums them in block order and rounds u to fp16 once, into the
-        // next u buffer.  Lane l covers tokens l>>4 (+2 per round), columns 4 (l & 15) .. +3.
+        // ================================= gather warp ==================================
+        // Shrink units of this CTA: sums the consumer warps' partials in warp order and writes
+        // the unit's partial as tagged words.  Expand units ahead of the consumers: waits until
+        // the partial words of every hidden block carry this launch's tag, sums them in block
+        // order and rounds u to fp16 once, into the next u buffer (lane l covers tokens l>>4,
+        // +2 per round, columns 4 (l & 15) .. +3).
         const uint32_t tag = a.tag;
         uint32_t uj = 0;   // u buffers filled
+        uint32_t sr = 0;   // shrink partials summed
         for (int k = 0;; ++k) {
             Unit u;
             const bool have = take_record(k, u);
             release_record(k);
             if (!have) break;
-            if (!(u.packed & 32u)) continue;
+            if (!(u.packed & 32u)) {
+                const int nt = (int)(u.packed & 31u) + 1;
+                const int c = (int)((u.packed >> 12) & 15u), b = (int)((u.packed >> 9) & 7u);
+                const int rows = min(kRC, u.rank - kRC * c), ld = 16 * ceil_div(rows, 16);
+                wait_phase<false>(psfull, sr & 1, abort, status);
+                unsigned long long *dst = a.L.upart + u.uoff + ((int64_t)c * NB + b) * nt * kRC;
+#pragma unroll 1
+                for (int e = 4 * lane; e < nt * ld; e += 128) {
+                    const int t = e / ld, j = e - t * ld;
+                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int g = 0; g < kConsumerWarps; ++g) {
+                        const float4 pv = *reinterpret_cast<const float4 *>(pset + g * kRegionFloats + t * kRC + j);
+                        v.x += pv.x;
+                        v.y += pv.y;
+                        v.z += pv.z;
+                        v.w += pv.w;
+                    }
+                    unsigned long long *o = dst + t * kRC + j;
+                    if (j < rows) st_word(o, v.x, tag);
+                    if (j + 1 < rows) st_word(o + 1, v.y, tag);
+                    if (j + 2 < rows) st_word(o + 2, v.z, tag);
+                    if (j + 3 < rows) st_word(o + 3, v.w, tag);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(psempty);
+                ++sr;
+                continue;
+            }
             const int nt = (int)(u.packed & 31u) + 1;
             const int nch = ceil_div(u.rank, kRC);
             const int j4 = 4 * (lane & 15);
@@ -933,30 +982,24 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
     RingPos cur{0, 0};   // the next stage to consume
     uint32_t uj = 0;     // u buffers consumed
     auto wait_at = [&](const RingPos &p) { wait_phase<false>(&full[p.slot], p.phase, abort, status); };
-    // every consumer warp's shared-memory writes before it are visible to all of them after
-    // it; an mbarrier rather than a named barrier so that after an abort no warp waits for
-    // warps that have left
-    uint32_t cph = 0;
-    auto consumers_sync = [&]() {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(cbar);
-        wait_phase<false>(cbar, cph, abort, status);
-        cph ^= 1u;
-    };
-    float *region = ptmp + w * kRegionFloats;   // this warp's scratch: shrink partials or y0 values
-    for (int k = 0;; ++k) {
-        const uint32_t q = k % QD;
-        Unit u;
-        const bool have = take_record(k, u);
-        const int tk = recs[q].tok[gid];
-        release_record(k);
-        if (!have) break;
+    uint32_t sj = 0;     // shrink units done (uses of the partial set)
+    float *region = pset + w * kRegionFloats;   // this warp's shrink partials
+    // The record of the next unit is read while the current one runs.
+    Unit u;
+    bool have = take_record(0, u);
+    int tk = recs[0].tok[gid];
+    release_record(0);
+    for (int k = 0; have; ++k) {
         const UnitShape sh_ = unit_shape(u);
         const int nt = sh_.nt;
         const int kb = s_blk[sh_.b], KS = s_blk[sh_.b + 1] - kb;
         const RingPos tpos = cur;   // the token stage
         cur.next();
         wait_at(tpos);
+        Unit nu;
+        const bool nhave = take_record(k + 1, nu);
+        const int ntk = recs[(k + 1) % QD].tok[gid];
+        release_record(k + 1);
         const uint32_t tstage = ring_s + tpos.slot * stageB;
 
         if (!sh_.expand) {
@@ -975,6 +1018,8 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[tpos.slot]);
+            // the partial set is free once the gather warp has summed the previous shrink unit
+            if (sj > 0) wait_phase<false>(psempty, (sj - 1) & 1, abort, status);
 #pragma unroll 1
             for (int blk = 0; blk < nb; ++blk) {
                 const RingPos lo = cur;
@@ -1008,111 +1053,137 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
                     region[(2 * tig + 1) * kRC + 16 * blk + gid + 8 * h] = pacc[0][2 * h + 1] + pacc[1][2 * h + 1];
                 }
             }
-            consumers_sync();   // every warp's partials are written
-            {
-                // the unit's partial (the 8 warp partials summed in order), one tagged word per
-                // value, straight to the scratch the gather warp polls
-                unsigned long long *dst = a.L.upart + u.uoff + ((int64_t)sh_.c * NB + sh_.b) * nt * kRC;
-                const int ld = 16 * nb;
-                for (int e = tid; e < nt * ld; e += kConsumers) {
-                    const int t = e / ld, j = e - t * ld;
-                    float v = 0.f;
-#pragma unroll
-                    for (int g = 0; g < kConsumerWarps; ++g)
-                        v += ptmp[g * kRegionFloats + t * kRC + j];
-                    st_word(dst + t * kRC + j, v, a.tag);
-                }
-            }
-            consumers_sync();   // the partials are read: the regions are free for the next unit
-            continue;
-        }
-
-        // ---- expand: y = u B over the block's columns, the item's tokens on the MMA's M (rows
-        //      0-7; rows 8-15 zero) and the columns on its N; warp w takes the column pairs
-        //      [pp0, pp1) (16 columns each), over the rank chunks ----
-        const int npair = KS / 16;
-        const int pp0 = (w * npair) / kConsumerWarps, pp1 = ((w + 1) * npair) / kConsumerWarps;
-        // the y0 values of this lane's outputs (token gid, columns 16 (pp0+p) + 8 n2 + 2 tig, +1),
-        // kept in the warp's region as [value][lane] until the epilogue, so the token stage is
-        // free at once
-        uint32_t *yv = reinterpret_cast<uint32_t *>(region);
-        {
-            const uint8_t *trow = ring + tpos.slot * stageB + gid * P;
-#pragma unroll
-            for (int p = 0; p < kPairs; ++p)
-#pragma unroll
-                for (int n2 = 0; n2 < 2; ++n2)
-                    if (pp0 + p < pp1)
-                        yv[(2 * p + n2) * 32 + lane] =
-                            *reinterpret_cast<const uint32_t *>(trow + (16 * (pp0 + p) + 8 * n2 + 2 * tig) * 2);
+            // hand the partial to the gather warp, which sums the 8 warps' partials in order
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[tpos.slot]);
-        }
-        float acc[2 * kPairs][4];
+            if (lane == 0) mbar_arrive(psfull);
+            ++sj;
+        } else {
+            // ---- expand: y = u B over the block's columns, the item's tokens on the MMA's M
+            //      (rows 0-7; rows 8-15 zero) and the columns on its N; warp w takes the column
+            //      pairs [pp0, pp1) (16 columns each), over the rank chunks ----
+            const int npair = KS / 16;
+            const int pp0 = (w * npair) / kConsumerWarps, pp1 = ((w + 1) * npair) / kConsumerWarps;
+            // A unit of at most 64 rank rows (9 stages) keeps its token stage (y0) until the
+            // epilogue; a longer one would hold the ring, so it first copies this lane's y0
+            // values (token gid, columns 16 (pp0+p) + 8 n2 + 2 tig, +1) to the warp's region,
+            // once the gather warp has summed the partials the region held.
+            const bool hold = u.rank <= kRC;
+            uint32_t *yv = reinterpret_cast<uint32_t *>(region);
+            if (!hold) {
+                if (sj > 0) wait_phase<false>(psempty, (sj - 1) & 1, abort, status);
+                const uint8_t *trow = ring + tpos.slot * stageB + gid * P;
 #pragma unroll
-        for (int n8 = 0; n8 < 2 * kPairs; ++n8)
+                for (int p = 0; p < kPairs; ++p)
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                acc[n8][e] = 0.f;
+                    for (int n2 = 0; n2 < 2; ++n2)
+                        if (pp0 + p < pp1)
+                            yv[(2 * p + n2) * 32 + lane] =
+                                *reinterpret_cast<const uint32_t *>(trow + (16 * (pp0 + p) + 8 * n2 + 2 * tig) * 2);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[tpos.slot]);
+            }
+            float acc[2 * kPairs][4];
 #pragma unroll 1
-        for (int c = 0; c < sh_.nch; ++c) {
-            const uint32_t qu = uj % QU;
-            wait_phase<false>(&ufull[qu], (uj / QU) & 1, abort, status);
-            const int rows = chunk_rows(u, sh_, c), nb = ceil_div(rows, 16), ns = ceil_div(rows, 8);
-            const uint32_t ub = ubuf_s + qu * (kTok * kUPitch * 2);
+            for (int c = 0; c < sh_.nch; ++c) {
+                const uint32_t qu = uj % QU;
+                wait_phase<false>(&ufull[qu], (uj / QU) & 1, abort, status);
+                const int rows = chunk_rows(u, sh_, c), nb = ceil_div(rows, 16), ns = ceil_div(rows, 8);
+                const uint32_t ub = ubuf_s + qu * (kTok * kUPitch * 2);
 #pragma unroll 1
-            for (int blk = 0; blk < nb; ++blk) {
-                const RingPos lo = cur;
-                cur.next();
-                const bool has_hi = 2 * blk + 1 < ns;
-                const RingPos hi = cur;
-                if (has_hi) cur.next();
-                wait_at(lo);
-                if (has_hi) wait_at(hi);
-                // u rows (the MMA's A operand): the item's tokens in rows 0-7, zeros in rows 8-15
-                uint32_t af[4];
-                ldsm_x4((q4 & 1) ? zrow_s + (16 * blk + 8 * (q4 >> 1)) * 2
-                                 : ub + (rr * kUPitch + 16 * blk + 8 * (q4 >> 1)) * 2, af);
-                // B rows (the MMA's B operand, transposed on load): 0-7 from stage lo, 8-15 from hi
-                const uint32_t brow = (q4 & 1) ? (has_hi ? ring_s + hi.slot * stageB + rr * P : zrow_s)
-                                               : ring_s + lo.slot * stageB + rr * P;
+                for (int blk = 0; blk < nb; ++blk) {
+                    const RingPos lo = cur;
+                    cur.next();
+                    const bool has_hi = 2 * blk + 1 < ns;
+                    const RingPos hi = cur;
+                    if (has_hi) cur.next();
+                    wait_at(lo);
+                    if (has_hi) wait_at(hi);
+                    // u rows (the MMA's A operand): the item's tokens in rows 0-7, zeros in rows 8-15
+                    uint32_t af[4];
+                    ldsm_x4((q4 & 1) ? zrow_s + (16 * blk + 8 * (q4 >> 1)) * 2
+                                     : ub + (rr * kUPitch + 16 * blk + 8 * (q4 >> 1)) * 2, af);
+                    // B rows (the MMA's B operand, transposed on load): 0-7 from stage lo, 8-15 from hi
+                    const uint32_t brow = (q4 & 1) ? (has_hi ? ring_s + hi.slot * stageB + rr * P : zrow_s)
+                                                   : ring_s + lo.slot * stageB + rr * P;
+                    if (c == 0 && blk == 0) {
+                        // the first block starts the accumulators (zero C operand)
 #pragma unroll
-                for (int p = 0; p < kPairs; ++p) {
-                    if (pp0 + p < pp1) {
-                        uint32_t bf[4];
-                        ldsm_x4_t(brow + (16 * (pp0 + p) + 8 * (q4 >> 1)) * 2, bf);
-                        mma16816(acc[2 * p], af, bf[0], bf[1]);
-                        mma16816(acc[2 * p + 1], af, bf[2], bf[3]);
+                        for (int p = 0; p < kPairs; ++p) {
+                            if (pp0 + p < pp1) {
+                                uint32_t bf[4];
+                                ldsm_x4_t(brow + (16 * (pp0 + p) + 8 * (q4 >> 1)) * 2, bf);
+                                mma16816_zc(acc[2 * p], af, bf[0], bf[1]);
+                                mma16816_zc(acc[2 * p + 1], af, bf[2], bf[3]);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int p = 0; p < kPairs; ++p) {
+                            if (pp0 + p < pp1) {
+                                uint32_t bf[4];
+                                ldsm_x4_t(brow + (16 * (pp0 + p) + 8 * (q4 >> 1)) * 2, bf);
+                                mma16816(acc[2 * p], af, bf[0], bf[1]);
+                                mma16816(acc[2 * p + 1], af, bf[2], bf[3]);
+                            }
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&empty[lo.slot]);
+                        if (has_hi) mbar_arrive(&empty[hi.slot]);
                     }
                 }
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&empty[lo.slot]);
-                    if (has_hi) mbar_arrive(&empty[hi.slot]);
-                }
+                if (lane == 0) mbar_arrive(&uempty[qu]);
+                ++uj;
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&uempty[qu]);
-            ++uj;
-        }
-        if (!*abort && gid < nt) {
             // ---- epilogue: y = y0 + s * acc for token gid: columns 2 tig, 2 tig + 1 of each n-tile ----
             const float scl = u.scaling;
             __half *yrow = a.y[sh_.pj] + (int64_t)tk * d + kb;
+            const bool store = !*abort && gid < nt;
+            if (hold) {
+                // y0 of four n-tiles (rows 0-7 of the token stage) per fragment load
+                const uint32_t yaddr = tstage + rr * P + (16 * pp0 + 8 * q4) * 2;
 #pragma unroll
-            for (int p = 0; p < kPairs; ++p) {
-                if (pp0 + p < pp1) {
+                for (int p2 = 0; p2 < kPairs / 2; ++p2) {
+                    if (pp0 + 2 * p2 < pp1) {
+                        uint32_t yf[4];
+                        ldsm_x4(yaddr + p2 * 64, yf);
 #pragma unroll
-                    for (int n2 = 0; n2 < 2; ++n2) {
-                        const int col = 16 * (pp0 + p) + 8 * n2 + 2 * tig;
-                        const float2 y0 = __half22float2(*reinterpret_cast<const __half2 *>(&yv[(2 * p + n2) * 32 + lane]));
-                        const float *ac = acc[2 * p + n2];
-                        *reinterpret_cast<__half2 *>(yrow + col) =
-                            __floats2half2_rn(fmaf(scl, ac[0], y0.x), fmaf(scl, ac[1], y0.y));
+                        for (int i = 0; i < 4; ++i) {
+                            const int p = 2 * p2 + (i >> 1), n2 = i & 1;
+                            if (store && pp0 + p < pp1) {
+                                const int col = 16 * (pp0 + p) + 8 * n2 + 2 * tig;
+                                const float2 y0 = __half22float2(*reinterpret_cast<const __half2 *>(&yf[i]));
+                                const float *ac = acc[2 * p + n2];
+                                *reinterpret_cast<__half2 *>(yrow + col) =
+                                    __floats2half2_rn(fmaf(scl, ac[0], y0.x), fmaf(scl, ac[1], y0.y));
+                            }
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[tpos.slot]);
+            } else if (store) {
+#pragma unroll
+                for (int p = 0; p < kPairs; ++p) {
+                    if (pp0 + p < pp1) {
+#pragma unroll
+                        for (int n2 = 0; n2 < 2; ++n2) {
+                            const int col = 16 * (pp0 + p) + 8 * n2 + 2 * tig;
+                            const float2 y0 =
+                                __half22float2(*reinterpret_cast<const __half2 *>(&yv[(2 * p + n2) * 32 + lane]));
+                            const float *ac = acc[2 * p + n2];
+                            *reinterpret_cast<__half2 *>(yrow + col) =
+                                __floats2half2_rn(fmaf(scl, ac[0], y0.x), fmaf(scl, ac[1], y0.y));
+                        }
                     }
                 }
             }
         }
+        u = nu;
+        tk = ntk;
+        have = nhave;
     }
 }
 
@@ -1138,7 +1209,7 @@ inline size_t delta_smem_bytes(int hidden)
 {
     const size_t P = (size_t)delta_pitch(hidden);
     return NST * 8 * P + P + (size_t)kPtmpFloats * 4 + (size_t)QU * kTok * kUPitch * 2 + QD * sizeof(Rec) +
-           (2 * NST + 2 * QD + 2 * QU + 1) * 8;
+           (2 * NST + 2 * QD + 2 * QU + 2) * 8;
 }
 
 // Kernel attributes and the delta grid's resident CTAs, per device (the attributes are
