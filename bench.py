@@ -9,9 +9,14 @@ for every projection of the workload.  Metric: LoRA-delta tokens/s per layer
   python bench.py [--workload NAME] [--steps K] [--warmup W] [--gpus N]
   python bench.py --impl reference ...      # the fp64 CPU oracle on the host cores
 
-For N > 1 (torchrun, one process per GPU) every rank serves its own batch (seed + rank):
-the delta has no cross-token exchange, so ranks are independent replicas (weak scaling)
-and the only collectives are the timing barrier and the max-over-ranks reduction.
+The default workload is the 13B decode batch over a zoo of 2000 pooled adapters (ranks 8
+to 64, 512 tokens, Zipf 0.5); the line also carries the 7B prefill batch and one layer of
+the mixed prefill + decode iteration as extra keys.
+
+For N > 1 every rank serves its own batch (seed + rank): the delta has no cross-token
+exchange, so ranks are independent replicas (weak scaling) and the only collectives are
+the timing barrier and the max-over-ranks reduction.  Under torchrun the ranks come from
+the environment; without it, ``--gpus N`` starts the N rank processes itself.
 
 Timing: W untimed warm-up steps; K timed steps, each preceded by a 2 x L2 write that
 evicts the pool and inputs from L2 (the flush itself is outside the per-step CUDA-event
@@ -34,7 +39,7 @@ sys.path.insert(0, ROOT)
 
 from rank_delta_paged_gb300 import workloads as W  # noqa: E402
 
-DEFAULT_WORKLOAD = "decode_7b"
+DEFAULT_WORKLOAD = "decode_13b_zoo"
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -57,17 +62,76 @@ def parse():
                     help="also run K batches of the zoo through acquire / apply / release (\"pressure\")")
     ap.add_argument("--layers", type=int, default=0, help="mixed_iteration: layers (0 = the default 32)")
     ap.add_argument("--pool-gib", type=float, default=0.0, help="mixed_iteration: pool size in GiB (0 = 40)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the extra prefill_7b and mixed-layer keys of the default line")
+    ap.add_argument("--profile-calls", type=int, default=0, metavar="N",
+                    help="for a profiler: N apply calls of the first layer, each after an L2 flush, "
+                         "and nothing else (no timing, no line)")
+    ap.add_argument("--dry-run", action="store_true",
+                    help="start the ranks and print the line's skeleton without touching a GPU "
+                         "(gloo; tests the launcher)")
     ap.add_argument("--apply", choices=["multi", "single"], default="multi",
                     help="multi: one slora_lora_apply_multi call per layer (all its projections); "
                          "single: one slora_lora_apply call per projection")
     return ap.parse_args()
 
 
-# DRAM bytes (read + write) per launch of the workload's dominant kernel, from one ncu
-# capture of the current kernel on the workload (profiles/delta_kernel_decode_7b.md and
-# profiles/prefill_kernel_prefill_7b.md give the commands); a workload without a capture
-# of the current kernel reports null.
-TRAFFIC = {"decode_7b_h4096_a100_t256_zipf1": 41918464, "prefill_7b_h4096_s16x512": 155555840}
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of a workload's
+# dominant kernel, each from one ncu capture (command below) of that kernel's sources as
+# identified by ``sources_sha``.  When the sources have changed since the capture the line
+# reports null: the counters describe a kernel that no longer exists.
+TRAFFIC_CAPTURE = ("ncu --clock-control none --metrics dram__bytes_read.sum,dram__bytes_write.sum "
+                   "-k regex:{kernel} -s 3 -c 1 python bench.py --workload {workload} --profile-calls 5")
+TRAFFIC = {
+    # workload name: (kernel, DRAM bytes per launch, sources_sha at capture)
+    "decode_13b_h5120_a2000_t512_zipf0.5": ("delta_kernel", 265030144 + 3911168, "5ba0e890c0d2f496"),
+}
+KERNEL_SOURCES = {
+    "delta_kernel": ("decode.cu", "ptx.h", "internal.h"),
+    "prefill_kernel": ("prefill.cu", "ptx.h", "tcgen05.h", "internal.h"),
+}
+
+
+def sources_sha(kernel: str) -> str:
+    """sha256 (first 16 hex digits) over the kernel's source files."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "rank_delta_paged_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_of(name: str):
+    """(bytes or None, note) for a workload's dominant kernel."""
+    if name not in TRAFFIC:
+        return None, "no ncu capture for this workload"
+    kernel, nbytes, sha = TRAFFIC[name]
+    if sources_sha(kernel) != sha:
+        return None, f"{kernel} sources changed since the ncu capture ({sha})"
+    return nbytes, f"one ncu capture of {kernel} (sources {sha})"
+
+
+def fp16_peak_tflops(dev) -> float:
+    """Dense fp16 tensor throughput measured here: torch.matmul of 8192^3 fp16 matrices
+    (2 N^3 flops), best of 10 CUDA-event-timed products after warm-up."""
+    import torch
+    n = 8192
+    a = torch.randn(n, n, device=dev, dtype=torch.float16)
+    b = torch.randn(n, n, device=dev, dtype=torch.float16)
+    c = torch.empty(n, n, device=dev, dtype=torch.float16)
+    for _ in range(3):
+        torch.matmul(a, b, out=c)
+    best = float("inf")
+    for _ in range(10):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        torch.matmul(a, b, out=c)
+        e1.record()
+        e1.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    del a, b, c
+    return 2.0 * n ** 3 / (best / 1e3) / 1e12
 
 
 def peaks():
@@ -324,9 +388,129 @@ def config_of(w: W.Workload, l2: str):
             "kv_pages": w.kv_pages, "l2": l2}
 
 
+# ---------------------------------------------------------------- rank launcher
+def launch_ranks(args) -> int:
+    """Start ``args.gpus`` processes of this script, one per GPU, with the rank variables a
+    torchrun launch would set; rank 0's output is the run's output.  If a rank fails the
+    others are stopped (they would wait in a collective)."""
+    import socket
+    sock = socket.socket()
+    sock.bind(("127.0.0.1", 0))
+    port = sock.getsockname()[1]
+    sock.close()
+    procs = []
+    for r in range(args.gpus):
+        env = dict(os.environ, RANK=str(r), LOCAL_RANK=str(r), WORLD_SIZE=str(args.gpus),
+                   LOCAL_WORLD_SIZE=str(args.gpus), MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+        procs.append(subprocess.Popen([sys.executable, os.path.abspath(__file__)] + sys.argv[1:], env=env))
+    rc = 0
+    while procs:
+        for p in list(procs):
+            code = p.poll()
+            if code is None:
+                continue
+            procs.remove(p)
+            if code != 0:
+                rc = rc or code
+                for q in procs:
+                    q.terminate()
+        time.sleep(0.05)
+    return rc
+
+
+def dry_run(args, rank: int, world: int) -> int:
+    """The launcher's path without a GPU: every rank joins a gloo group and counts itself."""
+    import torch
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("gloo")
+    n = torch.ones(1)
+    if world > 1:
+        dist.all_reduce(n)
+    if rank == 0:
+        print(json.dumps({"metric": "lora_delta_tokens_per_s_per_layer", "value": None,
+                          "unit": "tokens/s/layer", "n_gpus": world, "dry_run": True,
+                          "ranks_started": int(n.item()), "impl": args.impl,
+                          "config": {"workload": args.workload}}), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+# ---------------------------------------------------------------- extra workloads
+def measure_extra(rdp, w, dev, flush, stream, hbm, fp16_tflops, reps=100):
+    """One call per layer of workload ``w`` (all its projections in one call), timed with
+    CUDA events after an L2 flush: the whole call, and the kernels after the plan."""
+    import torch
+    from rank_delta_paged_gb300.harness import PoolSession
+    sess = PoolSession(w, device=dev.index)
+    try:
+        sess.load(w.used_adapters(), stream)
+        per_layer = w.n_proj // w.n_layers
+        ins = [sess.device_inputs(p) for p in range(per_layer)]
+        xs = [i[0] for i in ins]
+        ys = [i[1].clone() for i in ins]
+        idx, seg = ins[0][2], ins[0][3]
+
+        def call(st):
+            if per_layer > 1:
+                rdp.slora_lora_apply_multi(sess.pool, list(range(per_layer)), xs, ys, w.T, idx, seg,
+                                           w.n_seg, None, st)
+            else:
+                rdp.slora_lora_apply(sess.pool, 0, xs[0], ys[0], w.T, idx, seg, w.n_seg, None, st)
+
+        for _ in range(3):
+            call(stream)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps)]
+        for e in ev:
+            for x in e:
+                x.record(stream)
+        torch.cuda.synchronize()
+        for a, b, c in ev:
+            flush.zero_()
+            a.record(stream)
+            rdp.slora_pool_set_stage_event(sess.pool, b)
+            call(stream)
+            c.record(stream)
+        torch.cuda.synchronize()
+        rdp.slora_pool_set_stage_event(sess.pool, None)
+        call_ms = statistics.median(a.elapsed_time(c) for a, b, c in ev)
+        kern_ms = statistics.median(b.elapsed_time(c) for a, b, c in ev)
+        status = sess.device_status()
+    finally:
+        sess.close()
+    nbytes = algorithmic_bytes(w) / w.n_proj * per_layer
+    flops = algorithmic_flops(w) / w.n_proj * per_layer
+    t = kern_ms / 1e3
+    attain = max(nbytes / (hbm * 1e9), flops / (fp16_tflops * 1e12))
+    return {
+        "workload": w.name, "tokens": w.T, "projections_per_call": per_layer, "prefill_segments": w.n_seg,
+        "value": w.T / (call_ms / 1e3), "unit": "tokens/s/layer", "ms_per_call": call_ms,
+        "kernel_ms": kern_ms, "status": status,
+        "roofline": {"bound": "hbm", "achieved": nbytes / t / 1e9, "peak": hbm, "unit": "GB/s",
+                     "frac": nbytes / t / 1e9 / hbm, "algorithmic_bytes_per_call": nbytes},
+        "tensor": {"achieved_tflops": flops / t / 1e12, "peak_tflops": fp16_tflops,
+                   "frac": flops / t / 1e12 / fp16_tflops, "flops_per_call": flops,
+                   "peak_kind": "measured in this run: torch.matmul fp16 8192^3, best of 10"},
+        "attainable_frac": attain / t,
+        "timing": "median of %d calls, each after a 2 x L2 write; kernel_ms from the event the pool "
+                  "records after the plan to the end of the call" % reps,
+    }
+
+
 # ---------------------------------------------------------------- our arm
 def main():
     args = parse()
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        return launch_ranks(args)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        print(f"bench.py: --gpus {args.gpus} but {world} rank(s) were started", file=sys.stderr)
+        return 2
+    if args.dry_run:
+        return dry_run(args, rank, world)
     if args.impl == "reference":
         return run_reference(args)
     import torch
@@ -335,9 +519,6 @@ def main():
     from rank_delta_paged_gb300.harness import PoolSession
     from rank_delta_paged_gb300.replicas import job_totals, replica_seed, tokens_per_s_per_layer
 
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     if world > 1:
         dist.init_process_group("nccl")
@@ -385,6 +566,15 @@ def main():
     def step():
         for l in range(w.n_layers):
             apply_layer(l, stream)
+
+    if args.profile_calls > 0:
+        for _ in range(args.profile_calls):
+            flush.zero_()
+            apply_layer(0, stream)
+        torch.cuda.synchronize()
+        status = sess.device_status()
+        sess.close()
+        return 0 if status == 0 else 3
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -591,6 +781,17 @@ def main():
     if status != 0:
         print(f"device status {status} after the run", file=sys.stderr)
         return 3
+    traffic, traffic_note = traffic_of(w.name)
+    extras = None
+    if args.workload == DEFAULT_WORKLOAD and not args.no_extras and rank == 0:
+        fp16 = fp16_peak_tflops(dev)
+        extras = {"fp16_dense_peak_tflops": fp16}
+        for name, kw in (("prefill_7b", {}), ("mixed_layer", {"n_layers": 1, "pool_bytes": 2 << 30})):
+            wx = W.by_name("mixed_iteration" if name == "mixed_layer" else name, seed=args.seed, **kw)
+            extras[name] = measure_extra(rdp, wx, dev, flush, stream, hbm, fp16)
+            if extras[name]["status"] != 0:
+                print(f"device status {extras[name]['status']} in {name}", file=sys.stderr)
+                return 3
 
     line = {
         "metric": "lora_delta_tokens_per_s_per_layer", "value": value, "unit": "tokens/s/layer",
@@ -603,7 +804,7 @@ def main():
                               else "one slora_lora_apply call per projection")),
         "gpu_launches": int(launches),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": TRAFFIC.get(w.name),
+                     "frac": achieved / hbm, "traffic": traffic, "traffic_source": traffic_note,
                      "kernel": "delta_kernel" + (" + prefill_kernel" if n_seg else "") +
                                (f" (one call of {call_projs} projections" if multi else " (one projection") +
                                "; median CUDA-event time between the plan and the end of the call)",
@@ -634,6 +835,8 @@ def main():
         line["pressure"] = pressure
     if bmm is not None:
         line["bmm"] = bmm
+    if extras is not None:
+        line["extra_workloads"] = extras
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, cores, sample = oracle_rate(w, args.cpu_seconds)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s/layer", "cores": cores,

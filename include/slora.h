@@ -317,7 +317,8 @@ slora_status slora_lora_apply_multi(slora_pool_t pool, int32_t n, const int32_t 
 
 /* ---------------------------------------------------------------------------
  * slora_lora_apply_bmm: the padded batched-GEMM path, kept as the comparison the S-LoRA
- * ablation calls the slower BMM path (blog page, section 4; explainer, "Prior limits").
+ * ablation calls the slower BMM path (explainer, "Results and evidence", Figure 5 narrative;
+ * explainer, "Prior limits").
  * Not the hot path: it exists to be measured against slora_lora_apply.  Decode tokens
  * only (no segments): every token gets a dense copy of its adapter's factors zero-padded
  * to R = the pool's largest registered rank rounded up to a multiple of 8 (a gather

@@ -1,8 +1,8 @@
 // The padded batched-GEMM path: the comparison the S-LoRA ablation calls the slower BMM
-// path (S-LoRA: Multiplexing Thousands of Fine-Tuned Adapters on a Single GPU, section 4:
-// removing the custom kernels in favour of padded batched matrix multiplications makes
-// serving slower; S-LoRA: Serving Thousands of Concurrent LoRA Adapters (explainer),
-// "Prior limits": per-adapter weights copied into contiguous, padded tensors).
+// path (S-LoRA: Serving Thousands of Concurrent LoRA Adapters (explainer), "Results and
+// evidence", Figure 5 narrative: replacing the custom kernels with a slower BMM path hurts
+// throughput and latency; same page, "Prior limits": per-adapter weights copied into
+// contiguous, padded tensors).
 //
 // Each decode token gets its own dense copy of its adapter's factors, zero-padded to the
 // pool's largest registered rank R: a gather kernel copies the token's A^T rows and its B

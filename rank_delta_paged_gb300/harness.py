@@ -82,9 +82,10 @@ def prefetch_overlap(sess: PoolSession, K: int = 6, stream=None) -> dict:
 
     The pool runs every load on its own side stream and only makes the caller's stream
     wait for it, so a serving loop that issues load(k), apply(k), load(k+1), apply(k+1), ...
-    on one stream already lets load(k+1) run under apply(k) (S-LoRA: Multiplexing Thousands
-    of Fine-Tuned Adapters on a Single GPU, section 4: the adapters of the next batch are
-    prefetched while the current batch computes).  K decode batches are drawn from the
+    on one stream already lets load(k+1) run under apply(k) (S-LoRA: Serving Thousands of
+    Concurrent LoRA Adapters (explainer), "Algorithm / figure walkthrough" step 2: the
+    factors of the next iteration's adapters are prefetched into the pool while the current
+    one computes).  K decode batches are drawn from the
     session's zoo (``Workload.later_batch``), starting from an empty pool; each loads the
     adapters not yet resident.  Timed on the stream with CUDA events:
 

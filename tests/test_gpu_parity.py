@@ -103,17 +103,32 @@ def test_decode_7b_full_size():
     assert_close(got, oracle.workload_reference(w), "decode_7b")
 
 
-def test_prefill_7b_full_size_sampled():
+def test_prefill_7b_full_size():
+    """16 segments of 512 tokens: every output element against the oracle."""
     w = W.prefill_7b()
     with session_all_loaded(w) as s:
         got = run(s)
         assert s.device_status() == 0
-    rng = np.random.default_rng(0)
-    edges = np.concatenate([np.arange(a, a + 3) for a in w.seg_indptr[:-1]] +
-                           [np.arange(b - 3, b) for b in w.seg_indptr[1:]])
-    sel = np.unique(np.concatenate([edges, rng.choice(w.T, 200, replace=False)])).astype(np.int32)
-    ref = oracle.workload_reference(w, sel=sel)
-    assert_close(got[sel], ref, "prefill_7b")
+    assert_close(got, oracle.workload_reference(w), "prefill_7b")
+
+
+@pytest.mark.parametrize("make", [
+    lambda: W.prefill_7b(values="delta"),
+    lambda: W.decode_13b_zoo(values="delta"),
+    lambda: W.mixed_iteration(n_layers=1, pool_bytes=2 << 30, values="delta"),
+], ids=["prefill_7b", "decode_13b_zoo", "mixed_layer"])
+def test_delta_only_full_configs(make):
+    """y0 = 0, so the bound 1e-3 + 1e-2 |ref| applies to the delta itself (for the prefill
+    path, which rounds x A to fp16, and for the decode path at 2000 pooled adapters)."""
+    w = make()
+    with PoolSession(w) as s:
+        s.load(w.used_adapters())
+        for p in range(w.n_proj):
+            got = run(s, p=p)
+            assert s.device_status() == 0
+            ref = oracle.workload_reference(w, p=p)
+            assert_close(got, ref, f"{w.name} delta-only p={p}")
+            assert np.abs(ref).max() > 0.01
 
 
 def test_prefill_ragged_segments():
@@ -158,8 +173,7 @@ def test_mixed_iteration_one_layer():
         s.load(used)
         for p in range(w.n_proj):
             got = run(s, p=p)
-            sel = np.unique(np.concatenate([w.decode_tokens(), np.arange(0, w.T, 37)])).astype(np.int32)
-            assert_close(got[sel], oracle.workload_reference(w, p=p, sel=sel), f"mixed p={p}")
+            assert_close(got, oracle.workload_reference(w, p=p), f"mixed p={p}")
         assert s.device_status() == 0
 
 

@@ -13,10 +13,17 @@ oracle with something independent of it:
   * ``pin_zero_B``           -- B = 0 leaves y0 unchanged, bit for bit
   * ``pin_base_only``        -- index -1 leaves y0 unchanged
   * ``pin_invariances``      -- token order and adapter numbering do not change results
+  * ``pin_projection_select``-- grouped numpy BLAS on projection 2 of a 3-projection
+                                workload: the projection's own x, y0, At and B are used
+  * ``pin_tolerance_mask``   -- the parity bound |got - ref| <= atol + rtol |ref| on
+                                hand-worked values on both sides of it (negative refs,
+                                got below and above ref, zero ref, NaN)
 
 ``test_mutants_are_caught`` plants mistakes in a copy of the oracle's C source (dropped
 scaling, wrong sign, transposed operand, dropped term, wrong token, ...), compiles each
 copy, and checks that the pins above reject every one of them.
+``test_python_mutants_are_caught`` does the same for the Python side of the oracle
+(projection selection, the tolerance mask).
 """
 import ctypes
 import json
@@ -170,8 +177,51 @@ def pin_invariances():
     assert np.array_equal(ref_r, ref)
 
 
+def pin_projection_select():
+    base = W.tiny_decode(seed=9, T=12)
+    w = W.Workload("tiny_3proj", base.hidden, 3, base.ranks, base.token_adapter_idx, None,
+                   num_pages=3 * base.num_pages, kv_pages=0, shuffle_seed=5, seed=21)
+    p = 2
+    x, y0 = w.x(p), w.y0(p)
+    # the projections really differ, so a wrong projection cannot agree by accident
+    assert not np.array_equal(x, w.x(0)) and not np.array_equal(y0, w.y0(0))
+    want = y0.astype(np.float64).copy()
+    for a in np.unique(w.token_adapter_idx):
+        if a < 0:
+            continue
+        rows = np.nonzero(w.token_adapter_idx == a)[0]
+        At, B = w.factors(int(a))
+        assert not np.array_equal(At[p], At[0])
+        X = x[rows].astype(np.float64)
+        want[rows] += float(w.scaling()[a]) * (X @ At[p].T.astype(np.float64)) @ B[p].astype(np.float64)
+    np.testing.assert_allclose(oracle.workload_reference(w, p=p), want, rtol=1e-12, atol=1e-12)
+
+
+def pin_tolerance_mask():
+    # bound = 1e-3 + 1e-2 |ref|: 0.011, 0.021, 0.001, 0.006, 1.001, 0.011
+    ref = np.array([1.0, -2.0, 0.0, -0.5, 100.0, -1.0])
+    bound = np.array([0.011, 0.021, 0.001, 0.006, 1.001, 0.011])
+    cases = [
+        (ref + 0.9 * bound, [True] * 6),     # inside, above ref
+        (ref - 0.9 * bound, [True] * 6),     # inside, below ref
+        (ref + 1.1 * bound, [False] * 6),    # outside, above ref
+        (ref - 1.1 * bound, [False] * 6),    # outside, below ref
+        # a got of larger magnitude than ref, just inside the bound
+        (np.array([1.0105, -2.0205, 0.0009, -0.5059, 100.999, -1.0108]), [True] * 6),
+        # a got of smaller magnitude than ref, just inside the bound (a bound taken on |got|
+        # would reject four of these); 0.0011 from a zero ref is outside
+        (np.array([0.9895, -1.9792, -0.0011, -0.49405, 99.005, -0.98905]),
+         [True, True, False, True, True, True]),
+        (np.array([np.nan, -2.0, 0.0, np.inf, 100.0, -1.0]), [False, True, True, False, True, True]),
+    ]
+    for got, want in cases:
+        mask = oracle.within_tolerance(got.astype(np.float64), ref, 1e-3, 1e-2)
+        assert mask.tolist() == want, (got.tolist(), mask.tolist(), want)
+
+
 PINS = [pin_half_decode, pin_golden, pin_merged_weight, pin_exact_rational,
-        pin_grouped_blas, pin_zero_B, pin_base_only, pin_invariances]
+        pin_grouped_blas, pin_zero_B, pin_base_only, pin_invariances,
+        pin_projection_select, pin_tolerance_mask]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
@@ -236,4 +286,39 @@ def test_mutants_are_caught():
     finally:
         oracle._lib = real
         shutil.rmtree(tmp, ignore_errors=True)
+    assert not survived, f"pins missed planted mistakes: {survived}"
+
+
+# Mistakes planted in the Python side of the oracle (projection selection and the parity
+# bound), each applied to a copy of the function's source in the module's namespace.
+PY_MUTANTS = {
+    "factor_of_projection_0": ("workload_reference", "factors[a] = (At[p], B[p])",
+                               "factors[a] = (At[0], B[p])"),
+    "B_of_projection_0": ("workload_reference", "factors[a] = (At[p], B[p])",
+                          "factors[a] = (At[p], B[0])"),
+    "x_of_projection_0": ("workload_reference", "x = w.x(p) if x is None else x",
+                          "x = w.x(0) if x is None else x"),
+    "rtol_times_got": ("within_tolerance", "rtol * np.abs(ref)", "rtol * np.abs(got)"),
+    "dropped_abs": ("within_tolerance", "np.abs(got.astype(np.float64) - ref)",
+                    "(got.astype(np.float64) - ref)"),
+    "rtol_dropped": ("within_tolerance", "atol + rtol * np.abs(ref)", "atol + np.abs(ref) * 0"),
+}
+
+
+def test_python_mutants_are_caught():
+    import inspect
+    import textwrap
+    survived = []
+    for name, (fn, old, new) in PY_MUTANTS.items():
+        real = getattr(oracle, fn)
+        src = textwrap.dedent(inspect.getsource(real))
+        assert old in src, name
+        ns = dict(vars(oracle))
+        exec(compile(src.replace(old, new, 1), f"<mutant {name}>", "exec"), ns)
+        setattr(oracle, fn, ns[fn])
+        try:
+            if _pins_pass():
+                survived.append(name)
+        finally:
+            setattr(oracle, fn, real)
     assert not survived, f"pins missed planted mistakes: {survived}"
