@@ -285,9 +285,10 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const __grid_constant__ Pla
     short *tslot = reinterpret_cast<short *>(gperm + kMaxPlanGroups);      // [Tc] hash slot of the token (-1: none)
     short *tpos = tslot + kMaxPlanTokens;                                  // [Tc] the token's place within its group
     DirEntry *sdir = reinterpret_cast<DirEntry *>(tpos + kMaxPlanTokens);  // [max_adapters] when dir_cache
-    __shared__ int warp_tot2[33][2];
-    __shared__ int s_lo, s_hi, s_G, s_nit;
+    __shared__ int warp_tot4[33][4];
+    __shared__ int s_lo, s_hi, s_G;
     __shared__ int s_bucket[kRankBuckets + 1], s_bcur[kRankBuckets + 1];
+    __shared__ int s_proj[kMaxApplyProj];   // the call's projection slots (indexed per unit)
     const int tid = threadIdx.x, lane = tid & 31;
 
     griddep_launch_dependents();
@@ -315,6 +316,7 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const __grid_constant__ Pla
         s_hi = hi;
         s_G = 0;
     }
+    if (tid < kMaxApplyProj) s_proj[tid] = a.proj[tid];
     if (tid <= kRankBuckets) {
         s_bucket[tid] = 0;
         s_bcur[tid] = 0;
@@ -410,95 +412,146 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const __grid_constant__ Pla
     }
     __syncthreads();
 
-    // 3. per-group offsets (tokens, items) in that order
+    // 3. per-group offsets in that order: tokens, items, shrink units, partial words.  A
+    //    group's items hold kTok tokens each but the last, so these four give every unit's
+    //    place in the list and in the partial scratch.
+    const int NP = a.n_proj, NB = a.nblk;
+    // the hash keys are not read after step 1; HS >= 2 G, so they hold both tables
+    int *pus = keys;        // [position] first shrink unit
+    int *puw = keys + G;    // [position] first partial word
     const int per_g = ceil_div(G > 0 ? G : 1, NT);
     const int p0 = tid * per_g;
-    int mine[2] = {0, 0};
-    for (int q = 0; q < per_g && p0 + q < G; ++q) {
-        const int n = hcnt[gslot[gperm[p0 + q]]];
-        mine[0] += n;
-        mine[1] += ceil_div(n, kTok);
-    }
-    int off[2], tot[2];
-    block_excl_scan<2>(mine, warp_tot2, off, tot);
+    int mine[4] = {0, 0, 0, 0};
     for (int q = 0; q < per_g && p0 + q < G; ++q) {
         const int g = gperm[p0 + q];
-        const int n = hcnt[gslot[g]];
+        const int n = hcnt[gslot[g]], nch = ceil_div(grank[g], kRC);
+        mine[0] += n;
+        mine[1] += ceil_div(n, kTok);
+        mine[2] += NP * NB * nch * ceil_div(n, kTok);
+        mine[3] += NP * NB * nch * kRC * n;
+    }
+    int off[4], tot[4];
+    block_excl_scan<4>(mine, warp_tot4, off, tot);
+    for (int q = 0; q < per_g && p0 + q < G; ++q) {
+        const int g = gperm[p0 + q];
+        const int n = hcnt[gslot[g]], nch = ceil_div(grank[g], kRC);
         gtok[g] = off[0];
         pit[p0 + q] = off[1];
+        pus[p0 + q] = off[2];
+        puw[p0 + q] = off[3];
         off[0] += n;
         off[1] += ceil_div(n, kTok);
+        off[2] += NP * NB * nch * ceil_div(n, kTok);
+        off[3] += NP * NB * nch * kRC * n;
     }
-    if (tid == 0) s_nit = tot[1];
-    __syncthreads();
-    const int n_items = s_nit;
-    const int NP = a.n_proj, NB = a.nblk;
-
-    // 4. the units of every item.  Each thread takes a contiguous run of items, so one scan
-    //    of (shrink units, partial floats) per item gives every item's place in the list.
-    //    An item finds its group position by binary search over the strictly increasing
-    //    first-item offsets.
-    struct ItemInfo {
-        int g, t0, nt, rank, nch;
-    };
-    auto item_info = [&](int i) {
-        int lo_p = 0, hi_p = G - 1;
-        while (lo_p < hi_p) {
-            const int mid = (lo_p + hi_p + 1) >> 1;
-            if (pit[mid] <= i) lo_p = mid; else hi_p = mid - 1;
-        }
-        ItemInfo f;
-        f.g = gperm[lo_p];
-        f.t0 = (i - pit[lo_p]) * kTok;
-        f.nt = min(kTok, hcnt[gslot[f.g]] - f.t0);
-        f.rank = grank[f.g];
-        f.nch = ceil_div(f.rank, kRC);
-        return f;
-    };
-    const int per_i = ceil_div(n_items > 0 ? n_items : 1, NT);
-    const int i0 = tid * per_i;
-    int cnt[2] = {0, 0};
-    for (int q = 0; q < per_i && i0 + q < n_items; ++q) {
-        const ItemInfo f = item_info(i0 + q);
-        cnt[0] += NP * NB * f.nch;
-        cnt[1] += NP * f.nch * NB * f.nt * kRC;
-    }
-    int uo[2], ut[2];
-    block_excl_scan<2>(cnt, warp_tot2, uo, ut);
-    const int n_shrink = ut[0];
+    const int n_items = tot[1];
+    const int n_shrink = tot[2];
     const int64_t n_units = (int64_t)n_shrink + (int64_t)n_items * NP * NB;
-    if (n_units > a.L.cap_units || (int64_t)ut[1] > a.L.cap_words) {
+    if (n_units > a.L.cap_units || (int64_t)tot[3] > a.L.cap_words) {
         if (tid == 0) plan_refuse(a);
         return;
     }
-    for (int q = 0; q < per_i && i0 + q < n_items; ++q) {
-        const int i = i0 + q;
-        const ItemInfo f = item_info(i);
-        Unit u;
-        u.tok_start = gtok[f.g] + f.t0;
-        u.rank = f.rank;
-        u.scaling = a.scaling ? a.scaling[gad[f.g]] : gscale[f.g];
-        const int per_proj = f.nch * NB * f.nt * kRC;
-        for (int pj = 0; pj < NP; ++pj) {
-            u.pt_base = gpt[f.g] + (int64_t)a.proj[pj] * 2 * f.rank;
-            u.uoff = uo[1] + pj * per_proj;
-            u.pad = 0;
-            for (int b = 0; b < NB; ++b) {
-                for (int c = 0; c < f.nch; ++c) {
-                    u.packed = unit_pack(f.nt, 0, pj, b, c);
-                    a.L.units[uo[0] + (pj * NB + b) * f.nch + c] = u;
-                }
-                u.packed = unit_pack(f.nt, 1, pj, b, 0);
-                a.L.units[n_shrink + (int64_t)i * NP * NB + pj * NB + b] = u;
-            }
-        }
-        uo[0] += NP * NB * f.nch;
-        uo[1] += NP * per_proj;
-    }
+    __syncthreads();
+
+    // the token order first: the token tables are free afterwards
     for (int i = tid; i < Tc; i += NT) {
         const int h = tslot[i];
         if (h >= 0)
             a.L.tok_order[gtok[hgrp[h]] + tpos[i]] = a.t_begin + i;
+    }
+    __syncthreads();
+
+    // 4. the units, one per thread in list order (consecutive threads write consecutive
+    //    units).  A unit's group position comes from a table of the group position of
+    //    every 32-unit chunk's first unit (kept in the token tables' space), followed
+    //    forward; lists too long for the table search the strictly increasing offsets.
+    //    Divisions by the per-call divisors use exact reciprocal multiplies.
+    const int n_exp = n_items * NP * NB;
+    const int cs = ceil_div(n_shrink, 32), ce = ceil_div(n_exp, 32);
+    const bool table = cs + ce <= kMaxPlanTokens;   // ints available in tslot + tpos
+    int *tabS = reinterpret_cast<int *>(tslot), *tabE = tabS + cs;
+    __shared__ unsigned long long s_mag[3][kMaxRank / kRC + 1];   // ceil(2^32 / d), per nch
+    __shared__ unsigned long long s_mag_e, s_mag_nb;
+    auto magic = [](uint32_t d) { return (unsigned long long)(0xffffffffu / d) + 1ull; };
+    if (tid <= kMaxRank / kRC) {
+        const uint32_t nch = tid < 1 ? 1u : (uint32_t)tid;
+        s_mag[0][tid] = magic((uint32_t)(NP * NB) * nch);
+        s_mag[1][tid] = magic((uint32_t)NB * nch);
+        s_mag[2][tid] = magic(nch);
+    }
+    if (tid == 0) {
+        s_mag_e = magic((uint32_t)(NP * NB));
+        s_mag_nb = magic((uint32_t)NB);
+    }
+    if (table) {
+        for (int q = 0; q < per_g && p0 + q < G; ++q) {
+            const int pos = p0 + q;
+            const int u_lo = pus[pos], u_hi = pos + 1 < G ? pus[pos + 1] : n_shrink;
+            for (int c = ceil_div(u_lo, 32); 32 * c < u_hi; ++c) tabS[c] = pos;
+            const int e_lo = pit[pos] * NP * NB, e_hi = pos + 1 < G ? pit[pos + 1] * NP * NB : n_exp;
+            for (int c = ceil_div(e_lo, 32); 32 * c < e_hi; ++c) tabE[c] = pos;
+        }
+    }
+    __syncthreads();
+    auto div = [](uint32_t x, unsigned long long m) { return (int)((x * m) >> 32); };
+    auto last_le = [&](const int *arr, int key) {
+        int lo_p = 0, hi_p = G - 1;
+        while (lo_p < hi_p) {
+            const int mid = (lo_p + hi_p + 1) >> 1;
+            if (arr[mid] <= key) lo_p = mid; else hi_p = mid - 1;
+        }
+        return lo_p;
+    };
+    for (int k = tid; k < n_units; k += NT) {
+        const bool expand = k >= n_shrink;
+        int pos, ig, l, nch, item = 0;   // group position, item within the group, unit within the item
+        if (!expand) {
+            if (table) {
+                pos = tabS[k >> 5];
+                while (pos + 1 < G && pus[pos + 1] <= k) ++pos;
+            } else {
+                pos = last_le(pus, k);
+            }
+            nch = ceil_div(grank[gperm[pos]], kRC);
+            const int r = k - pus[pos];
+            ig = div((uint32_t)r, s_mag[0][nch]);
+            l = r - ig * NP * NB * nch;
+        } else {
+            const int e = k - n_shrink;
+            item = div((uint32_t)e, s_mag_e);
+            l = e - item * NP * NB;
+            if (table) {
+                pos = tabE[e >> 5];
+                while (pos + 1 < G && pit[pos + 1] <= item) ++pos;
+            } else {
+                pos = last_le(pit, item);
+            }
+            ig = item - pit[pos];
+            nch = ceil_div(grank[gperm[pos]], kRC);
+        }
+        const int g = gperm[pos];
+        const int rank = grank[g];
+        const int t0 = ig * kTok, nt = min(kTok, hcnt[gslot[g]] - t0);
+        int pj, b, c;
+        if (!expand) {
+            pj = div((uint32_t)l, s_mag[1][nch]);
+            const int rem = l - pj * NB * nch;
+            b = div((uint32_t)rem, s_mag[2][nch]);
+            c = rem - b * nch;
+        } else {
+            pj = div((uint32_t)l, s_mag_nb);
+            b = l - pj * NB;
+            c = 0;
+        }
+        Unit u;
+        u.tok_start = gtok[g] + t0;
+        u.packed = unit_pack(nt, expand ? 1 : 0, pj, b, c);
+        u.rank = rank;
+        u.scaling = a.scaling ? a.scaling[gad[g]] : gscale[g];
+        u.pt_base = gpt[g] + (int64_t)s_proj[pj] * 2 * rank;
+        u.uoff = puw[pos] + ig * NP * NB * nch * kRC * kTok + pj * (nch * NB * nt * kRC);
+        u.pad = 0;
+        a.L.units[k] = u;
     }
     if (tid == 0) {
         a.L.hdr->n_groups = G;
