@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--prefetch", type=int, default=0, metavar="K",
                     help="also measure K later batches' adapter loads against the deltas (\"prefetch\")")
+    ap.add_argument("--load-mode", choices=["zero_copy", "copy_engine"], default="zero_copy",
+                    help="the pool's adapter load path for the end-to-end and load measurements")
     ap.add_argument("--bmm", action="store_true",
                     help="also time the padded batched-GEMM comparison path (decode-only workloads)")
     ap.add_argument("--pressure", type=int, default=0, metavar="K",
@@ -538,6 +540,8 @@ def main():
     w = W.by_name(args.workload, seed=replica_seed(args.seed, rank), **wkw)
     used = w.used_adapters()
     sess = PoolSession(w, device=local)
+    load_mode = {"zero_copy": rdp.SLORA_LOAD_ZERO_COPY, "copy_engine": rdp.SLORA_LOAD_COPY_ENGINE}[args.load_mode]
+    rdp.slora_pool_set_load_mode(sess.pool, load_mode)
     stream = torch.cuda.current_stream()
     sess.load(used, stream)
     dev = torch.device("cuda", local)
@@ -761,8 +765,11 @@ def main():
     load = {"adapters": len(used), "bytes": int(adapter_bytes),
             "wall_ms": statistics.median(load_wall), "stream_ms": statistics.median(load_dev),
             "gb_per_s": adapter_bytes / (statistics.median(load_wall) * 1e-3) / 1e9,
-            "includes": "host call (page allocation, page tables, launches) and the load kernel reading "
-                        "the pinned store over the CPU-GPU link; the directory update"}
+            "mode": args.load_mode,
+            "includes": "host call (page allocation, page tables, launches) and the load path (" +
+                        ("the load kernel reading the pinned store over the CPU-GPU link" if args.load_mode == "zero_copy"
+                         else "one cudaMemcpyAsync per adapter into the staging ring, the load kernel from it") +
+                        "); the directory update"}
     e2e_job_ms, _ = job_totals(statistics.mean(e2e_ms) if e2e_ms else float("nan"), float(w.T), dev, world)
     warm_job_ms, _ = job_totals(statistics.mean(warm_ms) if warm_ms else float("nan"), float(w.T), dev, world)
     e2e_value = tokens_per_s_per_layer(job_tokens, w.n_layers, e2e_job_ms)
@@ -770,7 +777,10 @@ def main():
     prefetch = None
     if args.prefetch > 0 and w.n_seg == 0:
         from rank_delta_paged_gb300.harness import prefetch_overlap
-        prefetch = prefetch_overlap(sess, args.prefetch, stream)
+        prefetch = {name: prefetch_overlap(sess, args.prefetch, stream, mode)
+                    for name, mode in (("zero_copy", rdp.SLORA_LOAD_ZERO_COPY),
+                                       ("copy_engine", rdp.SLORA_LOAD_COPY_ENGINE))}
+        rdp.slora_pool_set_load_mode(sess.pool, load_mode)
         sess.load(used, stream)
     pressure = None
     if args.pressure > 0:
@@ -816,7 +826,7 @@ def main():
                 "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": e2e_job_ms,
                 "includes": "H2D of x, y0, token map; cold load of the batch's adapters from the "
-                            "pinned store (the load kernel reads it over the CPU-GPU link); delta; D2H of y "
+                            "pinned store (load path: " + args.load_mode + "); delta; D2H of y "
                             "(the eviction before each step is outside the timed part)",
                 "warm": {"value": warm_value, "ms_per_step": warm_job_ms,
                          "h2d_bytes_per_step": int(h2d - adapter_bytes), "d2h_bytes_per_step": int(d2h),

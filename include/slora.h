@@ -181,7 +181,8 @@ slora_status slora_adapter_unregister(slora_pool_t pool, int32_t adapter_id,
  * load() takes 2 * rank * n_proj pages from the free list, writes the adapter's page
  * table into its pinned host copy, and on the pool's side stream runs the load kernel,
  * which reads the pinned store rows and their page ids straight from host memory
- * (over the CPU-GPU link: no staging buffer, no copy per adapter) and writes each row
+ * (over the CPU-GPU link: no staging buffer, no copy per adapter; the copy-engine mode
+ * of slora_pool_set_load_mode stages the rows in device memory first) and writes each row
  * to its page, bit for bit, and the page ids to the device page-table arena; then it
  * publishes the directory entry.  `stream` then waits on an event recorded after that
  * work, so kernels enqueued later on `stream` see the adapter; the host call does not
@@ -205,6 +206,35 @@ slora_status slora_adapter_evict(slora_pool_t pool, int32_t adapter_id, slora_st
 slora_status slora_adapters_evict(slora_pool_t pool, int32_t n, const int32_t *adapter_ids /*host*/,
                                   slora_stream_t stream);
 slora_status slora_adapter_is_resident(slora_pool_t pool, int32_t adapter_id, int32_t *out);
+
+/* ---------------------------------------------------------------------------
+ * Load path selection (explainer, "Algorithm / figure walkthrough" step 2: the next
+ * iteration's adapters are prefetched into the pool while the current one computes;
+ * "Limitations": host bandwidth bounds how fast adapters swap in).
+ *
+ * mode SLORA_LOAD_ZERO_COPY (the default): the load kernel reads the pinned store over
+ *   the CPU-GPU link itself, as described above.  Its CTAs take SM time from kernels
+ *   that run beside a load.
+ * mode SLORA_LOAD_COPY_ENGINE: every adapter's pinned store block goes to a device
+ *   staging ring with one cudaMemcpyAsync on the side stream (the copy engines move it;
+ *   no SM takes part), then one load kernel per ring-full of adapters writes the rows
+ *   from the staging ring (HBM) to their pages.  The ring is reused in stream order.
+ * staging_bytes: the ring's size for the copy-engine mode (0: 256 MiB); it grows, with a
+ *   synchronisation of the side stream, when a load meets an adapter larger than it.
+ *   This call allocates the ring (cudaMalloc) when the mode needs one and frees it when
+ *   the mode no longer does, after the side stream's pending work.  Results of later
+ *   loads do not depend on the mode: both write the same bits to the same pages.
+ * Returns SLORA_ERR_INVALID_ARG for another mode or a negative size.
+ * ------------------------------------------------------------------------- */
+enum { SLORA_LOAD_ZERO_COPY = 0, SLORA_LOAD_COPY_ENGINE = 1 };
+slora_status slora_pool_set_load_mode(slora_pool_t pool, int32_t mode, int64_t staging_bytes);
+slora_status slora_pool_get_load_mode(slora_pool_t pool, int32_t *mode, int64_t *staging_bytes);
+/* Measurement hook.  event: a cudaEvent_t created by the caller on the pool's device, or
+ * NULL to clear.  While set, every load that has work records it on the pool's side
+ * stream before that work, so the caller can see when a load started relative to work on
+ * its own streams.  The pool does not take ownership.  The S-LoRA pages have no
+ * counterpart for it. */
+slora_status slora_pool_set_load_start_event(slora_pool_t pool, void *event);
 
 /* ---------------------------------------------------------------------------
  * Residency under pool pressure (explainer, "The mechanism": adapters the running

@@ -30,6 +30,8 @@ __all__ = [
     "slora_adapter_pages", "slora_adapter_rank", "slora_page_read", "slora_get_device_status",
     "slora_pool_launch_count",
     "slora_pool_set_stage_event",
+    "slora_pool_set_load_mode", "slora_pool_get_load_mode", "slora_pool_set_load_start_event",
+    "SLORA_LOAD_ZERO_COPY", "SLORA_LOAD_COPY_ENGINE",
     "slora_adapters_evict",
     "slora_debug_set_prefill_cluster",
     "slora_lora_apply_multi",
@@ -72,6 +74,9 @@ _SIGS = {
     "slora_get_device_status": [_P, _P],
     "slora_pool_launch_count": [_P, _P],
     "slora_pool_set_stage_event": [_P, _P],
+    "slora_pool_set_load_mode": [_P, _I32, _I64],
+    "slora_pool_get_load_mode": [_P, _P, _P],
+    "slora_pool_set_load_start_event": [_P, _P],
     "slora_adapters_evict": [_P, _I32, _P, _P],
     "slora_debug_set_prefill_cluster": [_I32],
     "slora_lora_apply_multi": [_P, _I32, _P, _P, _P, _I32, _P, _P, _I32, _P, _P],
@@ -400,6 +405,30 @@ def slora_pool_launch_count(pool: int) -> int:
 def slora_debug_set_prefill_cluster(ctas: int) -> None:
     """Force the prefill kernel's CTAs per cluster (1, 2, 4, 8) for later calls; 0 = auto."""
     _call("slora_debug_set_prefill_cluster", int(ctas))
+
+
+SLORA_LOAD_ZERO_COPY = 0
+SLORA_LOAD_COPY_ENGINE = 1
+
+
+def slora_pool_set_load_mode(pool: int, mode: int, staging_bytes: int = 0) -> None:
+    """Choose the load path: SLORA_LOAD_ZERO_COPY or SLORA_LOAD_COPY_ENGINE (staging ring of
+    ``staging_bytes``, 0 = the library's default)."""
+    _call("slora_pool_set_load_mode", pool, int(mode), int(staging_bytes))
+
+
+def slora_pool_get_load_mode(pool: int):
+    """(mode, staging_bytes) of the pool's load path."""
+    m, b = ctypes.c_int32(), ctypes.c_int64()
+    _call("slora_pool_get_load_mode", pool, ctypes.byref(m), ctypes.byref(b))
+    return m.value, b.value
+
+
+def slora_pool_set_load_start_event(pool: int, event) -> None:
+    """Record `event` (a torch.cuda.Event, a raw cudaEvent_t as int, or None) on the pool's
+    side stream before the work of every later load; None clears it."""
+    handle = 0 if event is None else int(getattr(event, "cuda_event", event))
+    _call("slora_pool_set_load_start_event", pool, ctypes.c_void_p(handle))
 
 
 def slora_pool_set_stage_event(pool: int, event) -> None:

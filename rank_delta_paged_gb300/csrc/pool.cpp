@@ -61,6 +61,10 @@ struct slora_pool {
     std::vector<AdapterRec> adapters;
     int64_t launches = 0;  // kernels launched by this pool
     cudaEvent_t stage_event = nullptr;   // measurement hook: recorded between plan and delta
+    cudaEvent_t load_start_event = nullptr;   // measurement hook: recorded before a load's work
+    int32_t load_mode = SLORA_LOAD_ZERO_COPY;
+    uint8_t *staging = nullptr;          // copy-engine mode: device staging ring
+    int64_t staging_bytes = 0;
     int32_t max_rank = 0;  // largest registered rank (sizes the plan scratch)
     LruIndex lru;          // resident adapters by last acquire / load; pins of running batches
     int64_t n_loaded = 0, n_evicted = 0;
@@ -106,13 +110,14 @@ void free_pool_memory(slora_pool *p)
     if (p->dir_dev) cudaFree(p->dir_dev);
     if (p->status_dev) cudaFree(p->status_dev);
     if (p->plan.base) cudaFree(p->plan.base);
+    if (p->staging) cudaFree(p->staging);
     if (p->release_event) cudaEventDestroy(p->release_event);
     if (p->load_event) cudaEventDestroy(p->load_event);
     if (p->side) cudaStreamDestroy(p->side);
 }
 
-// Staging rows: enough for the largest registered adapter, at least 64 MiB, at most
-// 512 MiB (loads larger than that are split into several copy + scatter rounds).
+constexpr int64_t kDefaultStagingBytes = 256ll << 20;
+
 }  // namespace
 
 extern "C" {
@@ -359,8 +364,8 @@ slora_status slora_adapters_load(slora_pool_t p, int32_t n, const int32_t *ids, 
     cudaStream_t side = p->side;
     if (p->release_pending)
         CUDA_TRY(cudaStreamWaitEvent(side, p->release_event, 0));
-    // One kernel per 512 adapters reads the rows and their page ids straight from the
-    // pinned store and page table, writes the pages and the page-table arena.
+    if (p->load_start_event)
+        CUDA_TRY(cudaEventRecord(p->load_start_event, side));
     ScatterArgs sargs;
     sargs.n_runs = 0;
     auto flush = [&]() -> slora_status {
@@ -372,15 +377,53 @@ slora_status slora_adapters_load(slora_pool_t p, int32_t n, const int32_t *ids, 
         sargs.n_runs = 0;
         return SLORA_OK;
     };
-    for (int32_t id : todo) {
-        AdapterRec &a = p->adapters[(size_t)id];
-        ScatterRun &run = sargs.runs[sargs.n_runs++];
-        run.src = a.store_dev;
-        run.pt_src = a.pt_host_dev;
-        run.pt_index0 = a.pt_off;
-        run.nrows = adapter_rows(p, a);
-        if (sargs.n_runs == kMaxRunsPerLaunch && (st = flush()) != SLORA_OK)
-            return st;
+    if (p->load_mode == SLORA_LOAD_COPY_ENGINE) {
+        // One cudaMemcpyAsync per adapter moves its pinned store block (all its rows,
+        // contiguous) into the staging ring; one load kernel per ring-full writes the rows
+        // from the ring to their pages.  Copies into a reused part of the ring are ordered
+        // after the kernel that read it (one stream).
+        int64_t largest = 0;
+        for (int32_t id : todo)
+            largest = std::max(largest, adapter_rows(p, p->adapters[(size_t)id]) * p->hidden * 2);
+        if (largest > p->staging_bytes) {
+            CUDA_TRY(cudaStreamSynchronize(side));
+            if (p->staging) cudaFree(p->staging);
+            p->staging = nullptr;
+            p->staging_bytes = 0;
+            CUDA_TRY(cudaMalloc(&p->staging, (size_t)largest));
+            p->staging_bytes = largest;
+        }
+        int64_t off = 0;
+        for (int32_t id : todo) {
+            AdapterRec &a = p->adapters[(size_t)id];
+            const int64_t rows = adapter_rows(p, a), bytes = rows * p->hidden * 2;
+            if (off + bytes > p->staging_bytes || sargs.n_runs == kMaxRunsPerLaunch) {
+                if ((st = flush()) != SLORA_OK)
+                    return st;
+                off = 0;
+            }
+            CUDA_TRY(cudaMemcpyAsync(p->staging + off, a.store, (size_t)bytes, cudaMemcpyHostToDevice, side));
+            ScatterRun &run = sargs.runs[sargs.n_runs++];
+            run.src = p->staging + off;
+            run.pt_src = a.pt_host_dev;
+            run.pt_index0 = a.pt_off;
+            run.nrows = rows;
+            off += (bytes + 255) / 256 * 256;
+        }
+    } else {
+        // One kernel per kMaxRunsPerLaunch adapters reads the rows and their page ids
+        // straight from the pinned store and page table, writes the pages and the
+        // page-table arena.
+        for (int32_t id : todo) {
+            AdapterRec &a = p->adapters[(size_t)id];
+            ScatterRun &run = sargs.runs[sargs.n_runs++];
+            run.src = a.store_dev;
+            run.pt_src = a.pt_host_dev;
+            run.pt_index0 = a.pt_off;
+            run.nrows = adapter_rows(p, a);
+            if (sargs.n_runs == kMaxRunsPerLaunch && (st = flush()) != SLORA_OK)
+                return st;
+        }
     }
     if ((st = flush()) != SLORA_OK)
         return st;
@@ -727,6 +770,46 @@ slora_status slora_lora_apply_multi(slora_pool_t p, int32_t n, const int32_t *pr
     if (st != SLORA_OK)
         return st;
     return apply_list(p, "lora_apply_multi", pl, T, idx, seg_indptr, n_seg, scaling, stream);
+}
+
+slora_status slora_pool_set_load_mode(slora_pool_t p, int32_t mode, int64_t staging_bytes)
+{
+    if (!p)
+        return fail(SLORA_ERR_INVALID_ARG, "pool_set_load_mode: null pool");
+    if ((mode != SLORA_LOAD_ZERO_COPY && mode != SLORA_LOAD_COPY_ENGINE) || staging_bytes < 0)
+        return fail(SLORA_ERR_INVALID_ARG, "pool_set_load_mode: mode=%d staging_bytes=%lld", mode,
+                    (long long)staging_bytes);
+    DEVICE_SCOPE(p);
+    const int64_t want = mode == SLORA_LOAD_COPY_ENGINE ? (staging_bytes > 0 ? staging_bytes : kDefaultStagingBytes) : 0;
+    if (want != p->staging_bytes) {
+        CUDA_TRY(cudaStreamSynchronize(p->side));   // no load still reads the old ring
+        if (p->staging) cudaFree(p->staging);
+        p->staging = nullptr;
+        p->staging_bytes = 0;
+        if (want > 0) {
+            CUDA_TRY(cudaMalloc(&p->staging, (size_t)want));
+            p->staging_bytes = want;
+        }
+    }
+    p->load_mode = mode;
+    return SLORA_OK;
+}
+
+slora_status slora_pool_get_load_mode(slora_pool_t p, int32_t *mode, int64_t *staging_bytes)
+{
+    if (!p || !mode || !staging_bytes)
+        return fail(SLORA_ERR_INVALID_ARG, "pool_get_load_mode");
+    *mode = p->load_mode;
+    *staging_bytes = p->staging_bytes;
+    return SLORA_OK;
+}
+
+slora_status slora_pool_set_load_start_event(slora_pool_t p, void *event)
+{
+    if (!p)
+        return fail(SLORA_ERR_INVALID_ARG, "pool_set_load_start_event: null pool");
+    p->load_start_event = (cudaEvent_t)event;
+    return SLORA_OK;
 }
 
 slora_status slora_pool_set_stage_event(slora_pool_t p, void *event)

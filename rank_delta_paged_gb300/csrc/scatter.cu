@@ -1,7 +1,8 @@
-// Adapter load: rows of the pinned host store go straight to their pool pages, bit for
-// bit, and the page ids of those rows into the device page-table arena, in one kernel
-// that reads host memory over the CPU-GPU link (no staging buffer, no copy per adapter);
-// plus the adapter-directory update that publishes a load.
+// Adapter load: rows of an adapter store go to their pool pages, bit for bit, and the
+// page ids of those rows into the device page-table arena, in one kernel that reads the
+// rows either from the pinned host store over the CPU-GPU link (zero-copy mode) or from a
+// device staging ring the copy engines filled (copy-engine mode); plus the
+// adapter-directory update that publishes a load.
 // (S-LoRA: Serving Thousands of Concurrent LoRA Adapters (explainer), "The mechanism":
 // only the adapters the running batch needs are fetched into the paged pool; a block
 // table maps each logical row to its physical page.)
@@ -15,10 +16,11 @@ namespace {
 constexpr int kScatterThreads = 256;
 
 // One warp moves one row (hidden * 2 bytes, a multiple of 128 bytes): its page id from the
-// host page table into the arena, and the row itself with 16-byte loads from host memory.
-// The page id and up to 16 loads per lane (a whole row at hidden 4096) are in flight
-// together, so a row costs about one round trip over the CPU-GPU link.  Rows are found by
-// a binary search over the runs' row prefix.
+// host page table into the arena, and the row itself with 16-byte loads from its source
+// (host memory, or the staging ring in device memory).  The page id and up to 16 loads
+// per lane (a whole row at hidden 4096) are in flight together, so a row costs about one
+// round trip over the CPU-GPU link.  Rows are found by a binary search over the runs' row
+// prefix.
 __global__ void __launch_bounds__(kScatterThreads)
 scatter_kernel(int32_t *__restrict__ pt_arena, uint4 *__restrict__ pool, int64_t num_pages, int32_t row_vecs,
                const __grid_constant__ ScatterArgs args, int32_t *status)

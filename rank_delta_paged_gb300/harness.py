@@ -77,7 +77,7 @@ class PoolSession:
         self.close()
 
 
-def prefetch_overlap(sess: PoolSession, K: int = 6, stream=None) -> dict:
+def prefetch_overlap(sess: PoolSession, K: int = 6, stream=None, mode: Optional[int] = None) -> dict:
     """How far the adapter loads of later batches hide behind the deltas of earlier ones.
 
     The pool runs every load on its own side stream and only makes the caller's stream
@@ -95,10 +95,15 @@ def prefetch_overlap(sess: PoolSession, K: int = 6, stream=None) -> dict:
       serialized_ms  the same with the host waiting for the device after every apply, so no
                      load starts before the previous apply ends
       overlap_frac   (loads + applies - pipelined) / min(loads, applies)
-      link_gb_per_s  loaded bytes / loads_ms (the load kernel reads the pinned store over
-                     the CPU-GPU link)
+      link_gb_per_s  loaded bytes / loads_ms
+
+    ``mode`` selects the pool's load path first (SLORA_LOAD_ZERO_COPY: the load kernel reads
+    the pinned store over the CPU-GPU link; SLORA_LOAD_COPY_ENGINE: cudaMemcpyAsync into a
+    staging ring, then the load kernel from HBM); None keeps the pool's current one.
     """
-    from . import slora_lora_apply
+    from . import slora_lora_apply, slora_pool_get_load_mode, slora_pool_set_load_mode
+    if mode is not None:
+        slora_pool_set_load_mode(sess.pool, mode)
     w = sess.w
     batches = [w] + [w.later_batch(k) for k in range(1, K)]
     dev = torch.device("cuda", sess.device)
@@ -151,7 +156,8 @@ def prefetch_overlap(sess: PoolSession, K: int = 6, stream=None) -> dict:
             best[mode] = min(best.get(mode, t), t)
     evict_all()
     loads, applies, pipe = best["loads"], best["applies"], best["pipelined"]
-    return {"batches": K, "adapters_loaded": len(union), "bytes": int(nbytes),
+    return {"load_mode": ["zero_copy", "copy_engine"][slora_pool_get_load_mode(sess.pool)[0]],
+            "batches": K, "adapters_loaded": len(union), "bytes": int(nbytes),
             "loads_ms": loads, "applies_ms": applies, "pipelined_ms": pipe,
             "serialized_ms": best["serialized"],
             "overlap_frac": (loads + applies - pipe) / max(1e-9, min(loads, applies)),
