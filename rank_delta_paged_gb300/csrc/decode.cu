@@ -100,30 +100,70 @@ static_assert(2 * kPairs * 32 <= kRegionFloats, "y0 values fit a region");
 constexpr int kPtmpFloats = kRegionFloats * kConsumerWarps;
 
 struct PlanHeader {
-    int32_t n_groups, n_items, n_units, n_shrink;
+    int32_t n_groups, n_wg, n_units, n_shrink;   // n_wg: work groups (own items and packs)
     int32_t seg_lo, seg_hi, grab, pad;
 };
 
-// One unit of the delta kernel's work list: a shrink or an expand unit of one item (an
-// adapter and up to kTok of its tokens) and one projection of the call.
-//   packed: bits 0-4 tokens - 1, bit 5 expand, bits 6-8 projection slot, bits 9-11 hidden
-//           block, bits 12-15 rank chunk (shrink units)
-struct alignas(16) Unit {
-    int32_t tok_start;  // first position of the item's tokens in tok_order
-    uint32_t packed;
-    int32_t rank;
-    float scaling;      // the adapter's scaling (the call's override applied)
-    int64_t pt_base;    // arena index of the projection's page table (A^T rows, then B rows)
-    int32_t uoff;       // first word of the (item, projection)'s partials
-    int32_t pad;
-};
-static_assert(sizeof(Unit) == 32, "Unit layout");
+// Items (an adapter and up to kTok of its tokens) share a unit when they are small: the
+// last item of a group, of at most kPackTokens tokens and rank at most 2 kSlot, is
+// packable; packable items of rank <= kSlot fill kPackItems 16-row slots of one unit,
+// those of rank kSlot+1 .. 2 kSlot two 32-row slots.  Every item starts on a multiple of
+// 16 rows, so its K steps in the expand line up as in a unit of its own, and rows of
+// other items only add exact zeros to its sums.
+constexpr int kPackItems = 4;
+constexpr int kPackTokens = 2;
+constexpr int kSlot = 16;
+static_assert(kPackItems * kPackTokens <= kTok && kPackItems * kSlot == kRC, "a full pack fits one unit");
 
-__host__ __device__ inline uint32_t unit_pack(int nt, int expand, int pj, int b, int c)
+// One item of a unit.
+struct PackItem {
+    int64_t pt_base;    // arena index of the projection's page table (A^T rows, then B rows)
+    int32_t tok_start;  // first position of the item's tokens in tok_order
+    uint32_t geo;       // bits 0-6 first row in the unit, 7-17 rank, 18-20 first token in the
+                        // unit, 21-23 tokens - 1
+    float scaling;      // the adapter's scaling (the call's override applied)
+    int32_t uoff;       // first word of the (item, projection)'s partials
+};
+static_assert(sizeof(PackItem) == 24, "PackItem layout");
+
+__host__ __device__ inline uint32_t geo_pack(int row0, int rank, int t0, int nt)
+{
+    return (uint32_t)row0 | ((uint32_t)rank << 7) | ((uint32_t)t0 << 18) | ((uint32_t)(nt - 1) << 21);
+}
+__host__ __device__ inline int geo_row0(uint32_t g) { return (int)(g & 127u); }
+__host__ __device__ inline int geo_rank(uint32_t g) { return (int)((g >> 7) & 2047u); }
+__host__ __device__ inline int geo_t0(uint32_t g) { return (int)((g >> 18) & 7u); }
+__host__ __device__ inline int geo_nt(uint32_t g) { return (int)((g >> 21) & 7u) + 1; }
+
+// A unit as the delta kernel's warps see it: a shrink or an expand unit of one work group
+// (an item of its own, or a pack of items) and one projection of the call.  The plan writes
+// the work groups in this form for projection slot 0 with no unit fields (page-table bases
+// and partial offsets of slot 0, packed = tokens and items only); the lead warp adds the
+// unit's fields and the slot's offsets.
+//   packed: bits 0-4 tokens - 1 (all items), bit 5 expand, bits 6-8 projection slot,
+//           bits 9-11 hidden block, bits 12-15 rank chunk (shrink units), bits 16-17 items - 1
+//   rows:   rank rows: the item's rank (one item; chunks of kRC), or the last item's first
+//           row + its rank (a pack: one chunk)
+struct alignas(16) Unit {
+    uint32_t packed;
+    int32_t rows;
+    int32_t pad[2];
+    PackItem item[kPackItems];
+};
+static_assert(sizeof(Unit) == 112, "Unit layout");
+
+__host__ __device__ inline uint32_t unit_pack(int nt, int expand, int pj, int b, int c, int ni)
 {
     return (uint32_t)(nt - 1) | ((uint32_t)expand << 5) | ((uint32_t)pj << 6) | ((uint32_t)b << 9) |
-           ((uint32_t)c << 12);
+           ((uint32_t)c << 12) | ((uint32_t)(ni - 1) << 16);
 }
+
+// One entry of the work list: the work group and the unit's bits of `packed` (expand,
+// projection slot, hidden block, rank chunk).
+struct alignas(8) ListUnit {
+    int32_t wg;
+    uint32_t packed;
+};
 
 // The shrink units' partial sums: one 64-bit word per value, the fp32 bits in the low half
 // and the launch's tag in the high half, written with one relaxed store, so a reader that
@@ -131,9 +171,10 @@ __host__ __device__ inline uint32_t unit_pack(int nt, int expand, int pj, int b,
 struct PlanLayout {
     PlanHeader *hdr;
     int32_t *tok_order;
-    Unit *units;
+    Unit *wgs;              // work groups (projection slot 0, no unit fields)
+    ListUnit *units;        // the work list
     unsigned long long *upart;
-    int64_t cap_units, cap_words;
+    int64_t cap_wg, cap_units, cap_words;
 };
 
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -163,11 +204,13 @@ PlanLayout carve(void *base, int32_t cap_tokens, int32_t n_proj, int32_t nblk, i
     };
     const int64_t cap = cap_tokens;
     const int64_t nch = ceil_div(max_rank < 1 ? 1 : max_rank, kRC);
+    L.cap_wg = cap;
     L.cap_units = cap * n_proj * nblk * (nch + 1);
     L.cap_words = cap * n_proj * nblk * nch * kRC;
     L.hdr = (PlanHeader *)take(sizeof(PlanHeader));
     L.tok_order = (int32_t *)take(cap * 4);
-    L.units = (Unit *)take(L.cap_units * sizeof(Unit));
+    L.wgs = (Unit *)take(L.cap_wg * sizeof(Unit));
+    L.units = (ListUnit *)take(L.cap_units * sizeof(ListUnit));
     L.upart = (unsigned long long *)take(L.cap_words * 8);
     if (total)
         *total = off;
@@ -259,7 +302,7 @@ __device__ __forceinline__ void plan_refuse(const PlanArgs &a)
 {
     set_status(a.pv.status, SLORA_DEV_BAD_SEGMENT);
     a.L.hdr->n_groups = 0;
-    a.L.hdr->n_items = 0;
+    a.L.hdr->n_wg = 0;
     a.L.hdr->n_units = 0;
     a.L.hdr->n_shrink = 0;
     a.L.hdr->grab = 0;
@@ -285,7 +328,7 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const __grid_constant__ Pla
     short *tslot = reinterpret_cast<short *>(gperm + kMaxPlanGroups);      // [Tc] hash slot of the token (-1: none)
     short *tpos = tslot + kMaxPlanTokens;                                  // [Tc] the token's place within its group
     DirEntry *sdir = reinterpret_cast<DirEntry *>(tpos + kMaxPlanTokens);  // [max_adapters] when dir_cache
-    __shared__ int warp_tot4[33][4];
+    __shared__ int warp_tot8[33][8];
     __shared__ int s_lo, s_hi, s_G;
     __shared__ int s_bucket[kRankBuckets + 1], s_bcur[kRankBuckets + 1];
     __shared__ int s_proj[kMaxApplyProj];   // the call's projection slots (indexed per unit)
@@ -412,87 +455,117 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const __grid_constant__ Pla
     }
     __syncthreads();
 
-    // 3. per-group offsets in that order: tokens, items, shrink units, partial words.  A
-    //    group's items hold kTok tokens each but the last, so these four give every unit's
-    //    place in the list and in the partial scratch.
+    // 3. per-group offsets in that order.  A group's items hold kTok tokens each but the
+    //    last.  Its last item is packable when it has at most kPackTokens tokens and the
+    //    rank is at most 2 kSlot (class 1: rank <= kSlot, class 2: above); every other item
+    //    is a work group of its own.  Scanned per group: tokens, own items, their shrink
+    //    units, partial words, and per class the packable items and their tokens.
     const int NP = a.n_proj, NB = a.nblk;
     // the hash keys are not read after step 1; HS >= 2 G, so they hold both tables
-    int *pus = keys;        // [position] first shrink unit
+    int *pus = keys;        // [position] first shrink unit of the group's own items
     int *puw = keys + G;    // [position] first partial word
+    int *psolo = pit;       // [position] first own item (its work group)
+    auto pk_class = [](int rank, int lnt) {
+        return lnt <= kPackTokens && rank <= 2 * kSlot ? (rank <= kSlot ? 1 : 2) : 0;
+    };
     const int per_g = ceil_div(G > 0 ? G : 1, NT);
     const int p0 = tid * per_g;
-    int mine[4] = {0, 0, 0, 0};
+    int mine[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    auto group_counts = [&](int pos, int (&v)[8]) {
+        const int g = gperm[pos];
+        const int n = hcnt[gslot[g]], r = grank[g], nch = ceil_div(r, kRC);
+        const int m = ceil_div(n, kTok), lnt = n - kTok * (m - 1), cl = pk_class(r, lnt);
+        const int solo = m - (cl ? 1 : 0);
+        v[0] = n;
+        v[1] = solo;
+        v[2] = NP * NB * nch * solo;
+        v[3] = NP * NB * nch * kRC * n;
+        v[4] = cl == 1;
+        v[5] = cl == 1 ? lnt : 0;
+        v[6] = cl == 2;
+        v[7] = cl == 2 ? lnt : 0;
+        return cl;
+    };
     for (int q = 0; q < per_g && p0 + q < G; ++q) {
-        const int g = gperm[p0 + q];
-        const int n = hcnt[gslot[g]], nch = ceil_div(grank[g], kRC);
-        mine[0] += n;
-        mine[1] += ceil_div(n, kTok);
-        mine[2] += NP * NB * nch * ceil_div(n, kTok);
-        mine[3] += NP * NB * nch * kRC * n;
+        int v[8];
+        group_counts(p0 + q, v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mine[i] += v[i];
     }
-    int off[4], tot[4];
-    block_excl_scan<4>(mine, warp_tot4, off, tot);
-    for (int q = 0; q < per_g && p0 + q < G; ++q) {
-        const int g = gperm[p0 + q];
-        const int n = hcnt[gslot[g]], nch = ceil_div(grank[g], kRC);
-        gtok[g] = off[0];
-        pit[p0 + q] = off[1];
-        pus[p0 + q] = off[2];
-        puw[p0 + q] = off[3];
-        off[0] += n;
-        off[1] += ceil_div(n, kTok);
-        off[2] += NP * NB * nch * ceil_div(n, kTok);
-        off[3] += NP * NB * nch * kRC * n;
+    int off0[8], tot[8];
+    block_excl_scan<8>(mine, warp_tot8, off0, tot);
+    {
+        int off[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) off[i] = off0[i];
+        for (int q = 0; q < per_g && p0 + q < G; ++q) {
+            const int pos = p0 + q;
+            int v[8];
+            group_counts(pos, v);
+            gtok[gperm[pos]] = off[0];
+            psolo[pos] = off[1];
+            pus[pos] = off[2];
+            puw[pos] = off[3];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) off[i] += v[i];
+        }
     }
-    const int n_items = tot[1];
-    const int n_shrink = tot[2];
-    const int64_t n_units = (int64_t)n_shrink + (int64_t)n_items * NP * NB;
-    if (n_units > a.L.cap_units || (int64_t)tot[3] > a.L.cap_words) {
+    const int n_solo = tot[1], s_solo = tot[2], n_c1 = tot[4], n_c2 = tot[6];
+    const int n_p2 = ceil_div(n_c2, 2), n_p1 = ceil_div(n_c1, kPackItems);
+    const int n_wg = n_solo + n_p2 + n_p1;
+    const int n_shrink = s_solo + (n_p2 + n_p1) * NP * NB;
+    const int64_t n_units = (int64_t)n_shrink + (int64_t)n_wg * NP * NB;
+    if (n_units > a.L.cap_units || n_wg > a.L.cap_wg || (int64_t)tot[3] > a.L.cap_words) {
         if (tid == 0) plan_refuse(a);
         return;
     }
     __syncthreads();
 
-    // the token order first: the token tables are free afterwards
+    // the token order first: the hash-slot table is free afterwards
     for (int i = tid; i < Tc; i += NT) {
         const int h = tslot[i];
         if (h >= 0)
             a.L.tok_order[gtok[hgrp[h]] + tpos[i]] = a.t_begin + i;
     }
     __syncthreads();
-
-    // 4. the units, one per thread in list order (consecutive threads write consecutive
-    //    units).  A unit's group position comes from a table of the group position of
-    //    every 32-unit chunk's first unit (kept in the token tables' space), followed
-    //    forward; lists too long for the table search the strictly increasing offsets.
-    //    Divisions by the per-call divisors use exact reciprocal multiplies.
-    const int n_exp = n_items * NP * NB;
-    const int cs = ceil_div(n_shrink, 32), ce = ceil_div(n_exp, 32);
-    const bool table = cs + ce <= kMaxPlanTokens;   // ints available in tslot + tpos
-    int *tabS = reinterpret_cast<int *>(tslot), *tabE = tabS + cs;
-    __shared__ unsigned long long s_mag[3][kMaxRank / kRC + 1];   // ceil(2^32 / d), per nch
+    // packable items by class, in group order: their group position and the tokens of the
+    // class before them (class 1 at [0, n_c1), class 2 at [n_c1, n_c1 + n_c2))
+    int *cpos = hgrp, *ctp = hgrp + G;
+    {
+        int off[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) off[i] = off0[i];
+        for (int q = 0; q < per_g && p0 + q < G; ++q) {
+            const int pos = p0 + q;
+            int v[8];
+            const int cl = group_counts(pos, v);
+            if (cl == 1) {
+                cpos[off[4]] = pos;
+                ctp[off[4]] = off[5];
+            } else if (cl == 2) {
+                cpos[n_c1 + off[6]] = pos;
+                ctp[n_c1 + off[6]] = off[7];
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) off[i] += v[i];
+        }
+    }
+    __shared__ unsigned long long s_mag[kMaxRank / kRC + 1];   // ceil(2^32 / (NP NB nch)), per nch
     __shared__ unsigned long long s_mag_e, s_mag_nb;
     auto magic = [](uint32_t d) { return (unsigned long long)(0xffffffffu / d) + 1ull; };
-    if (tid <= kMaxRank / kRC) {
-        const uint32_t nch = tid < 1 ? 1u : (uint32_t)tid;
-        s_mag[0][tid] = magic((uint32_t)(NP * NB) * nch);
-        s_mag[1][tid] = magic((uint32_t)NB * nch);
-        s_mag[2][tid] = magic(nch);
-    }
+    if (tid <= kMaxRank / kRC) s_mag[tid] = magic((uint32_t)(NP * NB) * (uint32_t)(tid < 1 ? 1 : tid));
     if (tid == 0) {
         s_mag_e = magic((uint32_t)(NP * NB));
         s_mag_nb = magic((uint32_t)NB);
     }
-    if (table) {
-        for (int q = 0; q < per_g && p0 + q < G; ++q) {
-            const int pos = p0 + q;
-            const int u_lo = pus[pos], u_hi = pos + 1 < G ? pus[pos + 1] : n_shrink;
-            for (int c = ceil_div(u_lo, 32); 32 * c < u_hi; ++c) tabS[c] = pos;
-            const int e_lo = pit[pos] * NP * NB, e_hi = pos + 1 < G ? pit[pos + 1] * NP * NB : n_exp;
-            for (int c = ceil_div(e_lo, 32); 32 * c < e_hi; ++c) tabE[c] = pos;
-        }
-    }
     __syncthreads();
+
+    // 4. the units, one per thread in list order (consecutive threads write consecutive
+    //    units): the shrink units of the own items (groups in order, items in order), then
+    //    those of the packs (class 2, then class 1), then one expand unit per work group,
+    //    projection slot and hidden block in the same work-group order.  An own item finds
+    //    its group by binary search over the group offsets; divisions by the per-call
+    //    divisors use exact reciprocal multiplies (x d < 2^32 here).
     auto div = [](uint32_t x, unsigned long long m) { return (int)((x * m) >> 32); };
     auto last_le = [&](const int *arr, int key) {
         int lo_p = 0, hi_p = G - 1;
@@ -502,60 +575,94 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const __grid_constant__ Pla
         }
         return lo_p;
     };
+    // the work groups, one per thread: an own item (group found by binary search over the
+    // own-item offsets) or a pack
+    for (int w = tid; w < n_wg; w += NT) {
+        Unit u;
+        u.pad[0] = u.pad[1] = 0;
+        auto fill = [&](PackItem &it, int g, int item_in_group, int row0, int t0, int nt, int p) {
+            const int rank = grank[g], nch = ceil_div(rank, kRC);
+            it.pt_base = gpt[g];
+            it.tok_start = gtok[g] + kTok * item_in_group;
+            it.geo = geo_pack(row0, rank, t0, nt);
+            it.scaling = a.scaling ? a.scaling[gad[g]] : gscale[g];
+            it.uoff = puw[p] + item_in_group * NP * NB * nch * kRC * kTok;
+        };
+        int ni, nt_all;
+        if (w < n_solo) {
+            const int pos = last_le(psolo, w), ig = w - psolo[pos];
+            const int g = gperm[pos];
+            const int nt = min(kTok, hcnt[gslot[g]] - kTok * ig);
+            fill(u.item[0], g, ig, 0, 0, nt, pos);
+            ni = 1;
+            nt_all = nt;
+            u.rows = grank[g];
+        } else {
+            const int pack = w - n_solo;
+            const bool c2 = pack < n_p2;
+            const int cap = c2 ? 2 : kPackItems, slot = c2 ? 2 * kSlot : kSlot;
+            const int cbase = c2 ? n_c1 : 0, cnt = c2 ? n_c2 : n_c1;
+            const int ci0 = (c2 ? pack : pack - n_p2) * cap;
+            ni = min(cap, cnt - ci0);
+            const int tp0 = ctp[cbase + ci0];
+            int rows = 0;
+            nt_all = 0;
+#pragma unroll
+            for (int j = 0; j < kPackItems; ++j) {   // unrolled: the items stay in registers
+                if (j < ni) {
+                    const int p = cpos[cbase + ci0 + j], g = gperm[p];
+                    const int n = hcnt[gslot[g]], m = ceil_div(n, kTok), lnt = n - kTok * (m - 1);
+                    fill(u.item[j], g, m - 1, slot * j, ctp[cbase + ci0 + j] - tp0, lnt, p);
+                    rows = slot * j + grank[g];
+                    nt_all = ctp[cbase + ci0 + j] - tp0 + lnt;
+                }
+            }
+            u.rows = rows;
+        }
+#pragma unroll
+        for (int j = 1; j < kPackItems; ++j) {
+            if (j >= ni) {
+                u.item[j].pt_base = 0;
+                u.item[j].tok_start = 0;
+                u.item[j].geo = 0;
+                u.item[j].scaling = 0.f;
+                u.item[j].uoff = 0;
+            }
+        }
+        u.packed = unit_pack(nt_all, 0, 0, 0, 0, ni);
+        a.L.wgs[w] = u;
+    }
+    // the work list, one entry per thread
     for (int k = tid; k < n_units; k += NT) {
         const bool expand = k >= n_shrink;
-        int pos, ig, l, nch, item = 0;   // group position, item within the group, unit within the item
-        if (!expand) {
-            if (table) {
-                pos = tabS[k >> 5];
-                while (pos + 1 < G && pus[pos + 1] <= k) ++pos;
-            } else {
-                pos = last_le(pus, k);
-            }
-            nch = ceil_div(grank[gperm[pos]], kRC);
+        int pj, b, c = 0, wg;
+        if (!expand && k < s_solo) {
+            const int pos = last_le(pus, k);
+            const int nch = ceil_div(grank[gperm[pos]], kRC);
             const int r = k - pus[pos];
-            ig = div((uint32_t)r, s_mag[0][nch]);
-            l = r - ig * NP * NB * nch;
-        } else {
-            const int e = k - n_shrink;
-            item = div((uint32_t)e, s_mag_e);
-            l = e - item * NP * NB;
-            if (table) {
-                pos = tabE[e >> 5];
-                while (pos + 1 < G && pit[pos + 1] <= item) ++pos;
-            } else {
-                pos = last_le(pit, item);
-            }
-            ig = item - pit[pos];
-            nch = ceil_div(grank[gperm[pos]], kRC);
-        }
-        const int g = gperm[pos];
-        const int rank = grank[g];
-        const int t0 = ig * kTok, nt = min(kTok, hcnt[gslot[g]] - t0);
-        int pj, b, c;
-        if (!expand) {
-            pj = div((uint32_t)l, s_mag[1][nch]);
+            const int ig = div((uint32_t)r, s_mag[nch]);
+            const int l = r - ig * NP * NB * nch;
+            pj = l / (NB * nch);
             const int rem = l - pj * NB * nch;
-            b = div((uint32_t)rem, s_mag[2][nch]);
+            b = rem / nch;
             c = rem - b * nch;
+            wg = psolo[pos] + ig;
         } else {
+            const int e = expand ? k - n_shrink : k - s_solo;
+            const int q = div((uint32_t)e, s_mag_e);
+            const int l = e - q * NP * NB;
             pj = div((uint32_t)l, s_mag_nb);
             b = l - pj * NB;
-            c = 0;
+            wg = expand ? q : n_solo + q;
         }
-        Unit u;
-        u.tok_start = gtok[g] + t0;
-        u.packed = unit_pack(nt, expand ? 1 : 0, pj, b, c);
-        u.rank = rank;
-        u.scaling = a.scaling ? a.scaling[gad[g]] : gscale[g];
-        u.pt_base = gpt[g] + (int64_t)s_proj[pj] * 2 * rank;
-        u.uoff = puw[pos] + ig * NP * NB * nch * kRC * kTok + pj * (nch * NB * nt * kRC);
-        u.pad = 0;
-        a.L.units[k] = u;
+        ListUnit lu;
+        lu.wg = wg;
+        lu.packed = ((uint32_t)(expand ? 1 : 0) << 5) | ((uint32_t)pj << 6) | ((uint32_t)b << 9) | ((uint32_t)c << 12);
+        a.L.units[k] = lu;
     }
     if (tid == 0) {
         a.L.hdr->n_groups = G;
-        a.L.hdr->n_items = n_items;
+        a.L.hdr->n_wg = n_wg;
         a.L.hdr->n_units = (int32_t)n_units;
         a.L.hdr->n_shrink = n_shrink;
         a.L.hdr->seg_lo = lo;
@@ -575,15 +682,18 @@ struct DeltaArgs {
     int32_t pitch;          // bytes per row of a ring stage: 2 * largest block + 16
     int32_t nblk;           // hidden blocks
     uint32_t tag;           // this launch's partial-sum tag (never 0)
+    int32_t proj[kMaxApplyProj];   // projection of each slot of the call
 };
 
-// A unit as the lead warp hands it to the other warps: the descriptor, the item's token
-// ids and the page ids of its first rank chunk (A^T rows of a shrink unit's chunk, B rows
-// of an expand unit's chunk 0).
+// A unit as the lead warp hands it to the other warps: the descriptor, the token ids of
+// its rows, each row's item, and the page ids of its first rank chunk (A^T rows of a shrink
+// unit's chunk, B rows of an expand unit's chunk 0).
+constexpr int32_t kGapRow = -2;   // page id of a row between a pack's items: zeros, not an error
 struct alignas(16) Rec {
     Unit u;
-    int32_t tok[kTok];      // token ids of the item's rows (0 past its tokens)
-    int32_t pg[kRC];        // page ids of the first chunk's rows (-1 past the rank)
+    int32_t tok[kTok];      // token ids of the unit's token rows (0 past its tokens)
+    int32_t pg[kRC];        // page ids of the first chunk's rows (-1 past the rows, kGapRow in a gap)
+    int8_t titem[kTok];     // item of each token row
     int32_t end;            // no more units
     int32_t pad[3];
 };
@@ -619,19 +729,37 @@ __device__ __forceinline__ void mma16816_zc(float (&d)[4], const uint32_t (&a)[4
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
 }
 
-__device__ __forceinline__ Unit load_unit(const Unit *p)
+// A unit as 7 x 16 bytes in registers (every lane of the lead loads all of it).
+constexpr int kUnitVecs = (int)(sizeof(Unit) / 16);
+struct UnitRegs {
+    uint4 w[kUnitVecs];
+    // 32-bit word i of the unit (i a compile-time constant once loops are unrolled)
+    __device__ __forceinline__ uint32_t word(int i) const
+    {
+        const uint4 v = w[i >> 2];
+        return (i & 3) == 0 ? v.x : (i & 3) == 1 ? v.y : (i & 3) == 2 ? v.z : v.w;
+    }
+    __device__ __forceinline__ uint32_t packed() const { return word(0); }
+    __device__ __forceinline__ int rows() const { return (int)word(1); }
+    // item j's fields (PackItem at byte 16 + 24 j)
+    __device__ __forceinline__ int64_t pt_base(int j) const
+    {
+        return (int64_t)(((uint64_t)word(5 + 6 * j) << 32) | word(4 + 6 * j));
+    }
+    __device__ __forceinline__ int tok_start(int j) const { return (int)word(6 + 6 * j); }
+    __device__ __forceinline__ uint32_t geo(int j) const { return word(7 + 6 * j); }
+    __device__ __forceinline__ void set_word(int i, uint32_t x)
+    {
+        uint4 &v = w[i >> 2];
+        if ((i & 3) == 0) v.x = x; else if ((i & 3) == 1) v.y = x; else if ((i & 3) == 2) v.z = x; else v.w = x;
+    }
+};
+static_assert(sizeof(Unit) % 16 == 0 && offsetof(Unit, item) == 16, "Unit layout for UnitRegs");
+__device__ __forceinline__ void load_unit(const Unit *p, UnitRegs &r)
 {
     const uint4 *s = reinterpret_cast<const uint4 *>(p);
-    const uint4 w0 = __ldcg(s), w1 = __ldcg(s + 1);
-    Unit u;
-    u.tok_start = (int32_t)w0.x;
-    u.packed = w0.y;
-    u.rank = (int32_t)w0.z;
-    u.scaling = __uint_as_float(w0.w);
-    u.pt_base = (int64_t)(((uint64_t)w1.y << 32) | w1.x);
-    u.uoff = (int32_t)w1.z;
-    u.pad = (int32_t)w1.w;
-    return u;
+#pragma unroll
+    for (int i = 0; i < kUnitVecs; ++i) r.w[i] = __ldcg(s + i);
 }
 
 // Tagged partial words: relaxed 64-bit accesses at GPU scope (single-copy atomic).
@@ -665,22 +793,22 @@ struct UnitShape {
     int nt, expand, pj, b, c;
     int nch;         // rank chunks the unit covers (an expand covers every chunk of the rank)
 };
-__device__ __forceinline__ UnitShape unit_shape(const Unit &u)
+__device__ __forceinline__ UnitShape unit_shape(uint32_t packed, int rows)
 {
     UnitShape s;
-    s.nt = (int)(u.packed & 31u) + 1;
-    s.expand = (int)((u.packed >> 5) & 1u);
-    s.pj = (int)((u.packed >> 6) & 7u);
-    s.b = (int)((u.packed >> 9) & 7u);
-    s.c = (int)((u.packed >> 12) & 15u);
-    s.nch = s.expand ? ceil_div(u.rank, kRC) : 1;
+    s.nt = (int)(packed & 31u) + 1;
+    s.expand = (int)((packed >> 5) & 1u);
+    s.pj = (int)((packed >> 6) & 7u);
+    s.b = (int)((packed >> 9) & 7u);
+    s.c = (int)((packed >> 12) & 15u);
+    s.nch = s.expand ? ceil_div(rows, kRC) : 1;
     return s;
 }
 // rows of the i-th chunk the unit covers
-__device__ __forceinline__ int chunk_rows(const Unit &u, const UnitShape &s, int i)
+__device__ __forceinline__ int chunk_rows(int rows, const UnitShape &s, int i)
 {
     const int c = s.expand ? i : s.c;
-    return min(kRC, u.rank - kRC * c);
+    return min(kRC, rows - kRC * c);
 }
 
 // A unit's ring stages: one stage of its token rows (x of a shrink, y0 of an expand), then its
@@ -740,13 +868,14 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
     griddep_launch_dependents();
     const int n_units = __ldcg(&a.L.hdr->n_units);
 
-    // read record k (every reader walks the records in order); false at the end
-    auto take_record = [&](int k, Unit &u) -> bool {
+    // read record k's header (every reader walks the records in order); false at the end
+    auto take_record = [&](int k, uint32_t &packed, int &rows) -> bool {
         const uint32_t q = k % QD;
         wait_phase<false>(&rfull[q], (k / QD) & 1, abort, status);
         if (*abort) return false;
         const int end = recs[q].end;
-        u = recs[q].u;
+        packed = recs[q].u.packed;
+        rows = recs[q].u.rows;
         return !end;
     };
     auto release_record = [&](int k) {
@@ -762,40 +891,101 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
         // and the tokens and page ids of unit k are in flight together.
         const int G = (int)gridDim.x;
         const int32_t *pt = a.pv.pt_arena;
-        auto fetch_rest = [&](const Unit &u, int &tok, int32_t &p0, int32_t &p1) {
-            const int nt = (int)(u.packed & 31u) + 1;
-            tok = lane < nt ? __ldcg(a.L.tok_order + u.tok_start + lane) : 0;
-            int64_t base;
-            int rows;
-            if (u.packed & 32u) {
-                base = u.pt_base + u.rank;
-                rows = min(kRC, u.rank);
-            } else {
-                const int c = (int)((u.packed >> 12) & 15u);
-                base = u.pt_base + kRC * c;
-                rows = min(kRC, u.rank - kRC * c);
+        // the token id of token row `lane` and the page ids of rows `lane`, `lane` + 32 of the
+        // unit's first chunk, with the token's item; every lane holds the whole unit
+        auto fetch_rest = [&](const UnitRegs &u, int &tok, int &titem, int32_t &p0, int32_t &p1) {
+            const uint32_t packed = u.packed();
+            const int rows = u.rows();
+            const int nt = (int)(packed & 31u) + 1, ni = (int)((packed >> 16) & 3u) + 1;
+            const bool expand = (packed & 32u) != 0;
+            const int c = expand ? 0 : (int)((packed >> 12) & 15u);
+            int ti = 0, tstart = 0, t0 = 0;
+#pragma unroll
+            for (int j = 0; j < kPackItems; ++j) {
+                const uint32_t g = u.geo(j);
+                if (j < ni && lane >= geo_t0(g)) {
+                    ti = j;
+                    tstart = u.tok_start(j);
+                    t0 = geo_t0(g);
+                }
             }
-            p0 = lane < rows ? __ldcg(pt + base + lane) : -1;
-            p1 = lane + 32 < rows ? __ldcg(pt + base + lane + 32) : -1;
+            tok = lane < nt ? __ldcg(a.L.tok_order + tstart + lane - t0) : 0;
+            titem = ti;
+            const int rows_c = min(kRC, rows - kRC * c);
+            auto page_of = [&](int r) -> int32_t {
+                if (r >= rows_c) return -1;
+                int64_t base = 0;
+                int row0 = 0, rank = 0;
+#pragma unroll
+                for (int j = 0; j < kPackItems; ++j) {
+                    const uint32_t g = u.geo(j);
+                    if (j < ni && r >= geo_row0(g)) {
+                        row0 = geo_row0(g);
+                        rank = geo_rank(g);
+                        base = u.pt_base(j);
+                    }
+                }
+                const int within = r + kRC * c - row0;
+                return within < rank ? __ldcg(pt + base + (expand ? rank : 0) + within) : kGapRow;
+            };
+            p0 = page_of(lane);
+            p1 = page_of(lane + 32);
         };
-        // lane 0: the counter's value for the unit after `nu` (its index less G), first read in
-        // the next iteration so that the atomic's round trip overlaps this one
+        // unit k from its list entry and its work group: the unit's bits of packed, the
+        // projection slot's page-table bases and partial offsets
+        auto resolve = [&](const UnitRegs &wg, int2 lu, UnitRegs &u) {
+            u = wg;
+            const uint32_t lp = (uint32_t)lu.y;
+            const int pj = (int)((lp >> 6) & 7u);
+            const int proj = a.proj[pj];
+            const int ni = (int)((wg.packed() >> 16) & 3u) + 1;
+            u.set_word(0, wg.packed() | lp);
+#pragma unroll
+            for (int j = 0; j < kPackItems; ++j) {
+                if (j < ni) {
+                    const uint32_t g = wg.geo(j);
+                    const int rank = geo_rank(g), nch = ceil_div(rank, kRC);
+                    const int64_t ptb = wg.pt_base(j) + (int64_t)proj * 2 * rank;
+                    u.set_word(4 + 6 * j, (uint32_t)(uint64_t)ptb);
+                    u.set_word(5 + 6 * j, (uint32_t)((uint64_t)ptb >> 32));
+                    u.set_word(9 + 6 * j, wg.word(9 + 6 * j) + (uint32_t)(pj * nch * NB * geo_nt(g) * kRC));
+                }
+            }
+        };
+        auto load_lu = [&](int idx) { return __ldcg(reinterpret_cast<const int2 *>(a.L.units) + idx); };
+        // The loads run four units deep: in the iteration that publishes unit k, the token and
+        // page ids of unit k+1 (from its resolved descriptor), the work group of unit k+2 (from
+        // its list entry), the list entry of unit k+3 and the counter for unit k+4 are in
+        // flight.  lane 0 holds the counter's value (the unit's index less G).
         int grab = 0;
         if (lane == 0) grab = atomicAdd(&a.L.hdr->grab, 1);
-        bool cvalid = (int)blockIdx.x < n_units;
-        Unit cu{};
-        int ctok = 0;
+        bool cvalid = (int)blockIdx.x < n_units, v1 = false, v2 = false;
+        UnitRegs cu{}, nw{};
+        int2 nlu = make_int2(0, 0), nnlu = make_int2(0, 0);
+        int ctok = 0, cti = 0;
         int32_t cp0 = -1, cp1 = -1;
-        if (cvalid) {
-            cu = load_unit(a.L.units + blockIdx.x);
-            fetch_rest(cu, ctok, cp0, cp1);
-        }
-        int nidx = G + __shfl_sync(0xffffffffu, grab, 0);
-        bool nvalid = cvalid && nidx < n_units;
-        Unit nu{};
-        if (nvalid) {
-            nu = load_unit(a.L.units + nidx);
-            if (lane == 0) grab = atomicAdd(&a.L.hdr->grab, 1);
+        {
+            int2 lu0 = make_int2(0, 0);
+            UnitRegs w0{};
+            if (cvalid) lu0 = load_lu(blockIdx.x);
+            int idx = G + __shfl_sync(0xffffffffu, grab, 0);
+            v1 = cvalid && idx < n_units;
+            if (v1) {
+                nlu = load_lu(idx);
+                if (lane == 0) grab = atomicAdd(&a.L.hdr->grab, 1);
+            }
+            if (cvalid) load_unit(a.L.wgs + lu0.x, w0);
+            if (v1) load_unit(a.L.wgs + nlu.x, nw);
+            idx = G + __shfl_sync(0xffffffffu, grab, 0);
+            v2 = v1 && idx < n_units;
+            if (v2) {
+                nnlu = load_lu(idx);
+                if (lane == 0) grab = atomicAdd(&a.L.hdr->grab, 1);
+            }
+            if (cvalid) {
+                resolve(w0, lu0, cu);
+                fetch_rest(cu, ctok, cti, cp0, cp1);
+            }
         }
         for (int k = 0;; ++k) {
             const uint32_t q = k % QD;
@@ -807,23 +997,35 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
                 }
                 break;
             }
-            if (lane == 0) {
-                recs[q].u = cu;
-                recs[q].end = 0;
+            {
+                uint4 v = cu.w[0];
+#pragma unroll
+                for (int i = 1; i < kUnitVecs; ++i)
+                    if (lane == i) v = cu.w[i];
+                if (lane < kUnitVecs) reinterpret_cast<uint4 *>(&recs[q].u)[lane] = v;
             }
-            if (lane < kTok) recs[q].tok[lane] = ctok;
+            if (lane == 0) recs[q].end = 0;
+            if (lane < kTok) {
+                recs[q].tok[lane] = ctok;
+                recs[q].titem[lane] = (int8_t)cti;
+            }
             recs[q].pg[lane] = cp0;
             recs[q].pg[lane + 32] = cp1;
             __syncwarp();
             if (lane == 0) mbar_arrive(&rfull[q]);
             // advance the pipeline
-            cu = nu;
-            cvalid = nvalid;
-            if (cvalid) fetch_rest(cu, ctok, cp0, cp1);
-            nidx = G + __shfl_sync(0xffffffffu, grab, 0);
-            nvalid = cvalid && nidx < n_units;
-            if (nvalid) {
-                nu = load_unit(a.L.units + nidx);
+            cvalid = v1;
+            if (cvalid) {
+                resolve(nw, nlu, cu);
+                fetch_rest(cu, ctok, cti, cp0, cp1);
+            }
+            v1 = v2;
+            nlu = nnlu;
+            if (v1) load_unit(a.L.wgs + nlu.x, nw);
+            const int idx = G + __shfl_sync(0xffffffffu, grab, 0);
+            v2 = v1 && idx < n_units;
+            if (v2) {
+                nnlu = load_lu(idx);
                 if (lane == 0) grab = atomicAdd(&a.L.hdr->grab, 1);
             }
         }
@@ -841,14 +1043,16 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
         RingPos pos{0, 0};
         uint32_t sc = 0;   // stages of the CTA so far
         for (int k = 0;; ++k) {
-            Unit u;
-            const bool have = take_record(k, u);
+            uint32_t packed;
+            int rows;
+            const bool have = take_record(k, packed, rows);
             const uint32_t q = k % QD;
             if (!have) {
                 release_record(k);
                 break;
             }
-            const UnitShape sh = unit_shape(u);
+            const UnitShape sh = unit_shape(packed, rows);
+            const int64_t ptb0 = recs[q].u.item[0].pt_base;   // later chunks: one item only
             const int kb = s_blk[sh.b];
             const uint32_t sliceB = (uint32_t)(s_blk[sh.b + 1] - kb) * 2;
             const int r8 = lane & 7;
@@ -885,15 +1089,16 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
             // rank stages
 #pragma unroll 1
             for (int i = 0; i < sh.nch; ++i) {
-                const int rows = chunk_rows(u, sh, i);
-                const int ns = ceil_div(rows, 8);
-                const int64_t base = sh.expand ? u.pt_base + u.rank + (int64_t)kRC * i : u.pt_base + (int64_t)kRC * sh.c;
+                const int crow = chunk_rows(rows, sh, i);
+                const int ns = ceil_div(crow, 8);
+                // B rows of chunk i > 0 of an expand (a unit of one item: rows is its rank)
+                const int64_t base = ptb0 + rows + (int64_t)kRC * i;
 #pragma unroll 1
                 for (int s = 0; s < ns; ++s, ++sc, pos.next()) {
                     if ((int)(sc % kCopyWarps) != cw) continue;
                     const int row = 8 * s + r8;
                     int32_t pg = -1;
-                    if (row < rows) {
+                    if (row < crow) {
                         if (i == 0) {
 #pragma unroll
                             for (int j = 0; j < 8; ++j)
@@ -902,12 +1107,13 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
                             pg = __ldcg(pt + base + row);
                         }
                     }
-                    bool ok = row < rows && pg >= 0;
+                    bool ok = row < crow && pg >= 0;
                     if (ok && pg >= a.pv.num_pages) {
                         set_status(status, SLORA_DEV_BAD_PAGE);
                         ok = false;
                     }
-                    if (lane < 8 && row < rows && pg < 0) set_status(status, SLORA_DEV_BAD_PAGE);
+                    // kGapRow: the rows between a pack's items, zeros by design
+                    if (lane < 8 && row < crow && pg == -1) set_status(status, SLORA_DEV_BAD_PAGE);
                     issue(pool + (int64_t)(ok ? pg : 0) * d, ok, sh.expand != 0);
                 }
             }
@@ -931,16 +1137,42 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
         uint32_t uj = 0;   // u buffers filled
         uint32_t sr = 0;   // shrink partials summed
         for (int k = 0;; ++k) {
-            Unit u;
-            const bool have = take_record(k, u);
+            uint32_t packed;
+            int rows;
+            const bool have = take_record(k, packed, rows);
+            const uint32_t q = k % QD;
+            // the items' shapes and partial offsets, and each token row's item
+            uint32_t ig[kPackItems];
+            int iu[kPackItems];
+#pragma unroll
+            for (int j = 0; j < kPackItems; ++j) {
+                ig[j] = recs[q].u.item[j].geo;
+                iu[j] = recs[q].u.item[j].uoff;
+            }
+            const unsigned long long titems = *reinterpret_cast<const unsigned long long *>(recs[q].titem);
             release_record(k);
             if (!have) break;
-            if (!(u.packed & 32u)) {
-                const int nt = (int)(u.packed & 31u) + 1;
-                const int c = (int)((u.packed >> 12) & 15u), b = (int)((u.packed >> 9) & 7u);
-                const int rows = min(kRC, u.rank - kRC * c), ld = 16 * ceil_div(rows, 16);
+            const int nt = (int)(packed & 31u) + 1;
+            // token row t's item: first row, rank, first token, tokens, partial offset
+            auto item_of = [&](int t, int &row0, int &rank, int &t0, int &nti, int &uoff) {
+                const int j = (int)((titems >> (8 * t)) & 0xffu);
+                uint32_t g = ig[0];
+                uoff = iu[0];
+#pragma unroll
+                for (int jj = 1; jj < kPackItems; ++jj)
+                    if (jj == j) {
+                        g = ig[jj];
+                        uoff = iu[jj];
+                    }
+                row0 = geo_row0(g);
+                rank = geo_rank(g);
+                t0 = geo_t0(g);
+                nti = geo_nt(g);
+            };
+            if (!(packed & 32u)) {
+                const int c = (int)((packed >> 12) & 15u), b = (int)((packed >> 9) & 7u);
+                const int rows_c = min(kRC, rows - kRC * c), ld = 16 * ceil_div(rows_c, 16);
                 wait_phase<false>(psfull, sr & 1, abort, status);
-                unsigned long long *dst = a.L.upart + u.uoff + ((int64_t)c * NB + b) * nt * kRC;
 #pragma unroll 1
                 for (int e = 4 * lane; e < nt * ld; e += 128) {
                     const int t = e / ld, j = e - t * ld;
@@ -953,33 +1185,46 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
                         v.z += pv.z;
                         v.w += pv.w;
                     }
-                    unsigned long long *o = dst + t * kRC + j;
-                    if (j < rows) st_word(o, v.x, tag);
-                    if (j + 1 < rows) st_word(o + 1, v.y, tag);
-                    if (j + 2 < rows) st_word(o + 2, v.z, tag);
-                    if (j + 3 < rows) st_word(o + 3, v.w, tag);
+                    int row0, rank, t0, nti, uoff;
+                    item_of(t, row0, rank, t0, nti, uoff);
+                    const int rank_c = min(kRC, rank - kRC * c);
+                    unsigned long long *o =
+                        a.L.upart + uoff + ((int64_t)(c * NB + b) * nti + (t - t0)) * kRC + (j - row0);
+                    const int w0 = j - row0;
+                    if (w0 >= 0 && w0 < rank_c) st_word(o, v.x, tag);
+                    if (w0 + 1 >= 0 && w0 + 1 < rank_c) st_word(o + 1, v.y, tag);
+                    if (w0 + 2 >= 0 && w0 + 2 < rank_c) st_word(o + 2, v.z, tag);
+                    if (w0 + 3 >= 0 && w0 + 3 < rank_c) st_word(o + 3, v.w, tag);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(psempty);
                 ++sr;
                 continue;
             }
-            const int nt = (int)(u.packed & 31u) + 1;
-            const int nch = ceil_div(u.rank, kRC);
+            const int nch = ceil_div(rows, kRC);
             const int j4 = 4 * (lane & 15);
 #pragma unroll 1
             for (int c = 0; c < nch; ++c) {
                 const uint32_t qu = uj % QU;
                 if (uj >= QU) wait_phase<false>(&uempty[qu], ((uj / QU) - 1) & 1, abort, status);
-                const int rows = min(kRC, u.rank - kRC * c);
-                const unsigned long long *src = a.L.upart + u.uoff + (int64_t)c * NB * nt * kRC;
                 __half *ub = ubuf + qu * kTok * kUPitch;
 #pragma unroll 1
-                for (int t0 = 0; t0 < nt; t0 += 2) {
-                    const int t = t0 + (lane >> 4);
-                    const int nv = (t < nt && j4 < rows) ? min(4, rows - j4) : 0;   // this lane's values
-                    const unsigned long long *sp = src + (int64_t)t * kRC + j4;   // block 0; blocks nt*kRC apart
-                    const int bstride = nt * kRC;
+                for (int tr = 0; tr < nt; tr += 2) {
+                    const int t = tr + (lane >> 4);
+                    // this lane's values: columns j4 .. j4+3 of token row t lie in its item's rows
+                    // of the chunk (zeros elsewhere)
+                    int nv = 0, bstride = 0;
+                    const unsigned long long *sp = a.L.upart;
+                    if (t < nt) {
+                        int row0, rank, t0, nti, uoff;
+                        item_of(t, row0, rank, t0, nti, uoff);
+                        const int rank_c = min(kRC, rank - kRC * c), w0 = j4 - row0;
+                        if (w0 >= 0 && w0 < rank_c) {
+                            nv = min(4, rank_c - w0);
+                            sp = a.L.upart + uoff + ((int64_t)c * NB * nti + (t - t0)) * kRC + w0;   // block 0
+                            bstride = nti * kRC;                                                // blocks apart
+                        }
+                    }
                     float wv[kMaxBlocks][4];
                     // poll until every word carries the tag (each was written once, by its
                     // shrink unit, earlier in the list); bounded in time
@@ -1037,21 +1282,27 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
     auto wait_at = [&](const RingPos &p) { wait_phase<false>(&full[p.slot], p.phase, abort, status); };
     uint32_t sj = 0;     // shrink units done (uses of the partial set)
     float *region = pset + w * kRegionFloats;   // this warp's shrink partials
-    // The record of the next unit is read while the current one runs.
-    Unit u;
-    bool have = take_record(0, u);
+    // The record of the next unit is read while the current one runs: its header, the
+    // token id of this lane's row gid and the scaling of that token's item.
+    auto item_scaling = [&](uint32_t q) { return recs[q].u.item[recs[q].titem[gid] & (kPackItems - 1)].scaling; };
+    uint32_t upk;
+    int urows;
+    bool have = take_record(0, upk, urows);
     int tk = recs[0].tok[gid];
+    float scl = item_scaling(0);
     release_record(0);
     for (int k = 0; have; ++k) {
-        const UnitShape sh_ = unit_shape(u);
+        const UnitShape sh_ = unit_shape(upk, urows);
         const int nt = sh_.nt;
         const int kb = s_blk[sh_.b], KS = s_blk[sh_.b + 1] - kb;
         const RingPos tpos = cur;   // the token stage
         cur.next();
         wait_at(tpos);
-        Unit nu;
-        const bool nhave = take_record(k + 1, nu);
+        uint32_t npk;
+        int nrows;
+        const bool nhave = take_record(k + 1, npk, nrows);
         const int ntk = recs[(k + 1) % QD].tok[gid];
+        const float nscl = item_scaling((k + 1) % QD);
         release_record(k + 1);
         const uint32_t tstage = ring_s + tpos.slot * stageB;
 
@@ -1059,7 +1310,7 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
             // ---- shrink: u^T = A^T x^T, rank rows on the MMA's M and tokens on its N.  Warp w
             //      contracts K steps [w n/8, (w+1) n/8) of the block for every 16-row block of
             //      the chunk; the 8 warp partials are summed in warp order ----
-            const int rows = chunk_rows(u, sh_, 0), nb = ceil_div(rows, 16), ns = ceil_div(rows, 8);
+            const int rows = chunk_rows(urows, sh_, 0), nb = ceil_div(rows, 16), ns = ceil_div(rows, 8);
             const int nsteps = KS / 16;
             const int ks0 = (w * nsteps) / kConsumerWarps, nks = ((w + 1) * nsteps) / kConsumerWarps - ks0;
             uint32_t xf[kXs / 2][4];   // this warp's x fragments (the MMA's B operand), two K steps each
@@ -1120,7 +1371,7 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
             // epilogue; a longer one would hold the ring, so it first copies this lane's y0
             // values (token gid, columns 16 (pp0+p) + 8 n2 + 2 tig, +1) to the warp's region,
             // once the gather warp has summed the partials the region held.
-            const bool hold = u.rank <= kRC;
+            const bool hold = urows <= kRC;
             uint32_t *yv = reinterpret_cast<uint32_t *>(region);
             if (!hold) {
                 if (sj > 0) wait_phase<false>(psempty, (sj - 1) & 1, abort, status);
@@ -1140,7 +1391,7 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
             for (int c = 0; c < sh_.nch; ++c) {
                 const uint32_t qu = uj % QU;
                 wait_phase<false>(&ufull[qu], (uj / QU) & 1, abort, status);
-                const int rows = chunk_rows(u, sh_, c), nb = ceil_div(rows, 16), ns = ceil_div(rows, 8);
+                const int rows = chunk_rows(urows, sh_, c), nb = ceil_div(rows, 16), ns = ceil_div(rows, 8);
                 const uint32_t ub = ubuf_s + qu * (kTok * kUPitch * 2);
 #pragma unroll 1
                 for (int blk = 0; blk < nb; ++blk) {
@@ -1191,7 +1442,6 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
                 ++uj;
             }
             // ---- epilogue: y = y0 + s * acc for token gid: columns 2 tig, 2 tig + 1 of each n-tile ----
-            const float scl = u.scaling;
             __half *yrow = a.y[sh_.pj] + (int64_t)tk * d + kb;
             const bool store = !*abort && gid < nt;
             if (hold) {
@@ -1234,8 +1484,10 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
                 }
             }
         }
-        u = nu;
+        upk = npk;
+        urows = nrows;
         tk = ntk;
+        scl = nscl;
         have = nhave;
     }
 }
@@ -1384,6 +1636,7 @@ cudaError_t launch_lora_apply(const PoolView &pv, const ProjList &pl, int32_t T,
         da.pitch = delta_pitch(pv.hidden);
         da.nblk = NB;
         da.tag = tag;
+        for (int j = 0; j < pl.n; ++j) da.proj[j] = pl.proj[j];
         e = cudaLaunchKernelEx(&cfg2, delta_kernel, da);
         if (e != cudaSuccess) return e;
         *launches += 1;

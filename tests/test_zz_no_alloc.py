@@ -170,7 +170,7 @@ def test_noalloc_chunked_plans_with_many_adapter_ids():
 
 
 def test_noalloc_refuses_batch_beyond_its_scratch():
-    # 8000 decode tokens at hidden 4096 with rank-64 adapters need about 2.3 KB of scratch
+    # 8000 decode tokens at hidden 4096 with rank-64 adapters need about 2.2 KB of scratch
     # per token: more than the 16 MiB array
     ranks = np.array([64, 8], np.int32)
     idx = (np.arange(8000) % 2).astype(np.int32)
