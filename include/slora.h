@@ -436,6 +436,22 @@ slora_status slora_pool_set_stage_event(slora_pool_t pool, void *event);
  * SLORA_ERR_CUDA.  Other values return SLORA_ERR_INVALID_ARG.  The S-LoRA pages have no
  * counterpart for it. */
 slora_status slora_debug_set_prefill_cluster(int32_t ctas);
+/* Test hook: host-side fault injection in the adapter load path.  The nth later operation
+ * of `kind` (counted over every pool of the process) fails as if its call had failed:
+ *   SLORA_FAULT_COPY       a cudaMemcpyAsync into the staging ring (copy-engine mode)
+ *   SLORA_FAULT_SCATTER    a load-kernel launch
+ *   SLORA_FAULT_DIRECTORY  a directory-update launch
+ *   SLORA_FAULT_STAGING    the staging ring's growth allocation (copy-engine mode)
+ *   SLORA_FAULT_ARENA      a page-table arena allocation (as if the arena were fragmented)
+ * The load then returns SLORA_ERR_CUDA (SLORA_ERR_POOL_FULL for the arena) and takes
+ * itself back: the work its side stream already has completes, the directory entries of
+ * its adapters are cleared, their pages and arena ranges return to the free lists, and
+ * none of them is resident; a later load of the same adapters runs normally.  Nothing is
+ * made to fail on the GPU.  kind SLORA_FAULT_NONE or nth 0 clears a pending injection;
+ * other values return SLORA_ERR_INVALID_ARG.  The S-LoRA pages have no counterpart for it. */
+enum { SLORA_FAULT_NONE = 0, SLORA_FAULT_COPY = 1, SLORA_FAULT_SCATTER = 2, SLORA_FAULT_DIRECTORY = 3,
+       SLORA_FAULT_STAGING = 4, SLORA_FAULT_ARENA = 5 };
+slora_status slora_debug_inject_load_fault(int32_t kind, int32_t nth);
 
 #ifdef __cplusplus
 }

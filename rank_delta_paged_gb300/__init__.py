@@ -34,6 +34,8 @@ __all__ = [
     "SLORA_LOAD_ZERO_COPY", "SLORA_LOAD_COPY_ENGINE",
     "slora_adapters_evict",
     "slora_debug_set_prefill_cluster",
+    "slora_debug_inject_load_fault", "SLORA_FAULT_NONE", "SLORA_FAULT_COPY", "SLORA_FAULT_SCATTER",
+    "SLORA_FAULT_DIRECTORY", "SLORA_FAULT_STAGING", "SLORA_FAULT_ARENA",
     "slora_lora_apply_multi",
     "slora_lru_create", "slora_lru_destroy", "slora_lru_insert", "slora_lru_remove", "slora_lru_touch",
     "slora_lru_pin", "slora_lru_unpin", "slora_lru_victims",
@@ -79,6 +81,7 @@ _SIGS = {
     "slora_pool_set_load_start_event": [_P, _P],
     "slora_adapters_evict": [_P, _I32, _P, _P],
     "slora_debug_set_prefill_cluster": [_I32],
+    "slora_debug_inject_load_fault": [_I32, _I32],
     "slora_lora_apply_multi": [_P, _I32, _P, _P, _P, _I32, _P, _P, _I32, _P, _P],
     "slora_lru_create": [_PP],
     "slora_lru_destroy": [_P],
@@ -400,6 +403,15 @@ def slora_pool_launch_count(pool: int) -> int:
     v = ctypes.c_int64()
     _call("slora_pool_launch_count", pool, ctypes.byref(v))
     return v.value
+
+
+SLORA_FAULT_NONE, SLORA_FAULT_COPY, SLORA_FAULT_SCATTER = 0, 1, 2
+SLORA_FAULT_DIRECTORY, SLORA_FAULT_STAGING, SLORA_FAULT_ARENA = 3, 4, 5
+
+
+def slora_debug_inject_load_fault(kind: int, nth: int) -> None:
+    """Make the nth later load-path operation of `kind` fail on the host (test hook)."""
+    _call("slora_debug_inject_load_fault", int(kind), int(nth))
 
 
 def slora_debug_set_prefill_cluster(ctas: int) -> None:

@@ -4,6 +4,7 @@
 // Multiplexing Thousands of Fine-Tuned Adapters on a Single GPU, section 2).
 #include <algorithm>
 #include <cstdlib>
+#include <mutex>
 #include <cstring>
 #include <new>
 #include <unordered_set>
@@ -117,6 +118,22 @@ void free_pool_memory(slora_pool *p)
 }
 
 constexpr int64_t kDefaultStagingBytes = 256ll << 20;
+
+// Test hook: the nth later load-path operation of one kind fails as if its CUDA call (or,
+// for the arena, its allocation) had failed.  Process-wide; one injection at a time.
+std::mutex g_fault_mu;
+int32_t g_fault_kind = SLORA_FAULT_NONE;
+int32_t g_fault_left = 0;
+bool inject_fault(int32_t kind)
+{
+    std::lock_guard<std::mutex> lk(g_fault_mu);
+    if (g_fault_kind != kind || g_fault_left <= 0)
+        return false;
+    if (--g_fault_left > 0)
+        return false;
+    g_fault_kind = SLORA_FAULT_NONE;
+    return true;
+}
 
 }  // namespace
 
@@ -337,23 +354,31 @@ slora_status slora_adapters_load(slora_pool_t p, int32_t n, const int32_t *ids, 
     DEVICE_SCOPE(p);
     slora_status st = SLORA_OK;
 
-    // Host bookkeeping first (pages + arena), with rollback if the arena is too fragmented.
+    // Host bookkeeping first (pages + arena), taken back if the arena is too fragmented.
     std::vector<int32_t> done;
+    auto undo_host = [&]() {
+        for (int32_t d : done) {
+            AdapterRec &b = p->adapters[(size_t)d];
+            p->pages.release(adapter_rows(p, b), b.pt_host);
+            p->arena.release(b.pt_off, adapter_rows(p, b));
+            b.pt_off = -1;
+        }
+    };
     for (int32_t id : todo) {
         AdapterRec &a = p->adapters[(size_t)id];
         int64_t rows = adapter_rows(p, a);
-        int64_t off = p->arena.alloc(rows);
+        int64_t off = inject_fault(SLORA_FAULT_ARENA) ? -1 : p->arena.alloc(rows);
         if (off < 0) {
-            for (int32_t d : done) {
-                AdapterRec &b = p->adapters[(size_t)d];
-                p->pages.release(adapter_rows(p, b), b.pt_host);
-                p->arena.release(b.pt_off, adapter_rows(p, b));
-                b.pt_off = -1;
-            }
+            undo_host();
             return fail(SLORA_ERR_POOL_FULL, "adapters_load: page-table arena fragmented");
         }
         if (a.pt_read_pending) {   // a previous load kernel may still read pt_host
-            CUDA_TRY(cudaEventSynchronize(p->load_event));   // recorded after every load's work
+            const cudaError_t e = cudaEventSynchronize(p->load_event);   // recorded after every load's work
+            if (e != cudaSuccess) {
+                p->arena.release(off, rows);
+                undo_host();
+                return fail(SLORA_ERR_CUDA, "adapters_load: cudaEventSynchronize failed: %s", cudaGetErrorString(e));
+            }
             for (int32_t t : todo) p->adapters[(size_t)t].pt_read_pending = false;
         }
         p->pages.alloc(rows, a.pt_host);  // cannot fail: counted above
@@ -362,17 +387,56 @@ slora_status slora_adapters_load(slora_pool_t p, int32_t n, const int32_t *ids, 
     }
 
     cudaStream_t side = p->side;
+    // From here on a failure takes the load back: the side stream's work so far completes,
+    // the directory entries of the load's adapters are cleared, and their pages and arena
+    // ranges return to the free lists (nothing is left half loaded).
+    auto rollback = [&](slora_status err) -> slora_status {
+        cudaStreamSynchronize(side);
+        DirArgs clr;
+        clr.n = 0;
+        for (size_t i = 0; i < todo.size(); ++i) {
+            DirUpdate &u = clr.upd[clr.n++];
+            u.adapter_id = todo[i];
+            u.rank = 0;
+            u.scaling = 0.f;
+            u.pad = 0;
+            u.pt_off = -1;
+            if (clr.n == kMaxDirUpdatesPerLaunch || i + 1 == todo.size()) {
+                if (launch_dir_update(p->dir_dev, clr, side) == cudaSuccess)
+                    p->launches += 1;
+                clr.n = 0;
+            }
+        }
+        cudaStreamSynchronize(side);
+        for (int32_t d : done) {
+            AdapterRec &b = p->adapters[(size_t)d];
+            p->pages.release(adapter_rows(p, b), b.pt_host);
+            p->arena.release(b.pt_off, adapter_rows(p, b));
+            b.pt_off = -1;
+            b.pt_read_pending = false;
+        }
+        return err;
+    };
+#define LOAD_TRY(expr, kind)                                                                     \
+    do {                                                                                        \
+        const bool _inj = inject_fault(kind);                                                   \
+        cudaError_t _e = _inj ? cudaErrorLaunchFailure : (expr);                                 \
+        if (_e != cudaSuccess)                                                                  \
+            return rollback(fail(SLORA_ERR_CUDA, "%s failed: %s%s (%s:%d)", #expr, cudaGetErrorString(_e), \
+                                 _inj ? " (injected)" : "", __FILE__, __LINE__));               \
+    } while (0)
     if (p->release_pending)
-        CUDA_TRY(cudaStreamWaitEvent(side, p->release_event, 0));
+        LOAD_TRY(cudaStreamWaitEvent(side, p->release_event, 0), SLORA_FAULT_NONE);
     if (p->load_start_event)
-        CUDA_TRY(cudaEventRecord(p->load_start_event, side));
+        LOAD_TRY(cudaEventRecord(p->load_start_event, side), SLORA_FAULT_NONE);
     ScatterArgs sargs;
     sargs.n_runs = 0;
     auto flush = [&]() -> slora_status {
         if (sargs.n_runs == 0)
             return SLORA_OK;
-        CUDA_TRY(launch_scatter(p->pt_dev, p->pool_dev, p->num_pages, p->hidden, sargs, p->status_dev,
-                                p->num_sms, side));
+        LOAD_TRY(launch_scatter(p->pt_dev, p->pool_dev, p->num_pages, p->hidden, sargs, p->status_dev,
+                                p->num_sms, side),
+                 SLORA_FAULT_SCATTER);
         p->launches += 1;
         sargs.n_runs = 0;
         return SLORA_OK;
@@ -386,11 +450,11 @@ slora_status slora_adapters_load(slora_pool_t p, int32_t n, const int32_t *ids, 
         for (int32_t id : todo)
             largest = std::max(largest, adapter_rows(p, p->adapters[(size_t)id]) * p->hidden * 2);
         if (largest > p->staging_bytes) {
-            CUDA_TRY(cudaStreamSynchronize(side));
+            LOAD_TRY(cudaStreamSynchronize(side), SLORA_FAULT_NONE);
             if (p->staging) cudaFree(p->staging);
             p->staging = nullptr;
             p->staging_bytes = 0;
-            CUDA_TRY(cudaMalloc(&p->staging, (size_t)largest));
+            LOAD_TRY(cudaMalloc(&p->staging, (size_t)largest), SLORA_FAULT_STAGING);
             p->staging_bytes = largest;
         }
         int64_t off = 0;
@@ -402,7 +466,8 @@ slora_status slora_adapters_load(slora_pool_t p, int32_t n, const int32_t *ids, 
                     return st;
                 off = 0;
             }
-            CUDA_TRY(cudaMemcpyAsync(p->staging + off, a.store, (size_t)bytes, cudaMemcpyHostToDevice, side));
+            LOAD_TRY(cudaMemcpyAsync(p->staging + off, a.store, (size_t)bytes, cudaMemcpyHostToDevice, side),
+                     SLORA_FAULT_COPY);
             ScatterRun &run = sargs.runs[sargs.n_runs++];
             run.src = p->staging + off;
             run.pt_src = a.pt_host_dev;
@@ -440,13 +505,14 @@ slora_status slora_adapters_load(slora_pool_t p, int32_t n, const int32_t *ids, 
         u.pad = 0;
         u.pt_off = a.pt_off;
         if (dargs.n == kMaxDirUpdatesPerLaunch || i + 1 == todo.size()) {
-            CUDA_TRY(launch_dir_update(p->dir_dev, dargs, side));
+            LOAD_TRY(launch_dir_update(p->dir_dev, dargs, side), SLORA_FAULT_DIRECTORY);
             p->launches += 1;
             dargs.n = 0;
         }
     }
-    CUDA_TRY(cudaEventRecord(p->load_event, side));
-    CUDA_TRY(cudaStreamWaitEvent((cudaStream_t)stream, p->load_event, 0));
+    LOAD_TRY(cudaEventRecord(p->load_event, side), SLORA_FAULT_NONE);
+    LOAD_TRY(cudaStreamWaitEvent((cudaStream_t)stream, p->load_event, 0), SLORA_FAULT_NONE);
+#undef LOAD_TRY
     for (int32_t id : todo) {
         p->adapters[(size_t)id].resident = true;
         p->lru.insert(id);
@@ -801,6 +867,16 @@ slora_status slora_pool_get_load_mode(slora_pool_t p, int32_t *mode, int64_t *st
         return fail(SLORA_ERR_INVALID_ARG, "pool_get_load_mode");
     *mode = p->load_mode;
     *staging_bytes = p->staging_bytes;
+    return SLORA_OK;
+}
+
+slora_status slora_debug_inject_load_fault(int32_t kind, int32_t nth)
+{
+    if (kind < SLORA_FAULT_NONE || kind > SLORA_FAULT_ARENA || nth < 0)
+        return fail(SLORA_ERR_INVALID_ARG, "debug_inject_load_fault: kind=%d nth=%d", kind, nth);
+    std::lock_guard<std::mutex> lk(g_fault_mu);
+    g_fault_kind = nth > 0 ? kind : SLORA_FAULT_NONE;
+    g_fault_left = nth;
     return SLORA_OK;
 }
 
