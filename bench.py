@@ -86,7 +86,8 @@ TRAFFIC_CAPTURE = ("ncu --clock-control none --metrics dram__bytes_read.sum,dram
                    "-k regex:{kernel} -s 3 -c 1 python bench.py --workload {workload} --profile-calls 5")
 TRAFFIC = {
     # workload name: (kernel, DRAM bytes per launch, sources_sha at capture)
-    "decode_13b_h5120_a2000_t512_zipf0.5": ("delta_kernel", 265030144 + 3911168, "5ba0e890c0d2f496"),
+    "decode_13b_h5120_a2000_t512_zipf0.5": ("delta_kernel", 264884736 + 4268544, "8fa1b0041578dcdf"),
+    "decode_7b_h4096_a100_t256_zipf1": ("delta_kernel", 41947648 + 8448, "8fa1b0041578dcdf"),
 }
 KERNEL_SOURCES = {
     "delta_kernel": ("decode.cu", "ptx.h", "internal.h"),
