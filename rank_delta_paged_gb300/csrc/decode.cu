@@ -12,10 +12,10 @@
 //
 //   plan_kernel (one CTA): groups the decode tokens by adapter in a shared-memory hash
 //     table (caching each adapter's directory entry in its slot), cuts every group into
-//     items of up to 8 tokens, and writes the work list of the delta kernel: for every
-//     item and projection of the call, one shrink unit per (hidden block, 64-row rank
-//     chunk) and one expand unit per hidden block; all shrink units come first, items
-//     in descending rank.
+//     items of up to 8 tokens, packs small items into shared work groups, and writes the
+//     work list of the delta kernel: for every work group and projection of the call, one
+//     shrink unit per (hidden block, 64-row rank chunk) and one expand unit per hidden
+//     block; all shrink units come first, items in descending rank.
 //
 //   delta_kernel: one persistent CTA per SM takes units in list order (its first by its
 //     index, then from a counter in the plan), so every SM stays busy until the list ends:
@@ -31,10 +31,11 @@
 //     A^T or B rows) into a ring of 8-row stages with 1-D bulk copies; eight consumer
 //     warps contract them on the tensor cores with warp-level mma.sync m16n8k16 (fp16
 //     operands, fp32 accumulators; a shrink puts rank rows on M and tokens on N, an
-//     expand tokens on M and columns on N); a gather warp polls and sums the partials of
-//     the expand units ahead of the consumers, so no consumer waits on a global round
-//     trip.  Every page row is read once per item; the only cross-SM traffic is the small
-//     tagged partials.  Every wait is bounded in time.
+//     expand tokens on M and columns on N); a reduce warp sums the consumers' shrink
+//     partials and writes them as tagged words; a gather warp polls and sums the partials
+//     of the expand units ahead of the consumers, so no consumer waits on a global round
+//     trip.  Every page row is read once per item (small items share units); the only
+//     cross-SM traffic is the small tagged partials.  Every wait is bounded in time.
 //
 // Expand units only wait for shrink units that precede them in the list, and shrink
 // units never wait on another SM, so the list drains whatever number of CTAs is resident.
@@ -64,9 +65,10 @@ constexpr int kConsumerWarps = 8;                 // warps doing the contraction
 constexpr int kCopyWarps = 4;                     // warps issuing the bulk copies
 constexpr int kWarpLead = kConsumerWarps;         // fetches and publishes the units
 constexpr int kWarpCopy0 = kConsumerWarps + 1;    // first copy warp
-constexpr int kWarpGather = kWarpCopy0 + kCopyWarps;   // sums the shrink partials of the expand units ahead
+constexpr int kWarpReduce = kWarpCopy0 + kCopyWarps;   // sums the consumers' shrink partials
+constexpr int kWarpGather = kWarpReduce + 1;            // sums the shrink partials of the expand units ahead
 constexpr int kThreads = 32 * (kWarpGather + 1);
-constexpr int kRecReaders = kConsumerWarps + kCopyWarps + 1;   // warps that read every unit record
+constexpr int kRecReaders = kConsumerWarps + kCopyWarps + 2;   // warps that read every unit record
 constexpr int kTok = 8;                           // tokens per item: one MMA n-tile / one ring stage
 constexpr int kMaxSlice = 1024;                   // elements of a hidden block
 constexpr int kMaxBlocks = 8;                     // hidden blocks (hidden <= 8192)
@@ -93,7 +95,7 @@ static_assert(NST % kCopyWarps == 0, "each ring slot always filled by the same c
 constexpr int kXs = kMaxSlice / 16 / kConsumerWarps;
 constexpr int kPairs = kMaxSlice / 16 / kConsumerWarps;
 // A consumer warp's scratch region: a shrink unit's partial (8 tokens x 64 rank rows), summed
-// by the gather warp, or the y0 values of an expand unit of more than 64 rank rows (2 kPairs
+// by the reduce warp, or the y0 values of an expand unit of more than 64 rank rows (2 kPairs
 // n-tiles x 32 lanes, half2 each).
 constexpr int kRegionFloats = kTok * kRC;
 static_assert(2 * kPairs * 32 <= kRegionFloats, "y0 values fit a region");
@@ -827,7 +829,7 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
     uint64_t *full = bars, *empty = bars + NST;              // ring stages
     uint64_t *rfull = bars + 2 * NST, *rempty = rfull + QD;  // unit records
     uint64_t *ufull = rempty + QD, *uempty = ufull + QU;     // u buffers
-    uint64_t *psfull = uempty + QU, *psempty = psfull + 1;   // shrink partials (consumers -> gather warp)
+    uint64_t *psfull = uempty + QU, *psempty = psfull + 1;   // shrink partials (consumers -> reduce warp)
     __shared__ int s_abort;
     __shared__ int s_blk[kMaxBlocks + 1];                    // first element of each hidden block
 
@@ -1126,13 +1128,16 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
         return;
     }
 
-    if (warp == kWarpGather) {
-        // ================================= gather warp ==================================
-        // Shrink units of this CTA: sums the consumer warps' partials in warp order and writes
-        // the unit's partial as tagged words.  Expand units ahead of the consumers: waits until
-        // the partial words of every hidden block carry this launch's tag, sums them in block
-        // order and rounds u to fp16 once, into the next u buffer (lane l covers tokens l>>4,
-        // +2 per round, columns 4 (l & 15) .. +3).
+    if (warp == kWarpReduce || warp == kWarpGather) {
+        // ============================== reduce and gather warps ============================
+        // Reduce warp, shrink units of this CTA: sums the consumer warps' partials in warp
+        // order and writes the unit's partial as tagged words.  Gather warp, expand units ahead
+        // of the consumers: waits until the partial words of every hidden block carry this
+        // launch's tag, sums them in block order and rounds u to fp16 once, into the next u
+        // buffer (lane l covers tokens l>>4, +2 per round, columns 4 (l & 15) .. +3).  Two
+        // warps, so that the gather can start on the first expand units while the last shrink
+        // units of the CTA still run.
+        const bool reducer = warp == kWarpReduce;
         const uint32_t tag = a.tag;
         uint32_t uj = 0;   // u buffers filled
         uint32_t sr = 0;   // shrink partials summed
@@ -1170,6 +1175,7 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
                 nti = geo_nt(g);
             };
             if (!(packed & 32u)) {
+                if (!reducer) continue;
                 const int c = (int)((packed >> 12) & 15u), b = (int)((packed >> 9) & 7u);
                 const int rows_c = min(kRC, rows - kRC * c), ld = 16 * ceil_div(rows_c, 16);
                 wait_phase<false>(psfull, sr & 1, abort, status);
@@ -1201,6 +1207,7 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
                 ++sr;
                 continue;
             }
+            if (reducer) continue;
             const int nch = ceil_div(rows, kRC);
             const int j4 = 4 * (lane & 15);
 #pragma unroll 1
@@ -1322,8 +1329,6 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[tpos.slot]);
-            // the partial set is free once the gather warp has summed the previous shrink unit
-            if (sj > 0) wait_phase<false>(psempty, (sj - 1) & 1, abort, status);
 #pragma unroll 1
             for (int blk = 0; blk < nb; ++blk) {
                 const RingPos lo = cur;
@@ -1350,6 +1355,9 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
                     mbar_arrive(&empty[lo.slot]);
                     if (has_hi) mbar_arrive(&empty[hi.slot]);
                 }
+                // the partial set is free once the reduce warp has summed the previous shrink
+                // unit (waited for only now, so that the first block's loads and MMAs overlap it)
+                if (blk == 0 && sj > 0) wait_phase<false>(psempty, (sj - 1) & 1, abort, status);
                 // rows gid, gid + 8 of the block; tokens 2 tig, 2 tig + 1
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
@@ -1357,7 +1365,7 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
                     region[(2 * tig + 1) * kRC + 16 * blk + gid + 8 * h] = pacc[0][2 * h + 1] + pacc[1][2 * h + 1];
                 }
             }
-            // hand the partial to the gather warp, which sums the 8 warps' partials in order
+            // hand the partial to the reduce warp, which sums the 8 warps' partials in order
             __syncwarp();
             if (lane == 0) mbar_arrive(psfull);
             ++sj;
@@ -1370,7 +1378,7 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
             // A unit of at most 64 rank rows (9 stages) keeps its token stage (y0) until the
             // epilogue; a longer one would hold the ring, so it first copies this lane's y0
             // values (token gid, columns 16 (pp0+p) + 8 n2 + 2 tig, +1) to the warp's region,
-            // once the gather warp has summed the partials the region held.
+            // once the reduce warp has summed the partials the region held.
             const bool hold = urows <= kRC;
             uint32_t *yv = reinterpret_cast<uint32_t *>(region);
             if (!hold) {
