@@ -376,17 +376,17 @@ slora_status slora_lora_apply_bmm(slora_pool_t pool, int32_t proj, const void *x
  *
  * Scratch: one fixed 16 MiB device array inside the library, which every GPU that loads
  * the library holds until the process exits.  The call allocates and frees nothing.
- * Limit: the call's scratch must fit that array; it needs about
+ * Limit: one plan's scratch must fit that array; a plan of T' tokens needs about
  *   T' * (116 + NB * (8 * (nch + 1) + 512 * nch)) + 1280 bytes
  * (per token: its slot in the token order and at most one 112-byte work group; per hidden
  * block: the 8-byte work-list entries and the 64 eight-byte tagged partial sums of every
- * 64-row rank chunk), with
- * NB = ceil(hidden / 1024), nch = ceil(largest registered rank / 64), and
- * T' = min(T, 16384) when max_adapters <= 2048, else min(T, 2048) (larger batches then run
- * as several plans of 2048 tokens, each fitting the array on its own).  With ranks up to
- * 64 that is about 2.2 KB per token at hidden 4096 (a batch of up to about 7,500 tokens
- * fits) and 2.8 KB at hidden 5120 (about 6,000 tokens).  A call beyond it returns
- * SLORA_ERR_UNSUPPORTED with the sizes in slora_last_error() and launches nothing.
+ * 64-row rank chunk), with NB = ceil(hidden / 1024) and nch = ceil(largest registered
+ * rank / 64).  A batch runs as one plan when it fits (T' = min(T, 16384) when
+ * max_adapters <= 2048, else 2048), otherwise as several plans of half, a quarter, ... of
+ * that many tokens, the largest that fits (every token's result is the same whatever plan
+ * it is in).  With ranks up to 64 one plan holds about 7,500 tokens at hidden 4096 and
+ * 6,000 at hidden 5120.  Only when a plan of 64 tokens does not fit does the call return
+ * SLORA_ERR_UNSUPPORTED (with the sizes in slora_last_error()) and launch nothing.
  * The first call on a device looks up the array's device address (once per device,
  * with that device current); make that first call before any stream capture.
  * Every call on a device shares the one array and leaves its plan and partial sums

@@ -1584,7 +1584,8 @@ cudaError_t launch_lora_apply(const PoolView &pv, const ProjList &pl, int32_t T,
     cfg2.attrs = attr;
     cfg2.numAttrs = 1;
 
-    const int32_t chunk = plan_chunk(pv.max_adapters);
+    int32_t chunk = plan_chunk(pv.max_adapters);
+    if (scratch.max_chunk > 0 && scratch.max_chunk < chunk) chunk = scratch.max_chunk;
     const int32_t cap = scratch.cap_tokens < chunk ? scratch.cap_tokens : chunk;
     const int NB = n_blocks(pv.hidden);
     PlanLayout L = carve(scratch.base, cap, scratch.cap_proj, NB, scratch.max_rank, nullptr);

@@ -101,6 +101,7 @@ struct PlanScratch {
     int32_t cap_tokens = 0;   // tokens the layout was carved for
     int32_t max_rank = 0;     // largest adapter rank the layout was carved for
     int32_t cap_proj = 0;     // projections per call the layout was carved for
+    int32_t max_chunk = 0;    // tokens per plan at most (0: the plan's own limit)
     // Tag of the decode kernel's partial sums: each delta launch uses the next value.  0 means
     // the partial region must be cleared first (fresh scratch, or the sequence wrapped), so a
     // stale word can never carry a live tag.

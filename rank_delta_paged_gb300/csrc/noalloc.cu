@@ -23,6 +23,7 @@ namespace slora {
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = 16u << 20;   // 16 MiB
+constexpr int32_t kMinNoAllocChunk = 64;              // tokens per plan at least
 constexpr int kMaxDevices = 64;
 
 // Shared by every call of the entry point on a device; holds the last call's plan and
@@ -83,12 +84,19 @@ extern "C" slora_status slora_lora_apply_noalloc(slora_pool_t pool, int32_t proj
         return fail(SLORA_ERR_INVALID_ARG, "lora_apply_noalloc: n_seg=%d (at most min(T, %d))", n_seg,
                     kMaxSegments);
     const int32_t max_rank = hp.max_rank > 0 ? hp.max_rank : 1;
-    const size_t need = plan_scratch_bytes(T, max_rank, hp.pv.hidden, hp.pv.max_adapters, 1);
+    // The batch runs as plans of at most `chunk` tokens: the plan's own limit, halved until
+    // one plan's scratch fits the array (every token's arithmetic is the same whatever
+    // plan it is in); below kMinNoAllocChunk tokens the call is refused.
+    int32_t chunk = T;
+    while (chunk > kMinNoAllocChunk &&
+           plan_scratch_bytes(chunk, max_rank, hp.pv.hidden, hp.pv.max_adapters, 1) > kNoAllocScratchBytes)
+        chunk = (chunk + 1) / 2;
+    const size_t need = plan_scratch_bytes(chunk, max_rank, hp.pv.hidden, hp.pv.max_adapters, 1);
     if (need > kNoAllocScratchBytes)
         return fail(SLORA_ERR_UNSUPPORTED,
-                    "lora_apply_noalloc: this batch needs %zu bytes of scratch (T=%d, largest registered "
-                    "rank %d, hidden %d) but the static scratch holds %zu; use slora_lora_apply or a smaller batch",
-                    need, T, max_rank, hp.pv.hidden, kNoAllocScratchBytes);
+                    "lora_apply_noalloc: a plan of %d tokens needs %zu bytes of scratch (largest registered "
+                    "rank %d, hidden %d) but the static scratch holds %zu; use slora_lora_apply",
+                    chunk, need, max_rank, hp.pv.hidden, kNoAllocScratchBytes);
     DeviceScope dev_scope(hp.device);   // the caller's current device comes back on return
     cudaError_t e = dev_scope.error();
     if (e != cudaSuccess)
@@ -104,9 +112,10 @@ extern "C" slora_status slora_lora_apply_noalloc(slora_pool_t pool, int32_t proj
     PlanScratch ps;
     ps.base = scratch;
     ps.bytes = kNoAllocScratchBytes;
-    ps.cap_tokens = T;
+    ps.cap_tokens = chunk;
     ps.max_rank = max_rank;
     ps.cap_proj = 1;
+    ps.max_chunk = chunk;
     int launched = 0;
     {
         std::lock_guard<std::mutex> lk(g_mu);
