@@ -76,6 +76,11 @@ constexpr int kRC = 64;                           // rank rows per rank chunk
 constexpr int NST = 12;                           // ring depth (8-row stages)
 constexpr int QD = 8;                             // unit records in flight
 constexpr int QU = 4;                             // u buffers (gather warp -> consumers)
+#ifndef SLORA_CLAIM_AHEAD
+#define SLORA_CLAIM_AHEAD 5
+#endif
+constexpr int kClaimAhead = SLORA_CLAIM_AHEAD;    // units a CTA holds beyond those it has finished
+static_assert(kClaimAhead >= 2, "the consumers read the record after the one they work on");
 constexpr int kUPitch = kRC + 8;                  // halves per token row of a u buffer
 constexpr int kMaxRank = 1024;
 
@@ -831,6 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
     uint64_t *ufull = rempty + QD, *uempty = ufull + QU;     // u buffers
     uint64_t *psfull = uempty + QU, *psempty = psfull + 1;   // shrink partials (consumers -> reduce warp)
     __shared__ int s_abort;
+    __shared__ int s_done;                                   // units the consumers have finished
     __shared__ int s_blk[kMaxBlocks + 1];                    // first element of each hidden block
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -838,6 +844,7 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
     const int NB = a.nblk;
     int32_t *status = a.pv.status;
     volatile int *abort = &s_abort;
+    volatile int *done = &s_done;
     const uint32_t ring_s = smem_u32(ring), zrow_s = smem_u32(zrow);
     const uint32_t ubuf_s = smem_u32(ubuf);
 
@@ -863,6 +870,7 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
         mbar_init(psfull, kConsumerWarps);
         mbar_init(psempty, 1);
         s_abort = 0;
+        s_done = 0;
         fence_mbar_init();
     }
     __syncthreads();
@@ -888,9 +896,7 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
     if (warp == kWarpLead) {
         // ================================== lead (metadata) ==================================
         // Takes units in list order (the first by the CTA's index, then from the plan's
-        // counter) and publishes each with its token ids and first chunk's page ids.  The
-        // loads run three units deep: the counter for unit k+2, the descriptor of unit k+1
-        // and the tokens and page ids of unit k are in flight together.
+        // counter) and publishes each with its token ids and first chunk's page ids.
         const int G = (int)gridDim.x;
         const int32_t *pt = a.pv.pt_arena;
         // the token id of token row `lane` and the page ids of rows `lane`, `lane` + 32 of the
@@ -955,81 +961,114 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
             }
         };
         auto load_lu = [&](int idx) { return __ldcg(reinterpret_cast<const int2 *>(a.L.units) + idx); };
-        // The loads run four units deep: in the iteration that publishes unit k, the token and
-        // page ids of unit k+1 (from its resolved descriptor), the work group of unit k+2 (from
-        // its list entry), the list entry of unit k+3 and the counter for unit k+4 are in
-        // flight.  lane 0 holds the counter's value (the unit's index less G).
-        int grab = 0;
-        if (lane == 0) grab = atomicAdd(&a.L.hdr->grab, 1);
-        bool cvalid = (int)blockIdx.x < n_units, v1 = false, v2 = false;
-        UnitRegs cu{}, nw{};
-        int2 nlu = make_int2(0, 0), nnlu = make_int2(0, 0);
-        int ctok = 0, cti = 0;
-        int32_t cp0 = -1, cp1 = -1;
+        // A four-stage software pipeline; in one pass the record of a unit is published (its
+        // token and page ids were loaded in the pass before), the next unit is resolved and
+        // its token and page ids loaded, the work group of the one after it loaded, the list
+        // entry of a claimed unit loaded, and a new unit claimed from the plan's counter.
+        // Claims stay at most kClaimAhead units ahead of the units the consumers have
+        // finished: units claimed early are a static schedule, and at the end of the list
+        // the CTAs that claimed slower units would finish late.  A pass with nothing to
+        // publish leaves a bubble in the pipeline rather than waiting; only an empty pipeline
+        // waits (bounded) for the consumers.
+        bool vB = false, vC = false, vD = false;   // stage valid: list entry, work group, resolved unit
+        bool apend = false, exhausted = false;     // a claim in flight; the list has run out
+        int grab = 0;                              // lane 0: the last claim's counter value
+        int2 luB = make_int2(0, 0), luC = make_int2(0, 0);
+        UnitRegs wC{}, uD{};
+        int dtok = 0, dti = 0;
+        int32_t dp0 = -1, dp1 = -1;
+        int nclaimed = 0, kp = 0;                  // units claimed, records published
         {
-            int2 lu0 = make_int2(0, 0);
-            UnitRegs w0{};
-            if (cvalid) lu0 = load_lu(blockIdx.x);
-            int idx = G + __shfl_sync(0xffffffffu, grab, 0);
-            v1 = cvalid && idx < n_units;
-            if (v1) {
-                nlu = load_lu(idx);
-                if (lane == 0) grab = atomicAdd(&a.L.hdr->grab, 1);
-            }
-            if (cvalid) load_unit(a.L.wgs + lu0.x, w0);
-            if (v1) load_unit(a.L.wgs + nlu.x, nw);
-            idx = G + __shfl_sync(0xffffffffu, grab, 0);
-            v2 = v1 && idx < n_units;
-            if (v2) {
-                nnlu = load_lu(idx);
-                if (lane == 0) grab = atomicAdd(&a.L.hdr->grab, 1);
-            }
-            if (cvalid) {
-                resolve(w0, lu0, cu);
-                fetch_rest(cu, ctok, cti, cp0, cp1);
+            // the first unit is list entry blockIdx.x: its entry is loaded before the count of
+            // units is known (an index inside the list's allocation; used only if valid)
+            const int2 lu0 = load_lu((int)min((int64_t)blockIdx.x, a.L.cap_units - 1));
+            if ((int)blockIdx.x < n_units) {
+                luB = lu0;
+                vB = true;
+                nclaimed = 1;
+                if (kClaimAhead > 1) {
+                    if (lane == 0) grab = atomicAdd(&a.L.hdr->grab, 1);
+                    apend = true;
+                    ++nclaimed;
+                }
+            } else {
+                exhausted = true;
             }
         }
-        for (int k = 0;; ++k) {
-            const uint32_t q = k % QD;
-            if (k >= QD) wait_phase<false>(&rempty[q], ((k / QD) - 1) & 1, abort, status);
-            if (!cvalid || *abort) {
+        uint64_t t_wait = 0;
+        for (uint32_t it = 0;; ++it) {
+            if (vD) {
+                const uint32_t q = kp % QD;
+                if (kp >= QD) wait_phase<false>(&rempty[q], ((kp / QD) - 1) & 1, abort, status);
+                if (*abort) {
+                    vB = vC = vD = apend = false;
+                    exhausted = true;
+                } else {
+                    uint4 v = uD.w[0];
+#pragma unroll
+                    for (int i = 1; i < kUnitVecs; ++i)
+                        if (lane == i) v = uD.w[i];
+                    if (lane < kUnitVecs) reinterpret_cast<uint4 *>(&recs[q].u)[lane] = v;
+                    if (lane == 0) recs[q].end = 0;
+                    if (lane < kTok) {
+                        recs[q].tok[lane] = dtok;
+                        recs[q].titem[lane] = (int8_t)dti;
+                    }
+                    recs[q].pg[lane] = dp0;
+                    recs[q].pg[lane + 32] = dp1;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&rfull[q]);
+                    ++kp;
+                }
+            }
+            vD = vC;
+            if (vC) {
+                resolve(wC, luC, uD);
+                fetch_rest(uD, dtok, dti, dp0, dp1);
+            }
+            vC = vB;
+            if (vB) {
+                luC = luB;
+                load_unit(a.L.wgs + luB.x, wC);
+            }
+            vB = false;
+            if (apend) {
+                const int idx = G + __shfl_sync(0xffffffffu, grab, 0);
+                apend = false;
+                if (idx < n_units) {
+                    luB = load_lu(idx);
+                    vB = true;
+                } else {
+                    exhausted = true;
+                }
+            }
+            if (!exhausted && nclaimed - __shfl_sync(0xffffffffu, *done, 0) < kClaimAhead) {
+                if (lane == 0) grab = atomicAdd(&a.L.hdr->grab, 1);
+                apend = true;
+                ++nclaimed;
+            }
+            if (vB || vC || vD || apend) {
+                t_wait = 0;
+                continue;
+            }
+            if (exhausted) {
+                const uint32_t q = kp % QD;
+                if (kp >= QD) wait_phase<false>(&rempty[q], ((kp / QD) - 1) & 1, abort, status);
                 if (lane == 0) {
                     recs[q].end = 1;
                     mbar_arrive(&rfull[q]);
                 }
                 break;
             }
-            {
-                uint4 v = cu.w[0];
-#pragma unroll
-                for (int i = 1; i < kUnitVecs; ++i)
-                    if (lane == i) v = cu.w[i];
-                if (lane < kUnitVecs) reinterpret_cast<uint4 *>(&recs[q].u)[lane] = v;
+            // every claimed unit is published and the consumers are kClaimAhead behind: wait
+            // for them to finish one (bounded in time)
+            __nanosleep(64);
+            if (t_wait == 0) t_wait = global_timer_ns();
+            if ((it & 15u) == 0 && global_timer_ns() - t_wait > kWaitLimitNs) {
+                set_status(status, SLORA_DEV_TIMEOUT);
+                *abort = 1;
             }
-            if (lane == 0) recs[q].end = 0;
-            if (lane < kTok) {
-                recs[q].tok[lane] = ctok;
-                recs[q].titem[lane] = (int8_t)cti;
-            }
-            recs[q].pg[lane] = cp0;
-            recs[q].pg[lane + 32] = cp1;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&rfull[q]);
-            // advance the pipeline
-            cvalid = v1;
-            if (cvalid) {
-                resolve(nw, nlu, cu);
-                fetch_rest(cu, ctok, cti, cp0, cp1);
-            }
-            v1 = v2;
-            nlu = nnlu;
-            if (v1) load_unit(a.L.wgs + nlu.x, nw);
-            const int idx = G + __shfl_sync(0xffffffffu, grab, 0);
-            v2 = v1 && idx < n_units;
-            if (v2) {
-                nnlu = load_lu(idx);
-                if (lane == 0) grab = atomicAdd(&a.L.hdr->grab, 1);
-            }
+            if (*abort) exhausted = true;
         }
         return;
     }
@@ -1342,12 +1381,24 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
                 const uint32_t arow = (q4 & 1) ? (has_hi ? ring_s + hi.slot * stageB + rr * P : zrow_s)
                                                : ring_s + lo.slot * stageB + rr * P;
                 float pacc[2][4] = {};   // even / odd K steps: two independent MMA chains
+                if (nks == kXs) {
+                    // the usual case: every A^T fragment is loaded before the first MMA, so the
+                    // loads' latency is paid once per block rather than once per K step
+                    uint32_t af[kXs][4];
 #pragma unroll
-                for (int i = 0; i < kXs; ++i) {
-                    if (i < nks) {
-                        uint32_t af[4];
-                        ldsm_x4(arow + (16 * (ks0 + i) + 8 * (q4 >> 1)) * 2, af);   // A^T rows
-                        mma16816(pacc[i & 1], af, xf[i >> 1][2 * (i & 1)], xf[i >> 1][2 * (i & 1) + 1]);
+                    for (int i = 0; i < kXs; ++i)
+                        ldsm_x4(arow + (16 * (ks0 + i) + 8 * (q4 >> 1)) * 2, af[i]);   // A^T rows
+#pragma unroll
+                    for (int i = 0; i < kXs; ++i)
+                        mma16816(pacc[i & 1], af[i], xf[i >> 1][2 * (i & 1)], xf[i >> 1][2 * (i & 1) + 1]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < kXs; ++i) {
+                        if (i < nks) {
+                            uint32_t af[4];
+                            ldsm_x4(arow + (16 * (ks0 + i) + 8 * (q4 >> 1)) * 2, af);   // A^T rows
+                            mma16816(pacc[i & 1], af, xf[i >> 1][2 * (i & 1)], xf[i >> 1][2 * (i & 1) + 1]);
+                        }
                     }
                 }
                 __syncwarp();
@@ -1417,7 +1468,28 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
                     // B rows (the MMA's B operand, transposed on load): 0-7 from stage lo, 8-15 from hi
                     const uint32_t brow = (q4 & 1) ? (has_hi ? ring_s + hi.slot * stageB + rr * P : zrow_s)
                                                    : ring_s + lo.slot * stageB + rr * P;
-                    if (c == 0 && blk == 0) {
+                    if (pp1 - pp0 == kPairs) {
+                        // the usual case: the B fragments are loaded kAhead column pairs ahead of
+                        // their MMAs, so the loads' latency is paid once per block, not per pair
+                        constexpr int kAhead = 3;   // (more would spill registers)
+                        uint32_t bf[kAhead][4];
+#pragma unroll
+                        for (int p = 0; p < kAhead; ++p)
+                            ldsm_x4_t(brow + (16 * (pp0 + p) + 8 * (q4 >> 1)) * 2, bf[p]);
+                        const bool zc = c == 0 && blk == 0;
+#pragma unroll
+                        for (int p = 0; p < kPairs; ++p) {
+                            if (zc) {
+                                mma16816_zc(acc[2 * p], af, bf[p % kAhead][0], bf[p % kAhead][1]);
+                                mma16816_zc(acc[2 * p + 1], af, bf[p % kAhead][2], bf[p % kAhead][3]);
+                            } else {
+                                mma16816(acc[2 * p], af, bf[p % kAhead][0], bf[p % kAhead][1]);
+                                mma16816(acc[2 * p + 1], af, bf[p % kAhead][2], bf[p % kAhead][3]);
+                            }
+                            if (p + kAhead < kPairs)
+                                ldsm_x4_t(brow + (16 * (pp0 + p + kAhead) + 8 * (q4 >> 1)) * 2, bf[p % kAhead]);
+                        }
+                    } else if (c == 0 && blk == 0) {
                         // the first block starts the accumulators (zero C operand)
 #pragma unroll
                         for (int p = 0; p < kPairs; ++p) {
@@ -1492,6 +1564,7 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
                 }
             }
         }
+        if (w == 0 && lane == 0) *done = k + 1;
         upk = npk;
         urows = nrows;
         tk = ntk;
