@@ -18,9 +18,12 @@ exchange, so ranks are independent replicas (weak scaling) and the only collecti
 the timing barrier and the max-over-ranks reduction.  Under torchrun the ranks come from
 the environment; without it, ``--gpus N`` starts the N rank processes itself.
 
-Timing: W untimed warm-up steps; K timed steps, each preceded by a 2 x L2 write that
-evicts the pool and inputs from L2 (the flush itself is outside the per-step CUDA-event
-intervals); barrier + synchronize on both sides of the timed region; max over ranks.
+Timing: W untimed warm-up steps; K timed steps, each preceded by an L2 flush that evicts
+the pool and inputs from L2: a buffer of twice the L2 is written, then another of that
+size read, so that the L2 holds only clean lines of the second buffer (after a write alone
+the L2 is full of dirty lines whose write-back would fall inside the timed step); the
+flush is outside the per-step CUDA-event intervals; barrier + synchronize on both sides of
+the timed region; max over ranks.
 """
 from __future__ import annotations
 
@@ -296,9 +299,27 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm), "source": self.source}
 
 
+class L2Flush:
+    """Evicts the L2 before a timed step: writes a buffer of `nbytes`, then reads another of
+    that size, so that the L2 holds only clean lines of the second buffer (a write alone
+    would leave the written lines dirty, and their write-back would fall inside the next
+    timed region)."""
+
+    def __init__(self, nbytes: int, dev):
+        import torch
+        self.w = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        self.r = torch.ones(nbytes // 4, dtype=torch.int32, device=dev)
+        self.sink = torch.empty((), dtype=torch.int64, device=dev)
+
+    def __call__(self):
+        import torch
+        self.w.zero_()
+        torch.sum(self.r, dim=0, dtype=torch.int64, out=self.sink)
+
+
 def graph_timing(step_on, flush, stream, reps):
     """Median and mean CUDA-event time of one step replayed from a CUDA graph, each replay
-    preceded (outside its events) by a replay of a graph that writes the flush buffer."""
+    preceded (outside its events) by a replay of a graph that flushes the L2."""
     import torch
     try:
         side = torch.cuda.Stream()
@@ -308,7 +329,7 @@ def graph_timing(step_on, flush, stream, reps):
             step_on(side)      # warm the capture stream
             torch.cuda.current_stream().synchronize()
             with torch.cuda.graph(gf, stream=side):
-                flush.zero_()
+                flush()
             with torch.cuda.graph(gs, stream=side):
                 step_on(torch.cuda.current_stream())
             ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
@@ -470,7 +491,7 @@ def measure_extra(rdp, w, dev, flush, stream, hbm, fp16_tflops, reps=100):
                 x.record(stream)
         torch.cuda.synchronize()
         for a, b, c in ev:
-            flush.zero_()
+            flush()
             a.record(stream)
             rdp.slora_pool_set_stage_event(sess.pool, b)
             call(stream)
@@ -496,7 +517,7 @@ def measure_extra(rdp, w, dev, flush, stream, hbm, fp16_tflops, reps=100):
                    "frac": flops / t / 1e12 / fp16_tflops, "flops_per_call": flops,
                    "peak_kind": "measured in this run: torch.matmul fp16 8192^3, best of 10"},
         "attainable_frac": attain / t,
-        "timing": "median of %d calls, each after a 2 x L2 write; kernel_ms from the event the pool "
+        "timing": "median of %d calls, each after an L2 flush (2 x L2 written, then 2 x L2 read); kernel_ms from the event the pool "
                   "records after the plan to the end of the call" % reps,
     }
 
@@ -554,7 +575,7 @@ def main():
         ys.append(y0.clone())
     n_seg = w.n_seg
     l2 = int(torch.cuda.get_device_properties(local).L2_cache_size)
-    flush = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=dev)
+    flush = L2Flush(2 * max(l2, 64 << 20), dev)
 
     per_layer = w.n_proj // w.n_layers
     multi = args.apply == "multi" and per_layer > 1
@@ -574,7 +595,7 @@ def main():
 
     if args.profile_calls > 0:
         for _ in range(args.profile_calls):
-            flush.zero_()
+            flush()
             apply_layer(0, stream)
         torch.cuda.synchronize()
         status = sess.device_status()
@@ -595,7 +616,7 @@ def main():
         for _ in range(2):   # the faster of two passes: the first can include one-off costs
             g0.record(stream)
             for _ in range(5):
-                flush.zero_()
+                flush()
                 step()
             g1.record(stream)
             torch.cuda.synchronize()
@@ -614,7 +635,7 @@ def main():
     torch.cuda.synchronize()
     with ClockSampler(uuid) as clk:
         for k in range(K):
-            flush.zero_()
+            flush()
             starts[k].record(stream)
             step()
             ends[k].record(stream)
@@ -649,7 +670,7 @@ def main():
         ev.record(stream)   # creates the events
     torch.cuda.synchronize()
     for k in range(Kd):
-        flush.zero_()
+        flush()
         rdp.slora_pool_set_stage_event(sess.pool, d0[k])
         if multi:
             apply_layer(0, stream)
@@ -680,11 +701,11 @@ def main():
         c0 = [torch.cuda.Event(enable_timing=True) for _ in range(Kd)]
         c1 = [torch.cuda.Event(enable_timing=True) for _ in range(Kd)]
         for k in range(Kd):
-            flush.zero_()
+            flush()
             b0[k].record(stream)
             rdp.slora_lora_apply_bmm(sess.pool, 0, xs[0], yb, w.T, idx, ws, nb, None, stream)
             b1[k].record(stream)
-            flush.zero_()
+            flush()
             c0[k].record(stream)
             rdp.slora_lora_apply(sess.pool, 0, xs[0], ys[0], w.T, idx, seg, n_seg, None, stream)
             c1[k].record(stream)
@@ -809,7 +830,8 @@ def main():
         "n_gpus": world, "steps": K, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic (seeded; random-init adapters, no dataset)",
-        "config": dict(config_of(w, "flushed: 2 x L2 written before every timed step, outside the "
+        "config": dict(config_of(w, "flushed: 2 x L2 written, then another 2 x L2 read (the L2 left "
+                                    "holding clean lines only), before every timed step, outside the "
                                     "per-step CUDA-event intervals"),
                        apply=(f"one slora_lora_apply_multi call per layer ({per_layer} projections)" if multi
                               else "one slora_lora_apply call per projection")),

@@ -40,7 +40,7 @@
  *   - Device-side checks never trap: a kernel that meets a bad adapter index, a
  *     non-resident adapter, an out-of-range page or a segment whose tokens disagree on
  *     their adapter records a code in the pool's device status word and skips that
- *     work; slora_get_device_status() reads and clears it.
+ *     work (such a segment as a whole); slora_get_device_status() reads and clears it.
  */
 #ifndef SLORA_H
 #define SLORA_H

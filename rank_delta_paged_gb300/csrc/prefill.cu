@@ -359,9 +359,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 flag = kSkip;
                 m0 = lo + tile * MT;
                 mlen = min(MT, hi - m0);
-                const int ad = a.idx[m0];
+                // a segment whose tokens disagree on the adapter is skipped as a whole: every
+                // unit checks its whole segment
+                const int ad = a.idx[lo];
                 bool mixed = false;
-                for (int q = lane; q < mlen; q += 32) mixed |= a.idx[m0 + q] != ad;
+                for (int q = lo + lane; q < hi; q += 32) mixed |= a.idx[q] != ad;
                 if (__any_sync(0xffffffffu, mixed)) {
                     if (lane == 0) set_status(status, SLORA_DEV_BAD_SEGMENT);
                 } else if (ad == -1) {

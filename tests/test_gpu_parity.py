@@ -352,9 +352,27 @@ def test_segment_with_mixed_adapters_is_rejected():
         got = run(s)
         assert s.device_status() == rdp_dev("BAD_SEGMENT")
     y0 = w.y0()
-    # the mixed tile is skipped (y unchanged); the second segment is computed
+    # the mixed segment is skipped (y unchanged); the second segment is computed
     assert np.array_equal(got[:128].view(np.uint16), y0[:128].view(np.uint16))
     assert_close(got[128:], oracle.workload_reference(w, sel=np.arange(128, 178, dtype=np.int32)),
+                 "second segment")
+
+
+def test_segment_mixed_in_a_later_tile_is_rejected_whole():
+    """A segment of 300 tokens whose token 250 names another adapter: every token of the
+    segment keeps y0, whichever tiles the kernel cuts the segment into; the next segment is
+    computed."""
+    ranks = np.array([16, 32], np.int32)
+    idx = np.array([0] * 250 + [1] + [0] * 49 + [1] * 50, np.int32)
+    indptr = np.array([0, 300, 350], np.int32)
+    w = W.Workload("seg_mixed_late", 256, 1, ranks, idx, indptr, num_pages=8 * int(ranks.sum()),
+                   kv_pages=0, shuffle_seed=0, seed=4)
+    with session_all_loaded(w) as s:
+        got = run(s)
+        assert s.device_status() == rdp_dev("BAD_SEGMENT")
+    y0 = w.y0()
+    assert np.array_equal(got[:300].view(np.uint16), y0[:300].view(np.uint16))
+    assert_close(got[300:], oracle.workload_reference(w, sel=np.arange(300, 350, dtype=np.int32)),
                  "second segment")
 
 
