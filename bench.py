@@ -89,8 +89,8 @@ TRAFFIC_CAPTURE = ("ncu --clock-control none --metrics dram__bytes_read.sum,dram
                    "-k regex:{kernel} -s 3 -c 1 python bench.py --workload {workload} --profile-calls 5")
 TRAFFIC = {
     # workload name: (kernel, DRAM bytes per launch, sources_sha at capture)
-    "decode_13b_h5120_a2000_t512_zipf0.5": ("delta_kernel", 264844032 + 4235520, "2a5d7b1b9c6c5a32"),
-    "decode_7b_h4096_a100_t256_zipf1": ("delta_kernel", 42063360 + 16128, "2a5d7b1b9c6c5a32"),
+    "decode_13b_h5120_a2000_t512_zipf0.5": ("delta_kernel", 264847104 + 3527424, "f3b5df110b963e62"),
+    "decode_7b_h4096_a100_t256_zipf1": ("delta_kernel", 42066432 + 4608, "f3b5df110b963e62"),
 }
 KERNEL_SOURCES = {
     "delta_kernel": ("decode.cu", "ptx.h", "internal.h"),

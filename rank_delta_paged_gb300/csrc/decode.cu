@@ -981,7 +981,8 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
         {
             // the first unit is list entry blockIdx.x: its entry is loaded before the count of
             // units is known (an index inside the list's allocation; used only if valid)
-            const int2 lu0 = load_lu((int)min((int64_t)blockIdx.x, a.L.cap_units - 1));
+            const int2 lu0 = a.L.cap_units > 0 ? load_lu((int)min((int64_t)blockIdx.x, a.L.cap_units - 1))
+                                               : make_int2(0, 0);
             if ((int)blockIdx.x < n_units) {
                 luB = lu0;
                 vB = true;
