@@ -65,7 +65,9 @@ def parse():
                     help="also time the padded batched-GEMM comparison path (decode-only workloads)")
     ap.add_argument("--pressure", type=int, default=0, metavar="K",
                     help="also run K batches of the zoo through acquire / apply / release (\"pressure\")")
-    ap.add_argument("--layers", type=int, default=0, help="mixed_iteration: layers (0 = the default 32)")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="layers of the step (0 = the workload's own: 32 for mixed_iteration, 1 for decode_13b_zoo "
+                         "and decode_7b, whose layers are one projection each)")
     ap.add_argument("--pool-gib", type=float, default=0.0, help="mixed_iteration: pool size in GiB (0 = 40)")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the extra prefill_7b and mixed-layer keys of the default line")
@@ -317,6 +319,37 @@ class L2Flush:
         torch.sum(self.r, dim=0, out=self.sink)   # int32 in and out: no widened copy of the buffer
 
 
+def planned_timing(rdp, sess, w, xs, ys, idx, seg, n_seg, per_layer, flush, stream, reps):
+    """Median CUDA-event time of one step with the batch planned once for all its layers:
+    slora_plan_remake, then slora_plan_apply for every layer (each step after an L2 flush,
+    outside its events); the plan object is made before the timed steps."""
+    import torch
+    plan = rdp.slora_plan_create(sess.pool, per_layer, w.T, idx, seg, n_seg, None, stream)
+    try:
+        def step():
+            rdp.slora_plan_remake(plan, idx, seg, None, stream)
+            for l in range(w.n_layers):
+                ps = list(range(l * per_layer, (l + 1) * per_layer))
+                rdp.slora_plan_apply(plan, ps, [xs[p] for p in ps], [ys[p] for p in ps], stream)
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a, b in ev:
+            flush()
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize()
+        t = [a.elapsed_time(b) for a, b in ev]
+    finally:
+        rdp.slora_plan_destroy(plan)
+    ms = statistics.median(t)
+    return {"ms_per_step": ms, "value": w.T / (ms * 1e-3 / w.n_layers), "unit": "tokens/s/layer", "steps": reps,
+            "includes": "slora_plan_remake (the plan kernel) once, then slora_plan_apply (the decode kernel, and "
+                        "the segment kernel) for each of the step's layers"}
+
+
 def graph_timing(step_on, flush, stream, reps):
     """Median and mean CUDA-event time of one step replayed from a CUDA graph, each replay
     preceded (outside its events) by a replay of a graph that flushes the L2."""
@@ -554,9 +587,9 @@ def main():
             dist.barrier()
 
     wkw = {}
+    if args.workload in ("mixed_iteration", "decode_13b_zoo", "decode_7b") and args.layers > 0:
+        wkw["n_layers"] = args.layers
     if args.workload == "mixed_iteration":
-        if args.layers > 0:
-            wkw["n_layers"] = args.layers
         if args.pool_gib > 0:
             wkw["pool_bytes"] = int(args.pool_gib * (1 << 30))
     w = W.by_name(args.workload, seed=replica_seed(args.seed, rank), **wkw)
@@ -654,6 +687,12 @@ def main():
             apply_layer(l, st)
 
     graph = graph_timing(step_on, flush, stream, max(100, min(K, 2000)))
+    planned = None
+    if w.n_layers > 1:
+        # the same step with the batch planned once for all its layers
+        planned = planned_timing(rdp, sess, w, xs, ys, idx, seg, n_seg, per_layer, flush, stream,
+                                 max(50, min(K, 500)))
+        planned["speedup_vs_a_plan_per_layer"] = ms_per_step / planned["ms_per_step"]
 
     # dominant kernel roofline: the delta kernel(s) of one call (one projection, or one
     # layer's projections with --apply multi), timed on their own (the pool records an
@@ -856,6 +895,7 @@ def main():
                          "includes": "the same step with the batch's adapters already resident: H2D of x, "
                                      "y0, token map; delta; D2H of y"}},
         "graph": graph,
+        **({"planned": planned} if planned is not None else {}),
         "load": load,
         "flops_per_step": algorithmic_flops(w),
         "clocks": clk.summary(),

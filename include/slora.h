@@ -346,6 +346,51 @@ slora_status slora_lora_apply_multi(slora_pool_t pool, int32_t n, const int32_t 
                                     slora_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * A batch planned once and applied to every layer of an iteration.
+ *
+ * A serving iteration runs one batch through every layer, so the tokens and their adapters
+ * (one batch mixes requests of many adapters: S-LoRA: Serving Thousands of Concurrent LoRA
+ * Adapters (explainer), "The mechanism") are the same in every layer.  slora_plan_create makes the token plan of the decode path once (the grouping of
+ * the decode tokens by adapter, the work list, the adapters' page-table bases and scaling);
+ * slora_plan_apply then runs one layer: the decode kernel over the stored plan and the
+ * segments' tensor-core kernel, without the plan kernel.  Its results are bit for bit those
+ * of slora_lora_apply_multi with the same arguments.
+ *
+ *   n_slots            projections each apply covers (1..8), as n of slora_lora_apply_multi
+ *   T, token_adapter_idx, seg_indptr, n_seg, scaling
+ *                      as for slora_lora_apply_multi; copied into the plan (stream-ordered),
+ *                      so the caller's buffers may change after the call
+ *   plan (out)         the plan; device memory of about the pool's plan scratch for T tokens
+ *                      and n_slots projections, plus T + n_seg + 1 ints
+ *
+ * slora_plan_apply(plan, n, projs, x, y, stream): n must equal the plan's n_slots; projs,
+ * x and y as for slora_lora_apply_multi (x, y of this layer).  The plan describes the pool
+ * as it was when the plan was made: after any load or eviction in the pool (including those
+ * of slora_adapters_acquire) every apply of an older plan returns SLORA_ERR_INVALID_ARG and
+ * launches nothing.  Applies of one plan must not overlap in time (they share its counter
+ * and partial sums): issue them on one stream, or order the streams.
+ *
+ * slora_plan_remake(plan, token_adapter_idx, seg_indptr, scaling, stream) plans the next
+ * iteration's batch into the same plan: the same T, n_seg and n_slots as at creation, any
+ * token map, segments and scaling (NULL: the registered values), and the pool as it is now.
+ * It allocates nothing.  Enqueue it after the applies of the previous batch (same stream, or
+ * ordered streams).
+ *
+ * slora_plan_destroy waits for the device and frees the plan; NULL is a no-op.  Destroy a
+ * pool's plans before the pool.
+ * ------------------------------------------------------------------------- */
+typedef struct slora_plan *slora_plan_t;
+slora_status slora_plan_create(slora_pool_t pool, int32_t n_slots, int32_t T, const int32_t *token_adapter_idx,
+                               const int32_t *seg_indptr, int32_t n_seg, const float *scaling,
+                               slora_stream_t stream, slora_plan_t *plan);
+slora_status slora_plan_apply(slora_plan_t plan, int32_t n, const int32_t *projs /*host*/,
+                              const void *const *x /*host array*/, void *const *y /*host array*/,
+                              slora_stream_t stream);
+slora_status slora_plan_remake(slora_plan_t plan, const int32_t *token_adapter_idx, const int32_t *seg_indptr,
+                               const float *scaling, slora_stream_t stream);
+slora_status slora_plan_destroy(slora_plan_t plan);
+
+/* ---------------------------------------------------------------------------
  * slora_lora_apply_bmm: the padded batched-GEMM path, kept as the comparison the S-LoRA
  * ablation calls the slower BMM path (explainer, "Results and evidence", Figure 5 narrative;
  * explainer, "Prior limits").

@@ -36,7 +36,8 @@ __all__ = [
     "slora_debug_set_prefill_cluster",
     "slora_debug_inject_load_fault", "SLORA_FAULT_NONE", "SLORA_FAULT_COPY", "SLORA_FAULT_SCATTER",
     "SLORA_FAULT_DIRECTORY", "SLORA_FAULT_STAGING", "SLORA_FAULT_ARENA",
-    "slora_lora_apply_multi",
+    "slora_lora_apply_multi", "slora_plan_create", "slora_plan_apply", "slora_plan_remake",
+    "slora_plan_destroy",
     "slora_lru_create", "slora_lru_destroy", "slora_lru_insert", "slora_lru_remove", "slora_lru_touch",
     "slora_lru_pin", "slora_lru_unpin", "slora_lru_victims",
     "slora_adapters_acquire", "slora_adapters_release", "slora_pages_alloc_evict", "slora_pool_get_stats",
@@ -83,6 +84,10 @@ _SIGS = {
     "slora_debug_set_prefill_cluster": [_I32],
     "slora_debug_inject_load_fault": [_I32, _I32],
     "slora_lora_apply_multi": [_P, _I32, _P, _P, _P, _I32, _P, _P, _I32, _P, _P],
+    "slora_plan_create": [_P, _I32, _I32, _P, _P, _I32, _P, _P, _PP],
+    "slora_plan_apply": [_P, _I32, _P, _P, _P, _P],
+    "slora_plan_remake": [_P, _P, _P, _P, _P],
+    "slora_plan_destroy": [_P],
     "slora_lru_create": [_PP],
     "slora_lru_destroy": [_P],
     "slora_lru_insert": [_P, _I32],
@@ -287,6 +292,36 @@ def slora_lora_apply_multi(pool: int, projs, xs, ys, T: int, token_adapter_idx, 
     y_arr = (ctypes.c_void_p * max(n, 1))(*[_ptr(v) for v in ys])
     _call("slora_lora_apply_multi", pool, n, p_arr, x_arr, y_arr, T, _ptr(token_adapter_idx),
           _ptr(seg_indptr), n_seg, _ptr(scaling), _stream(stream))
+
+
+def slora_plan_create(pool: int, n_slots: int, T: int, token_adapter_idx, seg_indptr=None, n_seg: int = 0,
+                      scaling=None, stream=None) -> int:
+    """The plan of a batch for n_slots projections per apply, made once for the layers of an
+    iteration; returns the plan handle."""
+    out = ctypes.c_void_p()
+    _call("slora_plan_create", pool, n_slots, T, _ptr(token_adapter_idx), _ptr(seg_indptr), n_seg,
+          _ptr(scaling), _stream(stream), ctypes.byref(out))
+    return int(out.value)
+
+
+def slora_plan_apply(plan: int, projs, xs, ys, stream=None) -> None:
+    """One layer of a planned batch: projs[j], xs[j], ys[j] per projection slot."""
+    n = len(projs)
+    if len(xs) != n or len(ys) != n:
+        raise ValueError("projs, xs and ys must have the same length")
+    p_arr = (ctypes.c_int32 * max(n, 1))(*[int(v) for v in projs])
+    x_arr = (ctypes.c_void_p * max(n, 1))(*[_ptr(v) for v in xs])
+    y_arr = (ctypes.c_void_p * max(n, 1))(*[_ptr(v) for v in ys])
+    _call("slora_plan_apply", plan, n, p_arr, x_arr, y_arr, _stream(stream))
+
+
+def slora_plan_remake(plan: int, token_adapter_idx, seg_indptr=None, scaling=None, stream=None) -> None:
+    """The next batch (same T, n_seg and projections per apply) planned into the same plan."""
+    _call("slora_plan_remake", plan, _ptr(token_adapter_idx), _ptr(seg_indptr), _ptr(scaling), _stream(stream))
+
+
+def slora_plan_destroy(plan: int) -> None:
+    _call("slora_plan_destroy", plan)
 
 
 # ---- recency index (host only) and residency under pressure ------------------------

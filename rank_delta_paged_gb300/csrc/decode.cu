@@ -108,7 +108,9 @@ constexpr int kPtmpFloats = kRegionFloats * kConsumerWarps;
 
 struct PlanHeader {
     int32_t n_groups, n_wg, n_units, n_shrink;   // n_wg: work groups (own items and packs)
-    int32_t seg_lo, seg_hi, grab, pad;
+    int32_t seg_lo, seg_hi;
+    int32_t grab;    // the delta kernel's unit counter (0 before a launch)
+    int32_t exits;   // lead warps of the running delta launch that have taken their last unit
 };
 
 // Items (an adapter and up to kTok of its tokens) share a unit when they are small: the
@@ -313,6 +315,7 @@ __device__ __forceinline__ void plan_refuse(const PlanArgs &a)
     a.L.hdr->n_units = 0;
     a.L.hdr->n_shrink = 0;
     a.L.hdr->grab = 0;
+    a.L.hdr->exits = 0;
 }
 
 template <int NT>
@@ -675,6 +678,7 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const __grid_constant__ Pla
         a.L.hdr->seg_lo = lo;
         a.L.hdr->seg_hi = hi;
         a.L.hdr->grab = 0;
+        a.L.hdr->exits = 0;
     }
 }
 
@@ -1058,6 +1062,12 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
                 if (lane == 0) {
                     recs[q].end = 1;
                     mbar_arrive(&rfull[q]);
+                    // the last lead of the launch to be done claiming resets the counter, so
+                    // that the plan serves further launches (one per layer of an iteration)
+                    if (atomicAdd(&a.L.hdr->exits, 1) == (int)gridDim.x - 1) {
+                        atomicExch(&a.L.hdr->grab, 0);
+                        atomicExch(&a.L.hdr->exits, 0);
+                    }
                 }
                 break;
             }
@@ -1610,13 +1620,20 @@ constexpr int kMaxLaunchDevices = 64;
 std::mutex g_delta_mu;
 DeltaLaunchState g_delta_state[kMaxLaunchDevices];
 
-cudaError_t launch_lora_apply(const PoolView &pv, const ProjList &pl, int32_t T, const int32_t *idx,
-                              const int32_t *seg_indptr, int32_t n_seg, const float *scaling,
-                              PlanScratch &scratch, int num_sms, cudaStream_t stream, int *launches,
-                              cudaEvent_t after_plan)
+// The launches of a batch.  For every chunk of at most `chunk` tokens: the plan into the
+// chunk's scratch (make_plans) and the decode kernel over it (pl non-null); then the segment
+// kernel (pl non-null and n_seg > 0).  `scratch` holds one PlanScratch per chunk, or a single
+// one that every chunk reuses in turn (n_scratch == 1).
+static cudaError_t launch_batch(const PoolView &pv, const ProjList *pl, int32_t n_slots, int32_t T,
+                                const int32_t *idx, const int32_t *seg_indptr, int32_t n_seg,
+                                const float *scaling, PlanScratch *scratch, int n_scratch, bool make_plans,
+                                int num_sms, cudaStream_t stream, int *launches, cudaEvent_t after_plan)
 {
-    if (pv.hidden > kMaxBlocks * kMaxSlice || pl.n < 1 || pl.n > kMaxApplyProj || pl.n > scratch.cap_proj)
+    if (pv.hidden > kMaxBlocks * kMaxSlice || n_slots < 1 || n_slots > kMaxApplyProj || n_scratch < 1)
         return cudaErrorInvalidValue;
+    if (pl && pl->n != n_slots) return cudaErrorInvalidValue;
+    for (int i = 0; i < n_scratch; ++i)
+        if (n_slots > scratch[i].cap_proj) return cudaErrorInvalidValue;
     int device = 0;
     cudaError_t de = cudaGetDevice(&device);
     if (de != cudaSuccess) return de;
@@ -1659,77 +1676,114 @@ cudaError_t launch_lora_apply(const PoolView &pv, const ProjList &pl, int32_t T,
     cfg2.numAttrs = 1;
 
     int32_t chunk = plan_chunk(pv.max_adapters);
-    if (scratch.max_chunk > 0 && scratch.max_chunk < chunk) chunk = scratch.max_chunk;
-    const int32_t cap = scratch.cap_tokens < chunk ? scratch.cap_tokens : chunk;
+    if (scratch[0].max_chunk > 0 && scratch[0].max_chunk < chunk) chunk = scratch[0].max_chunk;
     const int NB = n_blocks(pv.hidden);
-    PlanLayout L = carve(scratch.base, cap, scratch.cap_proj, NB, scratch.max_rank, nullptr);
+    if (n_scratch > 1 && (int64_t)n_scratch * chunk < T) return cudaErrorInvalidValue;
 
-    for (int32_t tb = 0; tb < T; tb += chunk) {
+    for (int32_t tb = 0, c = 0; tb < T; tb += chunk, ++c) {
         const int32_t te = tb + chunk < T ? tb + chunk : T;
-        if (scratch.tag == 0) {
-            // fresh scratch or a wrapped tag sequence: no partial word may carry a tag in use
-            cudaError_t e = cudaMemsetAsync(L.upart, 0, (size_t)L.cap_words * 8, stream);
-            if (e != cudaSuccess) return e;
+        PlanScratch &sc = scratch[n_scratch > 1 ? c : 0];
+        const int32_t cap = sc.cap_tokens < chunk ? sc.cap_tokens : chunk;
+        if (te - tb > cap) return cudaErrorInvalidValue;
+        const PlanLayout L = carve(sc.base, cap, sc.cap_proj, NB, sc.max_rank, nullptr);
+        cudaError_t e = cudaSuccess;
+        uint32_t tag = 0;
+        if (pl) {
+            if (sc.tag == 0) {
+                // fresh scratch or a wrapped tag sequence: no partial word may carry a tag in use
+                e = cudaMemsetAsync(L.upart, 0, (size_t)L.cap_words * 8, stream);
+                if (e != cudaSuccess) return e;
+            }
+            tag = ++sc.tag;
+            if (sc.tag == 0xffffffffu) sc.tag = 0;
         }
-        const uint32_t tag = ++scratch.tag;
-        if (scratch.tag == 0xffffffffu) scratch.tag = 0;
-        const int32_t groups = (te - tb) < pv.max_adapters ? (te - tb) : pv.max_adapters;
-        int hs = 1024;
-        while (hs < 2 * groups && hs < kMaxHash) hs <<= 1;
-        const int dcache = pv.max_adapters <= kPlanDirCache ? 1 : 0;
-        PlanArgs pa{};
-        pa.pv = pv;
-        pa.idx = idx;
-        pa.T = T;
-        pa.seg_indptr = seg_indptr;
-        pa.n_seg = n_seg;
-        pa.t_begin = tb;
-        pa.t_end = te;
-        pa.hash_size = hs;
-        pa.dir_cache = dcache;
-        pa.n_proj = pl.n;
-        pa.nblk = NB;
-        for (int j = 0; j < pl.n; ++j) pa.proj[j] = pl.proj[j];
-        pa.scaling = scaling;
-        pa.L = L;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(1);
-        const bool small = te - tb <= kPlanThreadsSmall;
-        cfg.blockDim = dim3(small ? kPlanThreadsSmall : kPlanThreads);
-        cfg.dynamicSmemBytes = plan_smem_bytes(hs) + (dcache ? (size_t)pv.max_adapters * sizeof(DirEntry) : 0);
-        cfg.stream = stream;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        cudaError_t e = small ? cudaLaunchKernelEx(&cfg, plan_kernel<kPlanThreadsSmall>, pa)
-                              : cudaLaunchKernelEx(&cfg, plan_kernel<kPlanThreads>, pa);
-        if (e != cudaSuccess) return e;
-        *launches += 1;
-
-        if (after_plan && tb == 0) {
-            e = cudaEventRecord(after_plan, stream);
+        if (make_plans) {
+            const int32_t groups = (te - tb) < pv.max_adapters ? (te - tb) : pv.max_adapters;
+            int hs = 1024;
+            while (hs < 2 * groups && hs < kMaxHash) hs <<= 1;
+            const int dcache = pv.max_adapters <= kPlanDirCache ? 1 : 0;
+            PlanArgs pa{};
+            pa.pv = pv;
+            pa.idx = idx;
+            pa.T = T;
+            pa.seg_indptr = seg_indptr;
+            pa.n_seg = n_seg;
+            pa.t_begin = tb;
+            pa.t_end = te;
+            pa.hash_size = hs;
+            pa.dir_cache = dcache;
+            pa.n_proj = n_slots;
+            pa.nblk = NB;
+            if (pl)
+                for (int j = 0; j < pl->n; ++j) pa.proj[j] = pl->proj[j];
+            pa.scaling = scaling;
+            pa.L = L;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(1);
+            const bool small = te - tb <= kPlanThreadsSmall;
+            cfg.blockDim = dim3(small ? kPlanThreadsSmall : kPlanThreads);
+            cfg.dynamicSmemBytes = plan_smem_bytes(hs) + (dcache ? (size_t)pv.max_adapters * sizeof(DirEntry) : 0);
+            cfg.stream = stream;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            e = small ? cudaLaunchKernelEx(&cfg, plan_kernel<kPlanThreadsSmall>, pa)
+                      : cudaLaunchKernelEx(&cfg, plan_kernel<kPlanThreads>, pa);
             if (e != cudaSuccess) return e;
+            *launches += 1;
+            if (after_plan && tb == 0) {
+                e = cudaEventRecord(after_plan, stream);
+                if (e != cudaSuccess) return e;
+            }
         }
+        if (!pl) continue;
         DeltaArgs da{};
         da.pv = pv;
-        for (int j = 0; j < pl.n; ++j) {
-            da.x[j] = reinterpret_cast<const __half *>(pl.x[j]);
-            da.y[j] = reinterpret_cast<__half *>(pl.y[j]);
+        for (int j = 0; j < pl->n; ++j) {
+            da.x[j] = reinterpret_cast<const __half *>(pl->x[j]);
+            da.y[j] = reinterpret_cast<__half *>(pl->y[j]);
         }
         da.L = L;
         da.pitch = delta_pitch(pv.hidden);
         da.nblk = NB;
         da.tag = tag;
-        for (int j = 0; j < pl.n; ++j) da.proj[j] = pl.proj[j];
+        for (int j = 0; j < pl->n; ++j) da.proj[j] = pl->proj[j];
         e = cudaLaunchKernelEx(&cfg2, delta_kernel, da);
         if (e != cudaSuccess) return e;
         *launches += 1;
     }
-    if (n_seg > 0) {
-        cudaError_t e = launch_prefill(pv, pl, T, idx, seg_indptr, n_seg, scaling, num_sms, stream);
+    if (pl && n_seg > 0) {
+        cudaError_t e = launch_prefill(pv, *pl, T, idx, seg_indptr, n_seg, scaling, num_sms, stream);
         if (e != cudaSuccess) return e;
         *launches += 1;
     }
     return cudaSuccess;
 }
+
+cudaError_t launch_lora_apply(const PoolView &pv, const ProjList &pl, int32_t T, const int32_t *idx,
+                              const int32_t *seg_indptr, int32_t n_seg, const float *scaling,
+                              PlanScratch &scratch, int num_sms, cudaStream_t stream, int *launches,
+                              cudaEvent_t after_plan)
+{
+    return launch_batch(pv, &pl, pl.n, T, idx, seg_indptr, n_seg, scaling, &scratch, 1, true, num_sms, stream,
+                        launches, after_plan);
+}
+
+cudaError_t launch_plans(const PoolView &pv, int32_t n_slots, int32_t T, const int32_t *idx,
+                         const int32_t *seg_indptr, int32_t n_seg, const float *scaling, PlanScratch *chunks,
+                         int n_chunks, int num_sms, cudaStream_t stream, int *launches)
+{
+    return launch_batch(pv, nullptr, n_slots, T, idx, seg_indptr, n_seg, scaling, chunks, n_chunks, true, num_sms,
+                        stream, launches, nullptr);
+}
+
+cudaError_t launch_planned(const PoolView &pv, const ProjList &pl, int32_t T, const int32_t *idx,
+                           const int32_t *seg_indptr, int32_t n_seg, const float *scaling, PlanScratch *chunks,
+                           int n_chunks, int num_sms, cudaStream_t stream, int *launches)
+{
+    return launch_batch(pv, &pl, pl.n, T, idx, seg_indptr, n_seg, scaling, chunks, n_chunks, false, num_sms,
+                        stream, launches, nullptr);
+}
+
+int32_t plan_chunk_tokens(int32_t max_adapters) { return plan_chunk(max_adapters); }
 
 }  // namespace slora

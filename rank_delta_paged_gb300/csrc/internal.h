@@ -142,6 +142,17 @@ cudaError_t launch_lora_apply(const PoolView &pv, const ProjList &pl, int32_t T,
                               PlanScratch &scratch, int num_sms, cudaStream_t stream, int *launches,
                               cudaEvent_t after_plan = nullptr);
 
+// A batch planned once and applied to several layers (decode.cu): the plans of every chunk of
+// at most plan_chunk_tokens(max_adapters) tokens into chunks[c], then, per apply, the decode
+// kernel over each chunk's plan and the segment kernel.
+int32_t plan_chunk_tokens(int32_t max_adapters);
+cudaError_t launch_plans(const PoolView &pv, int32_t n_slots, int32_t T, const int32_t *idx,
+                         const int32_t *seg_indptr, int32_t n_seg, const float *scaling, PlanScratch *chunks,
+                         int n_chunks, int num_sms, cudaStream_t stream, int *launches);
+cudaError_t launch_planned(const PoolView &pv, const ProjList &pl, int32_t T, const int32_t *idx,
+                           const int32_t *seg_indptr, int32_t n_seg, const float *scaling, PlanScratch *chunks,
+                           int n_chunks, int num_sms, cudaStream_t stream, int *launches);
+
 // What the hot path needs to know about a pool, for entry points defined outside
 // pool.cpp (pool.cpp).  *launches points at the pool's kernel-launch counter.
 struct PoolHotPath {

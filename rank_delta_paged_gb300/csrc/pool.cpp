@@ -6,6 +6,7 @@
 #include <cstdlib>
 #include <mutex>
 #include <cstring>
+#include <memory>
 #include <new>
 #include <unordered_set>
 #include <vector>
@@ -69,6 +70,7 @@ struct slora_pool {
     int32_t max_rank = 0;  // largest registered rank (sizes the plan scratch)
     LruIndex lru;          // resident adapters by last acquire / load; pins of running batches
     int64_t n_loaded = 0, n_evicted = 0;
+    uint64_t residency_gen = 0;   // bumped whenever the adapter directory changes (plans check it)
 };
 
 namespace {
@@ -402,6 +404,7 @@ slora_status slora_adapters_load(slora_pool_t p, int32_t n, const int32_t *ids, 
             u.pad = 0;
             u.pt_off = -1;
             if (clr.n == kMaxDirUpdatesPerLaunch || i + 1 == todo.size()) {
+                ++p->residency_gen;
                 if (launch_dir_update(p->dir_dev, clr, side) == cudaSuccess)
                     p->launches += 1;
                 clr.n = 0;
@@ -505,6 +508,7 @@ slora_status slora_adapters_load(slora_pool_t p, int32_t n, const int32_t *ids, 
         u.pad = 0;
         u.pt_off = a.pt_off;
         if (dargs.n == kMaxDirUpdatesPerLaunch || i + 1 == todo.size()) {
+            ++p->residency_gen;
             LOAD_TRY(launch_dir_update(p->dir_dev, dargs, side), SLORA_FAULT_DIRECTORY);
             p->launches += 1;
             dargs.n = 0;
@@ -549,6 +553,7 @@ slora_status slora_adapter_evict(slora_pool_t p, int32_t id, slora_stream_t stre
     DirArgs dargs;
     dargs.n = 1;
     dargs.upd[0] = DirUpdate{id, a.rank, a.scaling, 0, -1};
+    ++p->residency_gen;
     CUDA_TRY(launch_dir_update(p->dir_dev, dargs, (cudaStream_t)stream));
     p->launches += 1;
     int64_t rows = adapter_rows(p, a);
@@ -593,6 +598,7 @@ slora_status slora_adapters_evict(slora_pool_t p, int32_t n, const int32_t *ids,
         const AdapterRec &a = p->adapters[(size_t)todo[i]];
         dargs.upd[dargs.n++] = DirUpdate{todo[i], a.rank, a.scaling, 0, -1};
         if (dargs.n == kMaxDirUpdatesPerLaunch || i + 1 == todo.size()) {
+            ++p->residency_gen;
             CUDA_TRY(launch_dir_update(p->dir_dev, dargs, (cudaStream_t)stream));
             p->launches += 1;
             dargs.n = 0;
@@ -836,6 +842,162 @@ slora_status slora_lora_apply_multi(slora_pool_t p, int32_t n, const int32_t *pr
     if (st != SLORA_OK)
         return st;
     return apply_list(p, "lora_apply_multi", pl, T, idx, seg_indptr, n_seg, scaling, stream);
+}
+
+// ---- batches planned once for several layers --------------------------------------------
+struct slora_plan {
+    slora_pool_t pool = nullptr;
+    uint64_t residency_gen = 0;   // the pool's when planned: applies need the same directory
+    int32_t n_slots = 0, T = 0, n_seg = 0;
+    void *mem = nullptr;          // copies of the token map, segments and scaling; chunk scratch
+    int32_t *idx = nullptr;
+    int32_t *seg = nullptr;
+    float *scale_mem = nullptr;   // room for a copy of the scaling override
+    const float *scaling = nullptr;   // scale_mem when the plan has an override, else null
+    std::vector<PlanScratch> chunks;
+};
+
+// Copies the batch's token map, segments and scaling into the plan and runs the plan kernels.
+static slora_status plan_batch(slora_plan *plan, const int32_t *idx, const int32_t *seg_indptr,
+                               const float *scaling, cudaStream_t s, const char *fn)
+{
+    slora_pool_t p = plan->pool;
+    cudaError_t e = cudaMemcpyAsync(plan->idx, idx, (size_t)plan->T * 4, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess && plan->n_seg > 0)
+        e = cudaMemcpyAsync(plan->seg, seg_indptr, (size_t)(plan->n_seg + 1) * 4, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess && scaling)
+        e = cudaMemcpyAsync(plan->scale_mem, scaling, (size_t)p->max_adapters * 4, cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess)
+        return fail(SLORA_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+    plan->scaling = scaling ? plan->scale_mem : nullptr;
+    PoolView pv{p->pool_dev, p->pt_dev, p->dir_dev, p->num_pages, p->hidden, p->n_proj, p->max_adapters,
+                p->status_dev};
+    int launched = 0;
+    e = launch_plans(pv, plan->n_slots, plan->T, plan->idx, plan->n_seg > 0 ? plan->seg : nullptr, plan->n_seg,
+                     plan->scaling, plan->chunks.data(), (int)plan->chunks.size(), p->num_sms, s, &launched);
+    p->launches += launched;
+    if (e != cudaSuccess)
+        return fail(SLORA_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
+    plan->residency_gen = p->residency_gen;
+    return SLORA_OK;
+}
+
+slora_status slora_plan_create(slora_pool_t p, int32_t n_slots, int32_t T, const int32_t *idx,
+                               const int32_t *seg_indptr, int32_t n_seg, const float *scaling,
+                               slora_stream_t stream, slora_plan_t *out)
+{
+    if (!p || !out)
+        return fail(SLORA_ERR_INVALID_ARG, "plan_create: null pool or out");
+    *out = nullptr;
+    if (n_slots < 1 || n_slots > kMaxApplyProj)
+        return fail(SLORA_ERR_INVALID_ARG, "plan_create: n_slots=%d (1..%d)", n_slots, kMaxApplyProj);
+    if (T < 1 || T > (1 << 20))
+        return fail(SLORA_ERR_INVALID_ARG, "plan_create: T=%d (1..%d)", T, 1 << 20);
+    if (!idx)
+        return fail(SLORA_ERR_INVALID_ARG, "plan_create: null token index pointer");
+    if (n_seg < 0 || (n_seg > 0 && !seg_indptr) || n_seg > T || n_seg > kMaxSegments)
+        return fail(SLORA_ERR_INVALID_ARG, "plan_create: n_seg=%d (at most min(T, %d))", n_seg, kMaxSegments);
+    DEVICE_SCOPE(p);
+    slora_status st = SLORA_OK;
+    const int32_t rank = std::max(p->max_rank, 1);
+    const int32_t chunk = plan_chunk_tokens(p->max_adapters);
+    const int n_chunks = (int)((T + (int64_t)chunk - 1) / chunk);
+    const int32_t cap = std::min(T, chunk);
+    auto up = [](size_t v) { return (v + 255) / 256 * 256; };
+    const size_t per_chunk = up(plan_scratch_bytes(cap, rank, p->hidden, p->max_adapters, n_slots));
+    const size_t b_idx = up((size_t)T * 4), b_seg = up((size_t)(n_seg + 1) * 4);
+    const size_t b_scale = up((size_t)p->max_adapters * 4);   // room for a scaling copy (create or remake)
+    auto plan = std::make_unique<slora_plan>();
+    plan->pool = p;
+    plan->n_slots = n_slots;
+    plan->T = T;
+    plan->n_seg = n_seg;
+    CUDA_TRY(cudaMalloc(&plan->mem, b_idx + b_seg + b_scale + per_chunk * n_chunks));
+    uint8_t *m = static_cast<uint8_t *>(plan->mem);
+    const cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaMemsetAsync(m + b_idx + b_seg + b_scale, 0, per_chunk * n_chunks, s);
+    if (e != cudaSuccess) {
+        cudaFree(plan->mem);
+        return fail(SLORA_ERR_CUDA, "plan_create: %s", cudaGetErrorString(e));
+    }
+    plan->idx = reinterpret_cast<int32_t *>(m);
+    plan->seg = reinterpret_cast<int32_t *>(m + b_idx);
+    plan->scale_mem = reinterpret_cast<float *>(m + b_idx + b_seg);
+    plan->chunks.resize((size_t)n_chunks);
+    for (int c = 0; c < n_chunks; ++c) {
+        PlanScratch &sc = plan->chunks[(size_t)c];
+        sc.base = m + b_idx + b_seg + b_scale + per_chunk * (size_t)c;
+        sc.bytes = per_chunk;
+        sc.cap_tokens = cap;
+        sc.max_rank = rank;
+        sc.cap_proj = n_slots;
+    }
+    st = plan_batch(plan.get(), idx, seg_indptr, scaling, s, "plan_create");
+    if (st != SLORA_OK) {
+        cudaStreamSynchronize(s);
+        cudaFree(plan->mem);
+        return st;
+    }
+    *out = plan.release();
+    return SLORA_OK;
+}
+
+slora_status slora_plan_remake(slora_plan_t plan, const int32_t *idx, const int32_t *seg_indptr,
+                               const float *scaling, slora_stream_t stream)
+{
+    if (!plan || !plan->pool)
+        return fail(SLORA_ERR_INVALID_ARG, "plan_remake: null plan");
+    if (!idx || (plan->n_seg > 0 && !seg_indptr))
+        return fail(SLORA_ERR_INVALID_ARG, "plan_remake: null token index or segment pointer");
+    DEVICE_SCOPE(plan->pool);
+    slora_status st = plan_batch(plan, idx, seg_indptr, scaling, (cudaStream_t)stream, "plan_remake");
+    return st;
+}
+
+slora_status slora_plan_apply(slora_plan_t plan, int32_t n, const int32_t *projs, const void *const *x,
+                              void *const *y, slora_stream_t stream)
+{
+    if (!plan || !plan->pool)
+        return fail(SLORA_ERR_INVALID_ARG, "plan_apply: null plan");
+    slora_pool_t p = plan->pool;
+    if (n != plan->n_slots)
+        return fail(SLORA_ERR_INVALID_ARG, "plan_apply: n=%d, the plan was made for %d projections", n,
+                    plan->n_slots);
+    if (p->residency_gen != plan->residency_gen)
+        return fail(SLORA_ERR_INVALID_ARG, "plan_apply: the pool's adapters were loaded or evicted since the "
+                                           "plan was made");
+    ProjList pl;
+    slora_status st = make_proj_list("plan_apply", p->n_proj, n, projs, x, y, &pl);
+    if (st != SLORA_OK)
+        return st;
+    DEVICE_SCOPE(p);
+    PoolView pv{p->pool_dev, p->pt_dev, p->dir_dev, p->num_pages, p->hidden, p->n_proj, p->max_adapters,
+                p->status_dev};
+    int launched = 0;
+    cudaError_t e = launch_planned(pv, pl, plan->T, plan->idx, plan->n_seg > 0 ? plan->seg : nullptr, plan->n_seg,
+                                   plan->scaling,
+                                   plan->chunks.data(), (int)plan->chunks.size(), p->num_sms,
+                                   (cudaStream_t)stream, &launched);
+    p->launches += launched;
+    if (e != cudaSuccess)
+        return fail(SLORA_ERR_CUDA, "plan_apply: launch failed: %s", cudaGetErrorString(e));
+    return SLORA_OK;
+}
+
+slora_status slora_plan_destroy(slora_plan_t plan)
+{
+    if (!plan)
+        return SLORA_OK;
+    slora_status st = SLORA_OK;
+    if (plan->pool) {
+        slora_pool_t p = plan->pool;
+        DEVICE_SCOPE(p);
+        // work still enqueued may read the plan: wait for the device, then free it
+        CUDA_TRY(cudaDeviceSynchronize());
+        CUDA_TRY(cudaFree(plan->mem));
+    }
+    delete plan;
+    return st;
 }
 
 slora_status slora_pool_set_load_mode(slora_pool_t p, int32_t mode, int64_t staging_bytes)

@@ -202,18 +202,20 @@ def tiny_decode(seed: int = 0, values: str = "normal", T: int = 8) -> Workload:
 
 
 def decode_7b(seed: int = 0, values: str = "normal", T: int = 256, n_adapters: int = 100,
-              hidden: int = 4096, alpha: float = 1.0) -> Workload:
-    """hidden 4096, 100 adapters of ranks U{8,16,32,64}, 256 decode tokens, Zipf(1) ids.
+              hidden: int = 4096, alpha: float = 1.0, n_layers: int = 1) -> Workload:
+    """hidden 4096, 100 adapters of ranks U{8,16,32,64}, 256 decode tokens, Zipf(1) ids;
+    n_layers layers of one projection each (the same batch through every layer).
 
     Pool: twice the zoo's pages, the other half held by KV, randomly interleaved.
     """
     rng = np.random.default_rng([seed, 0])
     ranks = rng.choice(np.array(RANKS_DECODE, dtype=np.int32), size=n_adapters)
     ids = zipf_ids(rng, n_adapters, T, alpha)
-    zoo_pages = int(2 * ranks.sum())
-    return Workload(f"decode_7b_h{hidden}_a{n_adapters}_t{T}_zipf{alpha:g}", hidden, 1, ranks,
+    zoo_pages = int(2 * ranks.sum()) * n_layers
+    suffix = f"_l{n_layers}" if n_layers > 1 else ""
+    return Workload(f"decode_7b_h{hidden}_a{n_adapters}_t{T}_zipf{alpha:g}{suffix}", hidden, n_layers, ranks,
                     ids, None, num_pages=2 * zoo_pages, kv_pages=zoo_pages,
-                    shuffle_seed=seed * 7919 + 13, seed=seed, values=values, alpha=alpha)
+                    shuffle_seed=seed * 7919 + 13, seed=seed, values=values, alpha=alpha, n_layers=n_layers)
 
 
 def prefill_7b(seed: int = 0, values: str = "normal", n_seg: int = 16, seg_len: int = 512,
@@ -233,16 +235,18 @@ def prefill_7b(seed: int = 0, values: str = "normal", n_seg: int = 16, seg_len: 
 
 
 def decode_13b_zoo(seed: int = 0, values: str = "normal", T: int = 512, n_adapters: int = 2000,
-                   hidden: int = 5120, alpha: float = 0.5) -> Workload:
+                   hidden: int = 5120, alpha: float = 0.5, n_layers: int = 1) -> Workload:
     """hidden 5120, 2000 adapters of ranks U{8,16,32,64} in the host store, 512 decode
-    tokens with Zipf(0.5) ids; the pool starts cold and the batch's adapters are loaded."""
+    tokens with Zipf(0.5) ids; the pool starts cold and the batch's adapters are loaded;
+    n_layers layers of one projection each (the same batch through every layer)."""
     rng = np.random.default_rng([seed, 0])
     ranks = rng.choice(np.array(RANKS_DECODE, dtype=np.int32), size=n_adapters)
     ids = zipf_ids(rng, n_adapters, T, alpha)
-    zoo_pages = int(2 * ranks.sum())
-    return Workload(f"decode_13b_h{hidden}_a{n_adapters}_t{T}_zipf{alpha:g}", hidden, 1, ranks,
+    zoo_pages = int(2 * ranks.sum()) * n_layers
+    suffix = f"_l{n_layers}" if n_layers > 1 else ""
+    return Workload(f"decode_13b_h{hidden}_a{n_adapters}_t{T}_zipf{alpha:g}{suffix}", hidden, n_layers, ranks,
                     ids, None, num_pages=2 * zoo_pages, kv_pages=zoo_pages,
-                    shuffle_seed=seed * 7919 + 19, seed=seed, values=values, alpha=alpha)
+                    shuffle_seed=seed * 7919 + 19, seed=seed, values=values, alpha=alpha, n_layers=n_layers)
 
 
 def mixed_iteration(seed: int = 0, values: str = "normal", n_layers: int = 32,
