@@ -694,6 +694,10 @@ struct DeltaArgs {
     int32_t nblk;           // hidden blocks
     uint32_t tag;           // this launch's partial-sum tag (never 0)
     int32_t proj[kMaxApplyProj];   // projection of each slot of the call
+    // The plan was complete before this launch began (a stored plan's later applies): the
+    // lead warp then publishes the CTA's first unit before the grid-dependency wait, so its
+    // loads overlap the end of the kernel before; it waits before it claims any unit.
+    int32_t plan_ready;
 };
 
 // A unit as the lead warp hands it to the other warps: the descriptor, the token ids of
@@ -878,7 +882,10 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
         fence_mbar_init();
     }
     __syncthreads();
-    griddep_wait();   // the plan of this batch is complete and visible
+    // the plan of this batch is complete and visible; the lead of a launch over a stored plan
+    // waits later (see DeltaArgs::plan_ready)
+    const bool lead_early = a.plan_ready != 0 && warp == kWarpLead;
+    if (!lead_early) griddep_wait();
     griddep_launch_dependents();
     const int n_units = __ldcg(&a.L.hdr->n_units);
 
@@ -982,6 +989,7 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
         int dtok = 0, dti = 0;
         int32_t dp0 = -1, dp1 = -1;
         int nclaimed = 0, kp = 0;                  // units claimed, records published
+        bool waited = !lead_early;                 // past the grid-dependency wait
         {
             // the first unit is list entry blockIdx.x: its entry is loaded before the count of
             // units is known (an index inside the list's allocation; used only if valid)
@@ -991,7 +999,7 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
                 luB = lu0;
                 vB = true;
                 nclaimed = 1;
-                if (kClaimAhead > 1) {
+                if (kClaimAhead > 1 && waited) {
                     if (lane == 0) grab = atomicAdd(&a.L.hdr->grab, 1);
                     apend = true;
                     ++nclaimed;
@@ -1047,7 +1055,13 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
                     exhausted = true;
                 }
             }
-            if (!exhausted && nclaimed - __shfl_sync(0xffffffffu, *done, 0) < kClaimAhead) {
+            if (!waited && kp >= 1) {
+                // the first unit is published: from here on the counter is used, which the
+                // launch before resets at its end
+                griddep_wait();
+                waited = true;
+            }
+            if (waited && !exhausted && nclaimed - __shfl_sync(0xffffffffu, *done, 0) < kClaimAhead) {
                 if (lane == 0) grab = atomicAdd(&a.L.hdr->grab, 1);
                 apend = true;
                 ++nclaimed;
@@ -1057,6 +1071,10 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
                 continue;
             }
             if (exhausted) {
+                if (!waited) {
+                    griddep_wait();
+                    waited = true;
+                }
                 const uint32_t q = kp % QD;
                 if (kp >= QD) wait_phase<false>(&rempty[q], ((kp / QD) - 1) & 1, abort, status);
                 if (lane == 0) {
@@ -1627,7 +1645,8 @@ DeltaLaunchState g_delta_state[kMaxLaunchDevices];
 static cudaError_t launch_batch(const PoolView &pv, const ProjList *pl, int32_t n_slots, int32_t T,
                                 const int32_t *idx, const int32_t *seg_indptr, int32_t n_seg,
                                 const float *scaling, PlanScratch *scratch, int n_scratch, bool make_plans,
-                                int num_sms, cudaStream_t stream, int *launches, cudaEvent_t after_plan)
+                                bool plan_ready, int num_sms, cudaStream_t stream, int *launches,
+                                cudaEvent_t after_plan)
 {
     if (pv.hidden > kMaxBlocks * kMaxSlice || n_slots < 1 || n_slots > kMaxApplyProj || n_scratch < 1)
         return cudaErrorInvalidValue;
@@ -1747,6 +1766,7 @@ static cudaError_t launch_batch(const PoolView &pv, const ProjList *pl, int32_t 
         da.nblk = NB;
         da.tag = tag;
         for (int j = 0; j < pl->n; ++j) da.proj[j] = pl->proj[j];
+        da.plan_ready = plan_ready && !make_plans ? 1 : 0;
         e = cudaLaunchKernelEx(&cfg2, delta_kernel, da);
         if (e != cudaSuccess) return e;
         *launches += 1;
@@ -1764,24 +1784,24 @@ cudaError_t launch_lora_apply(const PoolView &pv, const ProjList &pl, int32_t T,
                               PlanScratch &scratch, int num_sms, cudaStream_t stream, int *launches,
                               cudaEvent_t after_plan)
 {
-    return launch_batch(pv, &pl, pl.n, T, idx, seg_indptr, n_seg, scaling, &scratch, 1, true, num_sms, stream,
-                        launches, after_plan);
+    return launch_batch(pv, &pl, pl.n, T, idx, seg_indptr, n_seg, scaling, &scratch, 1, true, false, num_sms,
+                        stream, launches, after_plan);
 }
 
 cudaError_t launch_plans(const PoolView &pv, int32_t n_slots, int32_t T, const int32_t *idx,
                          const int32_t *seg_indptr, int32_t n_seg, const float *scaling, PlanScratch *chunks,
                          int n_chunks, int num_sms, cudaStream_t stream, int *launches)
 {
-    return launch_batch(pv, nullptr, n_slots, T, idx, seg_indptr, n_seg, scaling, chunks, n_chunks, true, num_sms,
-                        stream, launches, nullptr);
+    return launch_batch(pv, nullptr, n_slots, T, idx, seg_indptr, n_seg, scaling, chunks, n_chunks, true, false,
+                        num_sms, stream, launches, nullptr);
 }
 
 cudaError_t launch_planned(const PoolView &pv, const ProjList &pl, int32_t T, const int32_t *idx,
                            const int32_t *seg_indptr, int32_t n_seg, const float *scaling, PlanScratch *chunks,
-                           int n_chunks, int num_sms, cudaStream_t stream, int *launches)
+                           int n_chunks, bool plan_ready, int num_sms, cudaStream_t stream, int *launches)
 {
-    return launch_batch(pv, &pl, pl.n, T, idx, seg_indptr, n_seg, scaling, chunks, n_chunks, false, num_sms,
-                        stream, launches, nullptr);
+    return launch_batch(pv, &pl, pl.n, T, idx, seg_indptr, n_seg, scaling, chunks, n_chunks, false, plan_ready,
+                        num_sms, stream, launches, nullptr);
 }
 
 int32_t plan_chunk_tokens(int32_t max_adapters) { return plan_chunk(max_adapters); }

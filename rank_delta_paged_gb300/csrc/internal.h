@@ -149,9 +149,11 @@ int32_t plan_chunk_tokens(int32_t max_adapters);
 cudaError_t launch_plans(const PoolView &pv, int32_t n_slots, int32_t T, const int32_t *idx,
                          const int32_t *seg_indptr, int32_t n_seg, const float *scaling, PlanScratch *chunks,
                          int n_chunks, int num_sms, cudaStream_t stream, int *launches);
+// plan_ready: the plans were complete before this launch (not the first apply after the
+// plans were made), so the decode kernel may read them before its grid-dependency wait.
 cudaError_t launch_planned(const PoolView &pv, const ProjList &pl, int32_t T, const int32_t *idx,
                            const int32_t *seg_indptr, int32_t n_seg, const float *scaling, PlanScratch *chunks,
-                           int n_chunks, int num_sms, cudaStream_t stream, int *launches);
+                           int n_chunks, bool plan_ready, int num_sms, cudaStream_t stream, int *launches);
 
 // What the hot path needs to know about a pool, for entry points defined outside
 // pool.cpp (pool.cpp).  *launches points at the pool's kernel-launch counter.

@@ -855,6 +855,7 @@ struct slora_plan {
     float *scale_mem = nullptr;   // room for a copy of the scaling override
     const float *scaling = nullptr;   // scale_mem when the plan has an override, else null
     std::vector<PlanScratch> chunks;
+    int64_t applies = 0;          // applies since the plan was made or remade
 };
 
 // Copies the batch's token map, segments and scaling into the plan and runs the plan kernels.
@@ -879,6 +880,7 @@ static slora_status plan_batch(slora_plan *plan, const int32_t *idx, const int32
     if (e != cudaSuccess)
         return fail(SLORA_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
     plan->residency_gen = p->residency_gen;
+    plan->applies = 0;
     return SLORA_OK;
 }
 
@@ -974,13 +976,15 @@ slora_status slora_plan_apply(slora_plan_t plan, int32_t n, const int32_t *projs
     PoolView pv{p->pool_dev, p->pt_dev, p->dir_dev, p->num_pages, p->hidden, p->n_proj, p->max_adapters,
                 p->status_dev};
     int launched = 0;
+    // after the first apply of a plan its plan kernels have completed before any later
+    // apply starts (each decode launch waits for the kernel before it, back to the plan's)
     cudaError_t e = launch_planned(pv, pl, plan->T, plan->idx, plan->n_seg > 0 ? plan->seg : nullptr, plan->n_seg,
-                                   plan->scaling,
-                                   plan->chunks.data(), (int)plan->chunks.size(), p->num_sms,
-                                   (cudaStream_t)stream, &launched);
+                                   plan->scaling, plan->chunks.data(), (int)plan->chunks.size(),
+                                   plan->applies > 0, p->num_sms, (cudaStream_t)stream, &launched);
     p->launches += launched;
     if (e != cudaSuccess)
         return fail(SLORA_ERR_CUDA, "plan_apply: launch failed: %s", cudaGetErrorString(e));
+    ++plan->applies;
     return SLORA_OK;
 }
 
