@@ -695,8 +695,10 @@ struct DeltaArgs {
     uint32_t tag;           // this launch's partial-sum tag (never 0)
     int32_t proj[kMaxApplyProj];   // projection of each slot of the call
     // The plan was complete before this launch began (a stored plan's later applies): the
-    // lead warp then publishes the CTA's first unit before the grid-dependency wait, so its
-    // loads overlap the end of the kernel before; it waits before it claims any unit.
+    // lead warp then publishes the CTA's first unit before the grid-dependency wait, and the
+    // copy warps start its page-row stages, so that they overlap the end of the kernel
+    // before; the lead waits before it claims any unit, a copy warp before its first token
+    // stage (x or y0, which the kernel before may still be writing).
     int32_t plan_ready;
 };
 
@@ -885,7 +887,8 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
     // the plan of this batch is complete and visible; the lead of a launch over a stored plan
     // waits later (see DeltaArgs::plan_ready)
     const bool lead_early = a.plan_ready != 0 && warp == kWarpLead;
-    if (!lead_early) griddep_wait();
+    const bool copy_early = a.plan_ready != 0 && warp >= kWarpCopy0 && warp < kWarpCopy0 + kCopyWarps;
+    if (!lead_early && !copy_early) griddep_wait();
     griddep_launch_dependents();
     const int n_units = __ldcg(&a.L.hdr->n_units);
 
@@ -1112,6 +1115,7 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
         const int32_t *pt = a.pv.pt_arena;
         RingPos pos{0, 0};
         uint32_t sc = 0;   // stages of the CTA so far
+        bool waited = !copy_early;   // past the grid-dependency wait
         for (int k = 0;; ++k) {
             uint32_t packed;
             int rows;
@@ -1152,8 +1156,13 @@ __global__ void __launch_bounds__(kThreads, 1) delta_kernel(const __grid_constan
                 if (lane == 0) mbar_arrive_expect_tx(&full[pos.slot], (uint32_t)__popc(m) * sliceB);
             };
             // token stage
-            if ((int)(sc % kCopyWarps) == cw)
+            if ((int)(sc % kCopyWarps) == cw) {
+                if (!waited) {
+                    griddep_wait();
+                    waited = true;
+                }
                 issue((sh.expand ? a.y[sh.pj] : a.x[sh.pj]) + (int64_t)tok * d, r8 < sh.nt, false);
+            }
             ++sc;
             pos.next();
             // rank stages
