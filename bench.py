@@ -10,8 +10,9 @@ for every projection of the workload.  Metric: LoRA-delta tokens/s per layer
   python bench.py --impl reference ...      # the fp64 CPU oracle on the host cores
 
 The default workload is the 13B decode batch over a zoo of 2000 pooled adapters (ranks 8
-to 64, 512 tokens, Zipf 0.5); the line also carries the 7B prefill batch and one layer of
-the mixed prefill + decode iteration as extra keys.
+to 64, 512 tokens, Zipf 0.5); the line also carries the 7B prefill batch, one layer of
+the mixed prefill + decode iteration, and the headline batch through 8 layers (one call
+per layer against the batch planned once for the step) as extra keys.
 
 For N > 1 every rank serves its own batch (seed + rank): the delta has no cross-token
 exchange, so ranks are independent replicas (weak scaling) and the only collectives are
@@ -555,6 +556,66 @@ def measure_extra(rdp, w, dev, flush, stream, hbm, fp16_tflops, reps=100):
     }
 
 
+def measure_layers_extra(rdp, w, dev, flush, stream, hbm, reps=60):
+    """An iteration of workload ``w``'s layers (one projection each), timed with CUDA events
+    after an L2 flush: one slora_lora_apply per layer, and the batch planned once
+    (slora_plan_remake, then slora_plan_apply per layer)."""
+    import torch
+    from rank_delta_paged_gb300.harness import PoolSession
+    sess = PoolSession(w, device=dev.index)
+    try:
+        sess.load(w.used_adapters(), stream)
+        ins = [sess.device_inputs(p) for p in range(w.n_proj)]
+        xs = [i[0] for i in ins]
+        ys = [i[1].clone() for i in ins]
+        idx = ins[0][2]
+        plan = rdp.slora_plan_create(sess.pool, 1, w.T, idx, None, 0, None, stream)
+        try:
+            def per_layer_calls():
+                for p in range(w.n_proj):
+                    rdp.slora_lora_apply(sess.pool, p, xs[p], ys[p], w.T, idx, None, 0, None, stream)
+
+            def planned():
+                rdp.slora_plan_remake(plan, idx, None, None, stream)
+                for p in range(w.n_proj):
+                    rdp.slora_plan_apply(plan, [p], [xs[p]], [ys[p]], stream)
+
+            out = {}
+            for name, step in (("calls", per_layer_calls), ("planned", planned)):
+                for _ in range(3):
+                    step()
+                ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+                torch.cuda.synchronize()
+                for a, b in ev:
+                    flush()
+                    a.record(stream)
+                    step()
+                    b.record(stream)
+                torch.cuda.synchronize()
+                out[name] = statistics.median(a.elapsed_time(b) for a, b in ev)
+        finally:
+            rdp.slora_plan_destroy(plan)
+        status = sess.device_status()
+    finally:
+        sess.close()
+    layer_bytes = algorithmic_bytes(w) / w.n_proj
+    res = {"workload": w.name, "tokens": w.T, "layers": w.n_layers, "status": status,
+           "timing": "median of %d steps, each after an L2 flush (2 x L2 written, then 2 x L2 read)" % reps}
+    for name, ms in out.items():
+        per_layer_s = ms / 1e3 / w.n_layers
+        res[name] = {"ms_per_step": ms, "us_per_layer": per_layer_s * 1e6, "value": w.T / per_layer_s,
+                     "unit": "tokens/s/layer",
+                     "roofline_per_layer": {"achieved": layer_bytes / per_layer_s / 1e9, "peak": hbm, "unit": "GB/s",
+                                            "frac": layer_bytes / per_layer_s / 1e9 / hbm,
+                                            "algorithmic_bytes_per_layer": layer_bytes,
+                                            "includes": "every kernel of the step (plans included), per layer"}}
+    res["calls"]["includes"] = "one slora_lora_apply per layer (plan kernel + decode kernel each)"
+    res["planned"]["includes"] = ("slora_plan_remake once (the plan kernel), then slora_plan_apply per layer "
+                                  "(the decode kernel)")
+    res["speedup"] = out["calls"] / out["planned"]
+    return res
+
+
 # ---------------------------------------------------------------- our arm
 def main():
     args = parse()
@@ -863,6 +924,12 @@ def main():
             if extras[name]["status"] != 0:
                 print(f"device status {extras[name]['status']} in {name}", file=sys.stderr)
                 return 3
+        # the headline batch through 8 layers: one call per layer against one plan per step
+        wl = W.by_name(args.workload, seed=args.seed, n_layers=8)
+        extras["decode_13b_zoo_8_layers"] = measure_layers_extra(rdp, wl, dev, flush, stream, hbm)
+        if extras["decode_13b_zoo_8_layers"]["status"] != 0:
+            print("device status in the 8-layer step", file=sys.stderr)
+            return 3
 
     line = {
         "metric": "lora_delta_tokens_per_s_per_layer", "value": value, "unit": "tokens/s/layer",
