@@ -92,8 +92,8 @@ TRAFFIC_CAPTURE = ("ncu --clock-control none --metrics dram__bytes_read.sum,dram
                    "-k regex:{kernel} -s 3 -c 1 python bench.py --workload {workload} --profile-calls 5")
 TRAFFIC = {
     # workload name: (kernel, DRAM bytes per launch, sources_sha at capture)
-    "decode_13b_h5120_a2000_t512_zipf0.5": ("delta_kernel", 264847104 + 3527424, "f3b5df110b963e62"),
-    "decode_7b_h4096_a100_t256_zipf1": ("delta_kernel", 42066432 + 4608, "f3b5df110b963e62"),
+    "decode_13b_h5120_a2000_t512_zipf0.5": ("delta_kernel", 264910080 + 3497728, "0c1fbb5c09229e9f"),
+    "decode_7b_h4096_a100_t256_zipf1": ("delta_kernel", 42062592 + 4608, "0c1fbb5c09229e9f"),
 }
 KERNEL_SOURCES = {
     "delta_kernel": ("decode.cu", "ptx.h", "internal.h"),
