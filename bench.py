@@ -92,8 +92,8 @@ TRAFFIC_CAPTURE = ("ncu --clock-control none --metrics dram__bytes_read.sum,dram
                    "-k regex:{kernel} -s 3 -c 1 python bench.py --workload {workload} --profile-calls 5")
 TRAFFIC = {
     # workload name: (kernel, DRAM bytes per launch, sources_sha at capture)
-    "decode_13b_h5120_a2000_t512_zipf0.5": ("delta_kernel", 264910080 + 3497728, "0c1fbb5c09229e9f"),
-    "decode_7b_h4096_a100_t256_zipf1": ("delta_kernel", 42062592 + 4608, "0c1fbb5c09229e9f"),
+    "decode_13b_h5120_a2000_t512_zipf0.5": ("delta_kernel", 264910080 + 3497728, "ea1fbf78de3ce652"),
+    "decode_7b_h4096_a100_t256_zipf1": ("delta_kernel", 42062592 + 4608, "ea1fbf78de3ce652"),
 }
 KERNEL_SOURCES = {
     "delta_kernel": ("decode.cu", "ptx.h", "internal.h"),
@@ -101,13 +101,23 @@ KERNEL_SOURCES = {
 }
 
 
+def code_of(text: str) -> str:
+    """C++ / CUDA source without its comments, trailing blanks and empty lines (string
+    literals in these files hold no comment markers)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
 def sources_sha(kernel: str) -> str:
-    """sha256 (first 16 hex digits) over the kernel's source files."""
+    """sha256 (first 16 hex digits) over the code of the kernel's source files: comments and
+    blank lines do not count, so a capture stays valid across comment edits."""
     import hashlib
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "rank_delta_paged_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "rank_delta_paged_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update(code_of(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

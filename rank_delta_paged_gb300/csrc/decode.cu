@@ -37,6 +37,12 @@
 //     trip.  Every page row is read once per item (small items share units); the only
 //     cross-SM traffic is the small tagged partials.  Every wait is bounded in time.
 //
+// A plan may also be made once and used by several decode launches (the layers of an
+// iteration, slora_plan_apply): the last lead warp of a launch resets the unit counter, each
+// launch tags its partial sums anew, and from the second launch on the lead publishes its
+// CTA's first unit, and the copy warps start that unit's page rows, before the grid-dependency
+// wait.
+//
 // Expand units only wait for shrink units that precede them in the list, and shrink
 // units never wait on another SM, so the list drains whatever number of CTAs is resident.
 //
