@@ -67,8 +67,8 @@ def parse():
     ap.add_argument("--pressure", type=int, default=0, metavar="K",
                     help="also run K batches of the zoo through acquire / apply / release (\"pressure\")")
     ap.add_argument("--layers", type=int, default=0,
-                    help="layers of the step (0 = the workload's own: 32 for mixed_iteration, 1 for decode_13b_zoo "
-                         "and decode_7b, whose layers are one projection each)")
+                    help="layers of the step (0 = the workload's own: 32 for mixed_iteration, 1 for decode_13b_zoo, "
+                         "decode_7b and prefill_7b, whose layers are one projection each)")
     ap.add_argument("--pool-gib", type=float, default=0.0, help="mixed_iteration: pool size in GiB (0 = 40)")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the extra prefill_7b and mixed-layer keys of the default line")
@@ -658,7 +658,7 @@ def main():
             dist.barrier()
 
     wkw = {}
-    if args.workload in ("mixed_iteration", "decode_13b_zoo", "decode_7b") and args.layers > 0:
+    if args.workload in ("mixed_iteration", "decode_13b_zoo", "decode_7b", "prefill_7b") and args.layers > 0:
         wkw["n_layers"] = args.layers
     if args.workload == "mixed_iteration":
         if args.pool_gib > 0:

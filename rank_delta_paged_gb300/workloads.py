@@ -219,19 +219,21 @@ def decode_7b(seed: int = 0, values: str = "normal", T: int = 256, n_adapters: i
 
 
 def prefill_7b(seed: int = 0, values: str = "normal", n_seg: int = 16, seg_len: int = 512,
-               hidden: int = 4096, ranks: Optional[Sequence[int]] = None) -> Workload:
+               hidden: int = 4096, ranks: Optional[Sequence[int]] = None, n_layers: int = 1) -> Workload:
     """hidden 4096, 16 segments x 512 tokens, segment i on adapter i, ranks cycled over
-    {8, 16, 32, 64, 128}.  Pool interleaved with KV as in decode_7b."""
+    {8, 16, 32, 64, 128}; n_layers layers of one projection each.  Pool interleaved with KV
+    as in decode_7b."""
     if ranks is None:
         ranks = [RANKS_WIDE[i % len(RANKS_WIDE)] for i in range(n_seg)]
     ranks = np.asarray(ranks, dtype=np.int32)
     assert ranks.shape[0] == n_seg
     ids = np.repeat(np.arange(n_seg, dtype=np.int32), seg_len)
     indptr = (np.arange(n_seg + 1, dtype=np.int32) * seg_len).astype(np.int32)
-    zoo_pages = int(2 * ranks.sum())
-    return Workload(f"prefill_7b_h{hidden}_s{n_seg}x{seg_len}", hidden, 1, ranks, ids, indptr,
+    zoo_pages = int(2 * ranks.sum()) * n_layers
+    suffix = f"_l{n_layers}" if n_layers > 1 else ""
+    return Workload(f"prefill_7b_h{hidden}_s{n_seg}x{seg_len}{suffix}", hidden, n_layers, ranks, ids, indptr,
                     num_pages=2 * zoo_pages, kv_pages=zoo_pages,
-                    shuffle_seed=seed * 7919 + 17, seed=seed, values=values)
+                    shuffle_seed=seed * 7919 + 17, seed=seed, values=values, n_layers=n_layers)
 
 
 def decode_13b_zoo(seed: int = 0, values: str = "normal", T: int = 512, n_adapters: int = 2000,
