@@ -248,3 +248,47 @@ def test_plan_remake_for_the_next_batch_bit_exact():
     for j in range(2):
         assert np.array_equal(bits(got1[j]), bits(ref1[j])), j
         assert np.array_equal(bits(got2[j]), bits(ref2[j])), j
+
+
+def test_plan_scaling_override_copied_and_remade():
+    """A plan made with a scaling override keeps its own copy (the caller's array changes
+    after the call); a remake with another override, and one with none, take effect; each
+    apply bit for bit slora_lora_apply_multi with the same override, and within tolerance of
+    the oracle."""
+    ranks = np.array([16, 32, 8], np.int32)
+    idx = np.array([0, 1, 2, 1, 0, 2, 2, 1, 0], np.int32)
+    w = W.Workload("plan_scaling", 768, 2, ranks, idx, None, num_pages=2 * 2 * 2 * int(ranks.sum()),
+                   kv_pages=0, shuffle_seed=2, seed=6, n_layers=2)
+    first = np.array([0.5, -2.0, 3.0], np.float32)
+    second = np.array([1.5, 0.25, -1.0], np.float32)
+    didx = dev_i32(idx)
+
+    def multi_with(s, p, scaling):
+        y = dev_f16(w.y0(p))
+        sd = None if scaling is None else torch.from_numpy(scaling).cuda()
+        rdp.slora_lora_apply_multi(s.pool, [p], [dev_f16(w.x(p))], [y], w.T, didx, None, 0, sd)
+        torch.cuda.synchronize()
+        return to_np(y)
+
+    with PoolSession(w) as s:
+        s.load(range(w.n_adapters))
+        refs = {(p, name): multi_with(s, p, sc) for p in (0, 1)
+                for name, sc in (("first", first), ("second", second), ("none", None))}
+        sd = torch.from_numpy(first.copy()).cuda()
+        plan = rdp.slora_plan_create(s.pool, 1, w.T, didx, None, 0, sd)
+        try:
+            sd.fill_(7.0)   # the plan holds its own copy
+            got_first = [via_plan(plan, w, [p])[0] for p in (0, 1)]
+            rdp.slora_plan_remake(plan, didx, None, torch.from_numpy(second).cuda())
+            got_second = [via_plan(plan, w, [p])[0] for p in (0, 1)]
+            rdp.slora_plan_remake(plan, didx)
+            got_none = [via_plan(plan, w, [p])[0] for p in (0, 1)]
+            assert s.device_status() == 0
+        finally:
+            rdp.slora_plan_destroy(plan)
+    for p in (0, 1):
+        assert np.array_equal(bits(got_first[p]), bits(refs[(p, "first")])), p
+        assert np.array_equal(bits(got_second[p]), bits(refs[(p, "second")])), p
+        assert np.array_equal(bits(got_none[p]), bits(refs[(p, "none")])), p
+    factors = [(w.factors(a)[0][1], w.factors(a)[1][1]) for a in range(3)]
+    assert_close(got_second[1], oracle.lora_delta(w.x(1), w.y0(1), idx, ranks, second, factors), "remade override")
