@@ -350,18 +350,22 @@ slora_status slora_lora_apply_multi(slora_pool_t pool, int32_t n, const int32_t 
  *
  * A serving iteration runs one batch through every layer, so the tokens and their adapters
  * (one batch mixes requests of many adapters: S-LoRA: Serving Thousands of Concurrent LoRA
- * Adapters (explainer), "The mechanism") are the same in every layer.  slora_plan_create makes the token plan of the decode path once (the grouping of
- * the decode tokens by adapter, the work list, the adapters' page-table bases and scaling);
- * slora_plan_apply then runs one layer: the decode kernel over the stored plan and the
- * segments' tensor-core kernel, without the plan kernel.  Its results are bit for bit those
- * of slora_lora_apply_multi with the same arguments.
+ * Adapters (explainer), "The mechanism") are the same in every layer.  slora_plan_create
+ * makes the token plan of the decode path once (the grouping of the decode tokens by
+ * adapter, the work list, the adapters' page-table bases and scaling); slora_plan_apply
+ * then runs one layer: the decode kernel over the stored plan and the segments'
+ * tensor-core kernel, without the plan kernel.  Its results are bit for bit those of
+ * slora_lora_apply_multi with the same arguments.
  *
  *   n_slots            projections each apply covers (1..8), as n of slora_lora_apply_multi
  *   T, token_adapter_idx, seg_indptr, n_seg, scaling
- *                      as for slora_lora_apply_multi; copied into the plan (stream-ordered),
- *                      so the caller's buffers may change after the call
+ *                      as for slora_lora_apply_multi, with 1 <= T <= 1 << 20; copied into the
+ *                      plan (stream-ordered), so the caller's buffers may change after the call
  *   plan (out)         the plan; device memory of about the pool's plan scratch for T tokens
- *                      and n_slots projections, plus T + n_seg + 1 ints
+ *                      and n_slots projections, plus T + n_seg + 1 ints and max_adapters floats
+ *   errors             SLORA_ERR_INVALID_ARG for a null pool, out, token map or (n_seg > 0)
+ *                      segment pointer, or sizes out of range; SLORA_ERR_CUDA when the
+ *                      allocation or a launch fails (nothing is left allocated then)
  *
  * slora_plan_apply(plan, n, projs, x, y, stream): n must equal the plan's n_slots; projs,
  * x and y as for slora_lora_apply_multi (x, y of this layer).  The plan describes the pool
