@@ -485,6 +485,13 @@ slora_status slora_pool_set_stage_event(slora_pool_t pool, void *event);
  * SLORA_ERR_CUDA.  Other values return SLORA_ERR_INVALID_ARG.  The S-LoRA pages have no
  * counterpart for it. */
 slora_status slora_debug_set_prefill_cluster(int32_t ctas);
+/* Test hook.  1 (the default): when a batch of at most 32 segments has fewer 128-token
+ * units than the prefill kernel has resident clusters, its costliest units run split in
+ * two, each half on its own cluster, which repeats the unit's shrink and forms half of
+ * the unit's y columns; the result is bit for bit that of the unsplit unit.  0: no unit
+ * is split.  Applies to every later call in the process; other values return
+ * SLORA_ERR_INVALID_ARG.  The S-LoRA pages have no counterpart for it. */
+slora_status slora_debug_set_prefill_split(int32_t on);
 /* Test hook: host-side fault injection in the adapter load path.  The nth later operation
  * of `kind` (counted over every pool of the process) fails as if its call had failed:
  *   SLORA_FAULT_COPY       a cudaMemcpyAsync into the staging ring (copy-engine mode)

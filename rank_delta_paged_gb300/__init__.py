@@ -34,6 +34,7 @@ __all__ = [
     "SLORA_LOAD_ZERO_COPY", "SLORA_LOAD_COPY_ENGINE",
     "slora_adapters_evict",
     "slora_debug_set_prefill_cluster",
+    "slora_debug_set_prefill_split",
     "slora_debug_inject_load_fault", "SLORA_FAULT_NONE", "SLORA_FAULT_COPY", "SLORA_FAULT_SCATTER",
     "SLORA_FAULT_DIRECTORY", "SLORA_FAULT_STAGING", "SLORA_FAULT_ARENA",
     "slora_lora_apply_multi", "slora_plan_create", "slora_plan_apply", "slora_plan_remake",
@@ -82,6 +83,7 @@ _SIGS = {
     "slora_pool_set_load_start_event": [_P, _P],
     "slora_adapters_evict": [_P, _I32, _P, _P],
     "slora_debug_set_prefill_cluster": [_I32],
+    "slora_debug_set_prefill_split": [_I32],
     "slora_debug_inject_load_fault": [_I32, _I32],
     "slora_lora_apply_multi": [_P, _I32, _P, _P, _P, _I32, _P, _P, _I32, _P, _P],
     "slora_plan_create": [_P, _I32, _I32, _P, _P, _I32, _P, _P, _PP],
@@ -452,6 +454,11 @@ def slora_debug_inject_load_fault(kind: int, nth: int) -> None:
 def slora_debug_set_prefill_cluster(ctas: int) -> None:
     """Force the prefill kernel's CTAs per cluster (1, 2, 4, 8) for later calls; 0 = auto."""
     _call("slora_debug_set_prefill_cluster", int(ctas))
+
+
+def slora_debug_set_prefill_split(on: int) -> None:
+    """Allow (1, the default) or forbid (0) splitting prefill units by expand columns."""
+    _call("slora_debug_set_prefill_split", int(on))
 
 
 SLORA_LOAD_ZERO_COPY = 0

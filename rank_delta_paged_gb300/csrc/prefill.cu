@@ -18,7 +18,10 @@
 // by their adapter's rank, descending, in rounds of alternating direction); CTA c of a
 // cluster owns hidden slice c: the K range of its part
 // of the shrink and the N range of its part of the expand, so every byte of x, y0, y and
-// of the adapter's pages is moved by exactly one CTA.
+// of the adapter's pages is moved by exactly one CTA.  When such a batch has fewer units
+// than resident clusters, its costliest units are split in two by expand columns: each
+// half runs on its own cluster, repeats the whole shrink (so x and the A^T rows move
+// twice) and forms half of every CTA's columns of y.
 //
 // Warp roles (384 threads, one CTA per SM):
 //   warp 3      scheduler and token loader: maps the cluster's next unit to (segment,
@@ -98,7 +101,7 @@ struct alignas(64) UnitDesc {
     float sc;
     int32_t flag;
     int32_t pj;        // projection slot of the call
-    int32_t pad;
+    int32_t part;      // expand columns: 0 all of the CTA's, 1 the first half, 2 the second half
     int32_t pg[2 * kMaxPrefillRank];   // pool pages of the A^T rows, then of the B rows; -1 reads zeros
 };
 
@@ -119,6 +122,7 @@ struct PrefillArgs {
     int32_t C;       // CTAs per cluster
     int32_t slice;   // hidden elements per CTA, a multiple of 64
     int32_t nt;      // token-tile slots
+    int32_t split;   // units may be split in two by expand columns (every CTA has >= 2 tiles)
 };
 static_assert(sizeof(PrefillArgs) <= 4096, "kernel parameters");
 
@@ -257,6 +261,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const int k_lo = (int)crank * a.slice;
     const int k_hi = min(d, k_lo + a.slice);
     const int nkb = (k_hi - k_lo) / KBLK;   // shrink K blocks = expand column tiles
+    // A split unit runs on two clusters: each does the whole shrink (same arithmetic, so the
+    // same U) and expands half of every CTA's column tiles, so y is bit for bit the same.
+    const int nkh = (nkb + 1) / 2;
+    auto e_first = [nkh](int part) { return part == 2 ? nkh : 0; };
+    auto e_count = [nkb, nkh](int part) { return part == 0 ? nkb : (part == 1 ? nkh : nkb - nkh); };
 
     if (bad) {
         // nothing to do
@@ -269,9 +278,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         // segment s; the segments are sorted by their adapter's rank, descending (ties:
         // lower index first), and the units (tile, projection slot) of the sorted segments
         // go to the clusters in rounds of one unit per cluster, walked in alternating
-        // direction.  Larger batches take the units in order, cluster c every ncl-th.
+        // direction.  When the units leave clusters idle, the costliest ones are split in two
+        // by expand columns (places 2j and 2j + 1 of the deal are the halves of unit j).
+        // Larger batches take the units in order, cluster c every ncl-th.
         const bool lpt = a.n_seg <= 32;
-        int s_lo = 0, s_hi = 0, ord = 0, upref = 0, n_units = 0;
+        int s_lo = 0, s_hi = 0, ord = 0, upref = 0, n_units = 0, n_split = 0;
         if (lpt) {
             int key = 0x7fffffff;
             if (lane < a.n_seg) {
@@ -307,12 +318,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             }
             upref = incl;   // units of sorted places 0 .. lane
             n_units = __shfl_sync(0xffffffffu, incl, 31);
+            if (a.split) n_split = max(0, min(n_units, (int)ncl - n_units));
         }
         for (uint32_t i = 0;; ++i) {
-            int tile = -1, lo = 0, hi = 0, pj = 0;
+            int tile = -1, lo = 0, hi = 0, pj = 0, part = 0;
             if (lpt) {
-                const int p = (int)(i * ncl + ((i & 1) ? (ncl - 1 - cl) : cl));
-                if (p < n_units) {
+                int p = (int)(i * ncl + ((i & 1) ? (ncl - 1 - cl) : cl));
+                if (p < n_units + n_split) {
+                    if (p < 2 * n_split) {
+                        part = 1 + (p & 1);
+                        p >>= 1;
+                    } else {
+                        p -= n_split;
+                    }
                     const int q = __ffs(__ballot_sync(0xffffffffu, upref > p)) - 1;
                     const int prev = __shfl_sync(0xffffffffu, upref, q > 0 ? q - 1 : 0);
                     const int o = p - (q > 0 ? prev : 0);
@@ -405,15 +423,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 u->sc = sc;
                 u->flag = flag;
                 u->pj = pj;
+                u->part = part;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&dfull[i & 1]);
             if (flag == kEnd) break;
             // the unit's token tiles: x for the shrink, then y0 for the expand, as slots free up
             if (flag == kCompute && lane == 0) {
-                for (int st = 0; st < 2 * nkb; ++st) {
+                const int e0 = e_first(part), ne = e_count(part);
+                for (int st = 0; st < nkb + ne; ++st) {
                     const bool shrink = st < nkb;
-                    const int col = k_lo + (shrink ? st : st - nkb) * KBLK;
+                    const int col = k_lo + (shrink ? st : e0 + st - nkb) * KBLK;
                     const uint32_t sT = gT % nts;
                     wait_phase<false>(&emptyT[sT], ((gT / nts) & 1) ^ 1, abort, status);
                     if (*abort) break;
@@ -442,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             wait_phase<false>(&dfull[i & 1], (i >> 1) & 1, abort, status);
             if (__any_sync(0xffffffffu, *abort)) break;
             const UnitDesc *u = &desc[i & 1];
-            const int flag = u->flag, r_pad = u->r_pad;
+            const int flag = u->flag, r_pad = u->r_pad, e0 = e_first(u->part), ne = e_count(u->part);
             if (flag == kEnd) break;
             bool ab = false;
             if (flag == kCompute) {
@@ -454,9 +474,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     cur_sz = psz;
                 }
                 int sP = 0;
-                for (int st = 0; st < 2 * nkb; ++st) {
+                for (int st = 0; st < nkb + ne; ++st) {
                     const bool shrink = st < nkb;
-                    const int col = k_lo + (shrink ? st : st - nkb) * KBLK;
+                    const int col = k_lo + (shrink ? st : e0 + st - nkb) * KBLK;
                     wait_phase<false>(&emptyP[sP], ((pfill >> sP) & 1) ^ 1, abort, status);
                     if (__any_sync(0xffffffffu, *abort)) {
                         ab = true;
@@ -495,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             for (uint32_t i = 0;; ++i) {
                 wait_phase<false>(&dfull[i & 1], (i >> 1) & 1, abort, status);
                 if (*abort) break;
-                const int flag = desc[i & 1].flag, r_pad = desc[i & 1].r_pad;
+                const int flag = desc[i & 1].flag, r_pad = desc[i & 1].r_pad, ne = e_count(desc[i & 1].part);
                 mbar_arrive(&dempty[i & 1]);
                 if (flag == kEnd) break;
                 if (flag != kCompute) continue;
@@ -527,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 tc::fence_after_sync();
                 fence_proxy_async_all();
                 const uint32_t idesc_e = tc::idesc_f16_f32(MT, KBLK, 0, 1);
-                for (int nt = 0; nt < nkb; ++nt) {
+                for (int nt = 0; nt < ne; ++nt) {
                     const uint32_t b = e % NB;
                     wait_phase<false>(&fullP[sP], (pcons >> sP) & 1, abort, status);
                     if (e >= (uint32_t)NB) wait_phase<false>(&accempty[b], ((e / NB) - 1) & 1, abort, status);
@@ -568,6 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             if (epi_sync_or(*abort)) break;
             const UnitDesc *ud = &desc[i & 1];
             const int flag = ud->flag, m0 = ud->m0, mlen = ud->mlen, r_pad = ud->r_pad, pj = ud->pj;
+            const int e0 = e_first(ud->part), ne = e_count(ud->part);
             const float sc = ud->sc;
             __syncwarp();
             if (lane == 0) mbar_arrive(&dempty[i & 1]);
@@ -682,7 +703,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     mbar_arrive(&emptyT[slot]);
                 }
             };
-            for (int nt = 0; nt < nkb; ++nt) {
+            for (int nt = 0; nt < ne; ++nt) {
                 const uint32_t sT = g % nts, b = e % NB;
                 wait_phase<false>(&accfull[b], (e / NB) & 1, abort, status);
                 tc::fence_after_sync();
@@ -720,7 +741,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll
                 for (int cc = 0; cc < 8; ++cc)
                     *reinterpret_cast<uint4 *>(yt + m * 128 + ((cc ^ (m & 7)) << 4)) = yrow[cc];
-                const int n0 = k_lo + nt * KBLK;
+                const int n0 = k_lo + (e0 + nt) * KBLK;
                 if (full_tile) {
                     tc::fence_proxy_async_smem();
                     __syncwarp();
@@ -812,6 +833,7 @@ cudaError_t token_map(CUtensorMap *m, const void *base, int hidden, int T, int b
 }
 
 int g_forced_cluster = 0;
+int g_prefill_split = 1;
 
 inline int slice_for(int hidden, int C) { return (hidden / 64 + C - 1) / C * 64; }
 
@@ -932,6 +954,9 @@ cudaError_t launch_prefill(const PoolView &pv, const ProjList &pl, int32_t T, co
     pa.C = C;
     pa.slice = slice_for(pv.hidden, C);
     pa.nt = tslots_for(C);
+    // a unit splits in two by expand columns only when every CTA of a cluster has at least
+    // two column tiles (the last CTA's slice may be shorter)
+    pa.split = g_prefill_split && pa.slice / KBLK >= 2 && (pv.hidden - (C - 1) * pa.slice) / KBLK >= 2;
 
     attr[1].val.clusterDim.x = C;
     cfg.gridDim = dim3(C * ncl);
@@ -947,5 +972,14 @@ extern "C" slora_status slora_debug_set_prefill_cluster(int32_t ctas)
 {
     if (ctas != 0 && ctas != 1 && ctas != 2 && ctas != 4 && ctas != 8) return SLORA_ERR_INVALID_ARG;
     slora::g_forced_cluster = ctas;
+    return SLORA_OK;
+}
+
+// Test hook: allow (1, the default) or forbid (0) splitting a segment unit in two by
+// expand columns when the batch leaves clusters idle.
+extern "C" slora_status slora_debug_set_prefill_split(int32_t on)
+{
+    if (on != 0 && on != 1) return SLORA_ERR_INVALID_ARG;
+    slora::g_prefill_split = on;
     return SLORA_OK;
 }

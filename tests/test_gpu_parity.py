@@ -430,6 +430,28 @@ def test_prefill_cluster_normal_values(ctas):
     assert_close(got, oracle.workload_reference(w), f"prefill, {ctas} CTAs per cluster")
 
 
+@pytest.mark.parametrize("ctas", [0, 1, 8])
+def test_prefill_split_units_match_unsplit_bit_for_bit(ctas):
+    """A batch with fewer 128-token units than resident clusters runs its costliest units
+    split in two by expand columns (each half repeats the shrink on its own cluster):
+    normal-valued inputs give y bit for bit equal to the unsplit kernel's at the same
+    cluster size, and within the tolerance of the oracle."""
+    w = W.prefill_7b(n_seg=6, seg_len=300)   # 18 units, ragged last tiles, ranks 8..128
+    outs = []
+    rdp.slora_debug_set_prefill_cluster(ctas)
+    try:
+        with session_all_loaded(w) as s:
+            for split in (1, 0):
+                rdp.slora_debug_set_prefill_split(split)
+                outs.append(run(s))
+                assert s.device_status() == 0
+    finally:
+        rdp.slora_debug_set_prefill_split(1)
+        rdp.slora_debug_set_prefill_cluster(0)
+    assert np.array_equal(outs[0].view(np.uint16), outs[1].view(np.uint16))
+    assert_close(outs[0], oracle.workload_reference(w), f"split prefill, {ctas} CTAs per cluster")
+
+
 def test_load_of_more_adapters_than_one_launch_carries():
     """600 adapters in one load call: two launches of the load kernel (at most 512 adapters
     each), which read the pinned store directly; pages bit-exact on both sides of the
