@@ -485,9 +485,9 @@ slora_status slora_pool_set_stage_event(slora_pool_t pool, void *event);
  * SLORA_ERR_CUDA.  Other values return SLORA_ERR_INVALID_ARG.  The S-LoRA pages have no
  * counterpart for it. */
 slora_status slora_debug_set_prefill_cluster(int32_t ctas);
-/* Test hook.  1 (the default): when a batch of at most 32 segments has fewer 128-token
- * units than the prefill kernel has resident clusters, its costliest units run split in
- * two, each half on its own cluster, which repeats the unit's shrink and forms half of
+/* Test hook.  1 (the default): when a batch of at most 32 segments has at most half as
+ * many 128-token units as the prefill kernel has resident clusters, every unit runs split
+ * in two, each half on its own cluster, which repeats the unit's shrink and forms half of
  * the unit's y columns; the result is bit for bit that of the unsplit unit.  0: no unit
  * is split.  Applies to every later call in the process; other values return
  * SLORA_ERR_INVALID_ARG.  The S-LoRA pages have no counterpart for it. */

@@ -18,8 +18,8 @@
 // by their adapter's rank, descending, in rounds of alternating direction); CTA c of a
 // cluster owns hidden slice c: the K range of its part
 // of the shrink and the N range of its part of the expand, so every byte of x, y0, y and
-// of the adapter's pages is moved by exactly one CTA.  When such a batch has fewer units
-// than resident clusters, its costliest units are split in two by expand columns: each
+// of the adapter's pages is moved by exactly one CTA.  When such a batch has at most half
+// as many units as resident clusters, every unit is split in two by expand columns: each
 // half runs on its own cluster, repeats the whole shrink (so x and the A^T rows move
 // twice) and forms half of every CTA's columns of y.
 //
@@ -278,8 +278,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         // segment s; the segments are sorted by their adapter's rank, descending (ties:
         // lower index first), and the units (tile, projection slot) of the sorted segments
         // go to the clusters in rounds of one unit per cluster, walked in alternating
-        // direction.  When the units leave clusters idle, the costliest ones are split in two
-        // by expand columns (places 2j and 2j + 1 of the deal are the halves of unit j).
+        // direction.  When the units would leave at least half the clusters idle, every unit
+        // is split in two by expand columns (places 2j and 2j + 1 of the deal are the halves
+        // of unit j); splitting only some would not shorten the launch, which the unsplit
+        // units still set.
         // Larger batches take the units in order, cluster c every ncl-th.
         const bool lpt = a.n_seg <= 32;
         int s_lo = 0, s_hi = 0, ord = 0, upref = 0, n_units = 0, n_split = 0;
@@ -318,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             }
             upref = incl;   // units of sorted places 0 .. lane
             n_units = __shfl_sync(0xffffffffu, incl, 31);
-            if (a.split) n_split = max(0, min(n_units, (int)ncl - n_units));
+            if (a.split && 2 * n_units <= (int)ncl) n_split = n_units;
         }
         for (uint32_t i = 0;; ++i) {
             int tile = -1, lo = 0, hi = 0, pj = 0, part = 0;

@@ -430,12 +430,13 @@ def test_prefill_cluster_normal_values(ctas):
     assert_close(got, oracle.workload_reference(w), f"prefill, {ctas} CTAs per cluster")
 
 
-@pytest.mark.parametrize("ctas", [0, 1, 8])
+@pytest.mark.parametrize("ctas", [0, 1, 2, 4])
 def test_prefill_split_units_match_unsplit_bit_for_bit(ctas):
-    """A batch with fewer 128-token units than resident clusters runs its costliest units
-    split in two by expand columns (each half repeats the shrink on its own cluster):
-    normal-valued inputs give y bit for bit equal to the unsplit kernel's at the same
-    cluster size, and within the tolerance of the oracle."""
+    """A batch with at most half as many 128-token units as resident clusters runs every
+    unit split in two by expand columns (each half repeats the shrink on its own cluster;
+    18 units against 38 clusters of 4 CTAs or more of fewer): normal-valued inputs give y
+    bit for bit equal to the unsplit kernel's at the same cluster size, and within the
+    tolerance of the oracle."""
     w = W.prefill_7b(n_seg=6, seg_len=300)   # 18 units, ragged last tiles, ranks 8..128
     outs = []
     rdp.slora_debug_set_prefill_cluster(ctas)
