@@ -168,6 +168,41 @@ def test_multi_eight_entries_exact_inputs_bit_exact_vs_oracle():
         assert np.array_equal(bits(many[j]), bits(ref.astype(np.float16))), j
 
 
+@pytest.mark.parametrize("ctas", [2, 4])
+def test_multi_split_units_exact_bit_exact_vs_oracle(ctas):
+    """A small segment batch through a 3-entry call: 12 (tile, projection) units, so at 2
+    and 4 CTAs per cluster every unit runs split in two by expand columns.  Exact inputs:
+    every entry equals the oracle bit for bit, with the split and with it turned off."""
+    ranks = np.array([16, 128, 40], np.int32)
+    lens = [200, 190]
+    rng = np.random.default_rng(21)
+    dec = rng.integers(-1, len(ranks), size=20).astype(np.int32)
+    idx = np.concatenate([np.full(L, a) for a, L in zip([0, 1], lens)] + [dec]).astype(np.int32)
+    indptr = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    n_proj = 3
+    w = W.Workload("multi_split_exact", 4096, n_proj, ranks, idx, indptr,
+                   num_pages=2 * 2 * n_proj * int(ranks.sum()), kv_pages=2 * n_proj * int(ranks.sum()),
+                   shuffle_seed=22, seed=23, values="exact")
+    projs = [2, 0, 1]
+    xs = [w.x(p) for p in projs]
+    outs = {}
+    rdp.slora_debug_set_prefill_cluster(ctas)
+    try:
+        with PoolSession(w) as s:
+            s.load(range(w.n_adapters))
+            for split in (1, 0):
+                rdp.slora_debug_set_prefill_split(split)
+                outs[split] = multi(s, w, projs, xs)
+                assert s.device_status() == 0
+    finally:
+        rdp.slora_debug_set_prefill_split(1)
+        rdp.slora_debug_set_prefill_cluster(0)
+    for j, p in enumerate(projs):
+        ref = bits(oracle.workload_reference(w, p=p).astype(np.float16))
+        assert np.array_equal(bits(outs[1][j]), ref), ("split", j)
+        assert np.array_equal(bits(outs[0][j]), ref), ("unsplit", j)
+
+
 def test_multi_argument_errors_launch_nothing():
     w = W.tiny_decode()
     with PoolSession(w) as s:
