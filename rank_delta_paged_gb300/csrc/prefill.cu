@@ -96,6 +96,7 @@ constexpr size_t kSmemLimit = 227 * 1024;     // dynamic + static shared memory 
 constexpr size_t kStaticReserve = 1024;       // the kernel's static shared memory, rounded up
 
 constexpr int kCompute = 0, kSkip = 1, kEnd = 2;
+constexpr int kPgPerLane = 2 * kMaxPrefillRank / 32;   // page ids per scheduler lane
 struct alignas(64) UnitDesc {
     int32_t m0, mlen, rank, r_pad;
     float sc;
@@ -285,6 +286,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         // Larger batches take the units in order, cluster c every ncl-th.
         const bool lpt = a.n_seg <= 32;
         int s_lo = 0, s_hi = 0, ord = 0, upref = 0, n_units = 0, n_split = 0;
+        int l_ad = -1;                     // lane s: segment s's adapter (its first token's)
+        DirEntry l_e{0, 0.f, -1};          // and that adapter's directory entry
         if (lpt) {
             int key = 0x7fffffff;
             if (lane < a.n_seg) {
@@ -293,8 +296,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 int rank = 0;
                 if (s_hi > s_lo && s_lo >= 0 && s_lo < a.T) {
                     const int ad = a.idx[s_lo];
+                    l_ad = ad;
                     if (ad >= 0 && ad < a.pv.max_adapters) {
                         const DirEntry e = a.pv.dir[ad];
+                        l_e = e;
                         if (e.pt_off >= 0 && e.rank > 0) rank = min(e.rank, 255);
                     }
                 }
@@ -323,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             if (a.split && 2 * n_units <= (int)ncl) n_split = n_units;
         }
         for (uint32_t i = 0;; ++i) {
-            int tile = -1, lo = 0, hi = 0, pj = 0, part = 0;
+            int tile = -1, lo = 0, hi = 0, pj = 0, part = 0, seg_l = 0;
             if (lpt) {
                 int p = (int)(i * ncl + ((i & 1) ? (ncl - 1 - cl) : cl));
                 if (p < n_units + n_split) {
@@ -341,6 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     const int seg = __shfl_sync(0xffffffffu, ord, q);
                     lo = __shfl_sync(0xffffffffu, s_lo, seg);
                     hi = __shfl_sync(0xffffffffu, s_hi, seg);
+                    seg_l = seg;
                 }
             }
             const int vu = (int)(cl + i * ncl);            // unit: (tile mt, projection slot pj)
@@ -374,14 +380,36 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             }
             int flag = kEnd, m0 = 0, mlen = 0, rank = 0;
             float sc = 0.f;
-            int64_t pt = 0;
+            int32_t pgv[kPgPerLane];   // this lane's page ids of the unit (j = lane + 32 k)
             if (tile >= 0) {
                 flag = kSkip;
                 m0 = lo + tile * MT;
                 mlen = min(MT, hi - m0);
+                // The segment's adapter and directory entry come from the lanes of the sort
+                // (batches of at most 32 segments) or are loaded here; the page ids are loaded
+                // beside the check of the segment's tokens and used only if it passes, so the
+                // descriptor waits for one round of loads after the adapter is known.
+                int ad;
+                DirEntry e{0, 0.f, -1};
+                if (lpt) {
+                    ad = __shfl_sync(0xffffffffu, l_ad, seg_l);
+                    e.rank = __shfl_sync(0xffffffffu, l_e.rank, seg_l);
+                    e.scaling = __shfl_sync(0xffffffffu, l_e.scaling, seg_l);
+                    e.pt_off = __shfl_sync(0xffffffffu, l_e.pt_off, seg_l);
+                } else {
+                    ad = a.idx[lo];
+                    if (ad >= 0 && ad < a.pv.max_adapters) e = a.pv.dir[ad];
+                }
+                const bool usable = ad >= 0 && ad < a.pv.max_adapters && e.pt_off >= 0 && e.rank > 0 &&
+                                    e.rank <= kMaxPrefillRank;
+                const int64_t pt_u = usable ? e.pt_off + (int64_t)a.proj[pj] * 2 * e.rank : 0;
+#pragma unroll
+                for (int k = 0; k < kPgPerLane; ++k) {
+                    const int j = lane + 32 * k;
+                    pgv[k] = usable && j < 2 * e.rank ? a.pv.pt_arena[pt_u + j] : -1;
+                }
                 // a segment whose tokens disagree on the adapter is skipped as a whole: every
                 // unit checks its whole segment
-                const int ad = a.idx[lo];
                 bool mixed = false;
                 for (int q = lo + lane; q < hi; q += 32) mixed |= a.idx[q] != ad;
                 if (__any_sync(0xffffffffu, mixed)) {
@@ -390,16 +418,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     // base model only
                 } else if (ad < -1 || ad >= a.pv.max_adapters) {
                     if (lane == 0) set_status(status, SLORA_DEV_BAD_ADAPTER);
-                } else {
-                    const DirEntry e = a.pv.dir[ad];
-                    if (e.pt_off < 0 || e.rank <= 0) {
-                        if (lane == 0) set_status(status, SLORA_DEV_NOT_RESIDENT);
-                    } else if (e.rank <= kMaxPrefillRank) {   // larger ranks take the decode path
-                        flag = kCompute;
-                        rank = e.rank;
-                        sc = a.scaling ? a.scaling[ad] : e.scaling;
-                        pt = e.pt_off + (int64_t)a.proj[pj] * 2 * e.rank;
-                    }
+                } else if (e.pt_off < 0 || e.rank <= 0) {
+                    if (lane == 0) set_status(status, SLORA_DEV_NOT_RESIDENT);
+                } else if (e.rank <= kMaxPrefillRank) {   // larger ranks take the decode path
+                    flag = kCompute;
+                    rank = e.rank;
+                    sc = a.scaling ? a.scaling[ad] : e.scaling;
                 }
             }
             wait_phase<false>(&dempty[i & 1], ((i >> 1) & 1) ^ 1, abort, status);
@@ -407,13 +431,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             UnitDesc *u = &desc[i & 1];
             if (flag == kCompute) {
                 bool badp = false;
-                for (int j = lane; j < 2 * rank; j += 32) {
-                    int32_t p = a.pv.pt_arena[pt + j];
-                    if (p < 0 || p >= a.pv.num_pages) {
-                        badp = true;   // the row reads as zeros
-                        p = -1;
+#pragma unroll
+                for (int k = 0; k < kPgPerLane; ++k) {
+                    const int j = lane + 32 * k;
+                    if (j < 2 * rank) {
+                        int32_t p = pgv[k];
+                        if (p < 0 || p >= a.pv.num_pages) {
+                            badp = true;   // the row reads as zeros
+                            p = -1;
+                        }
+                        u->pg[j < rank ? j : kMaxPrefillRank + j - rank] = p;
                     }
-                    u->pg[j < rank ? j : kMaxPrefillRank + j - rank] = p;
                 }
                 if (__any_sync(0xffffffffu, badp) && lane == 0) set_status(status, SLORA_DEV_BAD_PAGE);
             }
