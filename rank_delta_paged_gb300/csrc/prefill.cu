@@ -87,6 +87,7 @@ constexpr int kTileBytes = MT * 128;          // 128 rows x 64 fp16, 128-byte ro
 constexpr int kUBytes = 2 * kTileBytes;       // U operand: 128 x 128 fp16, two 64-column atoms
 constexpr int NB = 4;                         // expand accumulator buffers in TMEM
 constexpr uint32_t kTmemCols = 512;           // U at 0..127, expand buffer b at 128 + 64 b
+static_assert(128 + NB * 64 + 16 <= (int)kTmemCols, "tensor-memory columns the warm-up load reads");
 constexpr int kXPitchMax = kMaxPrefillRank * 4 + 16;
 constexpr int kMaxClusterP = 8;
 constexpr int kPRingBytes = 3 * kTileBytes;   // page-row ring: slots of r_pad * 128 bytes
@@ -200,6 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
     __shared__ int s_stored[kMaxTSlots];   // epilogue warps done with an expand slot
+    __shared__ __align__(16) uint4 s_warm[kMaxClusterP];   // slot q: written by CTA q, never read
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int C = a.C;
@@ -613,6 +615,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         const uint32_t ua = smem_u32(Us);
         uint32_t g = 0, e = 0, ui = 0;
         int pend = -1;   // (lane 0) token slot this warp's last tensor-tile store may still be reading
+        if (C > 1) {
+            // A launch's first tensor-memory load and first stores into another CTA's shared
+            // memory take one to two microseconds each; made here, while the first unit's
+            // shrink runs, they are not paid inside its exchange.  Columns from 384 on are
+            // never written (U 0..127, the expand buffers 128..383), and each CTA stores
+            // only into its own slot of the peers' s_warm.
+            uint32_t wv[16];
+            tc::ld_32x32b_x16(tmem + lane_base + 128 + NB * 64, wv);
+            tc::ld_wait();
+            for (int q = 0; q < C; ++q)
+                if (q != (int)crank) st_cluster_v4(mapa(smem_u32(&s_warm[crank]), (uint32_t)q), make_uint4(wv[0], 0u, 0u, 0u));
+        }
         for (uint32_t i = 0;; ++i) {
             wait_phase<false>(&dfull[i & 1], (i >> 1) & 1, abort, status);
             if (epi_sync_or(*abort)) break;
