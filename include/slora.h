@@ -485,11 +485,12 @@ slora_status slora_pool_set_stage_event(slora_pool_t pool, void *event);
  * SLORA_ERR_CUDA.  Other values return SLORA_ERR_INVALID_ARG.  The S-LoRA pages have no
  * counterpart for it. */
 slora_status slora_debug_set_prefill_cluster(int32_t ctas);
-/* Test hook.  1 (the default): when a batch of at most 32 segments has at most half as
- * many 128-token units as the prefill kernel has resident clusters, every unit runs split
- * in two, each half on its own cluster, which repeats the unit's shrink and forms half of
- * the unit's y columns; the result is bit for bit that of the unsplit unit.  0: no unit
- * is split.  Applies to every later call in the process; other values return
+/* Test hook.  1 (the default): in a batch of at most 32 segments, the 128-token units of
+ * the prefill kernel's last, partial round of units (all of them when there is a single
+ * round) run split into 2 or 4 parts, the most that fit the clusters that round would leave
+ * idle; each part runs on its own cluster, repeats the unit's shrink and forms its share
+ * of the unit's y columns, so the result is bit for bit that of the unsplit unit.  0: no
+ * unit is split.  Applies to every later call in the process; other values return
  * SLORA_ERR_INVALID_ARG.  The S-LoRA pages have no counterpart for it. */
 slora_status slora_debug_set_prefill_split(int32_t on);
 /* Test hook: host-side fault injection in the adapter load path.  The nth later operation

@@ -103,7 +103,7 @@ struct alignas(64) UnitDesc {
     float sc;
     int32_t flag;
     int32_t pj;        // projection slot of the call
-    int32_t part;      // expand columns: 0 all of the CTA's, 1 the first half, 2 the second half
+    int32_t part;      // expand columns: 0 all of the CTA's tiles, else part j of P: 8 P + j
     int32_t pg[2 * kMaxPrefillRank];   // pool pages of the A^T rows, then of the B rows; -1 reads zeros
 };
 
@@ -124,7 +124,7 @@ struct PrefillArgs {
     int32_t C;       // CTAs per cluster
     int32_t slice;   // hidden elements per CTA, a multiple of 64
     int32_t nt;      // token-tile slots
-    int32_t split;   // units may be split in two by expand columns (every CTA has >= 2 tiles)
+    int32_t split;   // most parts a unit may be split into by expand columns (1, 2 or 4)
 };
 static_assert(sizeof(PrefillArgs) <= 4096, "kernel parameters");
 
@@ -264,11 +264,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const int k_lo = (int)crank * a.slice;
     const int k_hi = min(d, k_lo + a.slice);
     const int nkb = (k_hi - k_lo) / KBLK;   // shrink K blocks = expand column tiles
-    // A split unit runs on two clusters: each does the whole shrink (same arithmetic, so the
-    // same U) and expands half of every CTA's column tiles, so y is bit for bit the same.
-    const int nkh = (nkb + 1) / 2;
-    auto e_first = [nkh](int part) { return part == 2 ? nkh : 0; };
-    auto e_count = [nkb, nkh](int part) { return part == 0 ? nkb : (part == 1 ? nkh : nkb - nkh); };
+    // A unit split in P parts runs on P clusters: each does the whole shrink (same
+    // arithmetic, so the same U) and expands part j of every CTA's column tiles, tiles
+    // [nkb j / P, nkb (j + 1) / P), so y is bit for bit the same.
+    auto e_first = [nkb](int part) { return part == 0 ? 0 : nkb * (part & 7) / (part >> 3); };
+    auto e_count = [nkb](int part) {
+        return part == 0 ? nkb : nkb * ((part & 7) + 1) / (part >> 3) - nkb * (part & 7) / (part >> 3);
+    };
 
     if (bad) {
         // nothing to do
@@ -281,13 +283,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         // segment s; the segments are sorted by their adapter's rank, descending (ties:
         // lower index first), and the units (tile, projection slot) of the sorted segments
         // go to the clusters in rounds of one unit per cluster, walked in alternating
-        // direction.  When the units would leave at least half the clusters idle, every unit
-        // is split in two by expand columns (places 2j and 2j + 1 of the deal are the halves
-        // of unit j); splitting only some would not shorten the launch, which the unsplit
-        // units still set.
+        // direction.  The units of the last round, which would leave clusters idle (r units
+        // after `full` full rounds), are split by expand columns into the most parts P (2 or
+        // 4) with P r at most the clusters: places full ncl + P k + j of the deal are the
+        // parts of unit full ncl + k.  Every cluster then holds `full` units and at most one
+        // part; with a single round (full = 0) every unit is split.
         // Larger batches take the units in order, cluster c every ncl-th.
         const bool lpt = a.n_seg <= 32;
-        int s_lo = 0, s_hi = 0, ord = 0, upref = 0, n_units = 0, n_split = 0;
+        int s_lo = 0, s_hi = 0, ord = 0, upref = 0, n_units = 0;
+        int n_whole = 0, n_parts = 1, n_virt = 0;   // units dealt whole; parts of the rest; places
         int l_ad = -1;                     // lane s: segment s's adapter (its first token's)
         DirEntry l_e{0, 0.f, -1};          // and that adapter's directory entry
         if (lpt) {
@@ -327,18 +331,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             }
             upref = incl;   // units of sorted places 0 .. lane
             n_units = __shfl_sync(0xffffffffu, incl, 31);
-            if (a.split && 2 * n_units <= (int)ncl) n_split = n_units;
+            const int full = n_units / (int)ncl, r = n_units - full * (int)ncl;
+            n_whole = n_units;
+            if (r > 0)
+                for (int P = a.split; P > 1; P >>= 1)
+                    if (P * r <= (int)ncl) {
+                        n_whole = full * (int)ncl;
+                        n_parts = P;
+                        break;
+                    }
+            n_virt = n_whole + n_parts * (n_units - n_whole);
         }
         for (uint32_t i = 0;; ++i) {
             int tile = -1, lo = 0, hi = 0, pj = 0, part = 0, seg_l = 0;
             if (lpt) {
                 int p = (int)(i * ncl + ((i & 1) ? (ncl - 1 - cl) : cl));
-                if (p < n_units + n_split) {
-                    if (p < 2 * n_split) {
-                        part = 1 + (p & 1);
-                        p >>= 1;
-                    } else {
-                        p -= n_split;
+                if (p < n_virt) {
+                    if (p >= n_whole) {
+                        const int k = p - n_whole;
+                        part = 8 * n_parts + k % n_parts;
+                        p = n_whole + k / n_parts;
                     }
                     const int q = __ffs(__ballot_sync(0xffffffffu, upref > p)) - 1;
                     const int prev = __shfl_sync(0xffffffffu, upref, q > 0 ? q - 1 : 0);
@@ -998,9 +1010,12 @@ cudaError_t launch_prefill(const PoolView &pv, const ProjList &pl, int32_t T, co
     pa.C = C;
     pa.slice = slice_for(pv.hidden, C);
     pa.nt = tslots_for(C);
-    // a unit splits in two by expand columns only when every CTA of a cluster has at least
-    // two column tiles (the last CTA's slice may be shorter)
-    pa.split = g_prefill_split && pa.slice / KBLK >= 2 && (pv.hidden - (C - 1) * pa.slice) / KBLK >= 2;
+    // a unit splits into P parts by expand columns only when every CTA of a cluster has at
+    // least P column tiles (the last CTA's slice may be shorter)
+    {
+        const int nkb_min = std::min(pa.slice / KBLK, (pv.hidden - (C - 1) * pa.slice) / KBLK);
+        pa.split = !g_prefill_split ? 1 : (nkb_min >= 4 ? 4 : (nkb_min >= 2 ? 2 : 1));
+    }
 
     attr[1].val.clusterDim.x = C;
     cfg.gridDim = dim3(C * ncl);

@@ -430,13 +430,35 @@ def test_prefill_cluster_normal_values(ctas):
     assert_close(got, oracle.workload_reference(w), f"prefill, {ctas} CTAs per cluster")
 
 
+@pytest.mark.parametrize("ctas", [4, 8])
+def test_prefill_last_round_split_matches_unsplit_bit_for_bit(ctas):
+    """More units than clusters (44 against 38 clusters of 4 CTAs, or about 19 of 8): the
+    units of the last, partial round are split by expand columns over the clusters that
+    round would leave idle.  Normal-valued inputs: y bit for bit the unsplit kernel's at
+    the same cluster size, and within the tolerance of the oracle."""
+    w = W.prefill_7b(n_seg=11, seg_len=512)   # 44 units, ranks 8..128
+    outs = []
+    rdp.slora_debug_set_prefill_cluster(ctas)
+    try:
+        with session_all_loaded(w) as s:
+            for split in (1, 0):
+                rdp.slora_debug_set_prefill_split(split)
+                outs.append(run(s))
+                assert s.device_status() == 0
+    finally:
+        rdp.slora_debug_set_prefill_split(1)
+        rdp.slora_debug_set_prefill_cluster(0)
+    assert np.array_equal(outs[0].view(np.uint16), outs[1].view(np.uint16))
+    assert_close(outs[0], oracle.workload_reference(w), f"last-round split, {ctas} CTAs per cluster")
+
+
 @pytest.mark.parametrize("ctas", [0, 1, 2, 4])
 def test_prefill_split_units_match_unsplit_bit_for_bit(ctas):
-    """A batch with at most half as many 128-token units as resident clusters runs every
-    unit split in two by expand columns (each half repeats the shrink on its own cluster;
-    18 units against 38 clusters of 4 CTAs or more of fewer): normal-valued inputs give y
-    bit for bit equal to the unsplit kernel's at the same cluster size, and within the
-    tolerance of the oracle."""
+    """A batch of fewer 128-token units than resident clusters runs every unit split by
+    expand columns (in 4 parts against 76 or 152 clusters, in 2 against 38; each part
+    repeats the shrink on its own cluster): normal-valued inputs give y bit for bit equal
+    to the unsplit kernel's at the same cluster size, and within the tolerance of the
+    oracle."""
     w = W.prefill_7b(n_seg=6, seg_len=300)   # 18 units, ragged last tiles, ranks 8..128
     outs = []
     rdp.slora_debug_set_prefill_cluster(ctas)
