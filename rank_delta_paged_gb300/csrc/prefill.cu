@@ -18,10 +18,11 @@
 // by their adapter's rank, descending, in rounds of alternating direction); CTA c of a
 // cluster owns hidden slice c: the K range of its part
 // of the shrink and the N range of its part of the expand, so every byte of x, y0, y and
-// of the adapter's pages is moved by exactly one CTA.  When such a batch has at most half
-// as many units as resident clusters, every unit is split in two by expand columns: each
-// half runs on its own cluster, repeats the whole shrink (so x and the A^T rows move
-// twice) and forms half of every CTA's columns of y.
+// of the adapter's pages is moved by exactly one CTA.  In such a batch the units of the
+// last, partial round (all of them when there is one round) are split by expand columns
+// into 2 or 4 parts, the most the clusters that round would leave idle can take: each part
+// runs on its own cluster, repeats the whole shrink (so x and the A^T rows move again) and
+// forms its share of every CTA's columns of y.
 //
 // Warp roles (384 threads, one CTA per SM):
 //   warp 3      scheduler and token loader: maps the cluster's next unit to (segment,
