@@ -430,6 +430,31 @@ def test_prefill_cluster_normal_values(ctas):
     assert_close(got, oracle.workload_reference(w), f"prefill, {ctas} CTAs per cluster")
 
 
+@pytest.mark.parametrize("hidden,ctas", [(1024, 8), (768, 4)])
+def test_prefill_split_with_few_column_tiles_exact(hidden, ctas):
+    """CTAs with only 2 (hidden 1024 at 8 CTAs per cluster) or 3 (hidden 768 at 4) column
+    tiles of 64: units split in at most 2 parts, unevenly at 3 tiles.  Exact-arithmetic
+    inputs, a handful of units: y equals the oracle bit for bit, split or not."""
+    ranks = np.array([8, 64, 128], np.int32)
+    lens = [128, 100, 256]
+    idx = np.concatenate([np.full(L, i) for i, L in enumerate(lens)]).astype(np.int32)
+    indptr = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    w = W.Workload("prefill_few_tiles", hidden, 1, ranks, idx, indptr, num_pages=2 * 2 * int(ranks.sum()),
+                   kv_pages=int(ranks.sum()), shuffle_seed=31, seed=32, values="exact")
+    ref = oracle.workload_reference(w).astype(np.float16).view(np.uint16)
+    rdp.slora_debug_set_prefill_cluster(ctas)
+    try:
+        with session_all_loaded(w) as s:
+            for split in (1, 0):
+                rdp.slora_debug_set_prefill_split(split)
+                got = run(s)
+                assert s.device_status() == 0
+                assert np.array_equal(got.view(np.uint16), ref), split
+    finally:
+        rdp.slora_debug_set_prefill_split(1)
+        rdp.slora_debug_set_prefill_cluster(0)
+
+
 @pytest.mark.parametrize("ctas", [4, 8])
 def test_prefill_last_round_split_matches_unsplit_bit_for_bit(ctas):
     """More units than clusters (44 against 38 clusters of 4 CTAs, or about 19 of 8): the
